@@ -1,0 +1,100 @@
+"""Plant plausible mistakes in the CPU oracle and check that the pins catch each.
+
+Every mutation is applied to the oracle module on the CPU (monkeypatch) and
+undone after the test; nothing here touches the CUDA library.
+"""
+import math
+
+import numpy as np
+import pytest
+
+import oracle.masw_oracle as o
+import oracle_pins as P
+
+
+def _fails_some_pin():
+    for pin in P.ALL_PINS:
+        try:
+            pin(o)
+        except Exception:
+            return pin.__name__
+    return None
+
+
+def _attention_variant(kv_of=None, use_scale=True, v_from_k=False, drop_max_in_lse=False):
+    def attention(q, K, V, mask, scale):
+        q = np.asarray(q, dtype=np.float64)
+        K = np.asarray(K, dtype=np.float64)
+        V = np.asarray(V, dtype=np.float64)
+        Hq, D = q.shape
+        Hkv = K.shape[1]
+        G = Hq // Hkv
+        mask = np.asarray(mask, dtype=bool)
+        O = np.zeros((Hq, D))
+        lse = np.full(Hq, -np.inf)
+        for h in range(Hq):
+            kv = kv_of(h, G, Hkv) if kv_of else h // G
+            row = mask if mask.ndim == 1 else mask[h]
+            if not row.any():
+                continue
+            s = (K[:, kv, :] @ q[h]) * (scale if use_scale else 1.0)
+            s = np.where(row, s, -np.inf)
+            mx = s.max()
+            w = np.where(row, np.exp(s - mx), 0.0)
+            z = w.sum()
+            O[h] = (w @ (K if v_from_k else V)[:, kv, :]) / z
+            lse[h] = (0.0 if drop_max_in_lse else mx) + math.log(z)
+        return O, lse
+    return attention
+
+
+MUTATIONS = {
+    "window_off_by_one": ("local_window", lambda t, S, W: (max(S + 1, t - W + 2), t)),
+    "window_too_wide": ("local_window", lambda t, S, W: (max(S + 1, t - W), t)),
+    "slot_count_floor_t_over_r": ("slot_count", lambda t, S, W, r: t // r),
+    "slot_count_without_window": ("slot_count", lambda t, S, W, r: max(0, (t - S) // r)),
+    "boundary_without_offset": ("is_boundary", lambda t, S, W, r: t >= r and t % r == 0),
+    "slot_pos_id_same_as_tau": ("slot_pos_id", lambda m, S, W, r: S + W + m * r),
+    "gqa_modulo_mapping": ("attention", _attention_variant(kv_of=lambda h, G, Hkv: h % Hkv)),
+    "scale_missing": ("attention", _attention_variant(use_scale=False)),
+    "v_replaced_by_k": ("attention", _attention_variant(v_from_k=True)),
+    "lse_without_max": ("attention", _attention_variant(drop_max_in_lse=True)),
+    "slot_reads_itself": ("slot_write_mask",
+                          lambda tau, m, S, W, self_attend=False: _slot_mask_self(tau, m, S, W)),
+    "verify_causal_shift": ("verify_mask", lambda kv_len, Lq: _verify_shift(kv_len, Lq)),
+    "sink_dropped": ("draft_mask", lambda t, n_slots, S, W: _draft_no_sink(t, n_slots, S, W)),
+}
+
+_orig = {name: getattr(o, name) for name in
+         ("local_window", "slot_write_mask", "verify_mask", "draft_mask")}
+
+
+def _slot_mask_self(tau, m, S, W):
+    row = _orig["slot_write_mask"](tau, m, S, W)
+    row[-1] = True
+    return row
+
+
+def _verify_shift(kv_len, Lq):
+    mask = np.zeros((Lq, kv_len), dtype=bool)
+    for j in range(Lq):
+        mask[j, :kv_len - Lq + j] = True
+    mask[0, 0] = True
+    return mask
+
+
+def _draft_no_sink(t, n_slots, S, W):
+    row = _orig["draft_mask"](t, n_slots, S, W)
+    lo, hi = _orig["local_window"](t, S, W)
+    row[:min(S, t)] = False
+    if hi >= lo:
+        row[lo - 1:hi] = True
+    return row
+
+
+@pytest.mark.parametrize("name", sorted(MUTATIONS))
+def test_planted_mistake_is_caught(name, monkeypatch):
+    attr, fn = MUTATIONS[name]
+    monkeypatch.setattr(o, attr, fn)
+    caught = _fails_some_pin()
+    assert caught is not None, f"no pin caught the planted mistake {name}"
