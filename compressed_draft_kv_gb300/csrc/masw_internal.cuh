@@ -1,0 +1,273 @@
+// Internal declarations of libmasw: the index model, the handle, PTX helpers
+// (TMA bulk copies, mbarriers with bounded waits) and the split-KV merge
+// shared by the decode and verify kernels.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include <string>
+#include <vector>
+
+#include "../../include/masw.h"
+
+// ---------------------------------------------------------------------------
+// Index model of one (layer, sequence), 1-based token ids as on the pages
+// ([EN] §3.1 Eq. 4 and the bullets under it; §3.2 Algorithm 1).
+// ---------------------------------------------------------------------------
+namespace masw {
+
+__host__ __device__ inline int imax(int a, int b) { return a > b ? a : b; }
+__host__ __device__ inline int imin(int a, int b) { return a < b ? a : b; }
+
+// lowest token of M_local,t: max(S+1, t-W+1)
+__host__ __device__ inline int window_lo(int t, int S, int W) { return imax(S + 1, t - W + 1); }
+// |M_local,t| = clamp(t - S, 0, W)
+__host__ __device__ inline int n_local(int t, int S, int W) { return imax(0, imin(W, t - S)); }
+// slots once step t is done: one per r tokens that left the window
+__host__ __device__ inline int slot_count(int t, int S, int W, int r) {
+    return t - S - W >= r ? (t - S - W) / r : 0;
+}
+__host__ __device__ inline bool is_boundary(int t, int S, int W, int r) {
+    return t >= S + W + r && (t - S - W) % r == 0;
+}
+// ring row of non-sink token i in a ring of Wc rows
+__host__ __device__ inline int ring_row(int i, int S, int Wc) { return (i - S - 1) % Wc; }
+
+}  // namespace masw
+
+// ---------------------------------------------------------------------------
+// The handle.
+// ---------------------------------------------------------------------------
+struct masw_mem {
+    int S = 0, W = 0, r = 0, Hkv = 0, D = 0, L = 0, B = 0, dtype = MASW_BF16;
+    int max_seq_len = 0, R = 0, Wc = 0, M_max = 0, C = 0;  // C = rows per (l,b,h) block
+    int full_kv = 0, self_attend = 0;
+    float scale = 0.f;
+    size_t esize = 2;
+    void* pool_k = nullptr;
+    void* pool_v = nullptr;
+    void* full_k = nullptr;
+    void* full_v = nullptr;
+    int* d_t = nullptr;      // [L*B] raw tokens appended
+    int* d_m = nullptr;      // [L*B] slots in the chain
+    int* d_pos = nullptr;    // [L*B*M_max] 0-based slot position ids
+    int* d_err = nullptr;    // [4] error word (bounded wait ran out)
+    float* part = nullptr;   // split partials
+    size_t part_floats = 0;  // capacity of `part`
+    unsigned* tickets = nullptr;      // [B*Hkv] per-(row, head) split tickets
+    unsigned* seq_tickets = nullptr;  // [B] per-row head tickets (slot write)
+    std::vector<int> h_t, h_m;
+    int device = 0, num_sms = 0;
+    std::string err;
+};
+
+namespace masw {
+
+constexpr int kMaxSplit = 256;
+
+// bounded-wait budget: ~2^22 polls with backoff is seconds, far above any
+// legitimate TMA latency; running out records MASW_ETIMEOUT and returns.
+constexpr uint32_t kWaitPolls = 1u << 22;
+
+// ---------------------------------------------------------------------------
+// PTX helpers (bulk copies and mbarriers, sm_90 and later; valid on sm_103a).
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+__device__ __forceinline__ void fence_mbar_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+                 : "memory");
+}
+// contiguous global -> shared bulk copy (TMA engine), completes on `bar`
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            smem_u32(dst)),
+        "l"(src), "r"(bytes), "r"(smem_u32(bar))
+        : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+// Bounded wait on a phase of `bar`.  Returns false (and records the failure in
+// *err) if the phase did not complete within the poll budget.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* err) {
+    for (uint32_t i = 0; i < kWaitPolls; ++i) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (i > 64) __nanosleep(128);
+    }
+    if (err) atomicExch(err, MASW_ETIMEOUT);
+    return false;
+}
+
+__device__ __forceinline__ float bf16lo(uint32_t x) { return __uint_as_float(x << 16); }
+__device__ __forceinline__ float bf16hi(uint32_t x) { return __uint_as_float(x & 0xffff0000u); }
+
+template <typename T> struct Elem;
+template <> struct Elem<float> {
+    static constexpr int kPerVec = 4;  // elements per 16-byte vector
+    __device__ __forceinline__ static void unpack(const uint4& v, float* f) {
+        f[0] = __uint_as_float(v.x); f[1] = __uint_as_float(v.y);
+        f[2] = __uint_as_float(v.z); f[3] = __uint_as_float(v.w);
+    }
+};
+template <> struct Elem<__nv_bfloat16> {
+    static constexpr int kPerVec = 8;
+    __device__ __forceinline__ static void unpack(const uint4& v, float* f) {
+        f[0] = bf16lo(v.x); f[1] = bf16hi(v.x); f[2] = bf16lo(v.y); f[3] = bf16hi(v.y);
+        f[4] = bf16lo(v.z); f[5] = bf16hi(v.z); f[6] = bf16lo(v.w); f[7] = bf16hi(v.w);
+    }
+};
+
+// ---------------------------------------------------------------------------
+// Split-KV epilogue.  A CTA that has reduced its key range to (m, l, o) per
+// query row -- m the running max of log2-scaled scores, l = sum 2^(s-m),
+// o = sum 2^(s-m) v (unnormalised) -- either writes the final output (one
+// split) or stores a partial and, if it is the last split of its (row, head)
+// pair to arrive, merges all partials with the log-sum-exp identity
+//   O = sum_s 2^(m_s-M) o_s / sum_s 2^(m_s-M) l_s,
+//   LSE = (M + log2 sum_s 2^(m_s-M) l_s) ln 2.
+// The ticket is taken with an atomic after a device-scope fence (no spinning)
+// and reset by the last CTA, so the next launch finds it at zero.
+// ---------------------------------------------------------------------------
+struct EpiOut {
+    float* o;            // output base for this pair
+    float* lse;          // LSE base for this pair (nullable)
+    // query row n of the pair lives at (n / rows_per_group) * *_group_stride
+    // + (n % rows_per_group) * *_row_stride floats from the base
+    int rows_per_group;
+    int o_row_stride, o_group_stride;
+    int lse_row_stride, lse_group_stride;
+    __device__ __forceinline__ size_t o_off(int n) const {
+        return (size_t)(n / rows_per_group) * o_group_stride + (size_t)(n % rows_per_group) * o_row_stride;
+    }
+    __device__ __forceinline__ size_t lse_off(int n) const {
+        return (size_t)(n / rows_per_group) * lse_group_stride + (size_t)(n % rows_per_group) * lse_row_stride;
+    }
+};
+
+// Shared-memory floats split_epilogue needs in `sm_scratch`.
+__host__ __device__ constexpr int epilogue_scratch_floats(int nrows, int n_split) {
+    return nrows * n_split + 2 * nrows;
+}
+
+// Returns true in every thread of the CTA that wrote the final output of its pair.
+template <int D>
+__device__ bool split_epilogue(int nrows, const float* sm_m, const float* sm_l, const float* sm_o,
+                               const EpiOut& out, float* part, unsigned* ticket, int split, int n_split,
+                               float* sm_scratch) {
+    const int tid = threadIdx.x, nt = blockDim.x;
+    constexpr float kLn2 = 0.6931471805599453f;
+    if (n_split == 1) {
+        for (int i = tid; i < nrows * D; i += nt) {
+            const int row = i / D, d = i % D;
+            const float l = sm_l[row];
+            out.o[out.o_off(row) + d] = l > 0.f ? sm_o[row * D + d] / l : 0.f;
+        }
+        if (out.lse)
+            for (int row = tid; row < nrows; row += nt) {
+                const float l = sm_l[row];
+                out.lse[out.lse_off(row)] = l > 0.f ? (sm_m[row] + __log2f(l)) * kLn2 : -INFINITY;
+            }
+        return true;
+    }
+    // store this split's partial: part[split][row][D + 2]
+    float* mine = part + (size_t)split * nrows * (D + 2);
+    for (int i = tid; i < nrows * D; i += nt) {
+        const int row = i / D, d = i % D;
+        mine[row * (D + 2) + d] = sm_o[row * D + d];
+    }
+    for (int row = tid; row < nrows; row += nt) {
+        mine[row * (D + 2) + D] = sm_m[row];
+        mine[row * (D + 2) + D + 1] = sm_l[row];
+    }
+    __threadfence();
+    __syncthreads();
+    __shared__ unsigned s_last;
+    if (tid == 0) {
+        const unsigned prev = atomicAdd(ticket, 1u);
+        s_last = (prev == (unsigned)(n_split - 1));
+    }
+    __syncthreads();
+    if (!s_last) return false;
+    __threadfence();
+    // merge: warp w takes rows w, w+nwarps, ...; lanes stride over splits.
+    float* w = sm_scratch;                    // [nrows][n_split] weights
+    float* s_den = sm_scratch + nrows * n_split;
+    float* s_M = s_den + nrows;
+    const int lane = tid & 31, warp = tid >> 5, nwarps = nt >> 5;
+    for (int row = warp; row < nrows; row += nwarps) {
+        float M = -INFINITY;
+        for (int s = lane; s < n_split; s += 32)
+            M = fmaxf(M, __ldcg(part + ((size_t)s * nrows + row) * (D + 2) + D));
+        for (int off = 16; off; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+        float den = 0.f;
+        for (int s = lane; s < n_split; s += 32) {
+            const float ms = __ldcg(part + ((size_t)s * nrows + row) * (D + 2) + D);
+            const float ls = __ldcg(part + ((size_t)s * nrows + row) * (D + 2) + D + 1);
+            const float ws = (ms == -INFINITY) ? 0.f : exp2f(ms - M);
+            w[row * n_split + s] = ws;
+            den += ws * ls;
+        }
+        for (int off = 16; off; off >>= 1) den += __shfl_xor_sync(0xffffffffu, den, off);
+        if (lane == 0) {
+            s_den[row] = den;
+            s_M[row] = M;
+        }
+    }
+    __syncthreads();
+    for (int i = tid; i < nrows * D; i += nt) {
+        const int row = i / D, d = i % D;
+        float acc = 0.f;
+        for (int s = 0; s < n_split; ++s) {
+            const float ws = w[row * n_split + s];
+            if (ws != 0.f) acc += ws * __ldcg(part + ((size_t)s * nrows + row) * (D + 2) + d);
+        }
+        const float den = s_den[row];
+        out.o[out.o_off(row) + d] = den > 0.f ? acc / den : 0.f;
+    }
+    if (out.lse)
+        for (int row = tid; row < nrows; row += nt) {
+            const float den = s_den[row];
+            out.lse[out.lse_off(row)] = den > 0.f ? (s_M[row] + __log2f(den)) * kLn2 : -INFINITY;
+        }
+    if (tid == 0) *ticket = 0u;
+    return true;
+}
+
+}  // namespace masw
+
+// ---------------------------------------------------------------------------
+// Host helpers shared by the translation units.
+// ---------------------------------------------------------------------------
+int masw_set_error(masw_mem_t* mem, int code, const std::string& msg);
+#define MASW_CUDA_TRY(mem, call)                                                        \
+    do {                                                                                \
+        cudaError_t e_ = (call);                                                        \
+        if (e_ != cudaSuccess)                                                          \
+            return masw_set_error((mem), MASW_ECUDA, std::string(#call) + ": " +       \
+                                                         cudaGetErrorString(e_));      \
+    } while (0)
+
+// decode-kernel launcher (masw_decode.cu)
+enum DecodeMode { kModeDraft = 0, kModeFull = 1, kModeSlot = 2 };
+int masw_launch_decode(masw_mem_t* mem, int mode, int layer, const void* q, int n_q_heads, float* o,
+                       float* lse, const int* seq_ids, int n_rows, const void* k_g, const void* v_g,
+                       cudaStream_t stream);
+// floats of split scratch one decode launch with these sizes may use
+size_t masw_decode_part_floats(int rows, int Hkv, int G, int D, int n_split);

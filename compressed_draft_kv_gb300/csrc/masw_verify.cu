@@ -1,0 +1,398 @@
+// Target verify attention over an uncompressed cache ([EN] §3.3 Algorithm 2
+// step 5): Lq query positions per sequence, causal inside the block, GQA.
+//
+// This is the one dense contraction on the path (Lq*G query rows share every
+// K/V row, 24 flop per byte at Lq = 6, G = 4), so it runs on tensor cores:
+// mma.sync m16n8k16 bf16 -> fp32 with KEYS as the M dimension and the Lq*G
+// query rows as N (8 per tile), so 24 query rows fill three N tiles without
+// padding.  S^T = K Q^T is accumulated per 16-key tile from ldmatrix fragments
+// of an XOR-swizzled shared-memory stage (cp.async, 3 stages), softmax runs
+// online per query column in the log2 domain, P^T is turned from the
+// accumulator layout into a B operand with movmatrix, and O^T += V^T P^T uses
+// ldmatrix.trans on the same V stage.  Splits over the key axis are merged by
+// split_epilogue.
+#include "masw_internal.cuh"
+
+#include <cstring>
+
+namespace masw {
+
+struct VerifyParams {
+    const __nv_bfloat16* q;   // [B][Lq][Hq][D]
+    const __nv_bfloat16* k;   // [B][Hkv][Tmax][D]
+    const __nv_bfloat16* v;
+    const int* kv_len;        // [B]
+    float* o;                 // [B][Lq][Hq][D]
+    float* lse;               // [B][Lq][Hq] or null
+    float* part;              // [B*Hkv][n_split][NQ][D+2]
+    unsigned* tickets;        // [B*Hkv]
+    int B, Lq, Hq, Hkv, G, NQ, Tmax, n_split;
+    float scale_log2;
+};
+
+constexpr int kVD = 128;             // head_dim
+constexpr int kVKeys = 64;           // keys per stage (16 per warp)
+constexpr int kVRowB = kVD * 2;      // bytes per K/V row
+constexpr int kVStage = 2 * kVKeys * kVRowB;
+constexpr int kVNst = 3;
+constexpr int kVSmem = kVNst * kVStage;
+constexpr int kVMaxSplit = 64;       // bounds the merge scratch kept in shared memory
+constexpr int kVMaxNQ = 32;
+static_assert((2 * 4 * kVMaxNQ + 4 * kVMaxNQ * kVD + 2 * kVMaxNQ + kVMaxNQ * kVD +
+               epilogue_scratch_floats(kVMaxNQ, kVMaxSplit)) * 4 <= kVSmem,
+              "verify merge does not fit in the stage buffers");
+
+__device__ __forceinline__ uint32_t swz(int row, int chunk) {  // byte offset of a 16-B chunk
+    return (uint32_t)(row * kVRowB + ((chunk ^ (row & 7)) << 4));
+}
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, int src_bytes) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(addr));
+}
+__device__ __forceinline__ void mma16816(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                         uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+__device__ __forceinline__ uint32_t movmatrix_t(uint32_t x) {
+    uint32_t y;
+    asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
+    return y;
+}
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&v);
+}
+
+template <int NT>
+__global__ void __launch_bounds__(128) verify_kernel(const __grid_constant__ VerifyParams p) {
+    extern __shared__ __align__(128) uint8_t smem[];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int split = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+    const int G = p.G, NQ = p.NQ;
+
+    const int n_keys = p.kv_len[b];
+    const int chunk = (((n_keys + p.n_split - 1) / p.n_split) + kVKeys - 1) / kVKeys * kVKeys;
+    const int k0 = imin(n_keys, split * chunk);
+    const int k1 = imin(n_keys, k0 + chunk);
+    const int nstage = (k1 - k0 + kVKeys - 1) / kVKeys;
+
+    const __nv_bfloat16* kbase = p.k + ((size_t)b * p.Hkv + h) * (size_t)p.Tmax * kVD;
+    const __nv_bfloat16* vbase = p.v + ((size_t)b * p.Hkv + h) * (size_t)p.Tmax * kVD;
+    const uint32_t sbase = smem_u32(smem);
+
+    // one stage = 64 keys of K and V, 16-byte chunks XOR-swizzled by row;
+    // rows past k1 are zero-filled (src-size 0 reads nothing)
+    auto load_stage = [&](int c) {
+        const uint32_t sk = sbase + (uint32_t)(c % kVNst) * kVStage;
+        const uint32_t sv = sk + kVKeys * kVRowB;
+        const int key0 = k0 + c * kVKeys;
+#pragma unroll
+        for (int i = 0; i < (kVKeys * 16) / 128; ++i) {
+            const int idx = tid + i * 128;
+            const int row = idx >> 4, ch = idx & 15;
+            const int key = key0 + row;
+            const bool in = key < k1;
+            const size_t goff = (size_t)(in ? key : k0) * kVD + ch * 8;
+            cp_async16(sk + swz(row, ch), kbase + goff, in ? 16 : 0);
+            cp_async16(sv + swz(row, ch), vbase + goff, in ? 16 : 0);
+        }
+    };
+#pragma unroll
+    for (int c = 0; c < kVNst - 1; ++c) {
+        if (c < nstage) load_stage(c);
+        cp_async_commit();
+    }
+
+    // Q^T as B fragments: column n = query row (j = n / G, gi = n % G)
+    uint32_t qb[8][NT][2];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+        const int n = nt * 8 + (lane >> 2);
+        const bool real = n < NQ;
+        const int j = real ? n / G : 0, gi = real ? n % G : 0;
+        const __nv_bfloat16* qrow = p.q + (((size_t)b * p.Lq + j) * p.Hq + (size_t)h * G + gi) * kVD;
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks) {
+            const int d = ks * 16 + (lane & 3) * 2;
+            qb[ks][nt][0] = real ? *reinterpret_cast<const uint32_t*>(qrow + d) : 0u;
+            qb[ks][nt][1] = real ? *reinterpret_cast<const uint32_t*>(qrow + d + 8) : 0u;
+        }
+    }
+    // causal limit of this lane's two columns per N tile: key < lim
+    int lim[NT][2];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            const int n = nt * 8 + (lane & 3) * 2 + e;
+            lim[nt][e] = n < NQ ? imin(k1, n_keys - p.Lq + 1 + n / G) : k1;
+        }
+
+    float m_run[NT][2], l_run[NT][2];
+    float acc[8][NT][4];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+        m_run[nt][0] = m_run[nt][1] = -INFINITY;
+        l_run[nt][0] = l_run[nt][1] = 0.f;
+#pragma unroll
+        for (int mt = 0; mt < 8; ++mt) acc[mt][nt][0] = acc[mt][nt][1] = acc[mt][nt][2] = acc[mt][nt][3] = 0.f;
+    }
+
+    for (int c = 0; c < nstage; ++c) {
+        cp_async_wait<kVNst - 2>();
+        __syncthreads();
+        {   // refill the stage consumed in the previous iteration
+            const int cn = c + kVNst - 1;
+            if (cn < nstage) load_stage(cn);
+            cp_async_commit();
+        }
+        const uint32_t sk = sbase + (uint32_t)(c % kVNst) * kVStage;
+        const uint32_t sv = sk + kVKeys * kVRowB;
+        const int kw = warp * 16;
+        const int key_tile = k0 + c * kVKeys + kw;
+        if (key_tile < k1) {
+            float s[NT][4];
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
+#pragma unroll
+            for (int ks = 0; ks < 8; ++ks) {
+                uint32_t a0, a1, a2, a3;
+                const int row = kw + (lane & 7) + ((lane >> 3) & 1) * 8;
+                ldsm_x4(sk + swz(row, ks * 2 + (lane >> 4)), a0, a1, a2, a3);
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt) mma16816(s[nt], a0, a1, a2, a3, qb[ks][nt][0], qb[ks][nt][1]);
+            }
+            const int key_a = key_tile + (lane >> 2), key_b = key_a + 8;
+            uint32_t pb[NT][2];
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+                float x[4];
+                x[0] = key_a < lim[nt][0] ? s[nt][0] * p.scale_log2 : -INFINITY;
+                x[1] = key_a < lim[nt][1] ? s[nt][1] * p.scale_log2 : -INFINITY;
+                x[2] = key_b < lim[nt][0] ? s[nt][2] * p.scale_log2 : -INFINITY;
+                x[3] = key_b < lim[nt][1] ? s[nt][3] * p.scale_log2 : -INFINITY;
+                float pr[4];
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    float mx = fmaxf(x[e], x[e + 2]);
+                    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+                    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+                    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+                    const float m_new = fmaxf(m_run[nt][e], mx);
+                    const float m_use = m_new == -INFINITY ? 0.f : m_new;   // column fully masked so far
+                    const float alpha = exp2f(m_run[nt][e] - m_use);
+                    pr[e] = exp2f(x[e] - m_use);
+                    pr[e + 2] = exp2f(x[e + 2] - m_use);
+                    l_run[nt][e] = l_run[nt][e] * alpha + pr[e] + pr[e + 2];
+                    m_run[nt][e] = m_new;
+#pragma unroll
+                    for (int mt = 0; mt < 8; ++mt) {
+                        acc[mt][nt][e] *= alpha;
+                        acc[mt][nt][e + 2] *= alpha;
+                    }
+                }
+                pb[nt][0] = movmatrix_t(pack_bf16(pr[0], pr[1]));
+                pb[nt][1] = movmatrix_t(pack_bf16(pr[2], pr[3]));
+            }
+#pragma unroll
+            for (int mt = 0; mt < 8; ++mt) {
+                uint32_t a0, a1, a2, a3;
+                const int row = kw + (lane & 7) + (lane >> 4) * 8;
+                ldsm_x4_t(sv + swz(row, mt * 2 + ((lane >> 3) & 1)), a0, a1, a2, a3);
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt) mma16816(acc[mt][nt], a0, a1, a2, a3, pb[nt][0], pb[nt][1]);
+            }
+        }
+    }
+    cp_async_wait<0>();
+    __syncthreads();
+
+    // ---- warp results -> shared, then merge the 4 warps ----
+    constexpr int NQM = NT * 8;
+    float* wm = reinterpret_cast<float*>(smem);    // [4][NQM]
+    float* wl = wm + 4 * NQM;                       // [4][NQM]
+    float* wo = wl + 4 * NQM;                       // [4][NQM][D]
+    float* cm = wo + 4 * NQM * kVD;                 // [NQM]
+    float* cl = cm + NQM;
+    float* co = cl + NQM;                           // [NQM][D]
+    float* scratch = co + NQM * kVD;
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            float l = l_run[nt][e];
+            l += __shfl_xor_sync(0xffffffffu, l, 4);
+            l += __shfl_xor_sync(0xffffffffu, l, 8);
+            l += __shfl_xor_sync(0xffffffffu, l, 16);
+            const int n = nt * 8 + (lane & 3) * 2 + e;
+            if (lane < 4) {
+                wm[warp * NQM + n] = m_run[nt][e];
+                wl[warp * NQM + n] = l;
+            }
+#pragma unroll
+            for (int mt = 0; mt < 8; ++mt) {
+                const int d = mt * 16 + (lane >> 2);
+                wo[(warp * NQM + n) * kVD + d] = acc[mt][nt][e];
+                wo[(warp * NQM + n) * kVD + d + 8] = acc[mt][nt][e + 2];
+            }
+        }
+    __syncthreads();
+    if (tid < NQ) {
+        float M = -INFINITY;
+        for (int w = 0; w < 4; ++w) M = fmaxf(M, wm[w * NQM + tid]);
+        float l = 0.f;
+        for (int w = 0; w < 4; ++w)
+            if (wm[w * NQM + tid] != -INFINITY) l += exp2f(wm[w * NQM + tid] - M) * wl[w * NQM + tid];
+        cm[tid] = M;
+        cl[tid] = l;
+    }
+    __syncthreads();
+    for (int i = tid; i < NQ * kVD; i += 128) {
+        const int n = i / kVD;
+        const float M = cm[n];
+        float a = 0.f;
+        for (int w = 0; w < 4; ++w)
+            if (wm[w * NQM + n] != -INFINITY) a += exp2f(wm[w * NQM + n] - M) * wo[(w * NQM + n) * kVD + (i % kVD)];
+        co[i] = a;
+    }
+    __syncthreads();
+
+    EpiOut out;
+    out.o = p.o + ((size_t)b * p.Lq * p.Hq + (size_t)h * G) * kVD;
+    out.lse = p.lse ? p.lse + (size_t)b * p.Lq * p.Hq + (size_t)h * G : nullptr;
+    out.rows_per_group = G;
+    out.o_row_stride = kVD;
+    out.o_group_stride = p.Hq * kVD;
+    out.lse_row_stride = 1;
+    out.lse_group_stride = p.Hq;
+    float* part = p.part + (size_t)(b * p.Hkv + h) * p.n_split * NQ * (kVD + 2);
+    split_epilogue<kVD>(NQ, cm, cl, co, out, part, p.tickets + b * p.Hkv + h, split, p.n_split, scratch);
+}
+
+// split count shared by the launcher and the workspace query
+static int verify_splits(int B, int Hkv, int Tmax, int num_sms) {
+    const int pairs = B * Hkv;
+    int n = imax(1, (4 * num_sms + pairs - 1) / pairs);
+    n = imin(n, imax(1, (Tmax + 255) / 256));
+    return imin(n, kVMaxSplit);
+}
+
+static int num_sms_current(int* out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return MASW_ECUDA;
+    if (cudaDeviceGetAttribute(out, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return MASW_ECUDA;
+    return MASW_OK;
+}
+
+static size_t verify_part_bytes(int B, int Hkv, int NQ, int n_split) {
+    const size_t partb = (size_t)B * Hkv * n_split * NQ * (kVD + 2) * sizeof(float);
+    return ((partb + 255) / 256) * 256;
+}
+
+}  // namespace masw
+
+using namespace masw;
+
+static int verify_check(int B, int Lq, int Hq, int Hkv, int D, int Tmax) {
+    if (B < 1 || Lq < 1 || Hq < 1 || Hkv < 1 || Tmax < Lq) return MASW_EINVAL;
+    if (D != kVD) return MASW_EINVAL;
+    if (Hq % Hkv) return MASW_EINVAL;
+    if ((Hq / Hkv) * Lq > kVMaxNQ) return MASW_EINVAL;
+    if (B > 65535 || Hkv > 65535) return MASW_EINVAL;
+    return MASW_OK;
+}
+
+extern "C" int masw_verify_workspace_bytes(int B, int Lq, int Hq, int Hkv, int D, int Tmax, size_t* bytes) {
+    if (!bytes) return masw_set_error(nullptr, MASW_EINVAL, "bytes is NULL");
+    int rc = verify_check(B, Lq, Hq, Hkv, D, Tmax);
+    if (rc) return masw_set_error(nullptr, rc, "unsupported verify sizes (D must be 128, Lq*Hq/Hkv <= 32)");
+    int sms = 0;
+    if (num_sms_current(&sms)) return masw_set_error(nullptr, MASW_ECUDA, "cannot query the current device");
+    const int n_split = verify_splits(B, Hkv, Tmax, sms);
+    *bytes = verify_part_bytes(B, Hkv, (Hq / Hkv) * Lq, n_split) + (size_t)B * Hkv * sizeof(unsigned);
+    return MASW_OK;
+}
+
+template <int NT>
+static cudaError_t launch_verify(const VerifyParams& prm, cudaStream_t stream) {
+    static bool configured[64] = {};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (!configured[dev & 63]) {
+        cudaError_t e = cudaFuncSetAttribute(verify_kernel<NT>, cudaFuncAttributeMaxDynamicSharedMemorySize, kVSmem);
+        if (e != cudaSuccess) return e;
+        configured[dev & 63] = true;
+    }
+    dim3 grid(prm.n_split, prm.Hkv, prm.B);
+    verify_kernel<NT><<<grid, 128, kVSmem, stream>>>(prm);
+    return cudaGetLastError();
+}
+
+extern "C" int masw_verify_attn(const void* q, const void* k_cache, const void* v_cache, const int* kv_len, int B,
+                                int Lq, int Hq, int Hkv, int D, int Tmax, int dtype, float scale, float* o,
+                                float* lse, void* workspace, size_t workspace_bytes, masw_stream_t stream) {
+    if (!q || !k_cache || !v_cache || !kv_len || !o || !workspace)
+        return masw_set_error(nullptr, MASW_EINVAL, "verify: NULL pointer");
+    if (dtype != MASW_BF16) return masw_set_error(nullptr, MASW_EINVAL, "verify: only MASW_BF16 is supported");
+    int rc = verify_check(B, Lq, Hq, Hkv, D, Tmax);
+    if (rc) return masw_set_error(nullptr, rc, "verify: unsupported sizes (D must be 128, Lq*Hq/Hkv <= 32)");
+    if (((uintptr_t)q | (uintptr_t)k_cache | (uintptr_t)v_cache | (uintptr_t)workspace) & 15)
+        return masw_set_error(nullptr, MASW_EINVAL, "verify: q, caches and workspace must be 16-byte aligned");
+    if (((uintptr_t)o | (uintptr_t)lse | (uintptr_t)kv_len) & 3)
+        return masw_set_error(nullptr, MASW_EINVAL, "verify: o, lse and kv_len must be 4-byte aligned");
+    int sms = 0;
+    if (num_sms_current(&sms)) return masw_set_error(nullptr, MASW_ECUDA, "verify: cannot query the device");
+    const int G = Hq / Hkv, NQ = G * Lq;
+    const int n_split = verify_splits(B, Hkv, Tmax, sms);
+    const size_t partb = verify_part_bytes(B, Hkv, NQ, n_split);
+    if (workspace_bytes < partb + (size_t)B * Hkv * sizeof(unsigned))
+        return masw_set_error(nullptr, MASW_EINVAL, "verify: workspace too small");
+    VerifyParams prm;
+    std::memset(&prm, 0, sizeof(prm));
+    prm.q = (const __nv_bfloat16*)q;
+    prm.k = (const __nv_bfloat16*)k_cache;
+    prm.v = (const __nv_bfloat16*)v_cache;
+    prm.kv_len = kv_len;
+    prm.o = o;
+    prm.lse = lse;
+    prm.part = (float*)workspace;
+    prm.tickets = (unsigned*)((uint8_t*)workspace + partb);
+    prm.B = B;
+    prm.Lq = Lq;
+    prm.Hq = Hq;
+    prm.Hkv = Hkv;
+    prm.G = G;
+    prm.NQ = NQ;
+    prm.Tmax = Tmax;
+    prm.n_split = n_split;
+    prm.scale_log2 = (scale > 0.f ? scale : 1.0f / sqrtf((float)D)) * 1.4426950408889634f;
+    cudaStream_t st = (cudaStream_t)stream;
+    cudaError_t e = cudaMemsetAsync(prm.tickets, 0, (size_t)B * Hkv * sizeof(unsigned), st);
+    if (e != cudaSuccess) return masw_set_error(nullptr, MASW_ECUDA, std::string("verify: ") + cudaGetErrorString(e));
+    const int NT = (NQ + 7) / 8;
+    switch (NT) {
+        case 1: e = launch_verify<1>(prm, st); break;
+        case 2: e = launch_verify<2>(prm, st); break;
+        case 3: e = launch_verify<3>(prm, st); break;
+        default: e = launch_verify<4>(prm, st); break;
+    }
+    if (e != cudaSuccess) return masw_set_error(nullptr, MASW_ECUDA, std::string("verify: ") + cudaGetErrorString(e));
+    return MASW_OK;
+}

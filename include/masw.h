@@ -1,0 +1,232 @@
+/*
+ * masw.h -- C ABI of libmasw: GB300 (sm_103a) draft-side compressed KV memory
+ * and attention for Memory-Augmented Sliding-Window (MASW) drafting.
+ *
+ * Pages this interface follows (titles abbreviated):
+ *   [EN] "Strong Drafts Need Compact Memories: A Technical Review of
+ *        Memory-Augmented Sliding-Window (MASW) Drafting for Long-Context
+ *        Speculative Decoding", sections 2.3 (Eq. 2), 3.1 (Eq. 4), 3.2
+ *        (Algorithm 1) and 3.3 (Algorithm 2).
+ *
+ * Model of the state.  For every (layer l, sequence b) the library keeps the
+ * draft working memory of Eq. 4, M_t = M_sink u M_local,t u M_slot,t:
+ *   - M_sink : exact K/V of raw tokens 1..S, never evicted;
+ *   - M_local,t : exact K/V of raw tokens max(S+1, t-W+1) .. t, held in a ring
+ *     of W + R rows (R = rollback reserve, 0 by default); token i sits in ring
+ *     row (i-S-1) mod (W+R), so appending token i overwrites (evicts) token
+ *     i-W-R;
+ *   - M_slot,t : an append-only chain of memory slots, one K/V row per kv head
+ *     each, one slot per r raw tokens that have left the window.  Slot g_m is
+ *     written at boundary tau_m = S + W + m*r.
+ * Token ids on the pages are 1-based; the library stores row p = i-1 and
+ * reports 0-based position ids.
+ *
+ * Conventions for every call:
+ *   - Return value is a status: MASW_OK (0) or a negative MASW_E* code.  No C++
+ *     exception and no abort() crosses this interface.  masw_last_error()
+ *     gives a message for the last failing call on a handle.
+ *   - Pointers named "device" must be CUDA device (or managed) memory owned by
+ *     the caller; the library never frees them.  The memory pool, its counters
+ *     and its scratch are owned by the handle: allocated in masw_mem_create,
+ *     freed in masw_mem_destroy.
+ *   - Compute calls are asynchronous on the given stream (a cudaStream_t,
+ *     NULL = legacy default stream).  Argument and state errors are returned
+ *     synchronously, before anything is enqueued.  Errors raised inside a
+ *     kernel (a bounded wait that ran out) are recorded in a device flag and
+ *     returned by the next masw_sync().
+ *   - A handle is used from one host thread and one stream at a time; calls on
+ *     one handle that overlap on the GPU race on the pool and its scratch.
+ *   - Element types: MASW_BF16 (bfloat16) or MASW_F32 for Q/K/V inputs, chosen
+ *     at create time.  Attention outputs O are float32; LSE outputs are the
+ *     float32 natural-log normaliser log sum_j exp(scale * q.k_j).
+ *   - Layouts are C-contiguous, innermost dimension last.  Q/K/V pointers must
+ *     be 16-byte aligned, O/LSE pointers 4-byte aligned.
+ */
+#ifndef MASW_H
+#define MASW_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- status codes -------------------------------------------------------- */
+#define MASW_OK          0
+#define MASW_EINVAL     -1  /* bad argument (size, pointer, layer, dtype, head counts) */
+#define MASW_ENOMEM     -2  /* device allocation failed */
+#define MASW_ECAPACITY  -3  /* pool capacity exceeded (max_seq_len, slot chain) */
+#define MASW_ESTATE     -4  /* call not valid in the current state (e.g. not at a boundary) */
+#define MASW_ECUDA      -5  /* a CUDA runtime call failed */
+#define MASW_ETIMEOUT   -6  /* a bounded device-side wait ran out (kernel returned early) */
+
+/* ---- element types ------------------------------------------------------- */
+#define MASW_F32   0
+#define MASW_BF16  1
+
+/* ---- limits --------------------------------------------------------------- */
+#define MASW_MAX_BATCH  512   /* sequences per handle */
+#define MASW_MAX_GROUP  8     /* query heads per kv head (G = Hq / Hkv): 1,2,3,4,6,8 */
+
+typedef struct masw_mem masw_mem_t;
+typedef void* masw_stream_t;   /* a cudaStream_t */
+
+typedef struct {
+    int   batch;            /* sequences held, 1..MASW_MAX_BATCH (0 -> 1) */
+    int   dtype;            /* MASW_BF16 (default) or MASW_F32 */
+    int   max_seq_len;      /* longest sequence, in raw tokens; sizes the slot chain
+                               (m(max_seq_len) slots) and the full-KV cache.
+                               0 -> 32768 */
+    float softmax_scale;    /* 0 -> 1/sqrt(head_dim) (Eq. 2) */
+    int   slot_self_attend; /* 0 (default): slot query g_m does not read its own K/V;
+                               1: it does (standard causal diagonal) */
+    int   full_kv;          /* 1: also keep an uncompressed cache of max_seq_len
+                               rows per (layer, sequence, kv head) for masw_full_attn */
+    int   rollback_reserve; /* R extra ring rows; masw_rollback can undo up to R tokens */
+} masw_opts_t;
+
+typedef struct {
+    int t;          /* raw tokens appended (host mirror) */
+    int n_sink;     /* min(S, t) */
+    int n_local;    /* tokens in the local window: clamp(t - S, 0, W) */
+    int m;          /* slots in the chain (host mirror) */
+    int dev_t;      /* device counters, read back synchronously; equal to t, m */
+    int dev_m;      /*   unless a captured graph replay changed the state */
+    int ring_rows;  /* W + R */
+    int rows;       /* rows per (layer, sequence, kv head) block: S + W + R + M_max */
+    int slot_capacity; /* M_max */
+} masw_state_t;
+
+/* ---- lifetime -------------------------------------------------------------- */
+
+/* Create a pool for `layers` layers x opts->batch sequences x n_kv_heads heads
+ * of head_dim, with S sink tokens (S >= 0), W local-window tokens (W >= 1) and
+ * one slot per r evicted tokens (r >= 1) ([EN] §3.1 Eq. 4, §3.2 Algorithm 1).
+ * head_dim must be 64 or 128.  opts may be NULL (batch 1, bf16, max_seq_len
+ * 32768).  Allocates the pool (K and V: layers*batch*Hkv*(S+W+R+M_max)*D
+ * elements each), the optional full-KV cache, counters and split scratch on
+ * the current device.  On failure *out is NULL. */
+int masw_mem_create(int S, int W, int r, int n_kv_heads, int head_dim, int layers,
+                    const masw_opts_t* opts, masw_mem_t** out);
+
+/* Free everything the handle owns.  NULL is accepted.  Synchronises the device. */
+int masw_mem_destroy(masw_mem_t* mem);
+
+/* Message for the last failing call on `mem` (or on a NULL handle / stateless call). */
+const char* masw_last_error(const masw_mem_t* mem);
+
+/* ---- memory maintenance ---------------------------------------------------- */
+
+/* Append one raw token to every active sequence of `layer` ([EN] §3.3
+ * Algorithm 2 step 4): k, v are device [batch, Hkv, D] in the pool dtype.
+ * Token i = t+1 goes to sink row i-1 if i <= S, else to ring row (i-S-1) mod
+ * (W+R); that write is the eviction of [EN] §3.2 Algorithm 1 step 5.  With
+ * full_kv it is also written to row i-1 of the full cache.  active: host
+ * [batch] bytes, nonzero = append; NULL = all.  ECAPACITY when t would exceed
+ * max_seq_len. */
+int masw_append_kv(masw_mem_t* mem, int layer, const void* k, const void* v,
+                   const uint8_t* active, masw_stream_t stream);
+
+/* Memory-slot write at a compression boundary ([EN] §3.2 Algorithm 1 steps
+ * 2, 4 and 6) for the n sequences in the host list seq_ids.  For each listed
+ * sequence b, which must have t = tau_m = S + W + m*r for the next chain index
+ * m (ESTATE otherwise):
+ *   1. the slot query q_g attends, under the structured mask, to M_sink,
+ *      M_local,tau_m and slots 1..m-1 (and to itself only with
+ *      slot_self_attend); O_g and its LSE are returned;
+ *   2. K_g, V_g (already projected by the caller's mirrored W_K,g / W_V,g)
+ *      are appended as slot m;
+ *   3. slot m gets position id tau_m (0-based id of the raw token after it).
+ * q_g: device [n, n_q_heads, D]; k_g, v_g: device [n, Hkv, D]; o_g: device
+ * float [n, n_q_heads, D]; lse_g: device float [n, n_q_heads] or NULL.
+ * seq_ids must be distinct.  ECAPACITY when the chain is full.  Call it after
+ * masw_draft_attn of the boundary step, so that the query at tau_m sees m-1
+ * slots. */
+int masw_materialize_slot(masw_mem_t* mem, int layer, const int* seq_ids, int n,
+                          const void* q_g, const void* k_g, const void* v_g,
+                          float* o_g, float* lse_g, int n_q_heads, masw_stream_t stream);
+
+/* Undo the last t[b] - t_new[i] raw tokens of the listed sequences in every
+ * layer ([EN] §3.3 Algorithm 2 step 6): counters go back to t_new and slots
+ * with tau_m > t_new are dropped.  Needs 0 <= t - t_new <= R in every layer
+ * (ESTATE otherwise), because the ring rows of the restored window must not
+ * have been overwritten.  seq_ids, t_new: host arrays of n. */
+int masw_rollback(masw_mem_t* mem, const int* seq_ids, const int* t_new, int n,
+                  masw_stream_t stream);
+
+/* ---- attention --------------------------------------------------------------- */
+
+/* Draft decode attention over M_t ([EN] §2.3 Eq. 2 over the set of §3.1 Eq. 4):
+ * O[b, h] = softmax(scale * q[b,h] . K_j) V_j over j in sink u window u slots
+ * of (layer, b), kv head h / (n_q_heads / Hkv).  The segments are walked in
+ * place (ring in physical row order; softmax does not depend on order).
+ * q: device [batch, n_q_heads, D] (pool dtype); o: device float
+ * [batch, n_q_heads, D]; lse: device float [batch, n_q_heads] or NULL.
+ * A sequence with t = 0 gets O = 0 and LSE = -inf. */
+int masw_draft_attn(masw_mem_t* mem, int layer, const void* q, int n_q_heads,
+                    float* o, float* lse, masw_stream_t stream);
+
+/* Full-KV decode attention over raw tokens 1..t ([EN] §2.3 Eq. 2 with the
+ * whole prefix; the uncompressed draft the pages contrast against).  Same
+ * arguments as masw_draft_attn.  ESTATE unless the pool was created with
+ * full_kv = 1. */
+int masw_full_attn(masw_mem_t* mem, int layer, const void* q, int n_q_heads,
+                   float* o, float* lse, masw_stream_t stream);
+
+/* Target verify attention ([EN] §3.3 Algorithm 2 step 5), stateless: Lq query
+ * positions per sequence against an uncompressed cache, causal inside the
+ * block.  Query j (0-based) of sequence b sees keys 0 .. kv_len[b]-Lq+j
+ * (kv_len counts the block's own Lq tokens).  bf16 only.
+ * q: device [B, Lq, Hq, D]; k_cache, v_cache: device [B, Hkv, Tmax, D];
+ * kv_len: device int [B], each in [Lq, Tmax]; o: device float [B, Lq, Hq, D];
+ * lse: device float [B, Lq, Hq] or NULL; workspace: device scratch of at least
+ * masw_verify_workspace_bytes() bytes (contents need no initialisation; it
+ * must not be shared by calls that overlap on the GPU).  scale 0 -> 1/sqrt(D).
+ * D must be 128 and (Hq/Hkv) * Lq <= 32. */
+int masw_verify_attn(const void* q, const void* k_cache, const void* v_cache,
+                     const int* kv_len, int B, int Lq, int Hq, int Hkv, int D,
+                     int Tmax, int dtype, float scale, float* o, float* lse,
+                     void* workspace, size_t workspace_bytes, masw_stream_t stream);
+
+/* Bytes of workspace masw_verify_attn needs for these sizes on the current device. */
+int masw_verify_workspace_bytes(int B, int Lq, int Hq, int Hkv, int D, int Tmax,
+                                size_t* bytes);
+
+/* ---- plumbing for set-up, tests and benchmarks --------------------------------- */
+
+/* Set (layer, seq) to the state after t raw tokens whose K/V are k_raw, v_raw
+ * ([t, Hkv, D], host or device), with n_slots slots k_slots, v_slots
+ * ([n_slots, Hkv, D], host or device) as if materialised at tau_1..tau_n.
+ * EINVAL unless n_slots == max(0, (t-S-W)/r).  Synchronous. */
+int masw_mem_load(masw_mem_t* mem, int layer, int seq, int t,
+                  const void* k_raw, const void* v_raw,
+                  const void* k_slots, const void* v_slots, int n_slots);
+
+/* Copy the pool block of (layer, seq) -- K and V, each [Hkv, rows, D] with
+ * rows = S + W + R + M_max -- into caller memory (host or device).  Optional
+ * slot_pos: host int [M_max] receives the device-recorded 0-based position ids
+ * (-1 where no slot was ever written).  Synchronous. */
+int masw_mem_export(masw_mem_t* mem, int layer, int seq, void* k_out, void* v_out,
+                    int* slot_pos);
+
+/* Counters of (layer, seq): host mirror and device copy.  Synchronous. */
+int masw_query(masw_mem_t* mem, int layer, int seq, masw_state_t* out);
+
+/* Wait for the stream, then report any error recorded by a kernel since the
+ * last masw_sync (MASW_ETIMEOUT) or by the CUDA runtime (MASW_ECUDA). */
+int masw_sync(masw_mem_t* mem, masw_stream_t stream);
+
+/* Host-side index model, exported so it can be checked without a GPU.
+ * which: 0 = local-window lo (1-based), 1 = n_local, 2 = slot count m(t),
+ * 3 = is_boundary(t), 4 = ring row of token t ((t-S-1) mod (W+R), -1 for a
+ * sink token), 5 = working-set size.  Returns -1 for bad arguments. */
+int masw_index(int which, int t, int S, int W, int r, int R);
+
+/* Library version, "major.minor.patch". */
+const char* masw_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MASW_H */
