@@ -1,0 +1,430 @@
+"""GPU parity: every C-ABI call against the CPU oracle on the same seeded inputs.
+
+Indices (counters, ring placement, slot ids) are compared bit for bit; attention
+outputs within the stated tolerance (fp32 inputs: 2e-5 absolute; bf16 inputs:
+max abs <= 1e-2 and relative L2 <= 5e-3).
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle.masw_oracle as orc
+from compressed_draft_kv_gb300 import capi, synth
+from gpu_helpers import DEV, Pair, assert_close, to_np
+from libmasw_fixture import ensure_built
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    ensure_built()
+    torch.cuda.set_device(DEV)
+
+
+def test_tiny_f32_single_layer():
+    """8q/2kv heads, D=64, fp32, t=2048, S=4, W=256, r=256 (6 slots): a draft
+    step, appends up to tau_7 = 2052, the slot write there and eviction."""
+    p = Pair(4, 256, 256, 2, 64, 1, 1, "f32", 8, max_seq_len=4096, full_kv=True, tag="tiny")
+    try:
+        p.load(0, 0, 2048, seed=0)
+        assert p.ref.m(0, 0) == 6
+        p.check_state(0, 0)
+        p.draft(0)
+        p.draft(0, full=True)
+        for step in range(2049, 2054):
+            p.step = step
+            p.append(0)
+            p.draft(0)
+            p.draft(0, full=True)
+            if orc.is_boundary(step, 4, 256, 256):
+                assert step == 2052
+                p.materialize(0, [0])
+            p.check_state(0, 0)
+        assert p.ref.m(0, 0) == 7
+    finally:
+        p.close()
+
+
+def test_draft3b_shape_one_layer_8k():
+    """24q/8kv heads, D=128, bf16, t=8192 (13 slots), S=4, W=1024, r=512: five
+    draft steps; the boundary tau_14 = 8196 is crossed at the fourth."""
+    p = Pair(4, 1024, 512, 8, 128, 1, 1, "bf16", 24, max_seq_len=8192 + 16, full_kv=True, tag="cfg2")
+    try:
+        p.load(0, 0, 8192, seed=1)
+        assert p.ref.m(0, 0) == 13
+        p.draft(0)
+        for step in range(8193, 8198):
+            p.step = step
+            p.append(0)
+            p.draft(0)
+            p.draft(0, full=True)
+            if step == 8196:
+                p.materialize(0, [0])
+        p.check_state(0, 0)
+        assert p.ref.m(0, 0) == 14
+    finally:
+        p.close()
+
+
+@pytest.mark.parametrize("dtype,D,G", [("f32", 64, 4), ("bf16", 128, 3), ("bf16", 64, 8), ("f32", 128, 1)])
+def test_masw_equals_full_before_eviction(dtype, D, G):
+    """No slots and t <= S+W: the draft working set is the whole prefix."""
+    S, W = 5, 100
+    p = Pair(S, W, 16, 2, D, 1, 1, dtype, 2 * G, max_seq_len=256, full_kv=True, tag="eq")
+    try:
+        for t in range(1, S + W + 1):
+            p.step = t
+            p.append(0)
+            if t in (1, S, S + 1, 37, S + W):
+                q = p.rand((1, 2 * G, D), "q")
+                o1, l1, want, _ = p.draft(0, q=q)
+                o2, l2, want_f, _ = p.draft(0, q=q, full=True)
+                assert np.array_equal(want, want_f)
+                assert_close(o1, to_np(o2), "f32", f"draft vs full t={t}")
+        p.check_state(0, 0)
+    finally:
+        p.close()
+
+
+def test_one_hot_values_show_exact_exclusion():
+    """V_i = e_i: the output is the weight vector.  Raw tokens outside sink and
+    window get exactly 0 on the GPU, every visible column a positive weight;
+    the slot query reads neither evicted tokens nor itself."""
+    S, W, r, D = 2, 8, 4, 64
+    t = 40
+    p = Pair(S, W, r, 1, D, 1, 1, "f32", 2, max_seq_len=64, tag="onehot")
+    try:
+        n = orc.slot_count(t, S, W, r)
+        eye = torch.eye(D, dtype=torch.float32)
+        kr = synth.normal((t, 1, D), "f32", "onehot", "k") * 0.2
+        vr = eye[:t, None, :].contiguous()
+        ks = synth.normal((n, 1, D), "f32", "onehot", "ks") * 0.2
+        vs = eye[t:t + n, None, :].contiguous()
+        capi.masw_mem_load(p.h, 0, 0, kr, vr, ks, vs)
+        p.ref.load(0, 0, kr.numpy(), vr.numpy(), ks.numpy(), vs.numpy())
+        q = synth.normal((1, 2, D), "f32", "onehot", "q") * 0.2
+        o, _, want, _ = p.draft(0, q=q)
+        o = to_np(o)
+        vis = set(p.ref.sim[0][0].visible_raw())
+        for i in range(1, t + 1):
+            if i in vis:
+                assert (o[0, :, i - 1] > 0).all()
+            else:
+                assert (o[0, :, i - 1] == 0).all(), f"evicted token {i} has weight {o[0, :, i - 1]}"
+        assert (o[0, :, t:t + n] > 0).all()
+        # advance to the next boundary (tau_8 = 2 + 8 + 32 = 42); new tokens carry V = 0
+        for i in range(t + 1, 43):
+            k = synth.normal((1, 1, D), "f32", "onehot", "k", i) * 0.2
+            v = torch.zeros(1, 1, D)
+            capi.masw_append_kv(p.h, 0, k.to(DEV), v.to(DEV))
+            p.ref.append(0, k.numpy(), v.numpy())
+        assert orc.is_boundary(42, S, W, r)
+        vis = set(p.ref.sim[0][0].visible_raw())
+        qg = synth.normal((1, 2, D), "f32", "onehot", "qg") * 0.2
+        kg = synth.normal((1, 1, D), "f32", "onehot", "kg") * 0.2
+        vg = torch.zeros(1, 1, D)
+        vg[0, 0, D - 1] = 1.0
+        og = torch.empty(1, 2, D, device=DEV)
+        capi.masw_materialize_slot(p.h, 0, [0], qg.to(DEV), kg.to(DEV), vg.to(DEV), og)
+        want_g, _ = p.ref.materialize_slot(0, [0], qg.numpy(), kg.numpy(), vg.numpy())
+        og = to_np(og)
+        assert_close(og, want_g, "f32", "slot one-hot")
+        assert (og[0, :, D - 1] == 0).all(), "slot query read its own K/V"
+        for i in range(1, t + 1):
+            if i not in vis:
+                assert (og[0, :, i - 1] == 0).all()
+        assert (og[0, :, t:t + n] > 0).all()
+    finally:
+        p.close()
+
+
+def test_ragged_batch_active_mask_and_edges():
+    """Three sequences at different points (empty, sink-only, past several
+    boundaries), appends with an active mask, G = 8, D = 64, S = 0 excluded."""
+    S, W, r = 3, 40, 7
+    p = Pair(S, W, r, 2, 64, 2, 3, "bf16", 16, max_seq_len=400, full_kv=True, tag="ragged")
+    try:
+        for l in range(2):
+            p.load(l, 1, 2, seed=l)        # inside the sink
+            p.load(l, 2, 150, seed=l)      # 15 slots
+        o, lse, want, want_l = p.draft(0)
+        assert np.isneginf(want_l[0]).all() and (to_np(o)[0] == 0).all() and torch.isinf(lse[0]).all()
+        for step in range(1, 30):
+            p.step = step
+            active = [1, step % 2, 1]
+            for l in range(2):
+                p.append(l, active=active)
+                p.draft(l)
+                due = [b for b in range(3) if orc.is_boundary(p.ref.t(l, b), S, W, r)
+                       and p.ref.m(l, b) == orc.slot_count(p.ref.t(l, b), S, W, r) - 1]
+                if due:
+                    p.materialize(l, due)
+            if step % 7 == 0:
+                p.draft(1, full=True)
+        for l in range(2):
+            for b in range(3):
+                p.check_state(l, b)
+    finally:
+        p.close()
+
+
+def test_no_sink_r_larger_than_w_and_scale():
+    """S = 0 (pure window plus slots), r > W, an explicit softmax scale."""
+    p = Pair(0, 16, 40, 2, 128, 1, 2, "bf16", 4, max_seq_len=600, scale=0.05, tag="nosink")
+    try:
+        p.load(0, 0, 300, seed=3)
+        p.load(0, 1, 57, seed=4)
+        for step in range(60):
+            p.step = step
+            p.append(0)
+            p.draft(0)
+            due = [b for b in range(2) if orc.is_boundary(p.ref.t(0, b), 0, 16, 40)]
+            if due:
+                p.materialize(0, due)
+        p.check_state(0, 0)
+        p.check_state(0, 1)
+    finally:
+        p.close()
+
+
+def test_slot_self_attend_option():
+    p = Pair(2, 8, 4, 2, 64, 1, 1, "f32", 4, max_seq_len=64, self_attend=True, tag="selfatt")
+    try:
+        p.load(0, 0, 21, seed=0)
+        for step in range(6):
+            p.step = step
+            p.append(0)
+            p.draft(0)
+            if orc.is_boundary(p.ref.t(0, 0), 2, 8, 4):
+                p.materialize(0, [0])
+        p.check_state(0, 0)
+    finally:
+        p.close()
+
+
+def test_rollback_restores_state_and_refuses_too_deep():
+    S, W, r, R = 4, 32, 8, 6
+    p = Pair(S, W, r, 2, 128, 2, 2, "bf16", 6, max_seq_len=512, reserve=R, full_kv=True, tag="rb")
+    try:
+        for l in range(2):
+            p.load(l, 0, 66, seed=l)
+            p.load(l, 1, 100, seed=l + 9)
+        q = p.rand((2, 6, 128), "qfixed")
+        before = [to_np(p.draft(l, q=q)[0]) for l in range(2)]
+        for step in range(1, 6):          # seq 0 crosses tau_4 = 68 at step 2
+            p.step = step
+            for l in range(2):
+                p.append(l)
+                p.draft(l)
+                due = [b for b in range(2) if orc.is_boundary(p.ref.t(l, b), S, W, r)]
+                if due:
+                    p.materialize(l, due)
+        assert p.ref.m(0, 0) == orc.slot_count(71, S, W, r)
+        capi.masw_rollback(p.h, [0, 1], [66, 100])
+        p.ref.rollback([0, 1], [66, 100])
+        for l in range(2):
+            after = to_np(p.draft(l, q=q)[0])
+            assert np.array_equal(after, before[l])
+            for b in range(2):
+                p.check_state(l, b)
+        for step in range(7):
+            p.step = 100 + step
+            for l in range(2):
+                p.append(l)
+        with pytest.raises(capi.MaswError) as ei:
+            capi.masw_rollback(p.h, [0], [66])
+        assert ei.value.code == capi.MASW_ESTATE
+    finally:
+        p.close()
+
+
+def test_state_errors():
+    p = Pair(2, 8, 4, 2, 64, 1, 1, "f32", 4, max_seq_len=18, tag="err")
+    try:
+        p.load(0, 0, 13, seed=0)          # m(13) = 0; tau_1 = 14
+        qg = torch.zeros(1, 4, 64, device=DEV)
+        kg = torch.zeros(1, 2, 64, device=DEV)
+        og = torch.empty(1, 4, 64, device=DEV)
+        with pytest.raises(capi.MaswError) as ei:
+            capi.masw_materialize_slot(p.h, 0, [0], qg, kg, kg, og)
+        assert ei.value.code == capi.MASW_ESTATE
+        with pytest.raises(capi.MaswError) as ei:
+            capi.masw_full_attn(p.h, 0, qg, og)
+        assert ei.value.code == capi.MASW_ESTATE
+        with pytest.raises(capi.MaswError) as ei:
+            capi.masw_draft_attn(p.h, 0, torch.zeros(1, 10, 64, device=DEV), torch.empty(1, 10, 64, device=DEV))
+        assert ei.value.code == capi.MASW_EINVAL
+        for step in range(5):
+            p.step = step
+            p.append(0)
+        with pytest.raises(capi.MaswError) as ei:
+            p.append(0)
+        assert ei.value.code == capi.MASW_ECAPACITY
+        with pytest.raises(capi.MaswError) as ei:
+            capi.masw_draft_attn(p.h, 1, qg, og)
+        assert ei.value.code == capi.MASW_EINVAL
+        capi.masw_sync(p.h)
+    finally:
+        p.close()
+
+
+def _verify_case(B, Lq, Hq, Hkv, Tmax, kv_len, seed, scale=0.0, qscale=1.0):
+    D = 128
+    q = synth.normal((B, Lq, Hq, D), "bf16", "verify", seed, "q", scale=qscale)
+    k = synth.normal((B, Hkv, Tmax, D), "bf16", "verify", seed, "k")
+    v = synth.normal((B, Hkv, Tmax, D), "bf16", "verify", seed, "v")
+    kl = torch.tensor(kv_len, dtype=torch.int32)
+    o = torch.empty(B, Lq, Hq, D, device=DEV)
+    lse = torch.empty(B, Lq, Hq, device=DEV)
+    capi.masw_verify_attn(q.to(DEV), k.to(DEV), v.to(DEV), kl.to(DEV), o, lse, scale=scale)
+    torch.cuda.synchronize()
+    want, want_l = orc.verify_attn(q.float().numpy(), k.float().numpy(), v.float().numpy(), kv_len, scale or None)
+    assert_close(o, want, "bf16", f"verify O {B}x{Lq}x{Hq}/{Hkv}")
+    assert_close(lse, want_l, "bf16", "verify LSE")
+
+
+@pytest.mark.parametrize("B,Lq,Hq,Hkv,Tmax,kv_len", [
+    (2, 6, 32, 8, 700, [700, 333]),       # 8B-target shape, ragged, several splits
+    (1, 5, 24, 8, 97, [64]),              # NQ = 15: padded N tile
+    (3, 1, 8, 8, 300, [1, 17, 300]),      # G = 1, Lq = 1: plain decode; a 1-key cache
+    (1, 8, 32, 8, 4096, [4000]),          # NQ = 32: the largest block
+])
+def test_verify_against_oracle(B, Lq, Hq, Hkv, Tmax, kv_len):
+    _verify_case(B, Lq, Hq, Hkv, Tmax, kv_len, seed=B * 100 + Lq)
+
+
+def test_verify_peaky_softmax_and_scale():
+    _verify_case(2, 6, 32, 8, 512, [512, 200], seed=7, qscale=4.0)
+    _verify_case(1, 6, 32, 8, 256, [250], seed=8, scale=0.2)
+
+
+@pytest.mark.slow
+def test_verify_full_size():
+    """8B-target verify at full size: B=4, Lq=6, 32q/8kv, 32768 + 6 keys."""
+    T = 32768 + 6
+    _verify_case(4, 6, 32, 8, T, [T] * 4, seed=3)
+
+
+@pytest.mark.slow
+def test_draft3b_full_size_sampled():
+    """The benchmark's launch shape: batch 8, 24q/8kv, 32K prefix (61 slots),
+    S=4, W=1024, r=512.  Two sequences of the batch carry CPU-seeded data and
+    are checked against the oracle; the rest are filled on the device.  The
+    launch grid and split count depend on batch, heads and working-set length,
+    not on the number of layers, so two layers stand for 28."""
+    S, W, r, t0 = 4, 1024, 512, 32768
+    B, L, Hkv, D, Hq = 8, 2, 8, 128, 24
+    p = Pair(S, W, r, Hkv, D, L, B, "bf16", Hq, max_seq_len=t0 + 16, full_kv=True, tag="cfg3")
+    sampled = {(0, 3), (1, 7)}
+    try:
+        g = torch.Generator(device=DEV)
+        g.manual_seed(1234)
+        n = orc.slot_count(t0, S, W, r)
+        for l in range(L):
+            for b in range(B):
+                if (l, b) in sampled:
+                    p.load(l, b, t0, seed=2)
+                else:                               # unchecked rows: device-filled
+                    kr = torch.randn(t0, Hkv, D, generator=g, device=DEV).to(torch.bfloat16)
+                    ks = torch.randn(n, Hkv, D, generator=g, device=DEV).to(torch.bfloat16)
+                    capi.masw_mem_load(p.h, l, b, kr, kr, ks, ks)
+                    del kr, ks
+        for step in range(1, 6):
+            p.step = step
+            for l in range(L):
+                k = p.rand((B, Hkv, D), "k", l)
+                v = p.rand((B, Hkv, D), "v", l)
+                capi.masw_append_kv(p.h, l, k.to(DEV), v.to(DEV))
+                q = p.rand((B, Hq, D), "q", l)
+                o = torch.empty(B, Hq, D, device=DEV)
+                lse = torch.empty(B, Hq, device=DEV)
+                capi.masw_draft_attn(p.h, l, q.to(DEV), o, lse)
+                of = torch.empty(B, Hq, D, device=DEV)
+                capi.masw_full_attn(p.h, l, q.to(DEV), of)
+                for (sl, sb) in sampled:
+                    if sl != l:
+                        continue
+                    p.ref.append(l, k.float().numpy(), v.float().numpy(),
+                                 active=[bb == sb for bb in range(B)])
+                    qb = q.float().numpy()[sb:sb + 1]
+                    Kc, Vc = p.ref._columns(l, sb)
+                    mask = orc.draft_mask(p.ref.t(l, sb), p.ref.m(l, sb), S, W)
+                    wo, wl = orc.attention(qb[0], Kc, Vc, mask, p.ref.scale)
+                    assert_close(o[sb], wo, "bf16", f"cfg3 draft l={l} b={sb} step={step}")
+                    assert_close(lse[sb], wl, "bf16", "cfg3 draft LSE")
+                    fo, _ = orc.attention(qb[0], p.ref.raw_k[l][sb], p.ref.raw_v[l][sb],
+                                          orc.full_mask(p.ref.t(l, sb)), p.ref.scale)
+                    assert_close(of[sb], fo, "bf16", f"cfg3 full l={l} b={sb}")
+                if step == 4:       # tau_62 = 4 + 1024 + 62*512 = 32772 for every sequence
+                    assert orc.is_boundary(t0 + 4, S, W, r)
+                    qg = p.rand((B, Hq, D), "qg", l)
+                    kg = p.rand((B, Hkv, D), "kg", l)
+                    vg = p.rand((B, Hkv, D), "vg", l)
+                    og = torch.empty(B, Hq, D, device=DEV)
+                    capi.masw_materialize_slot(p.h, l, list(range(B)), qg.to(DEV), kg.to(DEV), vg.to(DEV), og)
+                    for (sl, sb) in sampled:
+                        if sl != l:
+                            continue
+                        w, _ = p.ref.materialize_slot(l, [sb], qg.float().numpy()[sb:sb + 1],
+                                                      kg.float().numpy()[sb:sb + 1], vg.float().numpy()[sb:sb + 1])
+                        assert_close(og[sb:sb + 1], w, "bf16", f"cfg3 slot l={l} b={sb}")
+        capi.masw_sync(p.h)
+        for (sl, sb) in sampled:
+            p.check_state(sl, sb)
+    finally:
+        p.close()
+
+
+def test_graph_replay_matches_eager():
+    """A captured speculative iteration (appends, draft attention, a slot
+    write at the boundary, rollback) replays with the same results: the
+    counters live on the device, so the graph's net effect is identity."""
+    S, W, r, R = 4, 64, 16, 8
+    B, L, Hq, Hkv, D = 2, 2, 6, 2, 128
+    p = Pair(S, W, r, Hkv, D, L, B, "bf16", Hq, max_seq_len=1024, reserve=R, tag="graph")
+    try:
+        t0 = S + W + 5 * r - 2     # boundary after 2 appends
+        for l in range(L):
+            for b in range(B):
+                p.load(l, b, t0, seed=l * 10 + b)
+        steps = 4
+        ks = [[p.rand((B, Hkv, D), "k", s, l).to(DEV) for l in range(L)] for s in range(steps)]
+        vs = [[p.rand((B, Hkv, D), "v", s, l).to(DEV) for l in range(L)] for s in range(steps)]
+        qs = [[p.rand((B, Hq, D), "q", s, l).to(DEV) for l in range(L)] for s in range(steps)]
+        qg = p.rand((B, Hq, D), "qg").to(DEV)
+        kg = p.rand((B, Hkv, D), "kg").to(DEV)
+        outs = [[torch.empty(B, Hq, D, device=DEV) for _ in range(L)] for _ in range(steps)]
+        og = torch.empty(B, Hq, D, device=DEV)
+
+        def iteration():
+            for s in range(steps):
+                for l in range(L):
+                    capi.masw_append_kv(p.h, l, ks[s][l], vs[s][l])
+                    capi.masw_draft_attn(p.h, l, qs[s][l], outs[s][l])
+                    if s == 1:
+                        capi.masw_materialize_slot(p.h, l, list(range(B)), qg, kg, kg, og)
+            capi.masw_rollback(p.h, list(range(B)), [t0] * B)
+
+        stream = torch.cuda.Stream()
+        with torch.cuda.stream(stream):
+            iteration()
+        torch.cuda.synchronize()
+        eager = [[o.clone() for o in row] for row in outs]
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            iteration()
+        for _ in range(3):
+            for row in outs:
+                for o in row:
+                    o.zero_()
+            graph.replay()
+            torch.cuda.synchronize()
+            for s in range(steps):
+                for l in range(L):
+                    assert torch.equal(outs[s][l], eager[s][l])
+        capi.masw_sync(p.h)
+        st = capi.masw_query(p.h, 0, 0)
+        assert st["dev_t"] == st["t"] == t0 and st["dev_m"] == st["m"] == orc.slot_count(t0, S, W, r)
+    finally:
+        p.close()
