@@ -1,0 +1,455 @@
+"""Benchmark: MASW draft-attention decode steps/s and HBM GB/s vs full-KV
+attention at a 32K prefix, on the 3B-draft-shaped workload (28 layers, batch 8,
+24 query / 8 kv heads, head_dim 128, bf16, S=4 sink, W=1024 window, r=512).
+
+One bench step = one speculative draft iteration of L_draft = 5 decode steps:
+per step and layer, append the new token's K/V and run draft attention over the
+compressed memory; at the fourth step every sequence crosses the compression
+boundary tau_62 = 32772, so a slot is written per layer right after that step's
+attention; the iteration ends by rolling the 5 speculative tokens back (as
+after a fully rejected draft), so every iteration starts from the same 32K
+state.  The iteration is captured once as a CUDA graph and replayed.  `value`
+counts decode steps (5 per bench step) per second.  The full-KV contrast runs
+the same loop with full-KV decode attention over the uncompressed cache.
+
+Inputs are synthetic N(0,1) bf16 (no datasets or weights are involved); the
+per-step working set (about 1 GB of K/V) is larger than the 129 MB L2, so no
+explicit flush is needed between iterations.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+WORKLOAD = "draft3b_28l_b8"
+METRIC = "MASW draft-attn decode steps/s (28 layers x batch 8, 32K prefix)"
+UNIT = "decode steps/s"
+
+
+def _peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+# ----------------------------------------------------------------- clocks --
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples during a timed region."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines: list[str] = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self._t = threading.Thread(target=self._read, daemon=True)
+            self._t.start()
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self) -> dict:
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = float(parts[2])
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        loaded = [x for x in sm if x > 0.5 * max(sm)] or sm
+        return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ------------------------------------------------------------- GPU bench --
+
+class DraftBench:
+    def __init__(self, torch, capi, synth, prefix: int):
+        self.torch, self.capi = torch, capi
+        w = dict(synth.WORKLOADS[WORKLOAD])
+        self.w = w
+        self.L, self.B, self.Hq, self.Hkv, self.D = w["layers"], w["batch"], w["Hq"], w["Hkv"], w["D"]
+        self.S, self.W, self.r = w["S"], w["W"], w["r"]
+        self.steps = w["steps"]
+        self.R = 16                      # the pages' 16-token raw-KV rollback window
+        self.prefix = prefix
+        self.dev = torch.device("cuda", torch.cuda.current_device())
+        dt = torch.bfloat16
+        self.h = capi.masw_mem_create(self.S, self.W, self.r, self.Hkv, self.D, self.L, batch=self.B,
+                                      dtype=capi.MASW_BF16, max_seq_len=prefix + 32, full_kv=True,
+                                      rollback_reserve=self.R)
+        n = max(0, (prefix - self.S - self.W) // self.r)
+        self.n_slots0 = n
+        g = torch.Generator(device=self.dev)
+        g.manual_seed(2)
+        # four distinct seeded draws, reused across (layer, sequence) blocks
+        draws = []
+        for _ in range(4):
+            kr = torch.randn(prefix, self.Hkv, self.D, generator=g, device=self.dev).to(dt)
+            vr = torch.randn(prefix, self.Hkv, self.D, generator=g, device=self.dev).to(dt)
+            ks = torch.randn(max(n, 1), self.Hkv, self.D, generator=g, device=self.dev).to(dt)[:n]
+            vs = torch.randn(max(n, 1), self.Hkv, self.D, generator=g, device=self.dev).to(dt)[:n]
+            draws.append((kr, vr, ks.contiguous() if n else None, vs.contiguous() if n else None))
+        for l in range(self.L):
+            for b in range(self.B):
+                kr, vr, ks, vs = draws[(l * self.B + b) % 4]
+                capi.masw_mem_load(self.h, l, b, kr, vr, ks, vs)
+        del draws
+        torch.cuda.empty_cache()
+        # per (step, layer) inputs
+        self.q = [[torch.randn(self.B, self.Hq, self.D, generator=g, device=self.dev).to(dt)
+                   for _ in range(self.L)] for _ in range(self.steps)]
+        self.k = [[torch.randn(self.B, self.Hkv, self.D, generator=g, device=self.dev).to(dt)
+                   for _ in range(self.L)] for _ in range(self.steps)]
+        self.v = [[torch.randn(self.B, self.Hkv, self.D, generator=g, device=self.dev).to(dt)
+                   for _ in range(self.L)] for _ in range(self.steps)]
+        self.qg = [torch.randn(self.B, self.Hq, self.D, generator=g, device=self.dev).to(dt) for _ in range(self.L)]
+        self.kg = [torch.randn(self.B, self.Hkv, self.D, generator=g, device=self.dev).to(dt) for _ in range(self.L)]
+        self.vg = [torch.randn(self.B, self.Hkv, self.D, generator=g, device=self.dev).to(dt) for _ in range(self.L)]
+        self.o = [[torch.empty(self.B, self.Hq, self.D, device=self.dev) for _ in range(self.L)]
+                  for _ in range(self.steps)]
+        self.lse = [[torch.empty(self.B, self.Hq, device=self.dev) for _ in range(self.L)]
+                    for _ in range(self.steps)]
+        self.og = [torch.empty(self.B, self.Hq, self.D, device=self.dev) for _ in range(self.L)]
+        self.seqs = list(range(self.B))
+        # the step (0-based) at which every sequence reaches a boundary, if any
+        self.bstep = None
+        for s in range(self.steps):
+            t = prefix + s + 1
+            if t >= self.S + self.W + self.r and (t - self.S - self.W) % self.r == 0:
+                self.bstep = s
+        self.stream = torch.cuda.Stream(device=self.dev)
+
+    # one speculative iteration through the C-ABI
+    def iteration(self, full: bool = False):
+        c = self.capi
+        attn = c.masw_full_attn if full else c.masw_draft_attn
+        launches = 0
+        for s in range(self.steps):
+            for l in range(self.L):
+                c.masw_append_kv(self.h, l, self.k[s][l], self.v[s][l])
+                attn(self.h, l, self.q[s][l], self.o[s][l], self.lse[s][l])
+                launches += 2
+                if s == self.bstep and not full:
+                    c.masw_materialize_slot(self.h, l, self.seqs, self.qg[l], self.kg[l], self.vg[l], self.og[l])
+                    launches += 1
+        c.masw_rollback(self.h, self.seqs, [self.prefix] * self.B)
+        return launches + 1
+
+    def capture(self, fn):
+        torch = self.torch
+        with torch.cuda.stream(self.stream):
+            fn()                     # eager warm-up (also configures kernels)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=self.stream):
+            n = fn()
+        torch.cuda.synchronize()
+        return g, n
+
+    def time_graph(self, g, warmup: int, steps: int, barrier=None):
+        torch = self.torch
+        for _ in range(warmup):
+            g.replay()
+        torch.cuda.synchronize()
+        if barrier:
+            barrier()
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(self.stream):
+            e0.record(self.stream)
+            for _ in range(steps):
+                g.replay()
+            e1.record(self.stream)
+        torch.cuda.synchronize()
+        if barrier:
+            barrier()
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / 1e3
+
+    def algorithmic_bytes_per_draft_launch(self):
+        """K/V entries of one layer's working set at t = prefix+1 (the first
+        step's attention) x 4096 B, plus Q (bf16), O and LSE (fp32)."""
+        t = self.prefix + 1
+        nloc = max(0, min(self.W, t - self.S))
+        m = max(0, (t - self.S - self.W) // self.r)
+        E = 2 * self.Hkv * self.D * 2
+        kv = self.B * (min(self.S, t) + nloc + m) * E
+        qo = self.B * self.Hq * self.D * (2 + 4) + self.B * self.Hq * 4
+        return kv + qo, kv, qo
+
+    def time_draft_kernel(self, reps: int):
+        """Average duration of one masw_draft_attn launch, timed with CUDA
+        events on the launching stream over `reps` replays of a graph holding
+        the 28 per-layer launches of one decode step (state fixed at t=prefix+1)."""
+        torch, c = self.torch, self.capi
+        with torch.cuda.stream(self.stream):
+            for l in range(self.L):
+                c.masw_append_kv(self.h, l, self.k[0][l], self.v[0][l])
+
+        def step():
+            for l in range(self.L):
+                c.masw_draft_attn(self.h, l, self.q[0][l], self.o[0][l], self.lse[0][l])
+            return self.L
+        g, n = self.capture(step)
+        secs = self.time_graph(g, 3, reps)
+        with torch.cuda.stream(self.stream):
+            c.masw_rollback(self.h, self.seqs, [self.prefix] * self.B)
+        torch.cuda.synchronize()
+        return secs / (reps * n), n * reps
+
+    def e2e(self, iters: int):
+        """The same iteration through the public API with host buffers: every
+        step's q, k, v are copied in from pinned host memory and every O is read
+        back to pinned host memory inside the timed region; no graph."""
+        torch, c = self.torch, self.capi
+        pin = lambda t: t.to("cpu").pin_memory()
+        hq = [[pin(x) for x in row] for row in self.q]
+        hk = [[pin(x) for x in row] for row in self.k]
+        hv = [[pin(x) for x in row] for row in self.v]
+        hqg, hkg, hvg = [pin(x) for x in self.qg], [pin(x) for x in self.kg], [pin(x) for x in self.vg]
+        ho = [[torch.empty(self.B, self.Hq, self.D).pin_memory() for _ in range(self.L)] for _ in range(self.steps)]
+        hog = [torch.empty(self.B, self.Hq, self.D).pin_memory() for _ in range(self.L)]
+        dq = torch.empty_like(self.q[0][0])
+        dk = torch.empty_like(self.k[0][0])
+        dv = torch.empty_like(self.v[0][0])
+        dqg, dkg, dvg = torch.empty_like(self.qg[0]), torch.empty_like(self.kg[0]), torch.empty_like(self.vg[0])
+        do = torch.empty(self.B, self.Hq, self.D, device=self.dev)
+        h2d = d2h = 0
+
+        def run():
+            nonlocal h2d, d2h
+            h2d = d2h = 0
+            for s in range(self.steps):
+                for l in range(self.L):
+                    dq.copy_(hq[s][l], non_blocking=True)
+                    dk.copy_(hk[s][l], non_blocking=True)
+                    dv.copy_(hv[s][l], non_blocking=True)
+                    h2d += dq.numel() * 2 + dk.numel() * 2 + dv.numel() * 2
+                    c.masw_append_kv(self.h, l, dk, dv)
+                    c.masw_draft_attn(self.h, l, dq, do)
+                    ho[s][l].copy_(do, non_blocking=True)
+                    d2h += do.numel() * 4
+                    if s == self.bstep:
+                        dqg.copy_(hqg[l], non_blocking=True)
+                        dkg.copy_(hkg[l], non_blocking=True)
+                        dvg.copy_(hvg[l], non_blocking=True)
+                        h2d += (dqg.numel() + dkg.numel() + dvg.numel()) * 2
+                        c.masw_materialize_slot(self.h, l, self.seqs, dqg, dkg, dvg, do)
+                        hog[l].copy_(do, non_blocking=True)
+                        d2h += do.numel() * 4
+            c.masw_rollback(self.h, self.seqs, [self.prefix] * self.B)
+            torch.cuda.current_stream().synchronize()
+
+        with torch.cuda.stream(self.stream):
+            run()
+            torch.cuda.synchronize()
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(self.stream)
+            for _ in range(iters):
+                run()
+            e1.record(self.stream)
+            torch.cuda.synchronize()
+        secs = e0.elapsed_time(e1) / 1e3
+        return secs, h2d, d2h
+
+    def close(self):
+        self.capi.masw_mem_destroy(self.h)
+
+
+# ------------------------------------------------------------ CPU oracle --
+
+def oracle_sample(seconds_budget: float = 12.0):
+    """The CPU oracle as it stands, on a bounded sample of the workload: one
+    (layer, sequence) of the 32K state, repeatedly appending a token and running
+    one draft attention; scaled to the metric's unit (28 layers x 8 sequences
+    per decode step)."""
+    import numpy as np
+    import oracle.masw_oracle as orc
+    from compressed_draft_kv_gb300 import synth
+    w = synth.WORKLOADS[WORKLOAD]
+    S, W, r, Hkv, D, Hq, prefix = w["S"], w["W"], w["r"], w["Hkv"], w["D"], w["Hq"], w["prefix"]
+    n = orc.slot_count(prefix, S, W, r)
+    kr = synth.normal((prefix, Hkv, D), "bf16", "cpu-sample", "k").float().numpy()
+    vr = synth.normal((prefix, Hkv, D), "bf16", "cpu-sample", "v").float().numpy()
+    ks = synth.normal((n, Hkv, D), "bf16", "cpu-sample", "ks").float().numpy()
+    vs = synth.normal((n, Hkv, D), "bf16", "cpu-sample", "vs").float().numpy()
+    mem = orc.MaswOracle(S, W, r, Hkv, D, 1, 1)
+    mem.load(0, 0, kr, vr, ks, vs)
+    done = 0
+    t0 = time.perf_counter()
+    while True:
+        k = synth.normal((1, Hkv, D), "bf16", "cpu-sample", "k1", done).float().numpy()
+        q = synth.normal((1, Hq, D), "bf16", "cpu-sample", "q1", done).float().numpy()
+        mem.append(0, k, k)
+        mem.draft_attn(0, q)
+        done += 1
+        el = time.perf_counter() - t0
+        if el > seconds_budget or done >= 200:
+            break
+    per_unit = el / done                              # one (layer, seq) draft step
+    steps_per_s = 1.0 / (per_unit * w["layers"] * w["batch"])
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    return {"value": steps_per_s, "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": f"{done} x (append + draft attention) of one (layer, sequence) at a {prefix}-token "
+                      f"prefix in {el:.1f} s, scaled x{w['layers'] * w['batch']} to one decode step; "
+                      f"numpy fp64, default BLAS threading"}
+
+
+# ------------------------------------------------------------------ main --
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="masw", choices=["masw", "reference"])
+    ap.add_argument("--prefix", type=int, default=None)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--e2e-iters", type=int, default=5)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+
+    from compressed_draft_kv_gb300 import synth
+    prefix = args.prefix or synth.WORKLOADS[WORKLOAD]["prefix"]
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        cb = oracle_sample(seconds_budget=max(5.0, min(60.0, 2.0 * args.steps)))
+        ms = 1e3 / cb["value"] * synth.WORKLOADS[WORKLOAD]["steps"]
+        print(json.dumps({
+            "impl": "reference", "metric": METRIC, "value": cb["value"], "unit": UNIT, "n_gpus": 0,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": f"{WORKLOAD} (CPU oracle sample)", "prefix": prefix},
+            "cpu_baseline": cb,
+            "e2e": {"value": cb["value"], "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        }))
+        return
+
+    import torch
+    from compressed_draft_kv_gb300 import capi
+    capi.load()
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA device")
+    torch.cuda.set_device(local)
+    barrier = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+        barrier = dist.barrier
+
+    wl = synth.WORKLOADS[WORKLOAD]
+    bench = DraftBench(torch, capi, synth, prefix)
+    try:
+        g_draft, launches = bench.capture(bench.iteration)
+        g_full, launches_full = bench.capture(lambda: bench.iteration(full=True))
+        with ClockSampler(local) as clk:
+            secs = bench.time_graph(g_draft, args.warmup, args.steps, barrier)
+        secs_full = bench.time_graph(g_full, args.warmup, max(3, args.steps // 4), barrier)
+        full_iters = max(3, args.steps // 4)
+        kern_s, _ = bench.time_draft_kernel(reps=50)
+        e2e_s, h2d, d2h = bench.e2e(args.e2e_iters)
+        capi.masw_sync(bench.h)
+    finally:
+        pass
+
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([secs, secs_full, e2e_s / args.e2e_iters], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        secs, secs_full, e2e_per = t.tolist()
+    else:
+        e2e_per = e2e_s / args.e2e_iters
+    dsteps = wl["steps"]
+    value = world * args.steps * dsteps / secs
+    full_value = world * full_iters * dsteps / secs_full
+    peak, peak_kind = _peaks()
+    total_b, kv_b, qo_b = bench.algorithmic_bytes_per_draft_launch()
+    achieved = total_b / kern_s / 1e9
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": secs / args.steps * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "layers": wl["layers"], "batch": wl["batch"], "q_heads": wl["Hq"],
+                   "kv_heads": wl["Hkv"], "head_dim": wl["D"], "prefix": prefix, "S": wl["S"], "W": wl["W"],
+                   "r": wl["r"], "rollback_reserve": bench.R, "decode_steps_per_bench_step": dsteps,
+                   "boundary_step": (bench.bstep + 1) if bench.bstep is not None else None,
+                   "l2": "working set per decode step ~1 GB > 129 MB L2; no flush",
+                   "launch": "CUDA graph of one speculative iteration", "parallelism": f"replicas x{world}"},
+        "full_kv": {"value": full_value, "unit": UNIT, "ms_per_step": secs_full / full_iters * 1e3},
+        "speedup_vs_full_kv": value / full_value,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": None, "peak_kind": peak_kind,
+                     "kernel": "decode_kernel<bf16,128,3> (masw_draft_attn)",
+                     "bytes_per_launch": total_b, "kv_bytes_per_launch": kv_b,
+                     "us_per_launch": kern_s * 1e6},
+        "gpu_launches": launches * args.steps,
+        "clocks": clk.summary(),
+        "e2e": {"value": world * dsteps / e2e_per, "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h,
+                "how": "eager C-ABI calls, q/k/v copied from pinned host and O read back every step"},
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = oracle_sample()
+    bench.close()
+    if rank == 0:
+        print(json.dumps(line))
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()
