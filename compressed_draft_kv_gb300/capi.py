@@ -21,7 +21,7 @@ MASW_MAX_BATCH, MASW_MAX_GROUP = 512, 8
 EXPORTS = [
     "masw_mem_create", "masw_mem_destroy", "masw_last_error", "masw_append_kv",
     "masw_materialize_slot", "masw_rollback", "masw_draft_attn", "masw_full_attn",
-    "masw_verify_attn", "masw_verify_workspace_bytes", "masw_mem_load", "masw_mem_export",
+    "masw_verify_attn", "masw_verify_workspace_bytes", "masw_verify_attn_noalloc", "masw_mem_load", "masw_mem_export",
     "masw_query", "masw_sync", "masw_index", "masw_version",
 ]
 
@@ -66,6 +66,7 @@ def load() -> ctypes.CDLL:
         "masw_full_attn": [P, I, P, I, P, P, P],
         "masw_verify_attn": [P, P, P, P, I, I, I, I, I, I, I, F, P, P, P, Z, P],
         "masw_verify_workspace_bytes": [I, I, I, I, I, I, ctypes.POINTER(Z)],
+        "masw_verify_attn_noalloc": [P, P, P, P, I, I, I, I, I, I, I, F, P, P, P],
         "masw_mem_load": [P, I, I, I, P, P, P, P, I],
         "masw_mem_export": [P, I, I, P, P, IP],
         "masw_query": [P, I, I, ctypes.POINTER(masw_state_t)],
@@ -182,6 +183,15 @@ def masw_verify_attn(q, k_cache, v_cache, kv_len, o, lse=None, workspace=None, s
     _check(load().masw_verify_attn(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(kv_len), B, Lq, Hq, Hkv, D, Tmax,
                                    MASW_BF16, scale, _ptr(o), _ptr(lse), _ptr(workspace), workspace.numel(),
                                    _stream(stream)))
+
+
+def masw_verify_attn_noalloc(q, k_cache, v_cache, kv_len, o, lse=None, scale=0.0, stream=None):
+    """masw_verify_attn for callers that cannot allocate: no workspace, the
+    library's own fixed device array holds the split partials."""
+    B, Lq, Hq, D = q.shape
+    Hkv, Tmax = k_cache.shape[1], k_cache.shape[2]
+    _check(load().masw_verify_attn_noalloc(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(kv_len), B, Lq, Hq, Hkv, D,
+                                           Tmax, MASW_BF16, scale, _ptr(o), _ptr(lse), _stream(stream)))
 
 
 # ---------------------------------------------------------------- plumbing --

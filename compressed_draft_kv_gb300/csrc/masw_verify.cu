@@ -396,3 +396,115 @@ extern "C" int masw_verify_attn(const void* q, const void* k_cache, const void* 
     if (e != cudaSuccess) return masw_set_error(nullptr, MASW_ECUDA, std::string("verify: ") + cudaGetErrorString(e));
     return MASW_OK;
 }
+
+// ---------------------------------------------------------------------------
+// Verify attention that allocates nothing.
+//
+// masw_verify_attn needs a workspace from its caller.  Some callers cannot
+// provide one: code that only ever receives input and output pointers (a
+// plugin slot in another engine, say), code whose device memory is all owned
+// by a framework's own allocator, or a latency-critical loop where a
+// cudaMalloc -- which can synchronise the whole device -- is not acceptable.
+// For them the split partials and tickets live in the array below, which is
+// part of the library image: every GPU that loads the library holds these
+// 4 MiB + 16 KiB until the process exits.
+//
+// Limits: B * Hkv <= kNoAllocMaxPairs; when the partials of the usual split
+// count would not fit in kNoAllocPartBytes the call uses fewer splits (one
+// split needs no partials at all), so it is never refused for length alone.
+// All calls share the array and each leaves its partials in it; the tickets
+// are cleared on the stream at the start of every call.  Two calls that
+// overlap on the GPU (different streams, or different host threads) race on
+// the array and give wrong results: serialise them.
+// ---------------------------------------------------------------------------
+#include <mutex>
+
+namespace masw {
+constexpr size_t kNoAllocPartBytes = (size_t)4 << 20;
+constexpr int kNoAllocMaxPairs = 4096;
+constexpr size_t kNoAllocBytes = kNoAllocPartBytes + (size_t)kNoAllocMaxPairs * sizeof(unsigned);
+}  // namespace masw
+
+static __device__ __align__(256) uint8_t g_noalloc_scratch[masw::kNoAllocBytes];
+
+// Device address of g_noalloc_scratch per device.  In host code the array's
+// name is only a host-side stand-in; the kernel must be given this address.
+static void* g_noalloc_ptr[64];
+static std::mutex g_noalloc_mu;
+
+static int noalloc_scratch(int dev, void** out) {
+    std::lock_guard<std::mutex> lock(g_noalloc_mu);
+    if (!g_noalloc_ptr[dev]) {
+        void* p = nullptr;
+        cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+        if (e != cudaSuccess || !p) {
+            cudaGetLastError();
+            return masw_set_error(nullptr, MASW_ECUDA, std::string("verify_noalloc: cudaGetSymbolAddress: ") +
+                                                           cudaGetErrorString(e));
+        }
+        g_noalloc_ptr[dev] = p;
+    }
+    *out = g_noalloc_ptr[dev];
+    return MASW_OK;
+}
+
+extern "C" int masw_verify_attn_noalloc(const void* q, const void* k_cache, const void* v_cache, const int* kv_len,
+                                        int B, int Lq, int Hq, int Hkv, int D, int Tmax, int dtype, float scale,
+                                        float* o, float* lse, masw_stream_t stream) {
+    if (!q || !k_cache || !v_cache || !kv_len || !o)
+        return masw_set_error(nullptr, MASW_EINVAL, "verify_noalloc: NULL pointer");
+    if (dtype != MASW_BF16) return masw_set_error(nullptr, MASW_EINVAL, "verify_noalloc: only MASW_BF16 is supported");
+    int rc = verify_check(B, Lq, Hq, Hkv, D, Tmax);
+    if (rc) return masw_set_error(nullptr, rc, "verify_noalloc: unsupported sizes (D must be 128, Lq*Hq/Hkv <= 32)");
+    if ((size_t)B * Hkv > (size_t)kNoAllocMaxPairs)
+        return masw_set_error(nullptr, MASW_EINVAL,
+                              "verify_noalloc: B * Hkv = " + std::to_string((size_t)B * Hkv) +
+                                  " exceeds the static scratch limit of " + std::to_string(kNoAllocMaxPairs) +
+                                  "; use masw_verify_attn with a workspace");
+    if (((uintptr_t)q | (uintptr_t)k_cache | (uintptr_t)v_cache) & 15)
+        return masw_set_error(nullptr, MASW_EINVAL, "verify_noalloc: q and caches must be 16-byte aligned");
+    if (((uintptr_t)o | (uintptr_t)lse | (uintptr_t)kv_len) & 3)
+        return masw_set_error(nullptr, MASW_EINVAL, "verify_noalloc: o, lse and kv_len must be 4-byte aligned");
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64 || num_sms_current(&sms)) {
+        cudaGetLastError();
+        return masw_set_error(nullptr, MASW_ECUDA, "verify_noalloc: cannot query the current device");
+    }
+    void* scratch = nullptr;
+    if ((rc = noalloc_scratch(dev, &scratch))) return rc;
+    const int G = Hq / Hkv, NQ = G * Lq;
+    int n_split = verify_splits(B, Hkv, Tmax, sms);
+    while (n_split > 1 && verify_part_bytes(B, Hkv, NQ, n_split) > kNoAllocPartBytes) --n_split;
+    VerifyParams prm;
+    std::memset(&prm, 0, sizeof(prm));
+    prm.q = (const __nv_bfloat16*)q;
+    prm.k = (const __nv_bfloat16*)k_cache;
+    prm.v = (const __nv_bfloat16*)v_cache;
+    prm.kv_len = kv_len;
+    prm.o = o;
+    prm.lse = lse;
+    prm.part = (float*)scratch;
+    prm.tickets = (unsigned*)((uint8_t*)scratch + kNoAllocPartBytes);
+    prm.B = B;
+    prm.Lq = Lq;
+    prm.Hq = Hq;
+    prm.Hkv = Hkv;
+    prm.G = G;
+    prm.NQ = NQ;
+    prm.Tmax = Tmax;
+    prm.n_split = n_split;
+    prm.scale_log2 = (scale > 0.f ? scale : 1.0f / sqrtf((float)D)) * 1.4426950408889634f;
+    cudaStream_t st = (cudaStream_t)stream;
+    cudaError_t e = cudaMemsetAsync(prm.tickets, 0, (size_t)B * Hkv * sizeof(unsigned), st);
+    if (e != cudaSuccess)
+        return masw_set_error(nullptr, MASW_ECUDA, std::string("verify_noalloc: ") + cudaGetErrorString(e));
+    switch ((NQ + 7) / 8) {
+        case 1: e = launch_verify<1>(prm, st); break;
+        case 2: e = launch_verify<2>(prm, st); break;
+        case 3: e = launch_verify<3>(prm, st); break;
+        default: e = launch_verify<4>(prm, st); break;
+    }
+    if (e != cudaSuccess)
+        return masw_set_error(nullptr, MASW_ECUDA, std::string("verify_noalloc: ") + cudaGetErrorString(e));
+    return MASW_OK;
+}

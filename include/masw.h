@@ -193,6 +193,27 @@ int masw_verify_attn(const void* q, const void* k_cache, const void* v_cache,
 int masw_verify_workspace_bytes(int B, int Lq, int Hq, int Hkv, int D, int Tmax,
                                 size_t* bytes);
 
+/* masw_verify_attn without a workspace argument and without allocating
+ * anything.  The pages have no counterpart: this is a library convenience.
+ * It is for callers that cannot hand over scratch memory or call cudaMalloc:
+ * code that only receives input and output pointers (for example a plugin
+ * slot in another inference engine), code whose device memory is owned by a
+ * framework's own allocator, or a loop that cannot afford the device-wide
+ * synchronisation a cudaMalloc may cause.  Arguments and results are those of
+ * masw_verify_attn.  The split partials live in a fixed array inside the
+ * library image (4 MiB + 16 KiB, held by every GPU that loads the library
+ * until the process exits); larger problems run with fewer key splits.
+ * Limit: B * Hkv <= 4096 (EINVAL beyond, with a message).  The first call on a
+ * device looks up the array's device address (cudaGetSymbolAddress); make that
+ * first call before any stream capture on that device.  Every call reuses the
+ * same array (tickets are cleared on the stream at the start of each call), so
+ * calls that overlap on the GPU -- other streams, other host threads -- race
+ * and must be serialised by the caller. */
+int masw_verify_attn_noalloc(const void* q, const void* k_cache, const void* v_cache,
+                             const int* kv_len, int B, int Lq, int Hq, int Hkv, int D,
+                             int Tmax, int dtype, float scale, float* o, float* lse,
+                             masw_stream_t stream);
+
 /* ---- plumbing for set-up, tests and benchmarks --------------------------------- */
 
 /* Set (layer, seq) to the state after t raw tokens whose K/V are k_raw, v_raw

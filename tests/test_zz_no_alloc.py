@@ -1,0 +1,64 @@
+"""The allocation-free verify entry point (masw_verify_attn_noalloc).
+
+It exists for callers that cannot give the library scratch memory or call
+cudaMalloc -- code that only receives input and output pointers, code whose
+device memory belongs to another allocator, or a loop that cannot afford the
+device-wide synchronisation an allocation may cause.  This test calls it through
+the C ABI twice in a row, with different shapes, and checks each result against
+masw_verify_attn (which takes a caller workspace) within the tolerance the other
+bf16 tests use.  The second shape is large enough that the fixed scratch holds
+fewer key splits than the workspace version uses.
+
+The file name makes pytest collect it last, so a run that stops at the first
+failure has run every other test before this one.
+"""
+import pytest
+import torch
+
+from compressed_draft_kv_gb300 import capi, synth
+from gpu_helpers import DEV, assert_close
+from libmasw_fixture import ensure_built
+
+pytestmark = pytest.mark.gpu
+
+
+def _inputs(B, Lq, Hq, Hkv, Tmax, kv_len, seed):
+    D = 128
+    q = synth.normal((B, Lq, Hq, D), "bf16", "noalloc", seed, "q").to(DEV)
+    k = synth.normal((B, Hkv, Tmax, D), "bf16", "noalloc", seed, "k").to(DEV)
+    v = synth.normal((B, Hkv, Tmax, D), "bf16", "noalloc", seed, "v").to(DEV)
+    kl = torch.tensor(kv_len, dtype=torch.int32, device=DEV)
+    return q, k, v, kl
+
+
+def test_noalloc_verify_matches_workspace_verify_twice():
+    ensure_built()
+    torch.cuda.set_device(DEV)
+    cases = [
+        (2, 6, 32, 8, 700, [700, 333], 1),
+        (4, 6, 32, 8, 8192, [8192, 5000, 7001, 64], 2),
+    ]
+    for B, Lq, Hq, Hkv, Tmax, kv_len, seed in cases:
+        q, k, v, kl = _inputs(B, Lq, Hq, Hkv, Tmax, kv_len, seed)
+        o_ref = torch.empty(B, Lq, Hq, 128, device=DEV)
+        l_ref = torch.empty(B, Lq, Hq, device=DEV)
+        capi.masw_verify_attn(q, k, v, kl, o_ref, l_ref)
+        o = torch.full((B, Lq, Hq, 128), float("nan"), device=DEV)
+        lse = torch.full((B, Lq, Hq), float("nan"), device=DEV)
+        capi.masw_verify_attn_noalloc(q, k, v, kl, o, lse)
+        torch.cuda.synchronize()
+        assert_close(o, o_ref.double().cpu().numpy(), "bf16", f"noalloc O B={B} T={Tmax}")
+        assert_close(lse, l_ref.double().cpu().numpy(), "bf16", f"noalloc LSE B={B} T={Tmax}")
+
+
+def test_noalloc_rejects_sizes_beyond_its_limit():
+    ensure_built()
+    torch.cuda.set_device(DEV)
+    q = torch.zeros(1, 1, 4097, 128, dtype=torch.bfloat16, device=DEV)
+    k = torch.zeros(1, 4097, 1, 128, dtype=torch.bfloat16, device=DEV)
+    kl = torch.ones(1, dtype=torch.int32, device=DEV)
+    o = torch.empty(1, 1, 4097, 128, device=DEV)
+    with pytest.raises(capi.MaswError) as ei:
+        capi.masw_verify_attn_noalloc(q, k, k, kl, o)
+    assert ei.value.code == capi.MASW_EINVAL
+    assert "static scratch limit" in str(ei.value)
