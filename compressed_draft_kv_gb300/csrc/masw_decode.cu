@@ -1,4 +1,5 @@
-// Split-KV decode attention over segmented K/V: the MASW draft working memory
+// Split-KV decode attention on CUDA cores, used for fp32 pools (bf16 pools
+// use the tensor-core kernel of masw_decode_mma.cu): the MASW draft working memory
 // (sink block, ring-indexed local window, slot chain), the slot-write query
 // under the structured mask, and the full-KV contrast cache.
 //
@@ -20,34 +21,6 @@
 #include <cstring>
 
 namespace masw {
-
-struct DecodeParams {
-    const void* q;        // [rows][Hq][D]
-    float* o;             // [rows][Hq][D]
-    float* lse;           // [rows][Hq] or null
-    const void* pool_k;   // [L][B][Hkv][C][D]
-    const void* pool_v;
-    const void* full_k;   // [L][B][Hkv][Tmax][D]
-    const void* full_v;
-    const void* k_g;      // slot mode: [rows][Hkv][D]
-    const void* v_g;
-    const int* d_t;
-    int* d_m;
-    int* d_pos;
-    int* d_err;
-    float* part;
-    unsigned* tickets;
-    unsigned* seq_tickets;
-    float scale_log2;     // softmax scale * log2(e)
-    int mode, layer, B, Hkv, Hq, S, W, Wc, C, Tmax, M_max, n_split, self_attend;
-    short seq_ids[MASW_MAX_BATCH];
-};
-
-struct Seg {
-    const uint8_t* k;
-    const uint8_t* v;
-    int len;
-};
 
 template <typename T, int D>
 struct DecodeCfg {
@@ -131,30 +104,7 @@ decode_kernel(const __grid_constant__ DecodeParams p) {
         const int t = p.d_t[lb];
         const int mcnt = p.d_m[lb];
         s_m_before = mcnt;
-        int n = 0;
-        if (p.mode == kModeFull) {
-            const size_t base = ((size_t)lb * p.Hkv + h) * (size_t)p.Tmax * ROWB;
-            if (t > 0) segs[n++] = Seg{(const uint8_t*)p.full_k + base, (const uint8_t*)p.full_v + base, t};
-        } else {
-            const size_t base = ((size_t)lb * p.Hkv + h) * (size_t)p.C * ROWB;
-            const uint8_t* kb = (const uint8_t*)p.pool_k + base;
-            const uint8_t* vb = (const uint8_t*)p.pool_v + base;
-            const int ns = imin(p.S, t);
-            if (ns > 0) segs[n++] = Seg{kb, vb, ns};
-            const int nl = n_local(t, p.S, p.W);
-            if (nl > 0) {
-                const int start = ring_row(window_lo(t, p.S, p.W), p.S, p.Wc);
-                const int first = imin(nl, p.Wc - start);
-                segs[n++] = Seg{kb + (size_t)(p.S + start) * ROWB, vb + (size_t)(p.S + start) * ROWB, first};
-                if (nl > first) segs[n++] = Seg{kb + (size_t)p.S * ROWB, vb + (size_t)p.S * ROWB, nl - first};
-            }
-            if (mcnt > 0)
-                segs[n++] = Seg{kb + (size_t)(p.S + p.Wc) * ROWB, vb + (size_t)(p.S + p.Wc) * ROWB, mcnt};
-            if (p.mode == kModeSlot && p.self_attend) {
-                const size_t off = ((size_t)z * p.Hkv + h) * ROWB;
-                segs[n++] = Seg{(const uint8_t*)p.k_g + off, (const uint8_t*)p.v_g + off, 1};
-            }
-        }
+        const int n = build_segments<ROWB>(p, lb, h, z, t, mcnt, segs);
         s_nseg = n;
         for (int s = 0; s < NST; ++s) mbar_init(&bars[s], 1);
         fence_mbar_init();
@@ -349,33 +299,7 @@ decode_kernel(const __grid_constant__ DecodeParams p) {
     const bool final_cta = split_epilogue<D>(G, cm, cl, co, out, part, p.tickets + z * p.Hkv + h, split,
                                              p.n_split, scratch);
 
-    if (p.mode == kModeSlot && final_cta) {
-        // the last (row, head) pair of this row to finish appends g_m's K/V to the
-        // chain: every CTA of the row has read the slot count by then
-        __shared__ unsigned s_last_head;
-        __threadfence();
-        __syncthreads();
-        if (tid == 0) s_last_head = atomicAdd(p.seq_tickets + z, 1u) == (unsigned)(p.Hkv - 1);
-        __syncthreads();
-        if (s_last_head) {
-            const int mb = s_m_before;
-            constexpr int VPR = ROWB / 16;
-            for (int i = tid; i < p.Hkv * VPR; i += blockDim.x) {
-                const int hh = i / VPR, cc = i % VPR;
-                const size_t dst = (((size_t)lb * p.Hkv + hh) * p.C + (size_t)(p.S + p.Wc + mb)) * ROWB + cc * 16;
-                const size_t src = ((size_t)z * p.Hkv + hh) * ROWB + cc * 16;
-                *reinterpret_cast<uint4*>((uint8_t*)p.pool_k + dst) =
-                    *reinterpret_cast<const uint4*>((const uint8_t*)p.k_g + src);
-                *reinterpret_cast<uint4*>((uint8_t*)p.pool_v + dst) =
-                    *reinterpret_cast<const uint4*>((const uint8_t*)p.v_g + src);
-            }
-            if (tid == 0) {
-                p.d_pos[(size_t)lb * p.M_max + mb] = p.d_t[lb];   // 0-based id of the raw token after g_m
-                p.d_m[lb] = mb + 1;
-                p.seq_tickets[z] = 0u;
-            }
-        }
-    }
+    if (p.mode == kModeSlot && final_cta) slot_append_tail<ROWB>(p, lb, z, s_m_before);
 }
 
 // ---------------------------------------------------------------------------
@@ -478,10 +402,7 @@ int masw_launch_decode(masw_mem_t* mem, int mode, int layer, const void* q, int 
     while (n_split > 1 && masw_decode_part_floats(n_rows, mem->Hkv, G, mem->D, n_split) > mem->part_floats)
         --n_split;
     prm.n_split = n_split;
-    if (mem->dtype == MASW_BF16) {
-        if (mem->D == 128) return launch_g<__nv_bfloat16, 128>(mem, prm, G, n_rows, stream);
-        return launch_g<__nv_bfloat16, 64>(mem, prm, G, n_rows, stream);
-    }
+    if (mem->dtype == MASW_BF16) return masw_launch_decode_mma(mem, prm, G, n_rows, kmax, stream);
     if (mem->D == 128) return launch_g<float, 128>(mem, prm, G, n_rows, stream);
     return launch_g<float, 64>(mem, prm, G, n_rows, stream);
 }

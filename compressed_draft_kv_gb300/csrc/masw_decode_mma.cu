@@ -1,0 +1,288 @@
+// Tensor-core split-KV decode attention for bf16 pools: draft attention over
+// the MASW working memory ([EN] §3.1 Eq. 4 with Eq. 2 of §2.3), the slot-write
+// query under the structured mask ([EN] §3.2 Algorithm 1 step 2), and full-KV
+// decode over the contrast cache.
+//
+// With grouped-query attention the G = Hq/Hkv query heads of a kv head read
+// the same K/V rows, so each 16-key tile is a small dense contraction
+// [16 keys x D] x [D x G].  It runs on mma.sync m16n8k16 (bf16 in, fp32
+// accumulate) with KEYS as the M dimension and the G <= 8 query heads as the N
+// tile: S^T = K Q^T from ldmatrix fragments, online softmax per query column in
+// the log2 domain, P^T moved from the accumulator layout into a B operand with
+// movmatrix, and O^T += V^T P^T with ldmatrix.trans fragments of the same V
+// stage.  About 150 warp instructions per 16 keys, against ~700 for the same
+// work on CUDA cores with shuffle reductions, so the kernel keeps up with HBM
+// at few warps per SM.
+//
+// Grid (n_split, Hkv, rows), 128 threads, one wave: n_split fills the resident
+// CTA slots of the GPU.  K/V rows of the CTA's share of the logical key list
+// are copied with 16-byte cp.async into XOR-swizzled shared-memory stages
+// (NST in flight); rows come from up to five contiguous segments (sink, the
+// window in one or two runs, the slot chain, a self-attended slot) and are
+// never gathered in HBM.  Split partials are merged by split_epilogue.
+#include "masw_internal.cuh"
+
+#include <cstring>
+
+namespace masw {
+
+template <int D>
+struct MmaCfg {
+    static constexpr int KPS = 64;               // keys per stage (16 per warp)
+    static constexpr int NST = 2;                // stages in flight
+    static constexpr int CH = D / 8;             // 16-byte chunks per row
+    static constexpr int ROWB = D * 2;           // bytes per bf16 row
+    static constexpr int STAGE = 2 * KPS * ROWB; // K then V
+    static constexpr int SMEM = NST * STAGE;
+    static constexpr int KS = D / 16;            // k-steps of Q.K, m-tiles of P.V
+    static_assert((2 * 4 * 8 + 4 * 8 * D + 2 * 8 + 8 * D + epilogue_scratch_floats(8, kMaxSplit)) * 4 <= SMEM,
+                  "merge does not fit in the stage buffers");
+};
+
+template <int ROWB>
+__device__ __forceinline__ uint32_t swz_off(int row, int ch) {
+    return (uint32_t)(row * ROWB + ((ch ^ (row & 7)) << 4));
+}
+
+template <int D>
+__global__ void __launch_bounds__(128) decode_mma_kernel(const __grid_constant__ DecodeParams p) {
+    using C = MmaCfg<D>;
+    constexpr int KPS = C::KPS, NST = C::NST, CH = C::CH, ROWB = C::ROWB, KS = C::KS;
+    extern __shared__ __align__(128) uint8_t smem[];
+    __shared__ Seg segs[5];
+    __shared__ int s_start[6];
+    __shared__ int s_nseg, s_m_before;
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int split = blockIdx.x, h = blockIdx.y, z = blockIdx.z;
+    const int b = (p.mode == kDevModeSlot) ? (int)p.seq_ids[z] : z;
+    const int lb = p.layer * p.B + b;
+    const int G = p.Hq / p.Hkv;
+
+    if (tid == 0) {
+        const int t = p.d_t[lb];
+        const int mcnt = p.d_m[lb];
+        s_m_before = mcnt;
+        const int n = build_segments<ROWB>(p, lb, h, z, t, mcnt, segs);
+        int acc = 0;
+        for (int s = 0; s < n; ++s) {
+            s_start[s] = acc;
+            acc += segs[s].len;
+        }
+        s_start[n] = acc;
+        s_nseg = n;
+    }
+    __syncthreads();
+    const int nseg = s_nseg;
+    const int total = s_start[nseg];
+    const int chunk = (((total + p.n_split - 1) / p.n_split) + 15) & ~15;
+    const int r0 = imin(total, split * chunk);
+    const int r1 = imin(total, r0 + chunk);
+    const int nstage = (r1 - r0 + KPS - 1) / KPS;
+    const uint32_t sbase = smem_u32(smem);
+
+    // stage c <- logical rows [r0 + c*KPS, +KPS); rows past r1 are zero-filled
+    auto load_stage = [&](int c) {
+        const uint32_t sk = sbase + (uint32_t)(c % NST) * C::STAGE;
+        const uint32_t sv = sk + KPS * ROWB;
+        const int key0 = r0 + c * KPS;
+#pragma unroll
+        for (int i = 0; i < (KPS * CH) / 128; ++i) {
+            const int idx = tid + i * 128;
+            const int row = idx / CH, ch = idx % CH;
+            const int j = key0 + row;
+            const uint8_t* ks = segs[0].k;
+            const uint8_t* vs = segs[0].v;
+            int bytes = 0;
+            if (j < r1) {
+                int s = 0;
+                while (s + 1 < nseg && j >= s_start[s + 1]) ++s;
+                const size_t off = (size_t)(j - s_start[s]) * ROWB + ch * 16;
+                ks = segs[s].k + off;
+                vs = segs[s].v + off;
+                bytes = 16;
+            }
+            cp_async16(sk + swz_off<ROWB>(row, ch), ks, bytes);
+            cp_async16(sv + swz_off<ROWB>(row, ch), vs, bytes);
+        }
+    };
+#pragma unroll
+    for (int c = 0; c < NST - 1; ++c) {
+        if (c < nstage) load_stage(c);
+        cp_async_commit();
+    }
+
+    // Q^T as B fragments: column n = query head h*G + n of row z (zero when n >= G)
+    uint32_t qb[KS][2];
+    {
+        const int n = lane >> 2;
+        const bool real = n < G;
+        const __nv_bfloat16* qrow = (const __nv_bfloat16*)p.q + ((size_t)z * p.Hq + (size_t)h * G + (real ? n : 0)) * D;
+#pragma unroll
+        for (int ks = 0; ks < KS; ++ks) {
+            const int d = ks * 16 + (lane & 3) * 2;
+            qb[ks][0] = real ? *reinterpret_cast<const uint32_t*>(qrow + d) : 0u;
+            qb[ks][1] = real ? *reinterpret_cast<const uint32_t*>(qrow + d + 8) : 0u;
+        }
+    }
+    const float sl2 = p.scale_log2;
+    float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f};
+    float acc[KS][4];
+#pragma unroll
+    for (int mt = 0; mt < KS; ++mt) acc[mt][0] = acc[mt][1] = acc[mt][2] = acc[mt][3] = 0.f;
+
+    for (int c = 0; c < nstage; ++c) {
+        cp_async_wait<NST - 2>();
+        __syncthreads();
+        {
+            const int cn = c + NST - 1;   // refill the stage consumed in the previous iteration
+            if (cn < nstage) load_stage(cn);
+            cp_async_commit();
+        }
+        const uint32_t sk = sbase + (uint32_t)(c % NST) * C::STAGE;
+        const uint32_t sv = sk + KPS * ROWB;
+        const int kw = warp * 16;
+        const int key_tile = r0 + c * KPS + kw;
+        if (key_tile < r1) {
+            float s[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int ks = 0; ks < KS; ++ks) {
+                uint32_t a0, a1, a2, a3;
+                ldsm_x4(sk + swz_off<ROWB>(kw + (lane & 7) + ((lane >> 3) & 1) * 8, ks * 2 + (lane >> 4)), a0, a1,
+                        a2, a3);
+                mma16816(s, a0, a1, a2, a3, qb[ks][0], qb[ks][1]);
+            }
+            const int key_a = key_tile + (lane >> 2), key_b = key_a + 8;
+            float x[4];
+            x[0] = key_a < r1 ? s[0] * sl2 : -INFINITY;
+            x[1] = key_a < r1 ? s[1] * sl2 : -INFINITY;
+            x[2] = key_b < r1 ? s[2] * sl2 : -INFINITY;
+            x[3] = key_b < r1 ? s[3] * sl2 : -INFINITY;
+            float pr[4];
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                float mx = fmaxf(x[e], x[e + 2]);
+                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+                const float m_new = fmaxf(m_run[e], mx);   // finite: key_tile < r1
+                const float alpha = exp2f(m_run[e] - m_new);
+                pr[e] = exp2f(x[e] - m_new);
+                pr[e + 2] = exp2f(x[e + 2] - m_new);
+                l_run[e] = l_run[e] * alpha + pr[e] + pr[e + 2];
+                m_run[e] = m_new;
+#pragma unroll
+                for (int mt = 0; mt < KS; ++mt) {
+                    acc[mt][e] *= alpha;
+                    acc[mt][e + 2] *= alpha;
+                }
+            }
+            const uint32_t pb0 = movmatrix_t(pack_bf16(pr[0], pr[1]));
+            const uint32_t pb1 = movmatrix_t(pack_bf16(pr[2], pr[3]));
+#pragma unroll
+            for (int mt = 0; mt < KS; ++mt) {
+                uint32_t a0, a1, a2, a3;
+                ldsm_x4_t(sv + swz_off<ROWB>(kw + (lane & 7) + (lane >> 4) * 8, mt * 2 + ((lane >> 3) & 1)), a0, a1,
+                          a2, a3);
+                mma16816(acc[mt], a0, a1, a2, a3, pb0, pb1);
+            }
+        }
+    }
+    cp_async_wait<0>();
+    __syncthreads();
+
+    // ---- warp results -> shared (8 columns), merge the 4 warps over the G real ones ----
+    float* wm = reinterpret_cast<float*>(smem);    // [4][8]
+    float* wl = wm + 32;                            // [4][8]
+    float* wo = wl + 32;                            // [4][8][D]
+    float* cm = wo + 32 * D;                        // [8]
+    float* cl = cm + 8;                             // [8]
+    float* co = cl + 8;                             // [8][D]
+    float* scratch = co + 8 * D;
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+        float l = l_run[e];
+        l += __shfl_xor_sync(0xffffffffu, l, 4);
+        l += __shfl_xor_sync(0xffffffffu, l, 8);
+        l += __shfl_xor_sync(0xffffffffu, l, 16);
+        const int n = (lane & 3) * 2 + e;
+        if (lane < 4) {
+            wm[warp * 8 + n] = m_run[e];
+            wl[warp * 8 + n] = l;
+        }
+#pragma unroll
+        for (int mt = 0; mt < KS; ++mt) {
+            const int d = mt * 16 + (lane >> 2);
+            wo[(warp * 8 + n) * D + d] = acc[mt][e];
+            wo[(warp * 8 + n) * D + d + 8] = acc[mt][e + 2];
+        }
+    }
+    __syncthreads();
+    if (tid < G) {
+        float M = -INFINITY;
+        for (int w = 0; w < 4; ++w) M = fmaxf(M, wm[w * 8 + tid]);
+        float l = 0.f;
+        for (int w = 0; w < 4; ++w)
+            if (wm[w * 8 + tid] != -INFINITY) l += exp2f(wm[w * 8 + tid] - M) * wl[w * 8 + tid];
+        cm[tid] = M;
+        cl[tid] = l;
+    }
+    __syncthreads();
+    for (int i = tid; i < G * D; i += 128) {
+        const int n = i / D;
+        const float M = cm[n];
+        float a = 0.f;
+        for (int w = 0; w < 4; ++w)
+            if (wm[w * 8 + n] != -INFINITY) a += exp2f(wm[w * 8 + n] - M) * wo[(w * 8 + n) * D + (i % D)];
+        co[i] = a;
+    }
+    __syncthreads();
+
+    EpiOut out;
+    out.o = p.o + ((size_t)z * p.Hq + (size_t)h * G) * D;
+    out.lse = p.lse ? p.lse + (size_t)z * p.Hq + (size_t)h * G : nullptr;
+    out.rows_per_group = G;
+    out.o_row_stride = D;
+    out.o_group_stride = 0;
+    out.lse_row_stride = 1;
+    out.lse_group_stride = 0;
+    float* part = p.part + (size_t)(z * p.Hkv + h) * p.n_split * G * (D + 2);
+    const bool final_cta =
+        split_epilogue<D>(G, cm, cl, co, out, part, p.tickets + z * p.Hkv + h, split, p.n_split, scratch);
+    if (p.mode == kDevModeSlot && final_cta) slot_append_tail<ROWB>(p, lb, z, s_m_before);
+}
+
+template <int D>
+static int launch_mma(masw_mem_t* mem, DecodeParams& prm, int G, int rows, int kmax, cudaStream_t stream) {
+    using C = MmaCfg<D>;
+    static int occ[64] = {};
+    const int dev = mem->device & 63;
+    if (!occ[dev]) {
+        MASW_CUDA_TRY(mem, cudaFuncSetAttribute(decode_mma_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                C::SMEM));
+        int n = 0;
+        MASW_CUDA_TRY(mem, cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_mma_kernel<D>, 128, C::SMEM));
+        occ[dev] = n > 0 ? n : 1;
+    }
+    // one wave: as many splits as fit the resident CTA slots, at least 64 keys each
+    const int pairs = rows * mem->Hkv;
+    const int slots = occ[dev] * mem->num_sms;
+    int n_split = imax(1, slots / pairs);
+    n_split = imin(n_split, imax(1, (kmax + 63) / 64));
+    n_split = imin(n_split, kMaxSplit);
+    while (n_split > 1 && masw_decode_part_floats(rows, mem->Hkv, G, D, n_split) > mem->part_floats) --n_split;
+    prm.n_split = n_split;
+    dim3 grid(n_split, mem->Hkv, rows);
+    decode_mma_kernel<D><<<grid, 128, C::SMEM, stream>>>(prm);
+    MASW_CUDA_TRY(mem, cudaGetLastError());
+    return MASW_OK;
+}
+
+}  // namespace masw
+
+int masw_launch_decode_mma(masw_mem_t* mem, masw::DecodeParams& prm, int G, int rows, int kmax,
+                           cudaStream_t stream) {
+    if (G < 1 || G > 8) return masw_set_error(mem, MASW_EINVAL, "query heads per kv head must be at most 8");
+    if (mem->D == 128) return masw::launch_mma<128>(mem, prm, G, rows, kmax, stream);
+    return masw::launch_mma<64>(mem, prm, G, rows, kmax, stream);
+}

@@ -135,6 +135,47 @@ template <> struct Elem<__nv_bfloat16> {
 };
 
 // ---------------------------------------------------------------------------
+// Tensor-core and async-copy helpers (mma.sync m16n8k16, ldmatrix, movmatrix,
+// cp.async): used where the GQA group turns K/V rows into a small dense
+// contraction.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, int src_bytes) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(addr));
+}
+__device__ __forceinline__ void mma16816(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                         uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+__device__ __forceinline__ uint32_t movmatrix_t(uint32_t x) {
+    uint32_t y;
+    asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
+    return y;
+}
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&v);
+}
+
+
+// ---------------------------------------------------------------------------
 // Split-KV epilogue.  A CTA that has reduced its key range to (m, l, o) per
 // query row -- m the running max of log2-scaled scores, l = sum 2^(s-m),
 // o = sum 2^(s-m) v (unnormalised) -- either writes the final output (one
@@ -250,6 +291,101 @@ __device__ bool split_epilogue(int nrows, const float* sm_m, const float* sm_l, 
     return true;
 }
 
+// ---------------------------------------------------------------------------
+// Decode launch parameters and the segment walker shared by the decode kernels.
+// ---------------------------------------------------------------------------
+enum DecodeModeDev { kDevModeDraft = 0, kDevModeFull = 1, kDevModeSlot = 2 };
+
+struct DecodeParams {
+    const void* q;        // [rows][Hq][D]
+    float* o;             // [rows][Hq][D]
+    float* lse;           // [rows][Hq] or null
+    const void* pool_k;   // [L][B][Hkv][C][D]
+    const void* pool_v;
+    const void* full_k;   // [L][B][Hkv][Tmax][D]
+    const void* full_v;
+    const void* k_g;      // slot mode: [rows][Hkv][D]
+    const void* v_g;
+    const int* d_t;
+    int* d_m;
+    int* d_pos;
+    int* d_err;
+    float* part;
+    unsigned* tickets;
+    unsigned* seq_tickets;
+    float scale_log2;     // softmax scale * log2(e)
+    int mode, layer, B, Hkv, Hq, S, W, Wc, C, Tmax, M_max, n_split, self_attend;
+    short seq_ids[MASW_MAX_BATCH];
+};
+
+struct Seg {
+    const uint8_t* k;
+    const uint8_t* v;
+    int len;
+};
+
+// Contiguous runs of K/V rows one (row z, kv head h) pair reads, in order:
+// the sink, the window (one run, or two when it wraps around the ring), the
+// slot chain, and -- for a slot write with self-attention -- the caller's own
+// K_g/V_g row.  Draft mode: [EN] §3.1 Eq. 4; slot mode: [EN] §3.2 Algorithm 1
+// step 2 (slots 1..m-1 only); full mode: every raw token.
+template <int ROWB>
+__device__ __forceinline__ int build_segments(const DecodeParams& p, int lb, int h, int z, int t, int mcnt,
+                                              Seg* segs) {
+    int n = 0;
+    if (p.mode == kDevModeFull) {
+        const size_t base = ((size_t)lb * p.Hkv + h) * (size_t)p.Tmax * ROWB;
+        if (t > 0) segs[n++] = Seg{(const uint8_t*)p.full_k + base, (const uint8_t*)p.full_v + base, t};
+        return n;
+    }
+    const size_t base = ((size_t)lb * p.Hkv + h) * (size_t)p.C * ROWB;
+    const uint8_t* kb = (const uint8_t*)p.pool_k + base;
+    const uint8_t* vb = (const uint8_t*)p.pool_v + base;
+    const int ns = imin(p.S, t);
+    if (ns > 0) segs[n++] = Seg{kb, vb, ns};
+    const int nl = n_local(t, p.S, p.W);
+    if (nl > 0) {
+        const int start = ring_row(window_lo(t, p.S, p.W), p.S, p.Wc);
+        const int first = imin(nl, p.Wc - start);
+        segs[n++] = Seg{kb + (size_t)(p.S + start) * ROWB, vb + (size_t)(p.S + start) * ROWB, first};
+        if (nl > first) segs[n++] = Seg{kb + (size_t)p.S * ROWB, vb + (size_t)p.S * ROWB, nl - first};
+    }
+    if (mcnt > 0) segs[n++] = Seg{kb + (size_t)(p.S + p.Wc) * ROWB, vb + (size_t)(p.S + p.Wc) * ROWB, mcnt};
+    if (p.mode == kDevModeSlot && p.self_attend) {
+        const size_t off = ((size_t)z * p.Hkv + h) * ROWB;
+        segs[n++] = Seg{(const uint8_t*)p.k_g + off, (const uint8_t*)p.v_g + off, 1};
+    }
+    return n;
+}
+
+// Slot write, after the attention of every (row z, head) pair is final: the
+// last pair of the row to finish appends g_m's K/V as chain entry m_before,
+// records its position id and bumps the slot counter.  Every CTA of the row
+// has read the old counter by then (each took its ticket after a fence).
+template <int ROWB>
+__device__ void slot_append_tail(const DecodeParams& p, int lb, int z, int m_before) {
+    __shared__ unsigned s_last_head;
+    const int tid = threadIdx.x;
+    __threadfence();
+    __syncthreads();
+    if (tid == 0) s_last_head = atomicAdd(p.seq_tickets + z, 1u) == (unsigned)(p.Hkv - 1);
+    __syncthreads();
+    if (!s_last_head) return;
+    constexpr int VPR = ROWB / 16;
+    for (int i = tid; i < p.Hkv * VPR; i += blockDim.x) {
+        const int hh = i / VPR, cc = i % VPR;
+        const size_t dst = (((size_t)lb * p.Hkv + hh) * p.C + (size_t)(p.S + p.Wc + m_before)) * ROWB + cc * 16;
+        const size_t src = ((size_t)z * p.Hkv + hh) * ROWB + cc * 16;
+        *reinterpret_cast<uint4*>((uint8_t*)p.pool_k + dst) = *reinterpret_cast<const uint4*>((const uint8_t*)p.k_g + src);
+        *reinterpret_cast<uint4*>((uint8_t*)p.pool_v + dst) = *reinterpret_cast<const uint4*>((const uint8_t*)p.v_g + src);
+    }
+    if (tid == 0) {
+        p.d_pos[(size_t)lb * p.M_max + m_before] = p.d_t[lb];   // 0-based id of the raw token after g_m
+        p.d_m[lb] = m_before + 1;
+        p.seq_tickets[z] = 0u;
+    }
+}
+
 }  // namespace masw
 
 // ---------------------------------------------------------------------------
@@ -271,3 +407,5 @@ int masw_launch_decode(masw_mem_t* mem, int mode, int layer, const void* q, int 
                        cudaStream_t stream);
 // floats of split scratch one decode launch with these sizes may use
 size_t masw_decode_part_floats(int rows, int Hkv, int G, int D, int n_split);
+// tensor-core decode for bf16 pools (masw_decode_mma.cu)
+int masw_launch_decode_mma(masw_mem_t* mem, masw::DecodeParams& prm, int G, int rows, int kmax, cudaStream_t stream);
