@@ -341,6 +341,49 @@ def oracle_sample(seconds_budget: float = 12.0):
                       f"numpy fp64, default BLAS threading"}
 
 
+# ------------------------------------------------------- profiling case --
+
+def profile_case(kind: str, prefix: int):
+    """A few launches of one kernel on the benchmark's per-launch shape (batch 8,
+    24q/8kv heads, 32K prefix) over 4 layers, for an ncu capture: each launch
+    reads a different layer's data, and ncu flushes caches between passes."""
+    import torch
+    from compressed_draft_kv_gb300 import capi, synth
+    capi.load()
+    w = synth.WORKLOADS[WORKLOAD]
+    L, B, Hq, Hkv, D, S, W, r = 4, w["batch"], w["Hq"], w["Hkv"], w["D"], w["S"], w["W"], w["r"]
+    dev = torch.device("cuda", 0)
+    g = torch.Generator(device=dev)
+    g.manual_seed(5)
+    if kind == "verify":
+        vb, Lq, Hq8 = 4, 6, 32
+        T = prefix + Lq
+        kc = torch.randn(vb, Hkv, T, D, generator=g, device=dev).to(torch.bfloat16)
+        vc = torch.randn(vb, Hkv, T, D, generator=g, device=dev).to(torch.bfloat16)
+        q = torch.randn(vb, Lq, Hq8, D, generator=g, device=dev).to(torch.bfloat16)
+        kl = torch.full((vb,), T, dtype=torch.int32, device=dev)
+        o = torch.empty(vb, Lq, Hq8, D, device=dev)
+        for _ in range(4):
+            capi.masw_verify_attn(q, kc, vc, kl, o)
+        torch.cuda.synchronize()
+        return
+    full = kind == "full"
+    h = capi.masw_mem_create(S, W, r, Hkv, D, L, batch=B, dtype=capi.MASW_BF16, max_seq_len=prefix + 8,
+                             full_kv=full)
+    n = max(0, (prefix - S - W) // r)
+    kr = torch.randn(prefix, Hkv, D, generator=g, device=dev).to(torch.bfloat16)
+    ks = torch.randn(n, Hkv, D, generator=g, device=dev).to(torch.bfloat16)
+    for l in range(L):
+        for b in range(B):
+            capi.masw_mem_load(h, l, b, kr, kr, ks, ks)
+    q = torch.randn(B, Hq, D, generator=g, device=dev).to(torch.bfloat16)
+    o = torch.empty(B, Hq, D, device=dev)
+    for l in range(L):
+        (capi.masw_full_attn if full else capi.masw_draft_attn)(h, l, q, o)
+    torch.cuda.synchronize()
+    capi.masw_mem_destroy(h)
+
+
 # ------------------------------------------------------------------ main --
 
 def main():
@@ -352,6 +395,8 @@ def main():
     ap.add_argument("--prefix", type=int, default=None)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-iters", type=int, default=5)
+    ap.add_argument("--profile-case", choices=["draft", "full", "verify"], default=None,
+                    help="run a few launches of one kernel on a small state (4 layers) for an ncu capture")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -362,6 +407,10 @@ def main():
 
     from compressed_draft_kv_gb300 import synth
     prefix = args.prefix or synth.WORKLOADS[WORKLOAD]["prefix"]
+
+    if args.profile_case:
+        profile_case(args.profile_case, prefix)
+        return
 
     if args.impl == "reference":
         if rank != 0:
