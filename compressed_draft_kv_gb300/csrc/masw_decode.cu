@@ -99,6 +99,8 @@ decode_kernel(const __grid_constant__ DecodeParams p) {
     const int split = blockIdx.x, h = blockIdx.y, z = blockIdx.z;
     const int b = (p.mode == kModeSlot) ? (int)p.seq_ids[z] : z;
     const int lb = p.layer * p.B + b;
+    pdl_wait();
+    pdl_trigger();
 
     if (tid == 0) {
         const int t = p.d_t[lb];
@@ -315,9 +317,8 @@ static int launch_t(masw_mem_t* mem, const DecodeParams& prm, int rows, cudaStre
                                                 cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES));
         configured[dev] = true;
     }
-    dim3 grid(prm.n_split, mem->Hkv, rows);
-    decode_kernel<T, D, G><<<grid, Cfg::THREADS, Cfg::SMEM_BYTES, stream>>>(prm);
-    MASW_CUDA_TRY(mem, cudaGetLastError());
+    MASW_CUDA_TRY(mem, masw_launch(decode_kernel<T, D, G>, dim3(prm.n_split, mem->Hkv, rows), dim3(Cfg::THREADS),
+                                   Cfg::SMEM_BYTES, stream, 1, prm));
     return MASW_OK;
 }
 

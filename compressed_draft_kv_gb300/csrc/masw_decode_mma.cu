@@ -22,7 +22,10 @@
 // never gathered in HBM.  Split partials are merged by split_epilogue.
 #include "masw_internal.cuh"
 
+#include <cooperative_groups.h>
 #include <cstring>
+
+namespace cg = cooperative_groups;
 
 namespace masw {
 
@@ -35,7 +38,7 @@ struct MmaCfg {
     static constexpr int STAGE = 2 * KPS * ROWB; // K then V
     static constexpr int SMEM = NST * STAGE;
     static constexpr int KS = D / 16;            // k-steps of Q.K, m-tiles of P.V
-    static_assert((2 * 4 * 8 + 4 * 8 * D + 2 * 8 + 8 * D + epilogue_scratch_floats(8, kMaxSplit)) * 4 <= SMEM,
+    static_assert((2 * 4 * 8 + 4 * 8 * (D + 8) + 2 * 8 + 8 * D + epilogue_scratch_floats(8, kMaxSplit)) * 4 <= SMEM,
                   "merge does not fit in the stage buffers");
 };
 
@@ -58,6 +61,8 @@ __global__ void __launch_bounds__(128) decode_mma_kernel(const __grid_constant__
     const int b = (p.mode == kDevModeSlot) ? (int)p.seq_ids[z] : z;
     const int lb = p.layer * p.B + b;
     const int G = p.Hq / p.Hkv;
+    pdl_wait();
+    pdl_trigger();
 
     if (tid == 0) {
         const int t = p.d_t[lb];
@@ -81,29 +86,31 @@ __global__ void __launch_bounds__(128) decode_mma_kernel(const __grid_constant__
     const int nstage = (r1 - r0 + KPS - 1) / KPS;
     const uint32_t sbase = smem_u32(smem);
 
-    // stage c <- logical rows [r0 + c*KPS, +KPS); rows past r1 are zero-filled
+    // stage c <- logical rows [r0 + c*KPS, +KPS); rows past r1 are zero-filled.
+    // Thread tid copies CPT consecutive 16-byte chunks of one row (K and V), so
+    // it looks the row's segment up once per stage.
+    constexpr int TPR = 128 / KPS;            // threads per row
+    constexpr int CPT = CH / TPR;             // chunks per thread
+    const int my_row = tid / TPR, my_ch0 = (tid % TPR) * CPT;
     auto load_stage = [&](int c) {
         const uint32_t sk = sbase + (uint32_t)(c % NST) * C::STAGE;
         const uint32_t sv = sk + KPS * ROWB;
-        const int key0 = r0 + c * KPS;
+        const int j = r0 + c * KPS + my_row;
+        const uint8_t* ks = segs[0].k;
+        const uint8_t* vs = segs[0].v;
+        int bytes = 0;
+        if (j < r1) {
+            int s = 0;
+            while (s + 1 < nseg && j >= s_start[s + 1]) ++s;
+            const size_t off = (size_t)(j - s_start[s]) * ROWB + my_ch0 * 16;
+            ks = segs[s].k + off;
+            vs = segs[s].v + off;
+            bytes = 16;
+        }
 #pragma unroll
-        for (int i = 0; i < (KPS * CH) / 128; ++i) {
-            const int idx = tid + i * 128;
-            const int row = idx / CH, ch = idx % CH;
-            const int j = key0 + row;
-            const uint8_t* ks = segs[0].k;
-            const uint8_t* vs = segs[0].v;
-            int bytes = 0;
-            if (j < r1) {
-                int s = 0;
-                while (s + 1 < nseg && j >= s_start[s + 1]) ++s;
-                const size_t off = (size_t)(j - s_start[s]) * ROWB + ch * 16;
-                ks = segs[s].k + off;
-                vs = segs[s].v + off;
-                bytes = 16;
-            }
-            cp_async16(sk + swz_off<ROWB>(row, ch), ks, bytes);
-            cp_async16(sv + swz_off<ROWB>(row, ch), vs, bytes);
+        for (int i = 0; i < CPT; ++i) {
+            cp_async16(sk + swz_off<ROWB>(my_row, my_ch0 + i), ks + (bytes ? i * 16 : 0), bytes);
+            cp_async16(sv + swz_off<ROWB>(my_row, my_ch0 + i), vs + (bytes ? i * 16 : 0), bytes);
         }
     };
 #pragma unroll
@@ -192,10 +199,11 @@ __global__ void __launch_bounds__(128) decode_mma_kernel(const __grid_constant__
     __syncthreads();
 
     // ---- warp results -> shared (8 columns), merge the 4 warps over the G real ones ----
+    constexpr int WS = D + 8;                       // padded row stride of wo
     float* wm = reinterpret_cast<float*>(smem);    // [4][8]
     float* wl = wm + 32;                            // [4][8]
-    float* wo = wl + 32;                            // [4][8][D]
-    float* cm = wo + 32 * D;                        // [8]
+    float* wo = wl + 32;                            // [4][8][WS]
+    float* cm = wo + 32 * WS;                       // [8]
     float* cl = cm + 8;                             // [8]
     float* co = cl + 8;                             // [8][D]
     float* scratch = co + 8 * D;
@@ -213,8 +221,8 @@ __global__ void __launch_bounds__(128) decode_mma_kernel(const __grid_constant__
 #pragma unroll
         for (int mt = 0; mt < KS; ++mt) {
             const int d = mt * 16 + (lane >> 2);
-            wo[(warp * 8 + n) * D + d] = acc[mt][e];
-            wo[(warp * 8 + n) * D + d + 8] = acc[mt][e + 2];
+            wo[(warp * 8 + n) * WS + d] = acc[mt][e];
+            wo[(warp * 8 + n) * WS + d + 8] = acc[mt][e + 2];
         }
     }
     __syncthreads();
@@ -233,11 +241,55 @@ __global__ void __launch_bounds__(128) decode_mma_kernel(const __grid_constant__
         const float M = cm[n];
         float a = 0.f;
         for (int w = 0; w < 4; ++w)
-            if (wm[w * 8 + n] != -INFINITY) a += exp2f(wm[w * 8 + n] - M) * wo[(w * 8 + n) * D + (i % D)];
+            if (wm[w * 8 + n] != -INFINITY) a += exp2f(wm[w * 8 + n] - M) * wo[(w * 8 + n) * WS + (i % D)];
         co[i] = a;
     }
     __syncthreads();
 
+    if (p.cluster) {
+        // The n_split CTAs of this (row, head) pair form one thread-block
+        // cluster: merge their (m, l, o) through distributed shared memory.
+        cg::cluster_group cluster = cg::this_cluster();
+        cluster.sync();                               // every CTA's cm/cl/co is final
+        const int nc = (int)cluster.num_blocks(), rank = (int)cluster.block_rank();
+        float* w = scratch;                           // [8][8] weights of rank r for row n
+        float* den = w + 64;                          // [8]
+        float* Mx = den + 8;                          // [8]
+        if (tid < G) {
+            float M = -INFINITY;
+            for (int r = 0; r < nc; ++r) M = fmaxf(M, *cluster.map_shared_rank(cm + tid, r));
+            float dn = 0.f;
+            for (int r = 0; r < nc; ++r) {
+                const float mr = *cluster.map_shared_rank(cm + tid, r);
+                const float wr = mr == -INFINITY ? 0.f : exp2f(mr - M);
+                w[tid * 8 + r] = wr;
+                dn += wr * *cluster.map_shared_rank(cl + tid, r);
+            }
+            den[tid] = dn;
+            Mx[tid] = M;
+        }
+        __syncthreads();
+        const int per = (G * D + nc - 1) / nc;
+        const int lo = rank * per, hi = imin(G * D, lo + per);
+        for (int i = lo + tid; i < hi; i += 128) {
+            const int n = i / D;
+            float a = 0.f;
+            for (int r = 0; r < nc; ++r) {
+                const float wr = w[n * 8 + r];
+                if (wr != 0.f) a += wr * *cluster.map_shared_rank(co + i, r);
+            }
+            const float dn = den[n];
+            p.o[((size_t)z * p.Hq + (size_t)h * G + n) * D + (i % D)] = dn > 0.f ? a / dn : 0.f;
+        }
+        if (rank == 0 && p.lse && tid < G) {
+            const float dn = den[tid];
+            p.lse[(size_t)z * p.Hq + (size_t)h * G + tid] =
+                dn > 0.f ? (Mx[tid] + __log2f(dn)) * 0.6931471805599453f : -INFINITY;
+        }
+        cluster.sync();                               // peers' shared memory stays alive until here
+        if (p.mode == kDevModeSlot && rank == 0) slot_append_tail<ROWB>(p, lb, z, s_m_before);
+        return;
+    }
     EpiOut out;
     out.o = p.o + ((size_t)z * p.Hq + (size_t)h * G) * D;
     out.lse = p.lse ? p.lse + (size_t)z * p.Hq + (size_t)h * G : nullptr;
@@ -270,11 +322,15 @@ static int launch_mma(masw_mem_t* mem, DecodeParams& prm, int G, int rows, int k
     int n_split = imax(1, slots / pairs);
     n_split = imin(n_split, imax(1, (kmax + 63) / 64));
     n_split = imin(n_split, kMaxSplit);
-    while (n_split > 1 && masw_decode_part_floats(rows, mem->Hkv, G, D, n_split) > mem->part_floats) --n_split;
+    // splits of one pair merge inside a thread-block cluster (distributed shared
+    // memory) when a portable cluster of <= 8 CTAs still fills most of the GPU
+    const bool cluster = n_split > 1 && n_split <= 8;
+    if (!cluster)
+        while (n_split > 1 && masw_decode_part_floats(rows, mem->Hkv, G, D, n_split) > mem->part_floats) --n_split;
     prm.n_split = n_split;
-    dim3 grid(n_split, mem->Hkv, rows);
-    decode_mma_kernel<D><<<grid, 128, C::SMEM, stream>>>(prm);
-    MASW_CUDA_TRY(mem, cudaGetLastError());
+    prm.cluster = cluster ? 1 : 0;
+    MASW_CUDA_TRY(mem, masw_launch(decode_mma_kernel<D>, dim3(n_split, mem->Hkv, rows), dim3(128), C::SMEM, stream,
+                                   cluster ? n_split : 1, prm));
     return MASW_OK;
 }
 

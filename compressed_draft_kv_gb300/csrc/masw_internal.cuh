@@ -8,6 +8,7 @@
 #include <stdint.h>
 
 #include <string>
+#include <utility>
 #include <vector>
 
 #include "../../include/masw.h"
@@ -114,6 +115,14 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* e
     if (err) atomicExch(err, MASW_ETIMEOUT);
     return false;
 }
+
+// Programmatic dependent launch.  Every library kernel is launched with the
+// programmatic-serialization attribute, so it may start while the previous
+// kernel on the stream is finishing; pdl_wait() blocks until that kernel has
+// completed and its memory is visible, and must come before any access to data
+// an earlier kernel may write.  pdl_trigger() lets the next kernel launch early.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
 __device__ __forceinline__ float bf16lo(uint32_t x) { return __uint_as_float(x << 16); }
 __device__ __forceinline__ float bf16hi(uint32_t x) { return __uint_as_float(x & 0xffff0000u); }
@@ -315,6 +324,7 @@ struct DecodeParams {
     unsigned* seq_tickets;
     float scale_log2;     // softmax scale * log2(e)
     int mode, layer, B, Hkv, Hq, S, W, Wc, C, Tmax, M_max, n_split, self_attend;
+    int cluster;          // 1: the n_split CTAs of a pair form a cluster and merge in DSMEM
     short seq_ids[MASW_MAX_BATCH];
 };
 
@@ -399,6 +409,33 @@ int masw_set_error(masw_mem_t* mem, int code, const std::string& msg);
             return masw_set_error((mem), MASW_ECUDA, std::string(#call) + ": " +       \
                                                          cudaGetErrorString(e_));      \
     } while (0)
+
+// Launch `kern` with the programmatic-serialization attribute (and an optional
+// cluster of cluster_x CTAs along x).
+template <typename... KArgs, typename... Args>
+cudaError_t masw_launch(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                        int cluster_x, Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[2];
+    int na = 0;
+    attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[na].val.programmaticStreamSerializationAllowed = 1;
+    ++na;
+    if (cluster_x > 1) {
+        attr[na].id = cudaLaunchAttributeClusterDimension;
+        attr[na].val.clusterDim.x = cluster_x;
+        attr[na].val.clusterDim.y = 1;
+        attr[na].val.clusterDim.z = 1;
+        ++na;
+    }
+    cfg.attrs = attr;
+    cfg.numAttrs = na;
+    return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
 
 // decode-kernel launcher (masw_decode.cu)
 enum DecodeMode { kModeDraft = 0, kModeFull = 1, kModeSlot = 2 };

@@ -49,6 +49,8 @@ struct AppendParams {
 // write overwrites, i.e. evicts, the token W+R positions older) and to row i-1
 // of the full cache; then the counter advances.
 __global__ void append_kernel(const __grid_constant__ AppendParams p) {
+    pdl_wait();
+    pdl_trigger();
     const int b = blockIdx.x;
     if (!((p.active[b >> 5] >> (b & 31)) & 1u)) return;
     const int lb = p.layer * p.B + b;
@@ -89,6 +91,8 @@ struct RollbackParams {
 // Counters of the listed sequences go back to t_new in every layer; slots with
 // tau_m > t_new are dropped (the chain keeps m(t_new) slots at most).
 __global__ void rollback_kernel(const __grid_constant__ RollbackParams p) {
+    pdl_wait();
+    pdl_trigger();
     const int b = p.seq[blockIdx.x];
     const int tn = p.t_new[blockIdx.x];
     for (int l = threadIdx.x; l < p.L; l += blockDim.x) {
@@ -329,8 +333,7 @@ int masw_append_kv(masw_mem_t* mem, int layer, const void* k, const void* v, con
         p.Wc = mem->Wc;
         p.C = mem->C;
         p.Tmax = mem->max_seq_len;
-        append_kernel<<<mem->B, 128, 0, (cudaStream_t)stream>>>(p);
-        MASW_CUDA_TRY(mem, cudaGetLastError());
+        MASW_CUDA_TRY(mem, masw_launch(append_kernel, dim3(mem->B), dim3(128), 0, (cudaStream_t)stream, 1, p));
         for (int b = 0; b < mem->B; ++b)
             if (!active || active[b]) mem->h_t[(size_t)layer * mem->B + b] += 1;
         return MASW_OK;
@@ -402,8 +405,7 @@ int masw_rollback(masw_mem_t* mem, const int* seq_ids, const int* t_new, int n, 
     p.W = mem->W;
     p.r = mem->r;
     p.n = n;
-    rollback_kernel<<<n, 32, 0, (cudaStream_t)stream>>>(p);
-    MASW_CUDA_TRY(mem, cudaGetLastError());
+    MASW_CUDA_TRY(mem, masw_launch(rollback_kernel, dim3(n), dim3(32), 0, (cudaStream_t)stream, 1, p));
     for (int i = 0; i < n; ++i)
         for (int l = 0; l < mem->L; ++l) {
             const size_t lb = (size_t)l * mem->B + seq_ids[i];

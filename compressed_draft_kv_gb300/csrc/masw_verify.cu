@@ -51,6 +51,8 @@ __global__ void __launch_bounds__(128) verify_kernel(const __grid_constant__ Ver
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int split = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
     const int G = p.G, NQ = p.NQ;
+    pdl_wait();
+    pdl_trigger();
 
     const int n_keys = p.kv_len[b];
     const int chunk = (((n_keys + p.n_split - 1) / p.n_split) + kVKeys - 1) / kVKeys * kVKeys;
@@ -305,9 +307,7 @@ static cudaError_t launch_verify(const VerifyParams& prm, cudaStream_t stream) {
         if (e != cudaSuccess) return e;
         configured[dev & 63] = true;
     }
-    dim3 grid(prm.n_split, prm.Hkv, prm.B);
-    verify_kernel<NT><<<grid, 128, kVSmem, stream>>>(prm);
-    return cudaGetLastError();
+    return masw_launch(verify_kernel<NT>, dim3(prm.n_split, prm.Hkv, prm.B), dim3(128), kVSmem, stream, 1, prm);
 }
 
 extern "C" int masw_verify_attn(const void* q, const void* k_cache, const void* v_cache, const int* kv_len, int B,
