@@ -22,10 +22,7 @@
 // never gathered in HBM.  Split partials are merged by split_epilogue.
 #include "masw_internal.cuh"
 
-#include <cooperative_groups.h>
 #include <cstring>
-
-namespace cg = cooperative_groups;
 
 namespace masw {
 
@@ -54,6 +51,8 @@ __global__ void __launch_bounds__(128) decode_mma_kernel(const __grid_constant__
     extern __shared__ __align__(128) uint8_t smem[];
     __shared__ Seg segs[5];
     __shared__ int s_start[6];
+    __shared__ const uint8_t* s_vk[5];
+    __shared__ const uint8_t* s_vv[5];
     __shared__ int s_nseg, s_m_before;
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -72,7 +71,13 @@ __global__ void __launch_bounds__(128) decode_mma_kernel(const __grid_constant__
         int acc = 0;
         for (int s = 0; s < n; ++s) {
             s_start[s] = acc;
+            s_vk[s] = segs[s].k - (size_t)acc * ROWB;   // row j of the list is s_vk[s] + j*ROWB
+            s_vv[s] = segs[s].v - (size_t)acc * ROWB;
             acc += segs[s].len;
+        }
+        if (n == 0) {
+            s_vk[0] = (const uint8_t*)p.pool_k;
+            s_vv[0] = (const uint8_t*)p.pool_v;
         }
         s_start[n] = acc;
         s_nseg = n;
@@ -87,30 +92,36 @@ __global__ void __launch_bounds__(128) decode_mma_kernel(const __grid_constant__
     const uint32_t sbase = smem_u32(smem);
 
     // stage c <- logical rows [r0 + c*KPS, +KPS); rows past r1 are zero-filled.
-    // Thread tid copies CPT consecutive 16-byte chunks of one row (K and V), so
-    // it looks the row's segment up once per stage.
-    constexpr int TPR = 128 / KPS;            // threads per row
-    constexpr int CPT = CH / TPR;             // chunks per thread
-    const int my_row = tid / TPR, my_ch0 = (tid % TPR) * CPT;
+    // Lanes take consecutive 16-byte chunks of a row (CH lanes per row), so each
+    // warp-wide cp.async covers whole rows; a thread's rows are RPP apart and
+    // walk the segment list monotonically (vbase[s] = segment base - start*ROWB).
+    constexpr int RPP = 128 / CH;             // rows per pass of the CTA
+    const int my_row = tid / CH, my_ch = tid % CH;
     auto load_stage = [&](int c) {
         const uint32_t sk = sbase + (uint32_t)(c % NST) * C::STAGE;
         const uint32_t sv = sk + KPS * ROWB;
-        const int j = r0 + c * KPS + my_row;
-        const uint8_t* ks = segs[0].k;
-        const uint8_t* vs = segs[0].v;
-        int bytes = 0;
-        if (j < r1) {
-            int s = 0;
-            while (s + 1 < nseg && j >= s_start[s + 1]) ++s;
-            const size_t off = (size_t)(j - s_start[s]) * ROWB + my_ch0 * 16;
-            ks = segs[s].k + off;
-            vs = segs[s].v + off;
-            bytes = 16;
-        }
+        const int j0 = r0 + c * KPS + my_row;
+        int s = 0;
+        while (s + 1 < nseg && j0 >= s_start[s + 1]) ++s;
+        int next = s + 1 < nseg ? s_start[s + 1] : 0x7fffffff;
 #pragma unroll
-        for (int i = 0; i < CPT; ++i) {
-            cp_async16(sk + swz_off<ROWB>(my_row, my_ch0 + i), ks + (bytes ? i * 16 : 0), bytes);
-            cp_async16(sv + swz_off<ROWB>(my_row, my_ch0 + i), vs + (bytes ? i * 16 : 0), bytes);
+        for (int i = 0; i < KPS / RPP; ++i) {
+            const int row = my_row + i * RPP;
+            const int j = j0 + i * RPP;
+            const uint8_t* ks = s_vk[0];
+            const uint8_t* vs = s_vv[0];
+            int bytes = 0;
+            if (j < r1) {
+                while (j >= next) {
+                    ++s;
+                    next = s + 1 < nseg ? s_start[s + 1] : 0x7fffffff;
+                }
+                ks = s_vk[s] + (size_t)j * ROWB + my_ch * 16;
+                vs = s_vv[s] + (size_t)j * ROWB + my_ch * 16;
+                bytes = 16;
+            }
+            cp_async16(sk + swz_off<ROWB>(row, my_ch), ks, bytes);
+            cp_async16(sv + swz_off<ROWB>(row, my_ch), vs, bytes);
         }
     };
 #pragma unroll
@@ -246,50 +257,6 @@ __global__ void __launch_bounds__(128) decode_mma_kernel(const __grid_constant__
     }
     __syncthreads();
 
-    if (p.cluster) {
-        // The n_split CTAs of this (row, head) pair form one thread-block
-        // cluster: merge their (m, l, o) through distributed shared memory.
-        cg::cluster_group cluster = cg::this_cluster();
-        cluster.sync();                               // every CTA's cm/cl/co is final
-        const int nc = (int)cluster.num_blocks(), rank = (int)cluster.block_rank();
-        float* w = scratch;                           // [8][8] weights of rank r for row n
-        float* den = w + 64;                          // [8]
-        float* Mx = den + 8;                          // [8]
-        if (tid < G) {
-            float M = -INFINITY;
-            for (int r = 0; r < nc; ++r) M = fmaxf(M, *cluster.map_shared_rank(cm + tid, r));
-            float dn = 0.f;
-            for (int r = 0; r < nc; ++r) {
-                const float mr = *cluster.map_shared_rank(cm + tid, r);
-                const float wr = mr == -INFINITY ? 0.f : exp2f(mr - M);
-                w[tid * 8 + r] = wr;
-                dn += wr * *cluster.map_shared_rank(cl + tid, r);
-            }
-            den[tid] = dn;
-            Mx[tid] = M;
-        }
-        __syncthreads();
-        const int per = (G * D + nc - 1) / nc;
-        const int lo = rank * per, hi = imin(G * D, lo + per);
-        for (int i = lo + tid; i < hi; i += 128) {
-            const int n = i / D;
-            float a = 0.f;
-            for (int r = 0; r < nc; ++r) {
-                const float wr = w[n * 8 + r];
-                if (wr != 0.f) a += wr * *cluster.map_shared_rank(co + i, r);
-            }
-            const float dn = den[n];
-            p.o[((size_t)z * p.Hq + (size_t)h * G + n) * D + (i % D)] = dn > 0.f ? a / dn : 0.f;
-        }
-        if (rank == 0 && p.lse && tid < G) {
-            const float dn = den[tid];
-            p.lse[(size_t)z * p.Hq + (size_t)h * G + tid] =
-                dn > 0.f ? (Mx[tid] + __log2f(dn)) * 0.6931471805599453f : -INFINITY;
-        }
-        cluster.sync();                               // peers' shared memory stays alive until here
-        if (p.mode == kDevModeSlot && rank == 0) slot_append_tail<ROWB>(p, lb, z, s_m_before);
-        return;
-    }
     EpiOut out;
     out.o = p.o + ((size_t)z * p.Hq + (size_t)h * G) * D;
     out.lse = p.lse ? p.lse + (size_t)z * p.Hq + (size_t)h * G : nullptr;
@@ -322,15 +289,10 @@ static int launch_mma(masw_mem_t* mem, DecodeParams& prm, int G, int rows, int k
     int n_split = imax(1, slots / pairs);
     n_split = imin(n_split, imax(1, (kmax + 63) / 64));
     n_split = imin(n_split, kMaxSplit);
-    // splits of one pair merge inside a thread-block cluster (distributed shared
-    // memory) when a portable cluster of <= 8 CTAs still fills most of the GPU
-    const bool cluster = n_split > 1 && n_split <= 8;
-    if (!cluster)
-        while (n_split > 1 && masw_decode_part_floats(rows, mem->Hkv, G, D, n_split) > mem->part_floats) --n_split;
+    while (n_split > 1 && masw_decode_part_floats(rows, mem->Hkv, G, D, n_split) > mem->part_floats) --n_split;
     prm.n_split = n_split;
-    prm.cluster = cluster ? 1 : 0;
     MASW_CUDA_TRY(mem, masw_launch(decode_mma_kernel<D>, dim3(n_split, mem->Hkv, rows), dim3(128), C::SMEM, stream,
-                                   cluster ? n_split : 1, prm));
+                                   1, prm));
     return MASW_OK;
 }
 

@@ -324,7 +324,6 @@ struct DecodeParams {
     unsigned* seq_tickets;
     float scale_log2;     // softmax scale * log2(e)
     int mode, layer, B, Hkv, Hq, S, W, Wc, C, Tmax, M_max, n_split, self_attend;
-    int cluster;          // 1: the n_split CTAs of a pair form a cluster and merge in DSMEM
     short seq_ids[MASW_MAX_BATCH];
 };
 
