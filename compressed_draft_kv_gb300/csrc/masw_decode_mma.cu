@@ -63,6 +63,19 @@ __global__ void __launch_bounds__(128) decode_mma_kernel(const __grid_constant__
     pdl_wait();
     pdl_trigger();
 
+    // Q^T as B fragments: column n = query head h*G + n of row z (zero when n >= G)
+    uint32_t qb[KS][2];
+    {
+        const int n = lane >> 2;
+        const bool real = n < G;
+        const __nv_bfloat16* qrow = (const __nv_bfloat16*)p.q + ((size_t)z * p.Hq + (size_t)h * G + (real ? n : 0)) * D;
+#pragma unroll
+        for (int ks = 0; ks < KS; ++ks) {
+            const int d = ks * 16 + (lane & 3) * 2;
+            qb[ks][0] = real ? *reinterpret_cast<const uint32_t*>(qrow + d) : 0u;
+            qb[ks][1] = real ? *reinterpret_cast<const uint32_t*>(qrow + d + 8) : 0u;
+        }
+    }
     if (tid == 0) {
         const int t = p.d_t[lb];
         const int mcnt = p.d_m[lb];
@@ -130,19 +143,6 @@ __global__ void __launch_bounds__(128) decode_mma_kernel(const __grid_constant__
         cp_async_commit();
     }
 
-    // Q^T as B fragments: column n = query head h*G + n of row z (zero when n >= G)
-    uint32_t qb[KS][2];
-    {
-        const int n = lane >> 2;
-        const bool real = n < G;
-        const __nv_bfloat16* qrow = (const __nv_bfloat16*)p.q + ((size_t)z * p.Hq + (size_t)h * G + (real ? n : 0)) * D;
-#pragma unroll
-        for (int ks = 0; ks < KS; ++ks) {
-            const int d = ks * 16 + (lane & 3) * 2;
-            qb[ks][0] = real ? *reinterpret_cast<const uint32_t*>(qrow + d) : 0u;
-            qb[ks][1] = real ? *reinterpret_cast<const uint32_t*>(qrow + d + 8) : 0u;
-        }
-    }
     const float sl2 = p.scale_log2;
     float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f};
     float acc[KS][4];

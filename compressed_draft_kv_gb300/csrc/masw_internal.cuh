@@ -216,13 +216,25 @@ __host__ __device__ constexpr int epilogue_scratch_floats(int nrows, int n_split
     return nrows * n_split + 2 * nrows;
 }
 
+__device__ __forceinline__ unsigned atom_add_acq_rel_gpu(unsigned* p, unsigned v) {
+    unsigned old;
+    asm volatile("atom.add.acq_rel.gpu.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+    return old;
+}
+
 // Returns true in every thread of the CTA that wrote the final output of its pair.
+// Partials are stored by all threads; after a CTA barrier thread 0 takes the
+// ticket with an acq_rel atomic (release of this CTA's stores, acquire of the
+// earlier splits' stores for the last one).  The last CTA merges all splits in
+// one pass per output element with an online log-sum-exp merge, loading the
+// (m, l, o) of up to 8 splits at a time so the L2 round trips overlap.
 template <int D>
 __device__ bool split_epilogue(int nrows, const float* sm_m, const float* sm_l, const float* sm_o,
                                const EpiOut& out, float* part, unsigned* ticket, int split, int n_split,
                                float* sm_scratch) {
     const int tid = threadIdx.x, nt = blockDim.x;
     constexpr float kLn2 = 0.6931471805599453f;
+    (void)sm_scratch;
     if (n_split == 1) {
         for (int i = tid; i < nrows * D; i += nt) {
             const int row = i / D, d = i % D;
@@ -236,66 +248,53 @@ __device__ bool split_epilogue(int nrows, const float* sm_m, const float* sm_l, 
             }
         return true;
     }
-    // store this split's partial: part[split][row][D + 2]
+    // store this split's partial: part[split][row][D + 2] = (o[D], m, l)
     float* mine = part + (size_t)split * nrows * (D + 2);
     for (int i = tid; i < nrows * D; i += nt) {
         const int row = i / D, d = i % D;
-        mine[row * (D + 2) + d] = sm_o[row * D + d];
+        __stcg(mine + row * (D + 2) + d, sm_o[row * D + d]);
     }
     for (int row = tid; row < nrows; row += nt) {
-        mine[row * (D + 2) + D] = sm_m[row];
-        mine[row * (D + 2) + D + 1] = sm_l[row];
+        __stcg(mine + row * (D + 2) + D, sm_m[row]);
+        __stcg(mine + row * (D + 2) + D + 1, sm_l[row]);
     }
-    __threadfence();
     __syncthreads();
     __shared__ unsigned s_last;
-    if (tid == 0) {
-        const unsigned prev = atomicAdd(ticket, 1u);
-        s_last = (prev == (unsigned)(n_split - 1));
-    }
+    if (tid == 0) s_last = atom_add_acq_rel_gpu(ticket, 1u) == (unsigned)(n_split - 1);
     __syncthreads();
     if (!s_last) return false;
-    __threadfence();
-    // merge: warp w takes rows w, w+nwarps, ...; lanes stride over splits.
-    float* w = sm_scratch;                    // [nrows][n_split] weights
-    float* s_den = sm_scratch + nrows * n_split;
-    float* s_M = s_den + nrows;
-    const int lane = tid & 31, warp = tid >> 5, nwarps = nt >> 5;
-    for (int row = warp; row < nrows; row += nwarps) {
-        float M = -INFINITY;
-        for (int s = lane; s < n_split; s += 32)
-            M = fmaxf(M, __ldcg(part + ((size_t)s * nrows + row) * (D + 2) + D));
-        for (int off = 16; off; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
-        float den = 0.f;
-        for (int s = lane; s < n_split; s += 32) {
-            const float ms = __ldcg(part + ((size_t)s * nrows + row) * (D + 2) + D);
-            const float ls = __ldcg(part + ((size_t)s * nrows + row) * (D + 2) + D + 1);
-            const float ws = (ms == -INFINITY) ? 0.f : exp2f(ms - M);
-            w[row * n_split + s] = ws;
-            den += ws * ls;
-        }
-        for (int off = 16; off; off >>= 1) den += __shfl_xor_sync(0xffffffffu, den, off);
-        if (lane == 0) {
-            s_den[row] = den;
-            s_M[row] = M;
-        }
-    }
-    __syncthreads();
+    const size_t stride = (size_t)nrows * (D + 2);
     for (int i = tid; i < nrows * D; i += nt) {
         const int row = i / D, d = i % D;
-        float acc = 0.f;
-        for (int s = 0; s < n_split; ++s) {
-            const float ws = w[row * n_split + s];
-            if (ws != 0.f) acc += ws * __ldcg(part + ((size_t)s * nrows + row) * (D + 2) + d);
+        const float* base = part + row * (D + 2);
+        float M = -INFINITY, den = 0.f, acc = 0.f;
+        for (int s0 = 0; s0 < n_split; s0 += 8) {
+            float ms[8], ls[8], os[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                const bool in = s0 + k < n_split;
+                const float* ps = base + (size_t)(in ? s0 + k : 0) * stride;
+                ms[k] = in ? __ldcg(ps + D) : -INFINITY;
+                ls[k] = in ? __ldcg(ps + D + 1) : 0.f;
+                os[k] = in ? __ldcg(ps + d) : 0.f;
+            }
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                if (ms[k] == -INFINITY) continue;
+                if (ms[k] > M) {
+                    const float sc = exp2f(M - ms[k]);   // M = -inf gives 0
+                    acc *= sc;
+                    den *= sc;
+                    M = ms[k];
+                }
+                const float w = exp2f(ms[k] - M);
+                acc += w * os[k];
+                den += w * ls[k];
+            }
         }
-        const float den = s_den[row];
         out.o[out.o_off(row) + d] = den > 0.f ? acc / den : 0.f;
+        if (d == 0 && out.lse) out.lse[out.lse_off(row)] = den > 0.f ? (M + __log2f(den)) * kLn2 : -INFINITY;
     }
-    if (out.lse)
-        for (int row = tid; row < nrows; row += nt) {
-            const float den = s_den[row];
-            out.lse[out.lse_off(row)] = den > 0.f ? (s_M[row] + __log2f(den)) * kLn2 : -INFINITY;
-        }
     if (tid == 0) *ticket = 0u;
     return true;
 }
