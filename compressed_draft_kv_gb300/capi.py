@@ -21,6 +21,7 @@ MASW_MAX_BATCH, MASW_MAX_GROUP = 512, 8
 EXPORTS = [
     "masw_mem_create", "masw_mem_destroy", "masw_last_error", "masw_append_kv",
     "masw_materialize_slot", "masw_rollback", "masw_draft_attn", "masw_full_attn",
+    "masw_draft_step", "masw_full_step",
     "masw_verify_attn", "masw_verify_workspace_bytes", "masw_verify_attn_noalloc", "masw_mem_load", "masw_mem_export",
     "masw_query", "masw_sync", "masw_index", "masw_version",
 ]
@@ -64,6 +65,8 @@ def load() -> ctypes.CDLL:
         "masw_rollback": [P, IP, IP, I, P],
         "masw_draft_attn": [P, I, P, I, P, P, P],
         "masw_full_attn": [P, I, P, I, P, P, P],
+        "masw_draft_step": [P, I, P, P, P, P, I, P, P, P],
+        "masw_full_step": [P, I, P, P, P, P, I, P, P, P],
         "masw_verify_attn": [P, P, P, P, I, I, I, I, I, I, I, F, P, P, P, Z, P],
         "masw_verify_workspace_bytes": [I, I, I, I, I, I, ctypes.POINTER(Z)],
         "masw_verify_attn_noalloc": [P, P, P, P, I, I, I, I, I, I, I, F, P, P, P],
@@ -165,6 +168,25 @@ def masw_draft_attn(handle, layer, q, o, lse=None, stream=None):
 
 def masw_full_attn(handle, layer, q, o, lse=None, stream=None):
     _check(load().masw_full_attn(handle, layer, _ptr(q), q.shape[1], _ptr(o), _ptr(lse), _stream(stream)), handle)
+
+
+def _active(active):
+    if active is None:
+        return None, None
+    arr = (ctypes.c_uint8 * len(active))(*[1 if a else 0 for a in active])
+    return arr, ctypes.cast(arr, ctypes.c_void_p)
+
+
+def masw_draft_step(handle, layer, q, k, v, o, lse=None, active=None, stream=None):
+    keep, act = _active(active)
+    _check(load().masw_draft_step(handle, layer, _ptr(q), _ptr(k), _ptr(v), act, q.shape[1], _ptr(o), _ptr(lse),
+                                  _stream(stream)), handle)
+
+
+def masw_full_step(handle, layer, q, k, v, o, lse=None, active=None, stream=None):
+    keep, act = _active(active)
+    _check(load().masw_full_step(handle, layer, _ptr(q), _ptr(k), _ptr(v), act, q.shape[1], _ptr(o), _ptr(lse),
+                                 _stream(stream)), handle)
 
 
 def masw_verify_workspace_bytes(B, Lq, Hq, Hkv, D, Tmax) -> int:

@@ -354,7 +354,7 @@ static int host_keys(const masw_mem_t* mem, int mode, int l, int b) {
 
 int masw_launch_decode(masw_mem_t* mem, int mode, int layer, const void* q, int n_q_heads, float* o,
                        float* lse, const int* seq_ids, int n_rows, const void* k_g, const void* v_g,
-                       cudaStream_t stream) {
+                       cudaStream_t stream, const unsigned* step_active) {
     const int G = n_q_heads / mem->Hkv;
     DecodeParams prm;
     std::memset(&prm, 0, sizeof(prm));
@@ -387,11 +387,15 @@ int masw_launch_decode(masw_mem_t* mem, int mode, int layer, const void* q, int 
     prm.Tmax = mem->max_seq_len;
     prm.M_max = mem->M_max;
     prm.self_attend = mem->self_attend;
+    if (step_active) {
+        prm.step = 1;
+        for (int i = 0; i < MASW_MAX_BATCH / 32; ++i) prm.active[i] = step_active[i];
+    }
     int kmax = 0;
     for (int i = 0; i < n_rows; ++i) {
         const int b = seq_ids ? seq_ids[i] : i;
         prm.seq_ids[i] = (short)b;
-        kmax = imax(kmax, host_keys(mem, mode, layer, b));
+        kmax = imax(kmax, host_keys(mem, mode, layer, b) + (step_active ? 1 : 0));
     }
     // split count: about three CTAs per SM in total, at least 64 keys per split,
     // and no more partials than the scratch holds

@@ -29,7 +29,7 @@ namespace masw {
 template <int D>
 struct MmaCfg {
     static constexpr int KPS = 64;               // keys per stage (16 per warp)
-    static constexpr int NST = 2;                // stages in flight
+    static constexpr int NST = 3;                // stages in flight
     static constexpr int CH = D / 8;             // 16-byte chunks per row
     static constexpr int ROWB = D * 2;           // bytes per bf16 row
     static constexpr int STAGE = 2 * KPS * ROWB; // K then V
@@ -53,13 +53,17 @@ __global__ void __launch_bounds__(128) decode_mma_kernel(const __grid_constant__
     __shared__ int s_start[6];
     __shared__ const uint8_t* s_vk[5];
     __shared__ const uint8_t* s_vv[5];
-    __shared__ int s_nseg, s_m_before;
+    __shared__ int s_nseg, s_m_before, s_t;
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int split = blockIdx.x, h = blockIdx.y, z = blockIdx.z;
     const int b = (p.mode == kDevModeSlot) ? (int)p.seq_ids[z] : z;
     const int lb = p.layer * p.B + b;
     const int G = p.Hq / p.Hkv;
+    if (tid == 0) {   // warm L2 with the counters while the previous kernel drains
+        asm volatile("prefetch.global.L2 [%0];" ::"l"(p.d_t + lb));
+        asm volatile("prefetch.global.L2 [%0];" ::"l"(p.d_m + lb));
+    }
     pdl_wait();
     pdl_trigger();
 
@@ -80,6 +84,7 @@ __global__ void __launch_bounds__(128) decode_mma_kernel(const __grid_constant__
         const int t = p.d_t[lb];
         const int mcnt = p.d_m[lb];
         s_m_before = mcnt;
+        s_t = t;
         const int n = build_segments<ROWB>(p, lb, h, z, t, mcnt, segs);
         int acc = 0;
         for (int s = 0; s < n; ++s) {
@@ -98,6 +103,8 @@ __global__ void __launch_bounds__(128) decode_mma_kernel(const __grid_constant__
     __syncthreads();
     const int nseg = s_nseg;
     const int total = s_start[nseg];
+    const bool fresh = p.step && ((p.active[z >> 5] >> (z & 31)) & 1u);
+    if (fresh && split == 0) step_store_row<ROWB>(p, lb, h, z, s_t);
     const int chunk = (((total + p.n_split - 1) / p.n_split) + 15) & ~15;
     const int r0 = imin(total, split * chunk);
     const int r1 = imin(total, r0 + chunk);
@@ -269,6 +276,7 @@ __global__ void __launch_bounds__(128) decode_mma_kernel(const __grid_constant__
     const bool final_cta =
         split_epilogue<D>(G, cm, cl, co, out, part, p.tickets + z * p.Hkv + h, split, p.n_split, scratch);
     if (p.mode == kDevModeSlot && final_cta) slot_append_tail<ROWB>(p, lb, z, s_m_before);
+    if (fresh && final_cta) step_count_tail(p, lb, z, s_t);
 }
 
 template <int D>

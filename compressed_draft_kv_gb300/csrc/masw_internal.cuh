@@ -312,9 +312,9 @@ struct DecodeParams {
     const void* pool_v;
     const void* full_k;   // [L][B][Hkv][Tmax][D]
     const void* full_v;
-    const void* k_g;      // slot mode: [rows][Hkv][D]
+    const void* k_g;      // slot mode: slot K/V [rows][Hkv][D]; step: new token K/V [B][Hkv][D]
     const void* v_g;
-    const int* d_t;
+    int* d_t;
     int* d_m;
     int* d_pos;
     int* d_err;
@@ -323,6 +323,8 @@ struct DecodeParams {
     unsigned* seq_tickets;
     float scale_log2;     // softmax scale * log2(e)
     int mode, layer, B, Hkv, Hq, S, W, Wc, C, Tmax, M_max, n_split, self_attend;
+    int step;             // 1: append the new token (k_g/v_g) of every active row first (fused step)
+    unsigned active[MASW_MAX_BATCH / 32];
     short seq_ids[MASW_MAX_BATCH];
 };
 
@@ -340,30 +342,79 @@ struct Seg {
 template <int ROWB>
 __device__ __forceinline__ int build_segments(const DecodeParams& p, int lb, int h, int z, int t, int mcnt,
                                               Seg* segs) {
+    // fused step: the query sees token t+1, whose K/V row comes straight from
+    // the caller's buffer; the pool holds tokens 1..t
+    const bool fresh = p.step && ((p.active[z >> 5] >> (z & 31)) & 1u);
+    const size_t new_off = ((size_t)z * p.Hkv + h) * ROWB;
     int n = 0;
     if (p.mode == kDevModeFull) {
         const size_t base = ((size_t)lb * p.Hkv + h) * (size_t)p.Tmax * ROWB;
         if (t > 0) segs[n++] = Seg{(const uint8_t*)p.full_k + base, (const uint8_t*)p.full_v + base, t};
+        if (fresh) segs[n++] = Seg{(const uint8_t*)p.k_g + new_off, (const uint8_t*)p.v_g + new_off, 1};
         return n;
     }
+    const int tq = fresh ? t + 1 : t;               // step the query sits at
     const size_t base = ((size_t)lb * p.Hkv + h) * (size_t)p.C * ROWB;
     const uint8_t* kb = (const uint8_t*)p.pool_k + base;
     const uint8_t* vb = (const uint8_t*)p.pool_v + base;
-    const int ns = imin(p.S, t);
+    const int ns = imin(p.S, t);                    // sink rows already in the pool
     if (ns > 0) segs[n++] = Seg{kb, vb, ns};
-    const int nl = n_local(t, p.S, p.W);
-    if (nl > 0) {
-        const int start = ring_row(window_lo(t, p.S, p.W), p.S, p.Wc);
-        const int first = imin(nl, p.Wc - start);
-        segs[n++] = Seg{kb + (size_t)(p.S + start) * ROWB, vb + (size_t)(p.S + start) * ROWB, first};
-        if (nl > first) segs[n++] = Seg{kb + (size_t)p.S * ROWB, vb + (size_t)p.S * ROWB, nl - first};
+    if (tq > p.S) {
+        const int lo = window_lo(tq, p.S, p.W);
+        const int nl = t - lo + 1;                  // window tokens already in the ring: lo..t
+        if (nl > 0) {
+            const int start = ring_row(lo, p.S, p.Wc);
+            const int first = imin(nl, p.Wc - start);
+            segs[n++] = Seg{kb + (size_t)(p.S + start) * ROWB, vb + (size_t)(p.S + start) * ROWB, first};
+            if (nl > first) segs[n++] = Seg{kb + (size_t)p.S * ROWB, vb + (size_t)p.S * ROWB, nl - first};
+        }
     }
     if (mcnt > 0) segs[n++] = Seg{kb + (size_t)(p.S + p.Wc) * ROWB, vb + (size_t)(p.S + p.Wc) * ROWB, mcnt};
+    if (fresh) segs[n++] = Seg{(const uint8_t*)p.k_g + new_off, (const uint8_t*)p.v_g + new_off, 1};
     if (p.mode == kDevModeSlot && p.self_attend) {
         const size_t off = ((size_t)z * p.Hkv + h) * ROWB;
         segs[n++] = Seg{(const uint8_t*)p.k_g + off, (const uint8_t*)p.v_g + off, 1};
     }
     return n;
+}
+
+// Fused step, split 0 of each (row, head): store the new token's K/V row of
+// head h in its sink or ring row (the ring write evicts token t+1-W-R, which no
+// CTA of this launch reads) and in the full-KV cache.
+template <int ROWB>
+__device__ void step_store_row(const DecodeParams& p, int lb, int h, int z, int t) {
+    const int i = t + 1;
+    const int row = i <= p.S ? i - 1 : p.S + ring_row(i, p.S, p.Wc);
+    const size_t src = ((size_t)z * p.Hkv + h) * ROWB;
+    const size_t dst = (((size_t)lb * p.Hkv + h) * p.C + row) * ROWB;
+    const bool to_full = p.full_k != nullptr && i <= p.Tmax;
+    const size_t fdst = (((size_t)lb * p.Hkv + h) * p.Tmax + (i - 1)) * (size_t)ROWB;
+    for (int c = threadIdx.x; c < ROWB / 16; c += blockDim.x) {
+        const uint4 kv = *reinterpret_cast<const uint4*>((const uint8_t*)p.k_g + src + c * 16);
+        const uint4 vv = *reinterpret_cast<const uint4*>((const uint8_t*)p.v_g + src + c * 16);
+        *reinterpret_cast<uint4*>((uint8_t*)p.pool_k + dst + c * 16) = kv;
+        *reinterpret_cast<uint4*>((uint8_t*)p.pool_v + dst + c * 16) = vv;
+        if (to_full) {
+            *reinterpret_cast<uint4*>((uint8_t*)p.full_k + fdst + c * 16) = kv;
+            *reinterpret_cast<uint4*>((uint8_t*)p.full_v + fdst + c * 16) = vv;
+        }
+    }
+}
+
+// Fused step, after the attention of every (row z, head) pair is final: the
+// last pair of the row bumps the token counter (every CTA of the row has read
+// the old value by then).
+__device__ inline void step_count_tail(const DecodeParams& p, int lb, int z, int t) {
+    __shared__ unsigned s_last_head;
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) s_last_head = atomicAdd(p.seq_tickets + z, 1u) == (unsigned)(p.Hkv - 1);
+    __syncthreads();
+    if (s_last_head && threadIdx.x == 0) {
+        if (p.full_k != nullptr && t + 1 > p.Tmax) atomicExch(p.d_err + 1, MASW_ECAPACITY);
+        p.d_t[lb] = t + 1;
+        p.seq_tickets[z] = 0u;
+    }
 }
 
 // Slot write, after the attention of every (row z, head) pair is final: the
@@ -439,7 +490,7 @@ cudaError_t masw_launch(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t sm
 enum DecodeMode { kModeDraft = 0, kModeFull = 1, kModeSlot = 2 };
 int masw_launch_decode(masw_mem_t* mem, int mode, int layer, const void* q, int n_q_heads, float* o,
                        float* lse, const int* seq_ids, int n_rows, const void* k_g, const void* v_g,
-                       cudaStream_t stream);
+                       cudaStream_t stream, const unsigned* step_active = nullptr);
 // floats of split scratch one decode launch with these sizes may use
 size_t masw_decode_part_floats(int rows, int Hkv, int G, int D, int n_split);
 // tensor-core decode for bf16 pools (masw_decode_mma.cu)

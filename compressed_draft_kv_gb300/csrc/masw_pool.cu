@@ -444,6 +444,52 @@ int masw_full_attn(masw_mem_t* mem, int layer, const void* q, int n_q_heads, flo
     return attn_common(mem, kModeFull, layer, q, n_q_heads, o, lse, stream);
 }
 
+static int step_common(masw_mem_t* mem, int mode, int layer, const void* q, const void* k, const void* v,
+                       const uint8_t* active, int n_q_heads, float* o, float* lse, masw_stream_t stream) {
+    if (!mem) return masw_set_error(nullptr, MASW_EINVAL, "step: NULL handle");
+    try {
+        if (int rc = check_layer(mem, layer)) return rc;
+        if (int rc = check_heads(mem, n_q_heads)) return rc;
+        if (!q || !o || !k || !v || !aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned4(o) || !aligned4(lse))
+            return masw_set_error(mem, MASW_EINVAL, "step: bad pointer (NULL or misaligned)");
+        if (mode == kModeFull && !mem->full_kv)
+            return masw_set_error(mem, MASW_ESTATE, "full_step: pool was created without full_kv");
+        if (mem->dtype != MASW_BF16) {
+            // fp32 pools: the same two steps as separate launches
+            int rc = masw_append_kv(mem, layer, k, v, active, stream);
+            if (rc) return rc;
+            return attn_common(mem, mode, layer, q, n_q_heads, o, lse, stream);
+        }
+        unsigned bits[MASW_MAX_BATCH / 32] = {0};
+        for (int b = 0; b < mem->B; ++b) {
+            if (active && !active[b]) continue;
+            if (mem->h_t[(size_t)layer * mem->B + b] + 1 > mem->max_seq_len)
+                return masw_set_error(mem, MASW_ECAPACITY, "step: sequence would exceed max_seq_len");
+            bits[b >> 5] |= 1u << (b & 31);
+        }
+        int rc = masw_launch_decode(mem, mode, layer, q, n_q_heads, o, lse, nullptr, mem->B, k, v,
+                                    (cudaStream_t)stream, bits);
+        if (rc) return rc;
+        for (int b = 0; b < mem->B; ++b)
+            if (!active || active[b]) mem->h_t[(size_t)layer * mem->B + b] += 1;
+        return MASW_OK;
+    } catch (const std::exception& e) {
+        return masw_set_error(mem, MASW_EINVAL, e.what());
+    } catch (...) {
+        return masw_set_error(mem, MASW_EINVAL, "step: unexpected error");
+    }
+}
+
+int masw_draft_step(masw_mem_t* mem, int layer, const void* q, const void* k, const void* v, const uint8_t* active,
+                    int n_q_heads, float* o, float* lse, masw_stream_t stream) {
+    return step_common(mem, kModeDraft, layer, q, k, v, active, n_q_heads, o, lse, stream);
+}
+
+int masw_full_step(masw_mem_t* mem, int layer, const void* q, const void* k, const void* v, const uint8_t* active,
+                   int n_q_heads, float* o, float* lse, masw_stream_t stream) {
+    return step_common(mem, kModeFull, layer, q, k, v, active, n_q_heads, o, lse, stream);
+}
+
 int masw_mem_load(masw_mem_t* mem, int layer, int seq, int t, const void* k_raw, const void* v_raw,
                   const void* k_slots, const void* v_slots, int n_slots) {
     if (!mem) return masw_set_error(nullptr, MASW_EINVAL, "load: NULL handle");

@@ -174,6 +174,25 @@ int masw_draft_attn(masw_mem_t* mem, int layer, const void* q, int n_q_heads,
 int masw_full_attn(masw_mem_t* mem, int layer, const void* q, int n_q_heads,
                    float* o, float* lse, masw_stream_t stream);
 
+/* One draft decode step of `layer` in a single launch: masw_append_kv followed
+ * by masw_draft_attn ([EN] §3.3 Algorithm 2 step 4 -- the new token joins the
+ * window, evicting the oldest, and the query at t+1 attends over M_{t+1}).
+ * k, v: device [batch, Hkv, D] (the new token); q: device [batch, n_q_heads, D];
+ * o, lse as in masw_draft_attn; active as in masw_append_kv (inactive
+ * sequences are not appended and their query sees M_t).  The new row is read
+ * straight from k/v by the attention and stored in the pool by the same launch.
+ * Results equal the two separate calls up to fp32 summation order.  fp32
+ * pools run the two calls as two launches. */
+int masw_draft_step(masw_mem_t* mem, int layer, const void* q, const void* k, const void* v,
+                    const uint8_t* active, int n_q_heads, float* o, float* lse,
+                    masw_stream_t stream);
+
+/* The same fused step for the full-KV contrast: masw_append_kv followed by
+ * masw_full_attn.  ESTATE unless the pool was created with full_kv = 1. */
+int masw_full_step(masw_mem_t* mem, int layer, const void* q, const void* k, const void* v,
+                   const uint8_t* active, int n_q_heads, float* o, float* lse,
+                   masw_stream_t stream);
+
 /* Target verify attention ([EN] §3.3 Algorithm 2 step 5), stateless: Lq query
  * positions per sequence against an uncompressed cache, causal inside the
  * block.  Query j (0-based) of sequence b sees keys 0 .. kv_len[b]-Lq+j

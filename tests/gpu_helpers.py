@@ -90,6 +90,23 @@ class Pair:
             assert_close(lse, want_l, self.dtype, f"{'full' if full else 'draft'} LSE l={layer}")
         return o, lse, want, want_l
 
+    def fstep(self, layer, active=None, full=False, check=True):
+        """Fused append + attention (masw_draft_step / masw_full_step)."""
+        k = self.rand((self.batch, self.Hkv, self.D), "k", layer)
+        v = self.rand((self.batch, self.Hkv, self.D), "v", layer)
+        q = self.rand((self.batch, self.Hq, self.D), "q", layer)
+        o = torch.empty(self.batch, self.Hq, self.D, device=DEV)
+        lse = torch.empty(self.batch, self.Hq, device=DEV)
+        fn = capi.masw_full_step if full else capi.masw_draft_step
+        fn(self.h, layer, q.to(DEV), k.to(DEV), v.to(DEV), o, lse, active=active)
+        self.ref.append(layer, k.float().numpy(), v.float().numpy(), active=active)
+        want, want_l = (self.ref.full_attn if full else self.ref.draft_attn)(layer, q.float().numpy())
+        if check:
+            capi.masw_sync(self.h)
+            assert_close(o, want, self.dtype, f"{'full' if full else 'draft'} step O l={layer} step={self.step}")
+            assert_close(lse, want_l, self.dtype, "step LSE")
+        return o
+
     def materialize(self, layer, seqs):
         n = len(seqs)
         qg = self.rand((n, self.Hq, self.D), "qg", layer)

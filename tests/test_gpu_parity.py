@@ -239,6 +239,47 @@ def test_rollback_restores_state_and_refuses_too_deep():
         p.close()
 
 
+@pytest.mark.parametrize("dtype,D,G", [("bf16", 128, 3), ("bf16", 64, 4), ("f32", 64, 2)])
+def test_fused_step_from_empty_through_boundaries(dtype, D, G):
+    """masw_draft_step (append + attention in one launch for bf16 pools) from
+    t = 0: the sink phase, window growth, ring wrap with a rollback reserve,
+    several boundaries with slot writes, a ragged active mask; the full-KV
+    step alongside."""
+    S, W, r, R, Hkv = 3, 20, 6, 4, 2
+    p = Pair(S, W, r, Hkv, D, 2, 3, dtype, G * Hkv, max_seq_len=128, full_kv=True, reserve=R, tag="fstep")
+    try:
+        for step in range(1, 70):
+            p.step = step
+            active = [1, 1 if step % 3 else 0, 1 if step > 10 else 0]
+            for l in range(2):
+                p.fstep(l, active=active)
+                due = [b for b in range(3) if orc.is_boundary(p.ref.t(l, b), S, W, r)
+                       and p.ref.m(l, b) == orc.slot_count(p.ref.t(l, b), S, W, r) - 1]
+                if due:
+                    p.materialize(l, due)
+            if step % 9 == 0:
+                p.draft(0, full=True)
+        for l in range(2):
+            for b in range(3):
+                p.check_state(l, b)
+    finally:
+        p.close()
+
+
+def test_fused_full_step():
+    p = Pair(4, 16, 8, 2, 128, 1, 2, "bf16", 8, max_seq_len=300, full_kv=True, tag="ffull")
+    try:
+        p.load(0, 0, 150, seed=1)
+        p.load(0, 1, 7, seed=2)
+        for step in range(12):
+            p.step = step
+            p.fstep(0, full=True)
+        p.check_state(0, 0)
+        p.check_state(0, 1)
+    finally:
+        p.close()
+
+
 def test_state_errors():
     p = Pair(2, 8, 4, 2, 64, 1, 1, "f32", 4, max_seq_len=18, tag="err")
     try:
