@@ -163,16 +163,16 @@ class DraftBench:
                 self.bstep = s
         self.stream = torch.cuda.Stream(device=self.dev)
 
-    # one speculative iteration through the C-ABI
+    # one speculative iteration through the C-ABI: per step and layer one fused
+    # append + attention launch, slot writes at the boundary step, rollback
     def iteration(self, full: bool = False):
         c = self.capi
-        attn = c.masw_full_attn if full else c.masw_draft_attn
+        step = c.masw_full_step if full else c.masw_draft_step
         launches = 0
         for s in range(self.steps):
             for l in range(self.L):
-                c.masw_append_kv(self.h, l, self.k[s][l], self.v[s][l])
-                attn(self.h, l, self.q[s][l], self.o[s][l], self.lse[s][l])
-                launches += 2
+                step(self.h, l, self.q[s][l], self.k[s][l], self.v[s][l], self.o[s][l], self.lse[s][l])
+                launches += 1
                 if s == self.bstep and not full:
                     c.masw_materialize_slot(self.h, l, self.seqs, self.qg[l], self.kg[l], self.vg[l], self.og[l])
                     launches += 1
@@ -212,34 +212,33 @@ class DraftBench:
         return e0.elapsed_time(e1) / 1e3
 
     def algorithmic_bytes_per_draft_launch(self):
-        """K/V entries of one layer's working set at t = prefix+1 (the first
-        step's attention) x 4096 B, plus Q (bf16), O and LSE (fp32)."""
+        """One fused draft step of one layer at t = prefix+1: the working set
+        (sink + window + slots, K and V, 4096 B per entry for 8 kv heads x 128
+        bf16) of every sequence, plus Q (bf16), the new token's K/V (read once,
+        written to the pool and to the full-KV cache) and O, LSE (fp32)."""
         t = self.prefix + 1
         nloc = max(0, min(self.W, t - self.S))
         m = max(0, (t - self.S - self.W) // self.r)
         E = 2 * self.Hkv * self.D * 2
         kv = self.B * (min(self.S, t) + nloc + m) * E
-        qo = self.B * self.Hq * self.D * (2 + 4) + self.B * self.Hq * 4
-        return kv + qo, kv, qo
+        other = self.B * self.Hq * self.D * 2 + self.B * E * 3 + self.B * self.Hq * (self.D + 1) * 4
+        return kv + other, kv, other
 
     def time_draft_kernel(self, reps: int):
-        """Average duration of one masw_draft_attn launch, timed with CUDA
-        events on the launching stream over `reps` replays of a graph holding
-        the 28 per-layer launches of one decode step (state fixed at t=prefix+1)."""
+        """Average duration of one fused masw_draft_step launch, timed with
+        CUDA events on the launching stream over `reps` replays of a graph of
+        the 28 per-layer launches of one decode step followed by the one-token
+        rollback that restores the state (counted against the step launches)."""
         torch, c = self.torch, self.capi
-        with torch.cuda.stream(self.stream):
-            for l in range(self.L):
-                c.masw_append_kv(self.h, l, self.k[0][l], self.v[0][l])
 
         def step():
             for l in range(self.L):
-                c.masw_draft_attn(self.h, l, self.q[0][l], self.o[0][l], self.lse[0][l])
+                c.masw_draft_step(self.h, l, self.q[0][l], self.k[0][l], self.v[0][l], self.o[0][l],
+                                  self.lse[0][l])
+            c.masw_rollback(self.h, self.seqs, [self.prefix] * self.B)
             return self.L
         g, n = self.capture(step)
         secs = self.time_graph(g, 3, reps)
-        with torch.cuda.stream(self.stream):
-            c.masw_rollback(self.h, self.seqs, [self.prefix] * self.B)
-        torch.cuda.synchronize()
         return secs / (reps * n), n * reps
 
     def e2e(self, iters: int):
@@ -270,8 +269,7 @@ class DraftBench:
                     dk.copy_(hk[s][l], non_blocking=True)
                     dv.copy_(hv[s][l], non_blocking=True)
                     h2d += dq.numel() * 2 + dk.numel() * 2 + dv.numel() * 2
-                    c.masw_append_kv(self.h, l, dk, dv)
-                    c.masw_draft_attn(self.h, l, dq, do)
+                    c.masw_draft_step(self.h, l, dq, dk, dv, do)
                     ho[s][l].copy_(do, non_blocking=True)
                     d2h += do.numel() * 4
                     if s == self.bstep:
@@ -481,7 +479,7 @@ def main():
         "speedup_vs_full_kv": value / full_value,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": None, "peak_kind": peak_kind,
-                     "kernel": "decode_kernel<bf16,128,3> (masw_draft_attn)",
+                     "kernel": "decode_mma_kernel<128> (masw_draft_step: fused append + draft attention)",
                      "bytes_per_launch": total_b, "kv_bytes_per_launch": kv_b,
                      "us_per_launch": kern_s * 1e6},
         "gpu_launches": launches * args.steps,
