@@ -22,7 +22,10 @@
 // never gathered in HBM.  Split partials are merged by split_epilogue.
 #include "masw_internal.cuh"
 
+#include <cooperative_groups.h>
 #include <cstring>
+
+namespace cg = cooperative_groups;
 
 namespace masw {
 
@@ -264,6 +267,53 @@ __global__ void __launch_bounds__(128) decode_mma_kernel(const __grid_constant__
     }
     __syncthreads();
 
+    if (p.cluster) {
+        // The n_split CTAs of this (row, head) pair form one thread-block
+        // cluster: merge their (m, l, o) through distributed shared memory.
+        cg::cluster_group cluster = cg::this_cluster();
+        cluster.sync();                               // every CTA's cm/cl/co is final
+        const int nc = (int)cluster.num_blocks(), rank = (int)cluster.block_rank();
+        float* w = scratch;                           // [8][8] weights of rank r for row n
+        float* den = w + 64;                          // [8]
+        float* Mx = den + 8;                          // [8]
+        if (tid < G) {
+            float M = -INFINITY;
+            for (int r = 0; r < nc; ++r) M = fmaxf(M, *cluster.map_shared_rank(cm + tid, r));
+            float dn = 0.f;
+            for (int r = 0; r < nc; ++r) {
+                const float mr = *cluster.map_shared_rank(cm + tid, r);
+                const float wr = mr == -INFINITY ? 0.f : exp2f(mr - M);
+                w[tid * 8 + r] = wr;
+                dn += wr * *cluster.map_shared_rank(cl + tid, r);
+            }
+            den[tid] = dn;
+            Mx[tid] = M;
+        }
+        __syncthreads();
+        const int per = (G * D + nc - 1) / nc;
+        const int lo = rank * per, hi = imin(G * D, lo + per);
+        for (int i = lo + tid; i < hi; i += 128) {
+            const int n = i / D;
+            float a = 0.f;
+            for (int r = 0; r < nc; ++r) {
+                const float wr = w[n * 8 + r];
+                if (wr != 0.f) a += wr * *cluster.map_shared_rank(co + i, r);
+            }
+            const float dn = den[n];
+            p.o[((size_t)z * p.Hq + (size_t)h * G + n) * D + (i % D)] = dn > 0.f ? a / dn : 0.f;
+        }
+        if (rank == 0 && p.lse && tid < G) {
+            const float dn = den[tid];
+            p.lse[(size_t)z * p.Hq + (size_t)h * G + tid] =
+                dn > 0.f ? (Mx[tid] + __log2f(dn)) * 0.6931471805599453f : -INFINITY;
+        }
+        cluster.sync();                               // peers' shared memory stays alive until here
+        if (rank == 0) {
+            if (p.mode == kDevModeSlot) slot_append_tail<ROWB>(p, lb, z, s_m_before);
+            if (fresh) step_count_tail(p, lb, z, s_t);
+        }
+        return;
+    }
     EpiOut out;
     out.o = p.o + ((size_t)z * p.Hq + (size_t)h * G) * D;
     out.lse = p.lse ? p.lse + (size_t)z * p.Hq + (size_t)h * G : nullptr;
@@ -279,6 +329,34 @@ __global__ void __launch_bounds__(128) decode_mma_kernel(const __grid_constant__
     if (fresh && final_cta) step_count_tail(p, lb, z, s_t);
 }
 
+// Clusters of `cs` CTAs of the decode kernel that can be resident at once (cached per device).
+template <int D>
+static int max_clusters(masw_mem_t* mem, int dev, int cs) {
+    static int cache[64][9] = {};
+    if (cs < 2 || cs > 8) return 0;
+    if (!cache[dev][cs]) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(cs * 64, 1, 1);
+        cfg.blockDim = dim3(128, 1, 1);
+        cfg.dynamicSmemBytes = MmaCfg<D>::SMEM;
+        cudaLaunchAttribute a;
+        a.id = cudaLaunchAttributeClusterDimension;
+        a.val.clusterDim.x = cs;
+        a.val.clusterDim.y = 1;
+        a.val.clusterDim.z = 1;
+        cfg.attrs = &a;
+        cfg.numAttrs = 1;
+        int n = 0;
+        if (cudaOccupancyMaxActiveClusters(&n, decode_mma_kernel<D>, &cfg) != cudaSuccess) {
+            cudaGetLastError();
+            n = 0;
+        }
+        cache[dev][cs] = n > 0 ? n : -1;
+    }
+    (void)mem;
+    return cache[dev][cs];
+}
+
 template <int D>
 static int launch_mma(masw_mem_t* mem, DecodeParams& prm, int G, int rows, int kmax, cudaStream_t stream) {
     using C = MmaCfg<D>;
@@ -291,16 +369,32 @@ static int launch_mma(masw_mem_t* mem, DecodeParams& prm, int G, int rows, int k
         MASW_CUDA_TRY(mem, cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_mma_kernel<D>, 128, C::SMEM));
         occ[dev] = n > 0 ? n : 1;
     }
-    // one wave: as many splits as fit the resident CTA slots, at least 64 keys each
+    // One wave.  Splits of a pair are merged inside a thread-block cluster
+    // (distributed shared memory, no global round trip) when clusters of that
+    // size can all be resident at once; otherwise (few pairs, many splits) the
+    // ticketed global merge is used.
     const int pairs = rows * mem->Hkv;
     const int slots = occ[dev] * mem->num_sms;
-    int n_split = imax(1, slots / pairs);
-    n_split = imin(n_split, imax(1, (kmax + 63) / 64));
-    n_split = imin(n_split, kMaxSplit);
-    while (n_split > 1 && masw_decode_part_floats(rows, mem->Hkv, G, D, n_split) > mem->part_floats) --n_split;
+    const int max_useful = imax(1, (kmax + 63) / 64);
+    int n_split = 1;
+    bool cluster = false;
+    for (int cs = imin(8, imin(max_useful, slots / imax(1, pairs))); cs >= 2; --cs) {
+        if (cs * pairs * 2 >= slots && max_clusters<D>(mem, dev, cs) >= pairs) {
+            n_split = cs;
+            cluster = true;
+            break;
+        }
+    }
+    if (!cluster) {
+        n_split = imax(1, slots / pairs);
+        n_split = imin(n_split, max_useful);
+        n_split = imin(n_split, kMaxSplit);
+        while (n_split > 1 && masw_decode_part_floats(rows, mem->Hkv, G, D, n_split) > mem->part_floats) --n_split;
+    }
     prm.n_split = n_split;
+    prm.cluster = cluster ? 1 : 0;
     MASW_CUDA_TRY(mem, masw_launch(decode_mma_kernel<D>, dim3(n_split, mem->Hkv, rows), dim3(128), C::SMEM, stream,
-                                   1, prm));
+                                   cluster ? n_split : 1, prm));
     return MASW_OK;
 }
 

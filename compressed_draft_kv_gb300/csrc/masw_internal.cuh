@@ -324,6 +324,7 @@ struct DecodeParams {
     float scale_log2;     // softmax scale * log2(e)
     int mode, layer, B, Hkv, Hq, S, W, Wc, C, Tmax, M_max, n_split, self_attend;
     int step;             // 1: append the new token (k_g/v_g) of every active row first (fused step)
+    int cluster;          // 1: the n_split CTAs of a pair form a cluster and merge in shared memory
     unsigned active[MASW_MAX_BATCH / 32];
     short seq_ids[MASW_MAX_BATCH];
 };
