@@ -164,18 +164,24 @@ class DraftBench:
         self.stream = torch.cuda.Stream(device=self.dev)
 
     # one speculative iteration through the C-ABI: per step and layer one fused
-    # append + attention launch, slot writes at the boundary step, rollback
+    # append + attention launch (at the boundary step also carrying every
+    # sequence's slot write), then the rollback of the 5 speculative tokens
     def iteration(self, full: bool = False):
         c = self.capi
-        step = c.masw_full_step if full else c.masw_draft_step
         launches = 0
         for s in range(self.steps):
             for l in range(self.L):
-                step(self.h, l, self.q[s][l], self.k[s][l], self.v[s][l], self.o[s][l], self.lse[s][l])
+                if full:
+                    c.masw_full_step(self.h, l, self.q[s][l], self.k[s][l], self.v[s][l], self.o[s][l],
+                                     self.lse[s][l])
+                elif s == self.bstep:
+                    c.masw_draft_step_slot(self.h, l, self.q[s][l], self.k[s][l], self.v[s][l], self.o[s][l],
+                                           self.seqs, self.qg[l], self.kg[l], self.vg[l], self.og[l],
+                                           lse=self.lse[s][l])
+                else:
+                    c.masw_draft_step(self.h, l, self.q[s][l], self.k[s][l], self.v[s][l], self.o[s][l],
+                                      self.lse[s][l])
                 launches += 1
-                if s == self.bstep and not full:
-                    c.masw_materialize_slot(self.h, l, self.seqs, self.qg[l], self.kg[l], self.vg[l], self.og[l])
-                    launches += 1
         c.masw_rollback(self.h, self.seqs, [self.prefix] * self.B)
         return launches + 1
 
@@ -258,6 +264,7 @@ class DraftBench:
         dv = torch.empty_like(self.v[0][0])
         dqg, dkg, dvg = torch.empty_like(self.qg[0]), torch.empty_like(self.kg[0]), torch.empty_like(self.vg[0])
         do = torch.empty(self.B, self.Hq, self.D, device=self.dev)
+        dog = torch.empty(self.B, self.Hq, self.D, device=self.dev)
         h2d = d2h = 0
 
         def run():
@@ -269,17 +276,18 @@ class DraftBench:
                     dk.copy_(hk[s][l], non_blocking=True)
                     dv.copy_(hv[s][l], non_blocking=True)
                     h2d += dq.numel() * 2 + dk.numel() * 2 + dv.numel() * 2
-                    c.masw_draft_step(self.h, l, dq, dk, dv, do)
-                    ho[s][l].copy_(do, non_blocking=True)
-                    d2h += do.numel() * 4
                     if s == self.bstep:
                         dqg.copy_(hqg[l], non_blocking=True)
                         dkg.copy_(hkg[l], non_blocking=True)
                         dvg.copy_(hvg[l], non_blocking=True)
                         h2d += (dqg.numel() + dkg.numel() + dvg.numel()) * 2
-                        c.masw_materialize_slot(self.h, l, self.seqs, dqg, dkg, dvg, do)
-                        hog[l].copy_(do, non_blocking=True)
-                        d2h += do.numel() * 4
+                        c.masw_draft_step_slot(self.h, l, dq, dk, dv, do, self.seqs, dqg, dkg, dvg, dog)
+                        hog[l].copy_(dog, non_blocking=True)
+                        d2h += dog.numel() * 4
+                    else:
+                        c.masw_draft_step(self.h, l, dq, dk, dv, do)
+                    ho[s][l].copy_(do, non_blocking=True)
+                    d2h += do.numel() * 4
             c.masw_rollback(self.h, self.seqs, [self.prefix] * self.B)
             torch.cuda.current_stream().synchronize()
 

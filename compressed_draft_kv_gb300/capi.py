@@ -21,7 +21,7 @@ MASW_MAX_BATCH, MASW_MAX_GROUP = 512, 8
 EXPORTS = [
     "masw_mem_create", "masw_mem_destroy", "masw_last_error", "masw_append_kv",
     "masw_materialize_slot", "masw_rollback", "masw_draft_attn", "masw_full_attn",
-    "masw_draft_step", "masw_full_step",
+    "masw_draft_step", "masw_full_step", "masw_draft_step_slot",
     "masw_verify_attn", "masw_verify_workspace_bytes", "masw_verify_attn_noalloc", "masw_mem_load", "masw_mem_export",
     "masw_query", "masw_sync", "masw_index", "masw_version",
 ]
@@ -67,6 +67,7 @@ def load() -> ctypes.CDLL:
         "masw_full_attn": [P, I, P, I, P, P, P],
         "masw_draft_step": [P, I, P, P, P, P, I, P, P, P],
         "masw_full_step": [P, I, P, P, P, P, I, P, P, P],
+        "masw_draft_step_slot": [P, I, P, P, P, P, I, P, P, IP, I, P, P, P, P, P, P],
         "masw_verify_attn": [P, P, P, P, I, I, I, I, I, I, I, F, P, P, P, Z, P],
         "masw_verify_workspace_bytes": [I, I, I, I, I, I, ctypes.POINTER(Z)],
         "masw_verify_attn_noalloc": [P, P, P, P, I, I, I, I, I, I, I, F, P, P, P],
@@ -187,6 +188,15 @@ def masw_full_step(handle, layer, q, k, v, o, lse=None, active=None, stream=None
     keep, act = _active(active)
     _check(load().masw_full_step(handle, layer, _ptr(q), _ptr(k), _ptr(v), act, q.shape[1], _ptr(o), _ptr(lse),
                                  _stream(stream)), handle)
+
+
+def masw_draft_step_slot(handle, layer, q, k, v, o, seq_ids, q_g, k_g, v_g, o_g, lse=None, lse_g=None,
+                         active=None, stream=None):
+    keep, act = _active(active)
+    ids, n = _int_array(seq_ids)
+    _check(load().masw_draft_step_slot(handle, layer, _ptr(q), _ptr(k), _ptr(v), act, q.shape[1], _ptr(o), _ptr(lse),
+                                       ids, n, _ptr(q_g), _ptr(k_g), _ptr(v_g), _ptr(o_g), _ptr(lse_g),
+                                       _stream(stream)), handle)
 
 
 def masw_verify_workspace_bytes(B, Lq, Hq, Hkv, D, Tmax) -> int:

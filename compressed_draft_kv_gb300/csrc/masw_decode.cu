@@ -297,6 +297,9 @@ decode_kernel(const __grid_constant__ DecodeParams p) {
     out.o_group_stride = 0;
     out.lse_row_stride = 1;
     out.lse_group_stride = 0;
+    out.o_alt = nullptr;
+    out.lse_alt = nullptr;
+    out.alt_from = -1;
     float* part = p.part + (size_t)(z * p.Hkv + h) * p.n_split * G * (D + 2);
     const bool final_cta = split_epilogue<D>(G, cm, cl, co, out, part, p.tickets + z * p.Hkv + h, split,
                                              p.n_split, scratch);
@@ -354,7 +357,7 @@ static int host_keys(const masw_mem_t* mem, int mode, int l, int b) {
 
 int masw_launch_decode(masw_mem_t* mem, int mode, int layer, const void* q, int n_q_heads, float* o,
                        float* lse, const int* seq_ids, int n_rows, const void* k_g, const void* v_g,
-                       cudaStream_t stream, const unsigned* step_active) {
+                       cudaStream_t stream, const unsigned* step_active, const SlotFuse* fuse) {
     const int G = n_q_heads / mem->Hkv;
     DecodeParams prm;
     std::memset(&prm, 0, sizeof(prm));
@@ -390,6 +393,16 @@ int masw_launch_decode(masw_mem_t* mem, int mode, int layer, const void* q, int 
     if (step_active) {
         prm.step = 1;
         for (int i = 0; i < MASW_MAX_BATCH / 32; ++i) prm.active[i] = step_active[i];
+    }
+    prm.rows_per_pair = G;
+    for (int i = 0; i < MASW_MAX_BATCH; ++i) prm.slot_of[i] = -1;
+    if (fuse) {
+        prm.q_slot = fuse->q_g;
+        prm.k_slot = fuse->k_g;
+        prm.v_slot = fuse->v_g;
+        prm.o_slot = fuse->o_g;
+        prm.lse_slot = fuse->lse_g;
+        for (int i = 0; i < fuse->n; ++i) prm.slot_of[fuse->seq_ids[i]] = (short)i;
     }
     int kmax = 0;
     for (int i = 0; i < n_rows; ++i) {

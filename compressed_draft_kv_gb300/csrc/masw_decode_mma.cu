@@ -63,6 +63,8 @@ __global__ void __launch_bounds__(128) decode_mma_kernel(const __grid_constant__
     const int b = (p.mode == kDevModeSlot) ? (int)p.seq_ids[z] : z;
     const int lb = p.layer * p.B + b;
     const int G = p.Hq / p.Hkv;
+    const int si = p.q_slot ? (int)p.slot_of[z] : -1;   // fused slot query of this row, if any
+    const int NR = si >= 0 ? 2 * G : G;                  // query columns of this pair
     if (tid == 0) {   // warm L2 with the counters while the previous kernel drains
         asm volatile("prefetch.global.L2 [%0];" ::"l"(p.d_t + lb));
         asm volatile("prefetch.global.L2 [%0];" ::"l"(p.d_m + lb));
@@ -70,12 +72,16 @@ __global__ void __launch_bounds__(128) decode_mma_kernel(const __grid_constant__
     pdl_wait();
     pdl_trigger();
 
-    // Q^T as B fragments: column n = query head h*G + n of row z (zero when n >= G)
+    // Q^T as B fragments: column n < G is query head h*G + n of row z; columns
+    // G..2G-1 are the fused slot query's heads; the rest are zero
     uint32_t qb[KS][2];
     {
         const int n = lane >> 2;
-        const bool real = n < G;
-        const __nv_bfloat16* qrow = (const __nv_bfloat16*)p.q + ((size_t)z * p.Hq + (size_t)h * G + (real ? n : 0)) * D;
+        const bool real = n < NR;
+        const __nv_bfloat16* qrow =
+            n < G ? (const __nv_bfloat16*)p.q + ((size_t)z * p.Hq + (size_t)h * G + n) * D
+                  : (real ? (const __nv_bfloat16*)p.q_slot + ((size_t)si * p.Hq + (size_t)h * G + (n - G)) * D
+                          : (const __nv_bfloat16*)p.q);
 #pragma unroll
         for (int ks = 0; ks < KS; ++ks) {
             const int d = ks * 16 + (lane & 3) * 2;
@@ -247,7 +253,7 @@ __global__ void __launch_bounds__(128) decode_mma_kernel(const __grid_constant__
         }
     }
     __syncthreads();
-    if (tid < G) {
+    if (tid < NR) {
         float M = -INFINITY;
         for (int w = 0; w < 4; ++w) M = fmaxf(M, wm[w * 8 + tid]);
         float l = 0.f;
@@ -257,7 +263,7 @@ __global__ void __launch_bounds__(128) decode_mma_kernel(const __grid_constant__
         cl[tid] = l;
     }
     __syncthreads();
-    for (int i = tid; i < G * D; i += 128) {
+    for (int i = tid; i < NR * D; i += 128) {
         const int n = i / D;
         const float M = cm[n];
         float a = 0.f;
@@ -267,6 +273,19 @@ __global__ void __launch_bounds__(128) decode_mma_kernel(const __grid_constant__
     }
     __syncthreads();
 
+    // rows 0..G-1 -> O of row z; rows G..2G-1 (fused slot query) -> O_g of slot row si
+    EpiOut out;
+    out.o = p.o + ((size_t)z * p.Hq + (size_t)h * G) * D;
+    out.lse = p.lse ? p.lse + (size_t)z * p.Hq + (size_t)h * G : nullptr;
+    out.rows_per_group = NR;
+    out.o_row_stride = D;
+    out.o_group_stride = 0;
+    out.lse_row_stride = 1;
+    out.lse_group_stride = 0;
+    out.o_alt = si >= 0 ? p.o_slot + ((size_t)si * p.Hq + (size_t)h * G) * D : nullptr;
+    out.lse_alt = (si >= 0 && p.lse_slot) ? p.lse_slot + (size_t)si * p.Hq + (size_t)h * G : nullptr;
+    out.alt_from = si >= 0 ? G : -1;
+    bool final_cta;
     if (p.cluster) {
         // The n_split CTAs of this (row, head) pair form one thread-block
         // cluster: merge their (m, l, o) through distributed shared memory.
@@ -276,7 +295,7 @@ __global__ void __launch_bounds__(128) decode_mma_kernel(const __grid_constant__
         float* w = scratch;                           // [8][8] weights of rank r for row n
         float* den = w + 64;                          // [8]
         float* Mx = den + 8;                          // [8]
-        if (tid < G) {
+        if (tid < NR) {
             float M = -INFINITY;
             for (int r = 0; r < nc; ++r) M = fmaxf(M, *cluster.map_shared_rank(cm + tid, r));
             float dn = 0.f;
@@ -290,8 +309,8 @@ __global__ void __launch_bounds__(128) decode_mma_kernel(const __grid_constant__
             Mx[tid] = M;
         }
         __syncthreads();
-        const int per = (G * D + nc - 1) / nc;
-        const int lo = rank * per, hi = imin(G * D, lo + per);
+        const int per = (NR * D + nc - 1) / nc;
+        const int lo = rank * per, hi = imin(NR * D, lo + per);
         for (int i = lo + tid; i < hi; i += 128) {
             const int n = i / D;
             float a = 0.f;
@@ -300,33 +319,24 @@ __global__ void __launch_bounds__(128) decode_mma_kernel(const __grid_constant__
                 if (wr != 0.f) a += wr * *cluster.map_shared_rank(co + i, r);
             }
             const float dn = den[n];
-            p.o[((size_t)z * p.Hq + (size_t)h * G + n) * D + (i % D)] = dn > 0.f ? a / dn : 0.f;
+            out.optr(n)[i % D] = dn > 0.f ? a / dn : 0.f;
         }
-        if (rank == 0 && p.lse && tid < G) {
+        if (rank == 0 && tid < NR) {
+            float* lp = out.lptr(tid);
             const float dn = den[tid];
-            p.lse[(size_t)z * p.Hq + (size_t)h * G + tid] =
-                dn > 0.f ? (Mx[tid] + __log2f(dn)) * 0.6931471805599453f : -INFINITY;
+            if (lp) *lp = dn > 0.f ? (Mx[tid] + __log2f(dn)) * 0.6931471805599453f : -INFINITY;
         }
         cluster.sync();                               // peers' shared memory stays alive until here
-        if (rank == 0) {
-            if (p.mode == kDevModeSlot) slot_append_tail<ROWB>(p, lb, z, s_m_before);
-            if (fresh) step_count_tail(p, lb, z, s_t);
-        }
-        return;
+        final_cta = rank == 0;
+    } else {
+        float* part = p.part + (size_t)(z * p.Hkv + h) * p.n_split * p.rows_per_pair * (D + 2);
+        final_cta = split_epilogue<D>(NR, cm, cl, co, out, part, p.tickets + z * p.Hkv + h, split, p.n_split,
+                                      scratch);
     }
-    EpiOut out;
-    out.o = p.o + ((size_t)z * p.Hq + (size_t)h * G) * D;
-    out.lse = p.lse ? p.lse + (size_t)z * p.Hq + (size_t)h * G : nullptr;
-    out.rows_per_group = G;
-    out.o_row_stride = D;
-    out.o_group_stride = 0;
-    out.lse_row_stride = 1;
-    out.lse_group_stride = 0;
-    float* part = p.part + (size_t)(z * p.Hkv + h) * p.n_split * G * (D + 2);
-    const bool final_cta =
-        split_epilogue<D>(G, cm, cl, co, out, part, p.tickets + z * p.Hkv + h, split, p.n_split, scratch);
-    if (p.mode == kDevModeSlot && final_cta) slot_append_tail<ROWB>(p, lb, z, s_m_before);
-    if (fresh && final_cta) step_count_tail(p, lb, z, s_t);
+    if (!final_cta) return;
+    if (p.mode == kDevModeSlot) slot_append_tail<ROWB>(p, lb, z, s_m_before);
+    else if (si >= 0) fused_row_tail<ROWB>(p, lb, z, s_t, s_m_before, fresh, si);
+    else if (fresh) step_count_tail(p, lb, z, s_t);
 }
 
 // Clusters of `cs` CTAs of the decode kernel that can be resident at once (cached per device).
@@ -359,6 +369,8 @@ static int max_clusters(masw_mem_t* mem, int dev, int cs) {
 
 template <int D>
 static int launch_mma(masw_mem_t* mem, DecodeParams& prm, int G, int rows, int kmax, cudaStream_t stream) {
+    const int GR = prm.q_slot ? 2 * G : G;   // partial rows per pair
+    prm.rows_per_pair = GR;
     using C = MmaCfg<D>;
     static int occ[64] = {};
     const int dev = mem->device & 63;
@@ -389,7 +401,7 @@ static int launch_mma(masw_mem_t* mem, DecodeParams& prm, int G, int rows, int k
         n_split = imax(1, slots / pairs);
         n_split = imin(n_split, max_useful);
         n_split = imin(n_split, kMaxSplit);
-        while (n_split > 1 && masw_decode_part_floats(rows, mem->Hkv, G, D, n_split) > mem->part_floats) --n_split;
+        while (n_split > 1 && masw_decode_part_floats(rows, mem->Hkv, GR, D, n_split) > mem->part_floats) --n_split;
     }
     prm.n_split = n_split;
     prm.cluster = cluster ? 1 : 0;
@@ -402,7 +414,8 @@ static int launch_mma(masw_mem_t* mem, DecodeParams& prm, int G, int rows, int k
 
 int masw_launch_decode_mma(masw_mem_t* mem, masw::DecodeParams& prm, int G, int rows, int kmax,
                            cudaStream_t stream) {
-    if (G < 1 || G > 8) return masw_set_error(mem, MASW_EINVAL, "query heads per kv head must be at most 8");
+    if (G < 1 || G > 8 || (prm.q_slot && G > 4))
+        return masw_set_error(mem, MASW_EINVAL, "query heads per kv head must be at most 8 (4 with a fused slot query)");
     if (mem->D == 128) return masw::launch_mma<128>(mem, prm, G, rows, kmax, stream);
     return masw::launch_mma<64>(mem, prm, G, rows, kmax, stream);
 }

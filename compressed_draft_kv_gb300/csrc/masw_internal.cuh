@@ -203,11 +203,19 @@ struct EpiOut {
     int rows_per_group;
     int o_row_stride, o_group_stride;
     int lse_row_stride, lse_group_stride;
-    __device__ __forceinline__ size_t o_off(int n) const {
-        return (size_t)(n / rows_per_group) * o_group_stride + (size_t)(n % rows_per_group) * o_row_stride;
+    // rows n >= alt_from go to o_alt / lse_alt instead (a second query set of
+    // the same pair, e.g. a slot query fused into a draft step); alt_from < 0: none
+    float* o_alt;
+    float* lse_alt;
+    int alt_from;
+    __device__ __forceinline__ float* optr(int n) const {
+        if (alt_from >= 0 && n >= alt_from) return o_alt + (size_t)(n - alt_from) * o_row_stride;
+        return o + (size_t)(n / rows_per_group) * o_group_stride + (size_t)(n % rows_per_group) * o_row_stride;
     }
-    __device__ __forceinline__ size_t lse_off(int n) const {
-        return (size_t)(n / rows_per_group) * lse_group_stride + (size_t)(n % rows_per_group) * lse_row_stride;
+    __device__ __forceinline__ float* lptr(int n) const {
+        if (alt_from >= 0 && n >= alt_from) return lse_alt ? lse_alt + (size_t)(n - alt_from) * lse_row_stride : nullptr;
+        return lse ? lse + (size_t)(n / rows_per_group) * lse_group_stride + (size_t)(n % rows_per_group) * lse_row_stride
+                   : nullptr;
     }
 };
 
@@ -239,13 +247,13 @@ __device__ bool split_epilogue(int nrows, const float* sm_m, const float* sm_l, 
         for (int i = tid; i < nrows * D; i += nt) {
             const int row = i / D, d = i % D;
             const float l = sm_l[row];
-            out.o[out.o_off(row) + d] = l > 0.f ? sm_o[row * D + d] / l : 0.f;
+            out.optr(row)[d] = l > 0.f ? sm_o[row * D + d] / l : 0.f;
         }
-        if (out.lse)
-            for (int row = tid; row < nrows; row += nt) {
-                const float l = sm_l[row];
-                out.lse[out.lse_off(row)] = l > 0.f ? (sm_m[row] + __log2f(l)) * kLn2 : -INFINITY;
-            }
+        for (int row = tid; row < nrows; row += nt) {
+            float* lp = out.lptr(row);
+            const float l = sm_l[row];
+            if (lp) *lp = l > 0.f ? (sm_m[row] + __log2f(l)) * kLn2 : -INFINITY;
+        }
         return true;
     }
     // store this split's partial: part[split][row][D + 2] = (o[D], m, l)
@@ -292,8 +300,11 @@ __device__ bool split_epilogue(int nrows, const float* sm_m, const float* sm_l, 
                 den += w * ls[k];
             }
         }
-        out.o[out.o_off(row) + d] = den > 0.f ? acc / den : 0.f;
-        if (d == 0 && out.lse) out.lse[out.lse_off(row)] = den > 0.f ? (M + __log2f(den)) * kLn2 : -INFINITY;
+        out.optr(row)[d] = den > 0.f ? acc / den : 0.f;
+        if (d == 0) {
+            float* lp = out.lptr(row);
+            if (lp) *lp = den > 0.f ? (M + __log2f(den)) * kLn2 : -INFINITY;
+        }
     }
     if (tid == 0) *ticket = 0u;
     return true;
@@ -325,6 +336,15 @@ struct DecodeParams {
     int mode, layer, B, Hkv, Hq, S, W, Wc, C, Tmax, M_max, n_split, self_attend;
     int step;             // 1: append the new token (k_g/v_g) of every active row first (fused step)
     int cluster;          // 1: the n_split CTAs of a pair form a cluster and merge in shared memory
+    // fused boundary step: slot query / K / V / outputs for the listed rows
+    // (slot_of[z] = index into them, -1 for rows not at a boundary)
+    const void* q_slot;
+    const void* k_slot;
+    const void* v_slot;
+    float* o_slot;
+    float* lse_slot;
+    int rows_per_pair;    // partial rows per pair in the split scratch (G, or 2G with slot queries)
+    short slot_of[MASW_MAX_BATCH];
     unsigned active[MASW_MAX_BATCH / 32];
     short seq_ids[MASW_MAX_BATCH];
 };
@@ -399,6 +419,45 @@ __device__ void step_store_row(const DecodeParams& p, int lb, int h, int z, int 
             *reinterpret_cast<uint4*>((uint8_t*)p.full_k + fdst + c * 16) = kv;
             *reinterpret_cast<uint4*>((uint8_t*)p.full_v + fdst + c * 16) = vv;
         }
+    }
+}
+
+// Fused step with a slot write, after the attention of every (row z, head)
+// pair is final: the last pair of the row appends the slot's K/V as chain entry
+// m_before (position id t+1, the 0-based id of the raw token after g_m), bumps
+// the slot counter and, for an appending row, the token counter.
+template <int ROWB>
+__device__ void fused_row_tail(const DecodeParams& p, int lb, int z, int t, int m_before, bool fresh, int si) {
+    __shared__ unsigned s_last_row;
+    const int tid = threadIdx.x;
+    __threadfence();
+    __syncthreads();
+    if (tid == 0) s_last_row = atomicAdd(p.seq_tickets + z, 1u) == (unsigned)(p.Hkv - 1);
+    __syncthreads();
+    if (!s_last_row) return;
+    if (si >= 0) {
+        constexpr int VPR = ROWB / 16;
+        for (int i = tid; i < p.Hkv * VPR; i += blockDim.x) {
+            const int hh = i / VPR, cc = i % VPR;
+            const size_t dst =
+                (((size_t)lb * p.Hkv + hh) * p.C + (size_t)(p.S + p.Wc + m_before)) * ROWB + cc * 16;
+            const size_t src = ((size_t)si * p.Hkv + hh) * ROWB + cc * 16;
+            *reinterpret_cast<uint4*>((uint8_t*)p.pool_k + dst) =
+                *reinterpret_cast<const uint4*>((const uint8_t*)p.k_slot + src);
+            *reinterpret_cast<uint4*>((uint8_t*)p.pool_v + dst) =
+                *reinterpret_cast<const uint4*>((const uint8_t*)p.v_slot + src);
+        }
+    }
+    if (tid == 0) {
+        if (si >= 0) {
+            p.d_pos[(size_t)lb * p.M_max + m_before] = t + 1;
+            p.d_m[lb] = m_before + 1;
+        }
+        if (fresh) {
+            if (p.full_k != nullptr && t + 1 > p.Tmax) atomicExch(p.d_err + 1, MASW_ECAPACITY);
+            p.d_t[lb] = t + 1;
+        }
+        p.seq_tickets[z] = 0u;
     }
 }
 
@@ -489,9 +548,18 @@ cudaError_t masw_launch(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t sm
 
 // decode-kernel launcher (masw_decode.cu)
 enum DecodeMode { kModeDraft = 0, kModeFull = 1, kModeSlot = 2 };
+struct SlotFuse {            // slot queries fused into a draft step
+    const int* seq_ids;
+    int n;
+    const void* q_g;
+    const void* k_g;
+    const void* v_g;
+    float* o_g;
+    float* lse_g;
+};
 int masw_launch_decode(masw_mem_t* mem, int mode, int layer, const void* q, int n_q_heads, float* o,
                        float* lse, const int* seq_ids, int n_rows, const void* k_g, const void* v_g,
-                       cudaStream_t stream, const unsigned* step_active = nullptr);
+                       cudaStream_t stream, const unsigned* step_active = nullptr, const SlotFuse* fuse = nullptr);
 // floats of split scratch one decode launch with these sizes may use
 size_t masw_decode_part_floats(int rows, int Hkv, int G, int D, int n_split);
 // tensor-core decode for bf16 pools (masw_decode_mma.cu)

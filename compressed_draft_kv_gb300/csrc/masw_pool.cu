@@ -490,6 +490,62 @@ int masw_full_step(masw_mem_t* mem, int layer, const void* q, const void* k, con
     return step_common(mem, kModeFull, layer, q, k, v, active, n_q_heads, o, lse, stream);
 }
 
+int masw_draft_step_slot(masw_mem_t* mem, int layer, const void* q, const void* k, const void* v,
+                         const uint8_t* active, int n_q_heads, float* o, float* lse, const int* seq_ids, int n,
+                         const void* q_g, const void* k_g, const void* v_g, float* o_g, float* lse_g,
+                         masw_stream_t stream) {
+    if (!mem) return masw_set_error(nullptr, MASW_EINVAL, "step_slot: NULL handle");
+    try {
+        if (int rc = check_layer(mem, layer)) return rc;
+        if (int rc = check_heads(mem, n_q_heads)) return rc;
+        if (!seq_ids || n < 1 || n > mem->B) return masw_set_error(mem, MASW_EINVAL, "step_slot: need 1 <= n <= batch");
+        if (!q || !o || !k || !v || !q_g || !k_g || !v_g || !o_g || !aligned16(q) || !aligned16(k) ||
+            !aligned16(v) || !aligned16(q_g) || !aligned16(k_g) || !aligned16(v_g) || !aligned4(o) ||
+            !aligned4(lse) || !aligned4(o_g) || !aligned4(lse_g))
+            return masw_set_error(mem, MASW_EINVAL, "step_slot: bad pointer (NULL or misaligned)");
+        // every listed sequence appends this step and lands on an unmaterialised boundary
+        std::vector<char> seen(mem->B, 0);
+        for (int i = 0; i < n; ++i) {
+            const int b = seq_ids[i];
+            if (b < 0 || b >= mem->B || seen[b]) return masw_set_error(mem, MASW_EINVAL, "step_slot: bad or repeated seq id");
+            seen[b] = 1;
+            if (active && !active[b]) return masw_set_error(mem, MASW_ESTATE, "step_slot: listed sequence is not active");
+            const int t1 = mem->h_t[(size_t)layer * mem->B + b] + 1;
+            const int m = mem->h_m[(size_t)layer * mem->B + b];
+            if (!is_boundary(t1, mem->S, mem->W, mem->r) || m != slot_count(t1, mem->S, mem->W, mem->r) - 1)
+                return masw_set_error(mem, MASW_ESTATE, "step_slot: sequence " + std::to_string(b) +
+                                                            " does not reach an unmaterialised boundary this step");
+            if (m + 1 > mem->M_max) return masw_set_error(mem, MASW_ECAPACITY, "step_slot: slot chain is full");
+        }
+        const int G = n_q_heads / mem->Hkv;
+        if (mem->dtype != MASW_BF16 || G > 4 || mem->self_attend) {
+            // no shared query tile: the two calls as two launches
+            int rc = masw_draft_step(mem, layer, q, k, v, active, n_q_heads, o, lse, stream);
+            if (rc) return rc;
+            return masw_materialize_slot(mem, layer, seq_ids, n, q_g, k_g, v_g, o_g, lse_g, n_q_heads, stream);
+        }
+        unsigned bits[MASW_MAX_BATCH / 32] = {0};
+        for (int b = 0; b < mem->B; ++b) {
+            if (active && !active[b]) continue;
+            if (mem->h_t[(size_t)layer * mem->B + b] + 1 > mem->max_seq_len)
+                return masw_set_error(mem, MASW_ECAPACITY, "step_slot: sequence would exceed max_seq_len");
+            bits[b >> 5] |= 1u << (b & 31);
+        }
+        SlotFuse fuse{seq_ids, n, q_g, k_g, v_g, o_g, lse_g};
+        int rc = masw_launch_decode(mem, kModeDraft, layer, q, n_q_heads, o, lse, nullptr, mem->B, k, v,
+                                    (cudaStream_t)stream, bits, &fuse);
+        if (rc) return rc;
+        for (int b = 0; b < mem->B; ++b)
+            if (!active || active[b]) mem->h_t[(size_t)layer * mem->B + b] += 1;
+        for (int i = 0; i < n; ++i) mem->h_m[(size_t)layer * mem->B + seq_ids[i]] += 1;
+        return MASW_OK;
+    } catch (const std::exception& e) {
+        return masw_set_error(mem, MASW_EINVAL, e.what());
+    } catch (...) {
+        return masw_set_error(mem, MASW_EINVAL, "step_slot: unexpected error");
+    }
+}
+
 int masw_mem_load(masw_mem_t* mem, int layer, int seq, int t, const void* k_raw, const void* v_raw,
                   const void* k_slots, const void* v_slots, int n_slots) {
     if (!mem) return masw_set_error(nullptr, MASW_EINVAL, "load: NULL handle");

@@ -249,6 +249,9 @@ __global__ void __launch_bounds__(128) verify_kernel(const __grid_constant__ Ver
     out.o_group_stride = p.Hq * kVD;
     out.lse_row_stride = 1;
     out.lse_group_stride = p.Hq;
+    out.o_alt = nullptr;
+    out.lse_alt = nullptr;
+    out.alt_from = -1;
     float* part = p.part + (size_t)(b * p.Hkv + h) * p.n_split * NQ * (kVD + 2);
     split_epilogue<kVD>(NQ, cm, cl, co, out, part, p.tickets + b * p.Hkv + h, split, p.n_split, scratch);
 }

@@ -187,6 +187,21 @@ int masw_draft_step(masw_mem_t* mem, int layer, const void* q, const void* k, co
                     const uint8_t* active, int n_q_heads, float* o, float* lse,
                     masw_stream_t stream);
 
+/* The draft step at a compression boundary in one launch: masw_draft_step
+ * followed by masw_materialize_slot for the n listed sequences, which must each
+ * be active and reach an unmaterialised boundary tau_m with this step's token
+ * (ESTATE otherwise).  At tau_m the slot query's structured mask ([EN] §3.2
+ * Algorithm 1 step 2: sink, window at tau_m, slots 1..m-1) is exactly the draft
+ * query's working set M_{tau_m} (which does not yet hold g_m, [EN] §3.2
+ * Algorithm 1 step 1), so both queries share every K/V row read.  Arguments:
+ * those of masw_draft_step, then those of masw_materialize_slot.  fp32 pools,
+ * more than 4 query heads per kv head, or slot_self_attend = 1 run the two
+ * calls as two launches. */
+int masw_draft_step_slot(masw_mem_t* mem, int layer, const void* q, const void* k, const void* v,
+                         const uint8_t* active, int n_q_heads, float* o, float* lse,
+                         const int* seq_ids, int n, const void* q_g, const void* k_g,
+                         const void* v_g, float* o_g, float* lse_g, masw_stream_t stream);
+
 /* The same fused step for the full-KV contrast: masw_append_kv followed by
  * masw_full_attn.  ESTATE unless the pool was created with full_kv = 1. */
 int masw_full_step(masw_mem_t* mem, int layer, const void* q, const void* k, const void* v,

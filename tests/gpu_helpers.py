@@ -107,6 +107,31 @@ class Pair:
             assert_close(lse, want_l, self.dtype, "step LSE")
         return o
 
+    def fstep_slot(self, layer, seqs, active=None):
+        """Fused draft step + slot write at a boundary (masw_draft_step_slot)."""
+        B, n = self.batch, len(seqs)
+        k = self.rand((B, self.Hkv, self.D), "k", layer)
+        v = self.rand((B, self.Hkv, self.D), "v", layer)
+        q = self.rand((B, self.Hq, self.D), "q", layer)
+        qg = self.rand((n, self.Hq, self.D), "qg", layer)
+        kg = self.rand((n, self.Hkv, self.D), "kg", layer)
+        vg = self.rand((n, self.Hkv, self.D), "vg", layer)
+        o = torch.empty(B, self.Hq, self.D, device=DEV)
+        lse = torch.empty(B, self.Hq, device=DEV)
+        og = torch.empty(n, self.Hq, self.D, device=DEV)
+        lg = torch.empty(n, self.Hq, device=DEV)
+        capi.masw_draft_step_slot(self.h, layer, q.to(DEV), k.to(DEV), v.to(DEV), o, seqs, qg.to(DEV), kg.to(DEV),
+                                  vg.to(DEV), og, lse, lg, active=active)
+        self.ref.append(layer, k.float().numpy(), v.float().numpy(), active=active)
+        want, want_l = self.ref.draft_attn(layer, q.float().numpy())
+        want_g, want_gl = self.ref.materialize_slot(layer, seqs, qg.float().numpy(), kg.float().numpy(),
+                                                    vg.float().numpy())
+        capi.masw_sync(self.h)
+        assert_close(o, want, self.dtype, f"step_slot O l={layer} step={self.step}")
+        assert_close(lse, want_l, self.dtype, "step_slot LSE")
+        assert_close(og, want_g, self.dtype, f"step_slot O_g l={layer}")
+        assert_close(lg, want_gl, self.dtype, "step_slot LSE_g")
+
     def materialize(self, layer, seqs):
         n = len(seqs)
         qg = self.rand((n, self.Hq, self.D), "qg", layer)

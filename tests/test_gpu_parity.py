@@ -266,6 +266,37 @@ def test_fused_step_from_empty_through_boundaries(dtype, D, G):
         p.close()
 
 
+@pytest.mark.parametrize("dtype,G,self_attend", [("bf16", 3, False), ("bf16", 4, False), ("bf16", 8, False),
+                                                  ("f32", 2, False), ("bf16", 2, True)])
+def test_fused_boundary_step(dtype, G, self_attend):
+    """masw_draft_step_slot: the slot write rides in the draft step's launch
+    (bf16, G <= 4) or falls back to two launches; ragged batch, some rows at a
+    boundary, some not, an inactive row."""
+    S, W, r, Hkv, D = 2, 24, 8, 2, 128 if dtype == "bf16" else 64
+    p = Pair(S, W, r, Hkv, D, 2, 4, dtype, G * Hkv, max_seq_len=256, reserve=3, self_attend=self_attend,
+             tag=f"fbnd{G}{int(self_attend)}")
+    try:
+        for l in range(2):
+            p.load(l, 0, 40, seed=1)
+            p.load(l, 1, 53, seed=2)
+            p.load(l, 3, 9, seed=3)
+        for step in range(1, 40):
+            p.step = step
+            active = [1, 1, 1 if step % 4 else 0, 1 if step > 5 else 0]
+            for l in range(2):
+                due = [b for b in range(4) if active[b] and orc.is_boundary(p.ref.t(l, b) + 1, S, W, r)
+                       and p.ref.m(l, b) == orc.slot_count(p.ref.t(l, b) + 1, S, W, r) - 1]
+                if due:
+                    p.fstep_slot(l, due, active=active)
+                else:
+                    p.fstep(l, active=active)
+        for l in range(2):
+            for b in range(4):
+                p.check_state(l, b)
+    finally:
+        p.close()
+
+
 def test_fused_full_step():
     p = Pair(4, 16, 8, 2, 128, 1, 2, "bf16", 8, max_seq_len=300, full_kv=True, tag="ffull")
     try:
