@@ -93,7 +93,7 @@ decode_kernel(const __grid_constant__ DecodeParams p) {
     extern __shared__ __align__(128) uint8_t smem[];
     __shared__ __align__(8) uint64_t bars[NST];
     __shared__ Seg segs[5];
-    __shared__ int s_nseg, s_m_before;
+    __shared__ int s_nseg, s_m_before, s_t;
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int split = blockIdx.x, h = blockIdx.y, z = blockIdx.z;
@@ -103,9 +103,10 @@ decode_kernel(const __grid_constant__ DecodeParams p) {
     pdl_trigger();
 
     if (tid == 0) {
-        const int t = p.d_t[lb];
-        const int mcnt = p.d_m[lb];
+        const int t = p.d_t[(size_t)lb * p.Hkv + h];
+        const int mcnt = p.d_m[(size_t)lb * p.Hkv + h];
         s_m_before = mcnt;
+        s_t = t;
         const int n = build_segments<ROWB>(p, lb, h, z, t, mcnt, segs);
         s_nseg = n;
         for (int s = 0; s < NST; ++s) mbar_init(&bars[s], 1);
@@ -304,7 +305,9 @@ decode_kernel(const __grid_constant__ DecodeParams p) {
     const bool final_cta = split_epilogue<D>(G, cm, cl, co, out, part, p.tickets + z * p.Hkv + h, split,
                                              p.n_split, scratch);
 
-    if (p.mode == kModeSlot && final_cta) slot_append_tail<ROWB>(p, lb, z, s_m_before);
+    if (p.mode == kModeSlot && final_cta)
+        pair_tail<ROWB>(p, lb, h, s_t, s_m_before, false, (const uint8_t*)p.k_g + (size_t)z * p.Hkv * ROWB,
+                        (const uint8_t*)p.v_g + (size_t)z * p.Hkv * ROWB, s_t);
 }
 
 // ---------------------------------------------------------------------------
@@ -376,7 +379,6 @@ int masw_launch_decode(masw_mem_t* mem, int mode, int layer, const void* q, int 
     prm.d_err = mem->d_err;
     prm.part = mem->part;
     prm.tickets = mem->tickets;
-    prm.seq_tickets = mem->seq_tickets;
     prm.scale_log2 = mem->scale * 1.4426950408889634f;
     prm.mode = mode;
     prm.layer = layer;

@@ -66,8 +66,8 @@ __global__ void __launch_bounds__(128) decode_mma_kernel(const __grid_constant__
     const int si = p.q_slot ? (int)p.slot_of[z] : -1;   // fused slot query of this row, if any
     const int NR = si >= 0 ? 2 * G : G;                  // query columns of this pair
     if (tid == 0) {   // warm L2 with the counters while the previous kernel drains
-        asm volatile("prefetch.global.L2 [%0];" ::"l"(p.d_t + lb));
-        asm volatile("prefetch.global.L2 [%0];" ::"l"(p.d_m + lb));
+        asm volatile("prefetch.global.L2 [%0];" ::"l"(p.d_t + (size_t)lb * p.Hkv + h));
+        asm volatile("prefetch.global.L2 [%0];" ::"l"(p.d_m + (size_t)lb * p.Hkv + h));
     }
     pdl_wait();
     pdl_trigger();
@@ -90,8 +90,8 @@ __global__ void __launch_bounds__(128) decode_mma_kernel(const __grid_constant__
         }
     }
     if (tid == 0) {
-        const int t = p.d_t[lb];
-        const int mcnt = p.d_m[lb];
+        const int t = p.d_t[(size_t)lb * p.Hkv + h];
+        const int mcnt = p.d_m[(size_t)lb * p.Hkv + h];
         s_m_before = mcnt;
         s_t = t;
         const int n = build_segments<ROWB>(p, lb, h, z, t, mcnt, segs);
@@ -334,9 +334,14 @@ __global__ void __launch_bounds__(128) decode_mma_kernel(const __grid_constant__
                                       scratch);
     }
     if (!final_cta) return;
-    if (p.mode == kDevModeSlot) slot_append_tail<ROWB>(p, lb, z, s_m_before);
-    else if (si >= 0) fused_row_tail<ROWB>(p, lb, z, s_t, s_m_before, fresh, si);
-    else if (fresh) step_count_tail(p, lb, z, s_t);
+    if (p.mode == kDevModeSlot)
+        pair_tail<ROWB>(p, lb, h, s_t, s_m_before, false, (const uint8_t*)p.k_g + (size_t)z * p.Hkv * ROWB,
+                        (const uint8_t*)p.v_g + (size_t)z * p.Hkv * ROWB, s_t);
+    else if (si >= 0)
+        pair_tail<ROWB>(p, lb, h, s_t, s_m_before, fresh, (const uint8_t*)p.k_slot + (size_t)si * p.Hkv * ROWB,
+                        (const uint8_t*)p.v_slot + (size_t)si * p.Hkv * ROWB, s_t + 1);
+    else if (fresh)
+        pair_tail<ROWB>(p, lb, h, s_t, s_m_before, true, nullptr, nullptr, 0);
 }
 
 // Clusters of `cs` CTAs of the decode kernel that can be resident at once (cached per device).

@@ -51,14 +51,13 @@ struct masw_mem {
     void* pool_v = nullptr;
     void* full_k = nullptr;
     void* full_v = nullptr;
-    int* d_t = nullptr;      // [L*B] raw tokens appended
-    int* d_m = nullptr;      // [L*B] slots in the chain
+    int* d_t = nullptr;      // [L*B*Hkv] raw tokens appended (one copy per kv head)
+    int* d_m = nullptr;      // [L*B*Hkv] slots in the chain (one copy per kv head)
     int* d_pos = nullptr;    // [L*B*M_max] 0-based slot position ids
     int* d_err = nullptr;    // [4] error word (bounded wait ran out)
     float* part = nullptr;   // split partials
     size_t part_floats = 0;  // capacity of `part`
     unsigned* tickets = nullptr;      // [B*Hkv] per-(row, head) split tickets
-    unsigned* seq_tickets = nullptr;  // [B] per-row head tickets (slot write)
     std::vector<int> h_t, h_m;
     int device = 0, num_sms = 0;
     std::string err;
@@ -331,7 +330,6 @@ struct DecodeParams {
     int* d_err;
     float* part;
     unsigned* tickets;
-    unsigned* seq_tickets;
     float scale_log2;     // softmax scale * log2(e)
     int mode, layer, B, Hkv, Hq, S, W, Wc, C, Tmax, M_max, n_split, self_attend;
     int step;             // 1: append the new token (k_g/v_g) of every active row first (fused step)
@@ -422,86 +420,36 @@ __device__ void step_store_row(const DecodeParams& p, int lb, int h, int z, int 
     }
 }
 
-// Fused step with a slot write, after the attention of every (row z, head)
-// pair is final: the last pair of the row appends the slot's K/V as chain entry
-// m_before (position id t+1, the 0-based id of the raw token after g_m), bumps
-// the slot counter and, for an appending row, the token counter.
+// After the attention of pair (row z, head h) is final -- its last split, or
+// rank 0 of its cluster -- every CTA of the pair has read this head's copy of
+// the counters, so the pair updates them on its own, with no cross-head
+// coordination: a slot write appends head h's K_g/V_g row as chain entry
+// m_before and records the slot's position id; a fused step bumps the token
+// counter.  (Counters are kept per (layer, sequence, kv head); all heads of a
+// sequence hold equal values between launches.)
 template <int ROWB>
-__device__ void fused_row_tail(const DecodeParams& p, int lb, int z, int t, int m_before, bool fresh, int si) {
-    __shared__ unsigned s_last_row;
+__device__ void pair_tail(const DecodeParams& p, int lb, int h, int t, int m_before, bool fresh,
+                          const uint8_t* slot_k, const uint8_t* slot_v, int pos_id) {
     const int tid = threadIdx.x;
-    __threadfence();
-    __syncthreads();
-    if (tid == 0) s_last_row = atomicAdd(p.seq_tickets + z, 1u) == (unsigned)(p.Hkv - 1);
-    __syncthreads();
-    if (!s_last_row) return;
-    if (si >= 0) {
-        constexpr int VPR = ROWB / 16;
-        for (int i = tid; i < p.Hkv * VPR; i += blockDim.x) {
-            const int hh = i / VPR, cc = i % VPR;
-            const size_t dst =
-                (((size_t)lb * p.Hkv + hh) * p.C + (size_t)(p.S + p.Wc + m_before)) * ROWB + cc * 16;
-            const size_t src = ((size_t)si * p.Hkv + hh) * ROWB + cc * 16;
-            *reinterpret_cast<uint4*>((uint8_t*)p.pool_k + dst) =
-                *reinterpret_cast<const uint4*>((const uint8_t*)p.k_slot + src);
-            *reinterpret_cast<uint4*>((uint8_t*)p.pool_v + dst) =
-                *reinterpret_cast<const uint4*>((const uint8_t*)p.v_slot + src);
+    const size_t ci = (size_t)lb * p.Hkv + h;
+    if (slot_k) {
+        const size_t dst = (ci * p.C + (size_t)(p.S + p.Wc + m_before)) * ROWB;
+        for (int c = tid; c < ROWB / 16; c += blockDim.x) {
+            *reinterpret_cast<uint4*>((uint8_t*)p.pool_k + dst + c * 16) =
+                *reinterpret_cast<const uint4*>(slot_k + (size_t)h * ROWB + c * 16);
+            *reinterpret_cast<uint4*>((uint8_t*)p.pool_v + dst + c * 16) =
+                *reinterpret_cast<const uint4*>(slot_v + (size_t)h * ROWB + c * 16);
         }
     }
     if (tid == 0) {
-        if (si >= 0) {
-            p.d_pos[(size_t)lb * p.M_max + m_before] = t + 1;
-            p.d_m[lb] = m_before + 1;
+        if (slot_k) {
+            if (h == 0) p.d_pos[(size_t)lb * p.M_max + m_before] = pos_id;
+            p.d_m[ci] = m_before + 1;
         }
         if (fresh) {
             if (p.full_k != nullptr && t + 1 > p.Tmax) atomicExch(p.d_err + 1, MASW_ECAPACITY);
-            p.d_t[lb] = t + 1;
+            p.d_t[ci] = t + 1;
         }
-        p.seq_tickets[z] = 0u;
-    }
-}
-
-// Fused step, after the attention of every (row z, head) pair is final: the
-// last pair of the row bumps the token counter (every CTA of the row has read
-// the old value by then).
-__device__ inline void step_count_tail(const DecodeParams& p, int lb, int z, int t) {
-    __shared__ unsigned s_last_head;
-    __threadfence();
-    __syncthreads();
-    if (threadIdx.x == 0) s_last_head = atomicAdd(p.seq_tickets + z, 1u) == (unsigned)(p.Hkv - 1);
-    __syncthreads();
-    if (s_last_head && threadIdx.x == 0) {
-        if (p.full_k != nullptr && t + 1 > p.Tmax) atomicExch(p.d_err + 1, MASW_ECAPACITY);
-        p.d_t[lb] = t + 1;
-        p.seq_tickets[z] = 0u;
-    }
-}
-
-// Slot write, after the attention of every (row z, head) pair is final: the
-// last pair of the row to finish appends g_m's K/V as chain entry m_before,
-// records its position id and bumps the slot counter.  Every CTA of the row
-// has read the old counter by then (each took its ticket after a fence).
-template <int ROWB>
-__device__ void slot_append_tail(const DecodeParams& p, int lb, int z, int m_before) {
-    __shared__ unsigned s_last_head;
-    const int tid = threadIdx.x;
-    __threadfence();
-    __syncthreads();
-    if (tid == 0) s_last_head = atomicAdd(p.seq_tickets + z, 1u) == (unsigned)(p.Hkv - 1);
-    __syncthreads();
-    if (!s_last_head) return;
-    constexpr int VPR = ROWB / 16;
-    for (int i = tid; i < p.Hkv * VPR; i += blockDim.x) {
-        const int hh = i / VPR, cc = i % VPR;
-        const size_t dst = (((size_t)lb * p.Hkv + hh) * p.C + (size_t)(p.S + p.Wc + m_before)) * ROWB + cc * 16;
-        const size_t src = ((size_t)z * p.Hkv + hh) * ROWB + cc * 16;
-        *reinterpret_cast<uint4*>((uint8_t*)p.pool_k + dst) = *reinterpret_cast<const uint4*>((const uint8_t*)p.k_g + src);
-        *reinterpret_cast<uint4*>((uint8_t*)p.pool_v + dst) = *reinterpret_cast<const uint4*>((const uint8_t*)p.v_g + src);
-    }
-    if (tid == 0) {
-        p.d_pos[(size_t)lb * p.M_max + m_before] = p.d_t[lb];   // 0-based id of the raw token after g_m
-        p.d_m[lb] = m_before + 1;
-        p.seq_tickets[z] = 0u;
     }
 }
 

@@ -54,7 +54,7 @@ __global__ void append_kernel(const __grid_constant__ AppendParams p) {
     const int b = blockIdx.x;
     if (!((p.active[b >> 5] >> (b & 31)) & 1u)) return;
     const int lb = p.layer * p.B + b;
-    const int t = p.d_t[lb];
+    const int t = p.d_t[(size_t)lb * p.Hkv];
     const int i = t + 1;
     const int row = (i <= p.S) ? i - 1 : p.S + ring_row(i, p.S, p.Wc);
     const int vpr = p.rowb / 16;
@@ -74,16 +74,14 @@ __global__ void append_kernel(const __grid_constant__ AppendParams p) {
         }
     }
     __syncthreads();
-    if (threadIdx.x == 0) {
-        if (p.full_k != nullptr && i > p.Tmax) atomicExch(p.d_err + 1, MASW_ECAPACITY);
-        p.d_t[lb] = i;
-    }
+    if (threadIdx.x == 0 && p.full_k != nullptr && i > p.Tmax) atomicExch(p.d_err + 1, MASW_ECAPACITY);
+    for (int hh = threadIdx.x; hh < p.Hkv; hh += blockDim.x) p.d_t[(size_t)lb * p.Hkv + hh] = i;
 }
 
 struct RollbackParams {
     int* d_t;
     int* d_m;
-    int L, B, S, W, r, n;
+    int L, B, Hkv, S, W, r, n;
     short seq[MASW_MAX_BATCH];
     int t_new[MASW_MAX_BATCH];
 };
@@ -95,10 +93,10 @@ __global__ void rollback_kernel(const __grid_constant__ RollbackParams p) {
     pdl_trigger();
     const int b = p.seq[blockIdx.x];
     const int tn = p.t_new[blockIdx.x];
-    for (int l = threadIdx.x; l < p.L; l += blockDim.x) {
-        const int lb = l * p.B + b;
-        p.d_t[lb] = tn;
-        p.d_m[lb] = imin(p.d_m[lb], slot_count(tn, p.S, p.W, p.r));
+    for (int i = threadIdx.x; i < p.L * p.Hkv; i += blockDim.x) {
+        const size_t ci = ((size_t)(i / p.Hkv) * p.B + b) * p.Hkv + (i % p.Hkv);
+        p.d_t[ci] = tn;
+        p.d_m[ci] = imin(p.d_m[ci], slot_count(tn, p.S, p.W, p.r));
     }
 }
 
@@ -138,7 +136,7 @@ int check_heads(masw_mem_t* mem, int n_q_heads) {
 
 void free_all(masw_mem_t* m) {
     void* ptrs[] = {m->pool_k, m->pool_v, m->full_k, m->full_v, m->d_t, m->d_m,
-                    m->d_pos, m->d_err, m->part, m->tickets, m->seq_tickets};
+                    m->d_pos, m->d_err, m->part, m->tickets};
     for (void* p : ptrs)
         if (p) cudaFree(p);
 }
@@ -271,7 +269,8 @@ int masw_mem_create(int S, int W, int r, int n_kv_heads, int head_dim, int layer
             return fail(MASW_ENOMEM, "create: full-KV cache allocation failed");
     }
     const size_t lb = (size_t)layers * m->B;
-    if (cudaMalloc(&m->d_t, lb * sizeof(int)) != cudaSuccess || cudaMalloc(&m->d_m, lb * sizeof(int)) != cudaSuccess ||
+    const size_t lbh = lb * n_kv_heads;
+    if (cudaMalloc(&m->d_t, lbh * sizeof(int)) != cudaSuccess || cudaMalloc(&m->d_m, lbh * sizeof(int)) != cudaSuccess ||
         cudaMalloc(&m->d_pos, std::max<size_t>(1, lb * m->M_max) * sizeof(int)) != cudaSuccess ||
         cudaMalloc(&m->d_err, 4 * sizeof(int)) != cudaSuccess)
         return fail(MASW_ENOMEM, "create: counter allocation failed");
@@ -280,14 +279,12 @@ int masw_mem_create(int S, int W, int r, int n_kv_heads, int head_dim, int layer
     const size_t splits = std::min<size_t>(kMaxSplit, std::max<size_t>(8, (3 * (size_t)m->num_sms + pairs - 1) / pairs));
     m->part_floats = pairs * splits * MASW_MAX_GROUP * (head_dim + 2);
     if (cudaMalloc(&m->part, m->part_floats * sizeof(float)) != cudaSuccess ||
-        cudaMalloc(&m->tickets, pairs * sizeof(unsigned)) != cudaSuccess ||
-        cudaMalloc(&m->seq_tickets, (size_t)m->B * sizeof(unsigned)) != cudaSuccess)
+        cudaMalloc(&m->tickets, pairs * sizeof(unsigned)) != cudaSuccess)
         return fail(MASW_ENOMEM, "create: scratch allocation failed");
-    if (cudaMemset(m->d_t, 0, lb * sizeof(int)) != cudaSuccess || cudaMemset(m->d_m, 0, lb * sizeof(int)) != cudaSuccess ||
+    if (cudaMemset(m->d_t, 0, lbh * sizeof(int)) != cudaSuccess || cudaMemset(m->d_m, 0, lbh * sizeof(int)) != cudaSuccess ||
         cudaMemset(m->d_pos, 0xff, std::max<size_t>(1, lb * m->M_max) * sizeof(int)) != cudaSuccess ||
         cudaMemset(m->d_err, 0, 4 * sizeof(int)) != cudaSuccess ||
         cudaMemset(m->tickets, 0, pairs * sizeof(unsigned)) != cudaSuccess ||
-        cudaMemset(m->seq_tickets, 0, (size_t)m->B * sizeof(unsigned)) != cudaSuccess ||
         cudaDeviceSynchronize() != cudaSuccess)
         return fail(MASW_ECUDA, "create: counter clear failed");
     *out = m;
@@ -401,6 +398,7 @@ int masw_rollback(masw_mem_t* mem, const int* seq_ids, const int* t_new, int n, 
     p.d_m = mem->d_m;
     p.L = mem->L;
     p.B = mem->B;
+    p.Hkv = mem->Hkv;
     p.S = mem->S;
     p.W = mem->W;
     p.r = mem->r;
@@ -599,8 +597,9 @@ int masw_mem_load(masw_mem_t* mem, int layer, int seq, int t, const void* k_raw,
         // counters and slot position ids
         std::vector<int> pos(std::max(1, mem->M_max), -1);
         for (int j = 0; j < n_slots; ++j) pos[j] = mem->S + mem->W + (j + 1) * mem->r;
-        MASW_CUDA_TRY(mem, cudaMemcpy(mem->d_t + lb, &t, sizeof(int), cudaMemcpyHostToDevice));
-        MASW_CUDA_TRY(mem, cudaMemcpy(mem->d_m + lb, &n_slots, sizeof(int), cudaMemcpyHostToDevice));
+        std::vector<int> tv(mem->Hkv, t), mv(mem->Hkv, n_slots);
+        MASW_CUDA_TRY(mem, cudaMemcpy(mem->d_t + lb * mem->Hkv, tv.data(), mem->Hkv * sizeof(int), cudaMemcpyHostToDevice));
+        MASW_CUDA_TRY(mem, cudaMemcpy(mem->d_m + lb * mem->Hkv, mv.data(), mem->Hkv * sizeof(int), cudaMemcpyHostToDevice));
         if (mem->M_max > 0)
             MASW_CUDA_TRY(mem, cudaMemcpy(mem->d_pos + lb * mem->M_max, pos.data(), mem->M_max * sizeof(int),
                                           cudaMemcpyHostToDevice));
@@ -643,8 +642,13 @@ int masw_query(masw_mem_t* mem, int layer, int seq, masw_state_t* out) {
     out->rows = mem->C;
     out->slot_capacity = mem->M_max;
     MASW_CUDA_TRY(mem, cudaDeviceSynchronize());
-    MASW_CUDA_TRY(mem, cudaMemcpy(&out->dev_t, mem->d_t + lb, sizeof(int), cudaMemcpyDeviceToHost));
-    MASW_CUDA_TRY(mem, cudaMemcpy(&out->dev_m, mem->d_m + lb, sizeof(int), cudaMemcpyDeviceToHost));
+    std::vector<int> tv(mem->Hkv), mv(mem->Hkv);
+    MASW_CUDA_TRY(mem, cudaMemcpy(tv.data(), mem->d_t + lb * mem->Hkv, mem->Hkv * sizeof(int), cudaMemcpyDeviceToHost));
+    MASW_CUDA_TRY(mem, cudaMemcpy(mv.data(), mem->d_m + lb * mem->Hkv, mem->Hkv * sizeof(int), cudaMemcpyDeviceToHost));
+    out->dev_t = tv[0];
+    out->dev_m = mv[0];
+    for (int h = 1; h < mem->Hkv; ++h)   // every kv head's copy must agree
+        if (tv[h] != tv[0] || mv[h] != mv[0]) out->dev_t = out->dev_m = -1;
     return MASW_OK;
 }
 
