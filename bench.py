@@ -384,8 +384,12 @@ def profile_case(kind: str, prefix: int):
             capi.masw_mem_load(h, l, b, kr, kr, ks, ks)
     q = torch.randn(B, Hq, D, generator=g, device=dev).to(torch.bfloat16)
     o = torch.empty(B, Hq, D, device=dev)
+    kn = torch.randn(B, Hkv, D, generator=g, device=dev).to(torch.bfloat16)
     for l in range(L):
-        (capi.masw_full_attn if full else capi.masw_draft_attn)(h, l, q, o)
+        if kind == "step":
+            capi.masw_draft_step(h, l, q, kn, kn, o)
+        else:
+            (capi.masw_full_attn if full else capi.masw_draft_attn)(h, l, q, o)
     torch.cuda.synchronize()
     capi.masw_mem_destroy(h)
 
@@ -401,7 +405,7 @@ def main():
     ap.add_argument("--prefix", type=int, default=None)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-iters", type=int, default=5)
-    ap.add_argument("--profile-case", choices=["draft", "full", "verify"], default=None,
+    ap.add_argument("--profile-case", choices=["draft", "step", "full", "verify"], default=None,
                     help="run a few launches of one kernel on a small state (4 layers) for an ncu capture")
     args = ap.parse_args()
     if args.warmup < 3:
