@@ -36,6 +36,29 @@ METRIC = "MASW draft-attn decode steps/s (28 layers x batch 8, 32K prefix)"
 UNIT = "decode steps/s"
 
 
+def _recorded_traffic():
+    """dram read+write bytes per launch of the fused-step kernel from the
+    committed ncu summary, if the kernel sources are unchanged since (hash of
+    masw_decode_mma.cu + masw_internal.cuh); None otherwise."""
+    import hashlib
+    import re
+    try:
+        csrc = os.path.join(ROOT, "compressed_draft_kv_gb300", "csrc")
+        h = hashlib.sha256()
+        for name in ("masw_decode_mma.cu", "masw_internal.cuh"):
+            with open(os.path.join(csrc, name), "rb") as f:
+                h.update(f.read())
+        with open(os.path.join(ROOT, "profiles", "decode_mma_step_b8_32k.md")) as f:
+            txt = f.read()
+        rec = re.search(r"first 16 hex\): `([0-9a-f]{16})`", txt)
+        val = re.search(r"traffic_bytes_per_launch: (\d+)", txt)
+        if rec and val and rec.group(1) == h.hexdigest()[:16]:
+            return int(val.group(1))
+    except OSError:
+        pass
+    return None
+
+
 def _peaks():
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
@@ -490,7 +513,7 @@ def main():
         "full_kv": {"value": full_value, "unit": UNIT, "ms_per_step": secs_full / full_iters * 1e3},
         "speedup_vs_full_kv": value / full_value,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                     "frac": achieved / peak, "traffic": None, "peak_kind": peak_kind,
+                     "frac": achieved / peak, "traffic": _recorded_traffic(), "peak_kind": peak_kind,
                      "kernel": "decode_mma_kernel<128> (masw_draft_step: fused append + draft attention)",
                      "bytes_per_launch": total_b, "kv_bytes_per_launch": kv_b,
                      "us_per_launch": kern_s * 1e6},
