@@ -57,6 +57,9 @@ __global__ void __launch_bounds__(128) decode_mma_kernel(const __grid_constant__
     __shared__ const uint8_t* s_vk[5];
     __shared__ const uint8_t* s_vv[5];
     __shared__ int s_nseg, s_m_before, s_t;
+    // cluster merge receive buffers (written by peer CTAs; never aliased with the stages)
+    __shared__ float r_m[64], r_l[64];
+    __shared__ float r_o[8 * D + 8];
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int split = blockIdx.x, h = blockIdx.y, z = blockIdx.z;
@@ -288,36 +291,45 @@ __global__ void __launch_bounds__(128) decode_mma_kernel(const __grid_constant__
     bool final_cta;
     if (p.cluster) {
         // The n_split CTAs of this (row, head) pair form one thread-block
-        // cluster: merge their (m, l, o) through distributed shared memory.
+        // cluster.  Each pushes its (m, l) to every rank and the slice of its o
+        // that rank k finalises into rank k's receive buffers (remote shared
+        // memory stores, no waiting), one cluster barrier makes them visible,
+        // and each rank merges its slice from its own shared memory.
         cg::cluster_group cluster = cg::this_cluster();
-        cluster.sync();                               // every CTA's cm/cl/co is final
         const int nc = (int)cluster.num_blocks(), rank = (int)cluster.block_rank();
-        float* w = scratch;                           // [8][8] weights of rank r for row n
+        const int per = (NR * D + nc - 1) / nc;
+        for (int i = tid; i < NR * D; i += 128) {
+            const int k = i / per;
+            cluster.map_shared_rank(r_o, k)[rank * per + (i - k * per)] = co[i];
+        }
+        if (tid < NR)
+            for (int k = 0; k < nc; ++k) {
+                cluster.map_shared_rank(r_m, k)[rank * 8 + tid] = cm[tid];
+                cluster.map_shared_rank(r_l, k)[rank * 8 + tid] = cl[tid];
+            }
+        cluster.sync();                               // every peer's pushes have landed here
+        float* w = scratch;                           // [8 rows][8 ranks] merge weights
         float* den = w + 64;                          // [8]
         float* Mx = den + 8;                          // [8]
         if (tid < NR) {
             float M = -INFINITY;
-            for (int r = 0; r < nc; ++r) M = fmaxf(M, *cluster.map_shared_rank(cm + tid, r));
+            for (int r = 0; r < nc; ++r) M = fmaxf(M, r_m[r * 8 + tid]);
             float dn = 0.f;
             for (int r = 0; r < nc; ++r) {
-                const float mr = *cluster.map_shared_rank(cm + tid, r);
+                const float mr = r_m[r * 8 + tid];
                 const float wr = mr == -INFINITY ? 0.f : exp2f(mr - M);
                 w[tid * 8 + r] = wr;
-                dn += wr * *cluster.map_shared_rank(cl + tid, r);
+                dn += wr * r_l[r * 8 + tid];
             }
             den[tid] = dn;
             Mx[tid] = M;
         }
         __syncthreads();
-        const int per = (NR * D + nc - 1) / nc;
         const int lo = rank * per, hi = imin(NR * D, lo + per);
         for (int i = lo + tid; i < hi; i += 128) {
             const int n = i / D;
             float a = 0.f;
-            for (int r = 0; r < nc; ++r) {
-                const float wr = w[n * 8 + r];
-                if (wr != 0.f) a += wr * *cluster.map_shared_rank(co + i, r);
-            }
+            for (int r = 0; r < nc; ++r) a += w[n * 8 + r] * r_o[r * per + (i - lo)];
             const float dn = den[n];
             out.optr(n)[i % D] = dn > 0.f ? a / dn : 0.f;
         }
@@ -326,7 +338,6 @@ __global__ void __launch_bounds__(128) decode_mma_kernel(const __grid_constant__
             const float dn = den[tid];
             if (lp) *lp = dn > 0.f ? (Mx[tid] + __log2f(dn)) * 0.6931471805599453f : -INFINITY;
         }
-        cluster.sync();                               // peers' shared memory stays alive until here
         final_cta = rank == 0;
     } else {
         float* part = p.part + (size_t)(z * p.Hkv + h) * p.n_split * p.rows_per_pair * (D + 2);
