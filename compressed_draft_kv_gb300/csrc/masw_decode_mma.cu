@@ -56,7 +56,7 @@ __global__ void __launch_bounds__(128) decode_mma_kernel(const __grid_constant__
     __shared__ int s_start[6];
     __shared__ const uint8_t* s_vk[5];
     __shared__ const uint8_t* s_vv[5];
-    __shared__ int s_nseg, s_m_before, s_t;
+    __shared__ int s_nseg, s_m_before, s_t, s_respec;
     // cluster merge receive buffers (written by peer CTAs; never aliased with the stages)
     __shared__ float r_m[64], r_l[64];
     __shared__ float r_o[8 * D + 8];
@@ -68,10 +68,30 @@ __global__ void __launch_bounds__(128) decode_mma_kernel(const __grid_constant__
     const int G = p.Hq / p.Hkv;
     const int si = p.q_slot ? (int)p.slot_of[z] : -1;   // fused slot query of this row, if any
     const int NR = si >= 0 ? 2 * G : G;                  // query columns of this pair
-    if (tid == 0) {   // warm L2 with the counters while the previous kernel drains
-        asm volatile("prefetch.global.L2 [%0];" ::"l"(p.d_t + (size_t)lb * p.Hkv + h));
-        asm volatile("prefetch.global.L2 [%0];" ::"l"(p.d_m + (size_t)lb * p.Hkv + h));
-    }
+    // Segment table, built speculatively before the PDL wait (the counters are
+    // read while the previous kernel drains) and verified after it; the copies
+    // of the first stages are issued on the speculative table, and rebuilt and
+    // reissued in the rare case the previous kernel changed this head's counters.
+    const size_t ci = (size_t)lb * p.Hkv + h;
+    auto build = [&](int t, int mcnt) {
+        s_m_before = mcnt;
+        s_t = t;
+        const int n = build_segments<ROWB>(p, lb, h, z, t, mcnt, segs);
+        int acc = 0;
+        for (int s = 0; s < n; ++s) {
+            s_start[s] = acc;
+            s_vk[s] = segs[s].k - (size_t)acc * ROWB;   // row j of the list is s_vk[s] + j*ROWB
+            s_vv[s] = segs[s].v - (size_t)acc * ROWB;
+            acc += segs[s].len;
+        }
+        if (n == 0) {
+            s_vk[0] = (const uint8_t*)p.pool_k;
+            s_vv[0] = (const uint8_t*)p.pool_v;
+        }
+        s_start[n] = acc;
+        s_nseg = n;
+    };
+    if (tid == 0) build(*(volatile const int*)(p.d_t + ci), *(volatile const int*)(p.d_m + ci));
     pdl_wait();
     pdl_trigger();
 
@@ -92,35 +112,14 @@ __global__ void __launch_bounds__(128) decode_mma_kernel(const __grid_constant__
             qb[ks][1] = real ? *reinterpret_cast<const uint32_t*>(qrow + d + 8) : 0u;
         }
     }
-    if (tid == 0) {
-        const int t = p.d_t[(size_t)lb * p.Hkv + h];
-        const int mcnt = p.d_m[(size_t)lb * p.Hkv + h];
-        s_m_before = mcnt;
-        s_t = t;
-        const int n = build_segments<ROWB>(p, lb, h, z, t, mcnt, segs);
-        int acc = 0;
-        for (int s = 0; s < n; ++s) {
-            s_start[s] = acc;
-            s_vk[s] = segs[s].k - (size_t)acc * ROWB;   // row j of the list is s_vk[s] + j*ROWB
-            s_vv[s] = segs[s].v - (size_t)acc * ROWB;
-            acc += segs[s].len;
-        }
-        if (n == 0) {
-            s_vk[0] = (const uint8_t*)p.pool_k;
-            s_vv[0] = (const uint8_t*)p.pool_v;
-        }
-        s_start[n] = acc;
-        s_nseg = n;
-    }
     __syncthreads();
-    const int nseg = s_nseg;
-    const int total = s_start[nseg];
+    int nseg = s_nseg;
+    int total = s_start[nseg];
     const bool fresh = p.step && ((p.active[z >> 5] >> (z & 31)) & 1u);
-    if (fresh && split == 0) step_store_row<ROWB>(p, lb, h, z, s_t);
-    const int chunk = (((total + p.n_split - 1) / p.n_split) + 15) & ~15;
-    const int r0 = imin(total, split * chunk);
-    const int r1 = imin(total, r0 + chunk);
-    const int nstage = (r1 - r0 + KPS - 1) / KPS;
+    int chunk = (((total + p.n_split - 1) / p.n_split) + 15) & ~15;
+    int r0 = imin(total, split * chunk);
+    int r1 = imin(total, r0 + chunk);
+    int nstage = (r1 - r0 + KPS - 1) / KPS;
     const uint32_t sbase = smem_u32(smem);
 
     // stage c <- logical rows [r0 + c*KPS, +KPS); rows past r1 are zero-filled.
@@ -161,7 +160,27 @@ __global__ void __launch_bounds__(128) decode_mma_kernel(const __grid_constant__
         if (c < nstage) load_stage(c);
         cp_async_commit();
     }
+    if (tid == 0) s_respec = (p.d_t[ci] != s_t || p.d_m[ci] != s_m_before) ? 1 : 0;
+    __syncthreads();
+    if (s_respec) {   // the previous kernel changed the counters: drop the speculative stages
+        cp_async_wait<0>();
+        __syncthreads();
+        if (tid == 0) build(p.d_t[ci], p.d_m[ci]);
+        __syncthreads();
+        nseg = s_nseg;
+        total = s_start[nseg];
+        chunk = (((total + p.n_split - 1) / p.n_split) + 15) & ~15;
+        r0 = imin(total, split * chunk);
+        r1 = imin(total, r0 + chunk);
+        nstage = (r1 - r0 + KPS - 1) / KPS;
+#pragma unroll
+        for (int c = 0; c < NST - 1; ++c) {
+            if (c < nstage) load_stage(c);
+            cp_async_commit();
+        }
+    }
 
+    if (fresh && split == 0) step_store_row<ROWB>(p, lb, h, z, s_t);
     const float sl2 = p.scale_log2;
     float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f};
     float acc[KS][4];
@@ -256,26 +275,6 @@ __global__ void __launch_bounds__(128) decode_mma_kernel(const __grid_constant__
         }
     }
     __syncthreads();
-    if (tid < NR) {
-        float M = -INFINITY;
-        for (int w = 0; w < 4; ++w) M = fmaxf(M, wm[w * 8 + tid]);
-        float l = 0.f;
-        for (int w = 0; w < 4; ++w)
-            if (wm[w * 8 + tid] != -INFINITY) l += exp2f(wm[w * 8 + tid] - M) * wl[w * 8 + tid];
-        cm[tid] = M;
-        cl[tid] = l;
-    }
-    __syncthreads();
-    for (int i = tid; i < NR * D; i += 128) {
-        const int n = i / D;
-        const float M = cm[n];
-        float a = 0.f;
-        for (int w = 0; w < 4; ++w)
-            if (wm[w * 8 + n] != -INFINITY) a += exp2f(wm[w * 8 + n] - M) * wo[(w * 8 + n) * WS + (i % D)];
-        co[i] = a;
-    }
-    __syncthreads();
-
     // rows 0..G-1 -> O of row z; rows G..2G-1 (fused slot query) -> O_g of slot row si
     EpiOut out;
     out.o = p.o + ((size_t)z * p.Hq + (size_t)h * G) * D;
@@ -298,15 +297,29 @@ __global__ void __launch_bounds__(128) decode_mma_kernel(const __grid_constant__
         cg::cluster_group cluster = cg::this_cluster();
         const int nc = (int)cluster.num_blocks(), rank = (int)cluster.block_rank();
         const int per = (NR * D + nc - 1) / nc;
+        // merge this CTA's 4 warps per element (one pass, no further block
+        // barrier) and push the CTA partial to the rank that finalises it
         for (int i = tid; i < NR * D; i += 128) {
-            const int k = i / per;
-            cluster.map_shared_rank(r_o, k)[rank * per + (i - k * per)] = co[i];
-        }
-        if (tid < NR)
-            for (int k = 0; k < nc; ++k) {
-                cluster.map_shared_rank(r_m, k)[rank * 8 + tid] = cm[tid];
-                cluster.map_shared_rank(r_l, k)[rank * 8 + tid] = cl[tid];
+            const int n = i / D, d = i % D;
+            float M = -INFINITY;
+#pragma unroll
+            for (int w = 0; w < 4; ++w) M = fmaxf(M, wm[w * 8 + n]);
+            float l = 0.f, a = 0.f;
+#pragma unroll
+            for (int w = 0; w < 4; ++w) {
+                const float mw = wm[w * 8 + n];
+                const float ew = mw == -INFINITY ? 0.f : exp2f(mw - M);
+                l += ew * wl[w * 8 + n];
+                a += ew * wo[(w * 8 + n) * WS + d];
             }
+            const int k = i / per;
+            cluster.map_shared_rank(r_o, k)[rank * per + (i - k * per)] = a;
+            if (d == 0)
+                for (int kk = 0; kk < nc; ++kk) {
+                    cluster.map_shared_rank(r_m, kk)[rank * 8 + n] = M;
+                    cluster.map_shared_rank(r_l, kk)[rank * 8 + n] = l;
+                }
+        }
         cluster.sync();                               // every peer's pushes have landed here
         float* w = scratch;                           // [8 rows][8 ranks] merge weights
         float* den = w + 64;                          // [8]
@@ -340,6 +353,25 @@ __global__ void __launch_bounds__(128) decode_mma_kernel(const __grid_constant__
         }
         final_cta = rank == 0;
     } else {
+        if (tid < NR) {
+            float M = -INFINITY;
+            for (int w = 0; w < 4; ++w) M = fmaxf(M, wm[w * 8 + tid]);
+            float l = 0.f;
+            for (int w = 0; w < 4; ++w)
+                if (wm[w * 8 + tid] != -INFINITY) l += exp2f(wm[w * 8 + tid] - M) * wl[w * 8 + tid];
+            cm[tid] = M;
+            cl[tid] = l;
+        }
+        __syncthreads();
+        for (int i = tid; i < NR * D; i += 128) {
+            const int n = i / D;
+            const float M = cm[n];
+            float a = 0.f;
+            for (int w = 0; w < 4; ++w)
+                if (wm[w * 8 + n] != -INFINITY) a += exp2f(wm[w * 8 + n] - M) * wo[(w * 8 + n) * WS + (i % D)];
+            co[i] = a;
+        }
+        __syncthreads();
         float* part = p.part + (size_t)(z * p.Hkv + h) * p.n_split * p.rows_per_pair * (D + 2);
         final_cta = split_epilogue<D>(NR, cm, cl, co, out, part, p.tickets + z * p.Hkv + h, split, p.n_split,
                                       scratch);
