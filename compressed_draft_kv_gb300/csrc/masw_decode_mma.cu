@@ -91,22 +91,7 @@ __global__ void __launch_bounds__(128) decode_mma_kernel(const __grid_constant__
         s_start[n] = acc;
         s_nseg = n;
     };
-    if (tid == 0) {
-        build(*(volatile const int*)(p.d_t + ci), *(volatile const int*)(p.d_m + ci));
-        // Warm L2 with this CTA's share of the (speculative) segment list while
-        // the previous kernel finishes.  Only a hint: the copies into shared
-        // memory happen after the wait and read whatever L2 then holds.
-        const int tot = s_start[s_nseg];
-        const int ch = (((tot + p.n_split - 1) / p.n_split) + 15) & ~15;
-        const int a0 = imin(tot, split * ch), a1 = imin(tot, a0 + ch);
-        for (int s = 0; s < s_nseg; ++s) {
-            const int lo = imax(a0, s_start[s]), hi = imin(a1, s_start[s + 1]);
-            if (lo < hi) {
-                bulk_prefetch_l2(s_vk[s] + (size_t)lo * ROWB, (uint32_t)(hi - lo) * ROWB);
-                bulk_prefetch_l2(s_vv[s] + (size_t)lo * ROWB, (uint32_t)(hi - lo) * ROWB);
-            }
-        }
-    }
+    if (tid == 0) build(*(volatile const int*)(p.d_t + ci), *(volatile const int*)(p.d_m + ci));
     pdl_wait();
     pdl_trigger();
 
