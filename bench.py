@@ -129,83 +129,109 @@ class ClockSampler:
 
 # ------------------------------------------------------------- GPU bench --
 
+def workload_prefixes(w: dict, synth) -> list[int]:
+    """Per-sequence prefix lengths.  Fixed-prefix workloads: the same prefix for
+    every sequence.  Ragged workloads: uniform on [prefix_lo, prefix_hi], each
+    snapped down to the nearest length at which sequence b reaches a
+    compression boundary at draft step (b mod steps) + 1, so every iteration
+    crosses boundaries at staggered steps."""
+    if "prefix" in w:
+        return [w["prefix"]] * w["batch"]
+    base = synth.ragged_prefixes(w["batch"], w["prefix_lo"], w["prefix_hi"], w["seed"])
+    out = []
+    for b, p0 in enumerate(base):
+        s_b = b % w["steps"] + 1
+        target = (w["S"] + w["W"] - s_b) % w["r"]
+        out.append(p0 - ((p0 - target) % w["r"]))
+    return out
+
+
 class DraftBench:
-    def __init__(self, torch, capi, synth, prefix: int):
+    """One speculative draft iteration of a workload, captured as a CUDA graph."""
+
+    def __init__(self, torch, capi, synth, workload: str, prefix: int | None = None):
         self.torch, self.capi = torch, capi
-        w = dict(synth.WORKLOADS[WORKLOAD])
+        w = dict(synth.WORKLOADS[workload])
+        if prefix is not None:
+            w["prefix"] = prefix
+            w.pop("prefix_lo", None)
         self.w = w
         self.L, self.B, self.Hq, self.Hkv, self.D = w["layers"], w["batch"], w["Hq"], w["Hkv"], w["D"]
         self.S, self.W, self.r = w["S"], w["W"], w["r"]
         self.steps = w["steps"]
         self.R = 16                      # the pages' 16-token raw-KV rollback window
-        self.prefix = prefix
+        self.prefixes = workload_prefixes(w, synth)
+        pmax = max(self.prefixes)
         self.dev = torch.device("cuda", torch.cuda.current_device())
         dt = torch.bfloat16
         self.h = capi.masw_mem_create(self.S, self.W, self.r, self.Hkv, self.D, self.L, batch=self.B,
-                                      dtype=capi.MASW_BF16, max_seq_len=prefix + 32, full_kv=True,
+                                      dtype=capi.MASW_BF16, max_seq_len=pmax + 32, full_kv=True,
                                       rollback_reserve=self.R)
-        n = max(0, (prefix - self.S - self.W) // self.r)
-        self.n_slots0 = n
+        nmax = max(0, (pmax - self.S - self.W) // self.r)
         g = torch.Generator(device=self.dev)
         g.manual_seed(2)
-        # four distinct seeded draws, reused across (layer, sequence) blocks
+        # four distinct seeded N(0,1) draws, reused across (layer, sequence) blocks
         draws = []
         for _ in range(4):
-            kr = torch.randn(prefix, self.Hkv, self.D, generator=g, device=self.dev).to(dt)
-            vr = torch.randn(prefix, self.Hkv, self.D, generator=g, device=self.dev).to(dt)
-            ks = torch.randn(max(n, 1), self.Hkv, self.D, generator=g, device=self.dev).to(dt)[:n]
-            vs = torch.randn(max(n, 1), self.Hkv, self.D, generator=g, device=self.dev).to(dt)[:n]
-            draws.append((kr, vr, ks.contiguous() if n else None, vs.contiguous() if n else None))
+            kr = torch.randn(pmax, self.Hkv, self.D, generator=g, device=self.dev).to(dt)
+            vr = torch.randn(pmax, self.Hkv, self.D, generator=g, device=self.dev).to(dt)
+            ks = torch.randn(max(nmax, 1), self.Hkv, self.D, generator=g, device=self.dev).to(dt)
+            vs = torch.randn(max(nmax, 1), self.Hkv, self.D, generator=g, device=self.dev).to(dt)
+            draws.append((kr, vr, ks, vs))
         for l in range(self.L):
             for b in range(self.B):
                 kr, vr, ks, vs = draws[(l * self.B + b) % 4]
-                capi.masw_mem_load(self.h, l, b, kr, vr, ks, vs)
+                t = self.prefixes[b]
+                n = max(0, (t - self.S - self.W) // self.r)
+                capi.masw_mem_load(self.h, l, b, kr[:t], vr[:t], ks[:n] if n else None, vs[:n] if n else None)
         del draws
         torch.cuda.empty_cache()
-        # per (step, layer) inputs
-        self.q = [[torch.randn(self.B, self.Hq, self.D, generator=g, device=self.dev).to(dt)
-                   for _ in range(self.L)] for _ in range(self.steps)]
-        self.k = [[torch.randn(self.B, self.Hkv, self.D, generator=g, device=self.dev).to(dt)
-                   for _ in range(self.L)] for _ in range(self.steps)]
-        self.v = [[torch.randn(self.B, self.Hkv, self.D, generator=g, device=self.dev).to(dt)
-                   for _ in range(self.L)] for _ in range(self.steps)]
-        self.qg = [torch.randn(self.B, self.Hq, self.D, generator=g, device=self.dev).to(dt) for _ in range(self.L)]
-        self.kg = [torch.randn(self.B, self.Hkv, self.D, generator=g, device=self.dev).to(dt) for _ in range(self.L)]
-        self.vg = [torch.randn(self.B, self.Hkv, self.D, generator=g, device=self.dev).to(dt) for _ in range(self.L)]
+        rn = lambda *shape: torch.randn(*shape, generator=g, device=self.dev).to(dt)
+        self.q = [[rn(self.B, self.Hq, self.D) for _ in range(self.L)] for _ in range(self.steps)]
+        self.k = [[rn(self.B, self.Hkv, self.D) for _ in range(self.L)] for _ in range(self.steps)]
+        self.v = [[rn(self.B, self.Hkv, self.D) for _ in range(self.L)] for _ in range(self.steps)]
+        self.qg = [rn(self.B, self.Hq, self.D) for _ in range(self.L)]
+        self.kg = [rn(self.B, self.Hkv, self.D) for _ in range(self.L)]
+        self.vg = [rn(self.B, self.Hkv, self.D) for _ in range(self.L)]
         self.o = [[torch.empty(self.B, self.Hq, self.D, device=self.dev) for _ in range(self.L)]
                   for _ in range(self.steps)]
         self.lse = [[torch.empty(self.B, self.Hq, device=self.dev) for _ in range(self.L)]
                     for _ in range(self.steps)]
         self.og = [torch.empty(self.B, self.Hq, self.D, device=self.dev) for _ in range(self.L)]
         self.seqs = list(range(self.B))
-        # the step (0-based) at which every sequence reaches a boundary, if any
-        self.bstep = None
-        for s in range(self.steps):
-            t = prefix + s + 1
-            if t >= self.S + self.W + self.r and (t - self.S - self.W) % self.r == 0:
-                self.bstep = s
+        # sequences that reach a compression boundary at each draft step
+        self.due = []
+        for s_ in range(self.steps):
+            d = []
+            for b in range(self.B):
+                t = self.prefixes[b] + s_ + 1
+                if t >= self.S + self.W + self.r and (t - self.S - self.W) % self.r == 0:
+                    d.append(b)
+            self.due.append(d)
         self.stream = torch.cuda.Stream(device=self.dev)
 
     # one speculative iteration through the C-ABI: per step and layer one fused
-    # append + attention launch (at the boundary step also carrying every
-    # sequence's slot write), then the rollback of the 5 speculative tokens
+    # append + attention launch (carrying the slot writes of the sequences at a
+    # boundary), then the rollback of the speculative tokens
     def iteration(self, full: bool = False):
         c = self.capi
         launches = 0
-        for s in range(self.steps):
+        for s_ in range(self.steps):
+            due = self.due[s_]
             for l in range(self.L):
                 if full:
-                    c.masw_full_step(self.h, l, self.q[s][l], self.k[s][l], self.v[s][l], self.o[s][l],
-                                     self.lse[s][l])
-                elif s == self.bstep:
-                    c.masw_draft_step_slot(self.h, l, self.q[s][l], self.k[s][l], self.v[s][l], self.o[s][l],
-                                           self.seqs, self.qg[l], self.kg[l], self.vg[l], self.og[l],
-                                           lse=self.lse[s][l])
+                    c.masw_full_step(self.h, l, self.q[s_][l], self.k[s_][l], self.v[s_][l], self.o[s_][l],
+                                     self.lse[s_][l])
+                elif due:
+                    n = len(due)
+                    c.masw_draft_step_slot(self.h, l, self.q[s_][l], self.k[s_][l], self.v[s_][l], self.o[s_][l],
+                                           due, self.qg[l][:n], self.kg[l][:n], self.vg[l][:n], self.og[l][:n],
+                                           lse=self.lse[s_][l])
                 else:
-                    c.masw_draft_step(self.h, l, self.q[s][l], self.k[s][l], self.v[s][l], self.o[s][l],
-                                      self.lse[s][l])
+                    c.masw_draft_step(self.h, l, self.q[s_][l], self.k[s_][l], self.v[s_][l], self.o[s_][l],
+                                      self.lse[s_][l])
                 launches += 1
-        c.masw_rollback(self.h, self.seqs, [self.prefix] * self.B)
+        c.masw_rollback(self.h, self.seqs, self.prefixes)
         return launches + 1
 
     def capture(self, fn):
@@ -240,31 +266,42 @@ class DraftBench:
         torch.cuda.synchronize()
         return e0.elapsed_time(e1) / 1e3
 
+    def kv_bytes_per_decode_step(self, full: bool = False):
+        """K/V bytes one decode step reads over all layers and sequences (at the
+        first draft step of the iteration)."""
+        E = 2 * self.Hkv * self.D * 2
+        tot = 0
+        for t0 in self.prefixes:
+            t = t0 + 1
+            if full:
+                rows = t
+            else:
+                rows = min(self.S, t) + max(0, min(self.W, t - self.S)) + max(0, (t - self.S - self.W) // self.r)
+            tot += rows * E
+        return tot * self.L
+
     def algorithmic_bytes_per_draft_launch(self):
         """One fused draft step of one layer at t = prefix+1: the working set
-        (sink + window + slots, K and V, 4096 B per entry for 8 kv heads x 128
-        bf16) of every sequence, plus Q (bf16), the new token's K/V (read once,
-        written to the pool and to the full-KV cache) and O, LSE (fp32)."""
-        t = self.prefix + 1
-        nloc = max(0, min(self.W, t - self.S))
-        m = max(0, (t - self.S - self.W) // self.r)
+        (sink + window + slots, K and V, 2*Hkv*D*2 bytes per entry) of every
+        sequence, plus Q (bf16), the new token's K/V (read once, written to the
+        pool and to the full-KV cache) and O, LSE (fp32)."""
         E = 2 * self.Hkv * self.D * 2
-        kv = self.B * (min(self.S, t) + nloc + m) * E
+        kv = self.kv_bytes_per_decode_step() // self.L
         other = self.B * self.Hq * self.D * 2 + self.B * E * 3 + self.B * self.Hq * (self.D + 1) * 4
         return kv + other, kv, other
 
     def time_draft_kernel(self, reps: int):
         """Average duration of one fused masw_draft_step launch, timed with
         CUDA events on the launching stream over `reps` replays of a graph of
-        the 28 per-layer launches of one decode step followed by the one-token
+        the per-layer launches of one decode step followed by the one-token
         rollback that restores the state (counted against the step launches)."""
-        torch, c = self.torch, self.capi
+        c = self.capi
 
         def step():
             for l in range(self.L):
                 c.masw_draft_step(self.h, l, self.q[0][l], self.k[0][l], self.v[0][l], self.o[0][l],
                                   self.lse[0][l])
-            c.masw_rollback(self.h, self.seqs, [self.prefix] * self.B)
+            c.masw_rollback(self.h, self.seqs, self.prefixes)
             return self.L
         g, n = self.capture(step)
         secs = self.time_graph(g, 3, reps)
@@ -282,9 +319,7 @@ class DraftBench:
         hqg, hkg, hvg = [pin(x) for x in self.qg], [pin(x) for x in self.kg], [pin(x) for x in self.vg]
         ho = [[torch.empty(self.B, self.Hq, self.D).pin_memory() for _ in range(self.L)] for _ in range(self.steps)]
         hog = [torch.empty(self.B, self.Hq, self.D).pin_memory() for _ in range(self.L)]
-        dq = torch.empty_like(self.q[0][0])
-        dk = torch.empty_like(self.k[0][0])
-        dv = torch.empty_like(self.v[0][0])
+        dq, dk, dv = torch.empty_like(self.q[0][0]), torch.empty_like(self.k[0][0]), torch.empty_like(self.v[0][0])
         dqg, dkg, dvg = torch.empty_like(self.qg[0]), torch.empty_like(self.kg[0]), torch.empty_like(self.vg[0])
         do = torch.empty(self.B, self.Hq, self.D, device=self.dev)
         dog = torch.empty(self.B, self.Hq, self.D, device=self.dev)
@@ -293,25 +328,27 @@ class DraftBench:
         def run():
             nonlocal h2d, d2h
             h2d = d2h = 0
-            for s in range(self.steps):
+            for s_ in range(self.steps):
+                due = self.due[s_]
                 for l in range(self.L):
-                    dq.copy_(hq[s][l], non_blocking=True)
-                    dk.copy_(hk[s][l], non_blocking=True)
-                    dv.copy_(hv[s][l], non_blocking=True)
-                    h2d += dq.numel() * 2 + dk.numel() * 2 + dv.numel() * 2
-                    if s == self.bstep:
-                        dqg.copy_(hqg[l], non_blocking=True)
-                        dkg.copy_(hkg[l], non_blocking=True)
-                        dvg.copy_(hvg[l], non_blocking=True)
-                        h2d += (dqg.numel() + dkg.numel() + dvg.numel()) * 2
-                        c.masw_draft_step_slot(self.h, l, dq, dk, dv, do, self.seqs, dqg, dkg, dvg, dog)
-                        hog[l].copy_(dog, non_blocking=True)
-                        d2h += dog.numel() * 4
+                    dq.copy_(hq[s_][l], non_blocking=True)
+                    dk.copy_(hk[s_][l], non_blocking=True)
+                    dv.copy_(hv[s_][l], non_blocking=True)
+                    h2d += (dq.numel() + dk.numel() + dv.numel()) * 2
+                    if due:
+                        n = len(due)
+                        dqg[:n].copy_(hqg[l][:n], non_blocking=True)
+                        dkg[:n].copy_(hkg[l][:n], non_blocking=True)
+                        dvg[:n].copy_(hvg[l][:n], non_blocking=True)
+                        h2d += n * (self.Hq + 2 * self.Hkv) * self.D * 2
+                        c.masw_draft_step_slot(self.h, l, dq, dk, dv, do, due, dqg[:n], dkg[:n], dvg[:n], dog[:n])
+                        hog[l][:n].copy_(dog[:n], non_blocking=True)
+                        d2h += n * self.Hq * self.D * 4
                     else:
                         c.masw_draft_step(self.h, l, dq, dk, dv, do)
-                    ho[s][l].copy_(do, non_blocking=True)
+                    ho[s_][l].copy_(do, non_blocking=True)
                     d2h += do.numel() * 4
-            c.masw_rollback(self.h, self.seqs, [self.prefix] * self.B)
+            c.masw_rollback(self.h, self.seqs, self.prefixes)
             torch.cuda.current_stream().synchronize()
 
         with torch.cuda.stream(self.stream):
@@ -324,11 +361,61 @@ class DraftBench:
                 run()
             e1.record(self.stream)
             torch.cuda.synchronize()
-        secs = e0.elapsed_time(e1) / 1e3
-        return secs, h2d, d2h
+        return e0.elapsed_time(e1) / 1e3, h2d, d2h
 
     def close(self):
         self.capi.masw_mem_destroy(self.h)
+
+
+def run_verify(torch, capi, synth, reps: int = 5):
+    """Target verify attention for the 8B-target shape: batch 4, Lq = 6 (L_draft
+    + 1), 32 query / 8 kv heads, head_dim 128, 32768 + 6 keys, 32 layers with
+    distinct caches (17.2 GB, larger than L2), timed as a graph of 32 launches."""
+    w = synth.WORKLOADS["verify8b_32k"]
+    B, Lq, Hq, Hkv, D, L = w["batch"], w["Lq"], w["Hq"], w["Hkv"], w["D"], w["layers"]
+    T = w["prefix"] + Lq
+    dev = torch.device("cuda", torch.cuda.current_device())
+    g = torch.Generator(device=dev)
+    g.manual_seed(3)
+    caches = []
+    for _ in range(L):
+        kc = torch.randn(B, Hkv, T, D, generator=g, device=dev).to(torch.bfloat16)
+        vc = torch.randn(B, Hkv, T, D, generator=g, device=dev).to(torch.bfloat16)
+        caches.append((kc, vc))
+    q = [torch.randn(B, Lq, Hq, D, generator=g, device=dev).to(torch.bfloat16) for _ in range(L)]
+    kl = torch.full((B,), T, dtype=torch.int32, device=dev)
+    o = torch.empty(B, Lq, Hq, D, device=dev)
+    ws = torch.empty(capi.masw_verify_workspace_bytes(B, Lq, Hq, Hkv, D, T), dtype=torch.uint8, device=dev)
+    st = torch.cuda.Stream(device=dev)
+
+    def run():
+        for l in range(L):
+            capi.masw_verify_attn(q[l], caches[l][0], caches[l][1], kl, o, workspace=ws)
+    with torch.cuda.stream(st):
+        run()
+    torch.cuda.synchronize()
+    gr = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(gr, stream=st):
+        run()
+    for _ in range(3):
+        gr.replay()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(st):
+        e0.record(st)
+        for _ in range(reps):
+            gr.replay()
+        e1.record(st)
+    torch.cuda.synchronize()
+    secs = e0.elapsed_time(e1) / 1e3 / reps
+    kv_bytes = L * B * Hkv * T * D * 2 * 2
+    flops = L * B * Hkv * 4 * (Hq // Hkv) * sum(T - Lq + 1 + j for j in range(Lq)) * D
+    del caches
+    torch.cuda.empty_cache()
+    return {"ms_per_verify": secs * 1e3, "layers": L, "batch": B, "lq": Lq, "keys": T,
+            "kv_bytes": kv_bytes, "gbs": kv_bytes / secs / 1e9, "tflops": flops / secs / 1e12,
+            "launches": 2 * L}
 
 
 # ------------------------------------------------------------ CPU oracle --
@@ -422,11 +509,16 @@ def profile_case(kind: str, prefix: int):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
-    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="masw", choices=["masw", "reference"])
-    ap.add_argument("--prefix", type=int, default=None)
+    ap.add_argument("--workload", default=WORKLOAD,
+                    choices=["draft3b_28l_b8", "draft8b_b32_ragged", "draft3b_1layer_8k"])
+    ap.add_argument("--prefix", type=int, default=None, help="override the prefix (all sequences)")
+    ap.add_argument("--sweep", action="store_true",
+                    help="MASW vs full-KV decode steps/s at prefixes 4K..32K (one JSON line)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-verify", action="store_true")
     ap.add_argument("--e2e-iters", type=int, default=5)
     ap.add_argument("--profile-case", choices=["draft", "step", "full", "verify"], default=None,
                     help="run a few launches of one kernel on a small state (4 layers) for an ncu capture")
@@ -439,7 +531,8 @@ def main():
     local = int(os.environ.get("LOCAL_RANK", "0"))
 
     from compressed_draft_kv_gb300 import synth
-    prefix = args.prefix or synth.WORKLOADS[WORKLOAD]["prefix"]
+    wl = synth.WORKLOADS[args.workload]
+    prefix = args.prefix or wl.get("prefix", 32768)
 
     if args.profile_case:
         profile_case(args.profile_case, prefix)
@@ -448,7 +541,7 @@ def main():
     if args.impl == "reference":
         if rank != 0:
             return
-        cb = oracle_sample(seconds_budget=max(5.0, min(60.0, 2.0 * args.steps)))
+        cb = oracle_sample(seconds_budget=max(5.0, min(60.0, 0.5 * args.steps)))
         ms = 1e3 / cb["value"] * synth.WORKLOADS[WORKLOAD]["steps"]
         print(json.dumps({
             "impl": "reference", "metric": METRIC, "value": cb["value"], "unit": UNIT, "n_gpus": 0,
@@ -472,20 +565,51 @@ def main():
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
         barrier = dist.barrier
 
-    wl = synth.WORKLOADS[WORKLOAD]
-    bench = DraftBench(torch, capi, synth, prefix)
-    try:
-        g_draft, launches = bench.capture(bench.iteration)
-        g_full, launches_full = bench.capture(lambda: bench.iteration(full=True))
-        with ClockSampler(local) as clk:
-            secs = bench.time_graph(g_draft, args.warmup, args.steps, barrier)
-        secs_full = bench.time_graph(g_full, args.warmup, max(3, args.steps // 4), barrier)
-        full_iters = max(3, args.steps // 4)
-        kern_s, _ = bench.time_draft_kernel(reps=50)
-        e2e_s, h2d, d2h = bench.e2e(args.e2e_iters)
-        capi.masw_sync(bench.h)
-    finally:
-        pass
+    if args.sweep:
+        rows = []
+        for pf in (4096, 8192, 16384, 24576, 32768):
+            bench = DraftBench(torch, capi, synth, args.workload, pf)
+            g_d, _ = bench.capture(bench.iteration)
+            g_f, _ = bench.capture(lambda: bench.iteration(full=True))
+            sd = bench.time_graph(g_d, args.warmup, max(10, args.steps // 4))
+            sf = bench.time_graph(g_f, 3, 5)
+            kd = bench.kv_bytes_per_decode_step()
+            kf = bench.kv_bytes_per_decode_step(full=True)
+            ns = bench.steps
+            rows.append({"prefix": pf, "masw_steps_per_s": max(10, args.steps // 4) * ns / sd,
+                         "full_steps_per_s": 5 * ns / sf,
+                         "masw_ms_per_step": sd / (max(10, args.steps // 4) * ns) * 1e3,
+                         "full_ms_per_step": sf / (5 * ns) * 1e3,
+                         "masw_kv_gb_per_step": kd / 1e9, "full_kv_gb_per_step": kf / 1e9})
+            bench.close()
+            del bench, g_d, g_f
+            torch.cuda.empty_cache()
+        if rank == 0:
+            print(json.dumps({"metric": METRIC + " vs prefix", "unit": UNIT, "workload": args.workload,
+                              "sweep": rows}))
+        return
+
+    bench = DraftBench(torch, capi, synth, args.workload, args.prefix)
+    g_draft, launches = bench.capture(bench.iteration)
+    g_full, launches_full = bench.capture(lambda: bench.iteration(full=True))
+    full_iters = max(3, args.steps // 5)
+    with ClockSampler(local) as clk:
+        secs = bench.time_graph(g_draft, args.warmup, args.steps, barrier)
+        secs_full = bench.time_graph(g_full, 3, full_iters, barrier)
+    kern_s, _ = bench.time_draft_kernel(reps=50)
+    e2e_s, h2d, d2h = bench.e2e(args.e2e_iters)
+    capi.masw_sync(bench.h)
+    total_b, kv_b, qo_b = bench.algorithmic_bytes_per_draft_launch()
+    kv_step = bench.kv_bytes_per_decode_step()
+    kv_step_full = bench.kv_bytes_per_decode_step(full=True)
+    prefixes = list(bench.prefixes)
+    due_steps = [s_ + 1 for s_ in range(bench.steps) if bench.due[s_]]
+    bench.close()
+    del g_draft, g_full, bench
+    torch.cuda.empty_cache()
+    verify = None
+    if not args.no_verify and args.workload == WORKLOAD:
+        verify = run_verify(torch, capi, synth)
 
     if world > 1:
         import torch.distributed as dist
@@ -498,34 +622,46 @@ def main():
     value = world * args.steps * dsteps / secs
     full_value = world * full_iters * dsteps / secs_full
     peak, peak_kind = _peaks()
-    total_b, kv_b, qo_b = bench.algorithmic_bytes_per_draft_launch()
     achieved = total_b / kern_s / 1e9
     line = {
-        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "metric": METRIC if args.workload == WORKLOAD else f"MASW draft-attn decode steps/s ({args.workload})",
+        "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": secs / args.steps * 1e3, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": WORKLOAD, "layers": wl["layers"], "batch": wl["batch"], "q_heads": wl["Hq"],
-                   "kv_heads": wl["Hkv"], "head_dim": wl["D"], "prefix": prefix, "S": wl["S"], "W": wl["W"],
-                   "r": wl["r"], "rollback_reserve": bench.R, "decode_steps_per_bench_step": dsteps,
-                   "boundary_step": (bench.bstep + 1) if bench.bstep is not None else None,
-                   "l2": "working set per decode step ~1 GB > 129 MB L2; no flush",
+        "config": {"workload": args.workload, "layers": wl["layers"], "batch": wl["batch"], "q_heads": wl["Hq"],
+                   "kv_heads": wl["Hkv"], "head_dim": wl["D"],
+                   "prefix": prefixes[0] if len(set(prefixes)) == 1 else f"ragged {min(prefixes)}..{max(prefixes)}",
+                   "S": wl["S"], "W": wl["W"], "r": wl["r"], "rollback_reserve": 16,
+                   "decode_steps_per_bench_step": dsteps, "boundary_steps": due_steps,
+                   "kv_gb_per_decode_step": kv_step / 1e9,
+                   "l2": "working set per decode step > 129 MB L2; no flush",
                    "launch": "CUDA graph of one speculative iteration", "parallelism": f"replicas x{world}"},
-        "full_kv": {"value": full_value, "unit": UNIT, "ms_per_step": secs_full / full_iters * 1e3},
+        "full_kv": {"value": full_value, "unit": UNIT, "ms_per_step": secs_full / full_iters * 1e3,
+                    "kv_gb_per_decode_step": kv_step_full / 1e9,
+                    "gbs": kv_step_full * full_iters * dsteps / secs_full / 1e9},
         "speedup_vs_full_kv": value / full_value,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                     "frac": achieved / peak, "traffic": _recorded_traffic(), "peak_kind": peak_kind,
+                     "frac": achieved / peak, "traffic": _recorded_traffic() if args.workload == WORKLOAD else None,
+                     "peak_kind": peak_kind,
                      "kernel": "decode_mma_kernel<128> (masw_draft_step: fused append + draft attention)",
                      "bytes_per_launch": total_b, "kv_bytes_per_launch": kv_b,
-                     "us_per_launch": kern_s * 1e6},
+                     "us_per_launch": kern_s * 1e6, "frac_of_8tbs": achieved / 8000.0},
         "gpu_launches": launches * args.steps,
         "clocks": clk.summary(),
         "e2e": {"value": world * dsteps / e2e_per, "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h,
                 "how": "eager C-ABI calls, q/k/v copied from pinned host and O read back every step"},
     }
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+    if verify:
+        # draft / target attention time per sequence: L_draft draft steps of the
+        # 3B-draft memory (batch 8) against one 8B-target verify (batch 4)
+        draft_per_seq = (secs / args.steps) / wl["batch"]
+        verify_per_seq = verify["ms_per_verify"] / 1e3 / verify["batch"]
+        verify["draft_over_verify_per_sequence"] = draft_per_seq / verify_per_seq
+        verify["hbm_frac"] = verify["gbs"] / peak
+        line["verify"] = verify
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and args.workload == WORKLOAD:
         line["cpu_baseline"] = oracle_sample()
-    bench.close()
     if rank == 0:
         print(json.dumps(line))
     if world > 1:
