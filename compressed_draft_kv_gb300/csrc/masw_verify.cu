@@ -38,7 +38,7 @@ constexpr int kVNst = 3;
 constexpr int kVSmem = kVNst * kVStage;
 constexpr int kVMaxSplit = 64;       // bounds the merge scratch kept in shared memory
 constexpr int kVMaxNQ = 32;
-static_assert((2 * 4 * kVMaxNQ + 4 * kVMaxNQ * kVD + 2 * kVMaxNQ + kVMaxNQ * kVD +
+static_assert((2 * 4 * kVMaxNQ + 4 * kVMaxNQ * (kVD + 8) + 2 * kVMaxNQ + kVMaxNQ * kVD +
                epilogue_scratch_floats(kVMaxNQ, kVMaxSplit)) * 4 <= kVSmem,
               "verify merge does not fit in the stage buffers");
 
@@ -193,10 +193,11 @@ __global__ void __launch_bounds__(128) verify_kernel(const __grid_constant__ Ver
 
     // ---- warp results -> shared, then merge the 4 warps ----
     constexpr int NQM = NT * 8;
+    constexpr int WS = kVD + 8;                     // padded row stride: conflict-free stores
     float* wm = reinterpret_cast<float*>(smem);    // [4][NQM]
     float* wl = wm + 4 * NQM;                       // [4][NQM]
-    float* wo = wl + 4 * NQM;                       // [4][NQM][D]
-    float* cm = wo + 4 * NQM * kVD;                 // [NQM]
+    float* wo = wl + 4 * NQM;                       // [4][NQM][WS]
+    float* cm = wo + 4 * NQM * WS;                  // [NQM]
     float* cl = cm + NQM;
     float* co = cl + NQM;                           // [NQM][D]
     float* scratch = co + NQM * kVD;
@@ -216,8 +217,8 @@ __global__ void __launch_bounds__(128) verify_kernel(const __grid_constant__ Ver
 #pragma unroll
             for (int mt = 0; mt < 8; ++mt) {
                 const int d = mt * 16 + (lane >> 2);
-                wo[(warp * NQM + n) * kVD + d] = acc[mt][nt][e];
-                wo[(warp * NQM + n) * kVD + d + 8] = acc[mt][nt][e + 2];
+                wo[(warp * NQM + n) * WS + d] = acc[mt][nt][e];
+                wo[(warp * NQM + n) * WS + d + 8] = acc[mt][nt][e + 2];
             }
         }
     __syncthreads();
@@ -236,7 +237,7 @@ __global__ void __launch_bounds__(128) verify_kernel(const __grid_constant__ Ver
         const float M = cm[n];
         float a = 0.f;
         for (int w = 0; w < 4; ++w)
-            if (wm[w * NQM + n] != -INFINITY) a += exp2f(wm[w * NQM + n] - M) * wo[(w * NQM + n) * kVD + (i % kVD)];
+            if (wm[w * NQM + n] != -INFINITY) a += exp2f(wm[w * NQM + n] - M) * wo[(w * NQM + n) * WS + (i % kVD)];
         co[i] = a;
     }
     __syncthreads();
@@ -256,10 +257,36 @@ __global__ void __launch_bounds__(128) verify_kernel(const __grid_constant__ Ver
     split_epilogue<kVD>(NQ, cm, cl, co, out, part, p.tickets + b * p.Hkv + h, split, p.n_split, scratch);
 }
 
-// split count shared by the launcher and the workspace query
-static int verify_splits(int B, int Hkv, int Tmax, int num_sms) {
+// Resident verify CTAs per SM for NT query tiles (cached per device).
+static int verify_occupancy(int NT) {
+    static int cache[64][5] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64 || NT < 1 || NT > 4) return 1;
+    if (!cache[dev][NT]) {
+        int n = 0;
+        cudaError_t e = cudaSuccess;
+        switch (NT) {
+            case 1: e = cudaFuncSetAttribute(verify_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, kVSmem);
+                    if (!e) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, verify_kernel<1>, 128, kVSmem); break;
+            case 2: e = cudaFuncSetAttribute(verify_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, kVSmem);
+                    if (!e) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, verify_kernel<2>, 128, kVSmem); break;
+            case 3: e = cudaFuncSetAttribute(verify_kernel<3>, cudaFuncAttributeMaxDynamicSharedMemorySize, kVSmem);
+                    if (!e) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, verify_kernel<3>, 128, kVSmem); break;
+            default: e = cudaFuncSetAttribute(verify_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize, kVSmem);
+                    if (!e) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, verify_kernel<4>, 128, kVSmem); break;
+        }
+        if (e != cudaSuccess) cudaGetLastError();
+        cache[dev][NT] = n > 0 ? n : 1;
+    }
+    return cache[dev][NT];
+}
+
+// Split count shared by the launcher and the workspace query: one wave of the
+// resident CTA slots, at least 256 keys per split.
+static int verify_splits(int B, int Hkv, int Tmax, int num_sms, int NT) {
     const int pairs = B * Hkv;
-    int n = imax(1, (4 * num_sms + pairs - 1) / pairs);
+    const int slots = verify_occupancy(NT) * num_sms;
+    int n = imax(1, slots / pairs);
     n = imin(n, imax(1, (Tmax + 255) / 256));
     return imin(n, kVMaxSplit);
 }
@@ -295,8 +322,9 @@ extern "C" int masw_verify_workspace_bytes(int B, int Lq, int Hq, int Hkv, int D
     if (rc) return masw_set_error(nullptr, rc, "unsupported verify sizes (D must be 128, Lq*Hq/Hkv <= 32)");
     int sms = 0;
     if (num_sms_current(&sms)) return masw_set_error(nullptr, MASW_ECUDA, "cannot query the current device");
-    const int n_split = verify_splits(B, Hkv, Tmax, sms);
-    *bytes = verify_part_bytes(B, Hkv, (Hq / Hkv) * Lq, n_split) + (size_t)B * Hkv * sizeof(unsigned);
+    const int NQ = (Hq / Hkv) * Lq;
+    const int n_split = verify_splits(B, Hkv, Tmax, sms, (NQ + 7) / 8);
+    *bytes = verify_part_bytes(B, Hkv, NQ, n_split) + (size_t)B * Hkv * sizeof(unsigned);
     return MASW_OK;
 }
 
@@ -328,7 +356,7 @@ extern "C" int masw_verify_attn(const void* q, const void* k_cache, const void* 
     int sms = 0;
     if (num_sms_current(&sms)) return masw_set_error(nullptr, MASW_ECUDA, "verify: cannot query the device");
     const int G = Hq / Hkv, NQ = G * Lq;
-    const int n_split = verify_splits(B, Hkv, Tmax, sms);
+    const int n_split = verify_splits(B, Hkv, Tmax, sms, (NQ + 7) / 8);
     const size_t partb = verify_part_bytes(B, Hkv, NQ, n_split);
     if (workspace_bytes < partb + (size_t)B * Hkv * sizeof(unsigned))
         return masw_set_error(nullptr, MASW_EINVAL, "verify: workspace too small");
@@ -441,7 +469,7 @@ extern "C" int masw_verify_attn_noalloc(const void* q, const void* k_cache, cons
     void* scratch = nullptr;
     if ((rc = noalloc_scratch(dev, &scratch))) return rc;
     const int G = Hq / Hkv, NQ = G * Lq;
-    int n_split = verify_splits(B, Hkv, Tmax, sms);
+    int n_split = verify_splits(B, Hkv, Tmax, sms, (NQ + 7) / 8);
     while (n_split > 1 && verify_part_bytes(B, Hkv, NQ, n_split) > kNoAllocPartBytes) --n_split;
     VerifyParams prm;
     std::memset(&prm, 0, sizeof(prm));
