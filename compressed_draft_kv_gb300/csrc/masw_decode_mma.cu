@@ -227,12 +227,10 @@ __global__ void __launch_bounds__(128) decode_mma_kernel(const __grid_constant__
                 pr[e + 2] = exp2f(x[e + 2] - m_new);
                 l_run[e] = l_run[e] * alpha + pr[e] + pr[e + 2];
                 m_run[e] = m_new;
-                if (__any_sync(0xffffffffu, alpha != 1.f)) {   // alpha == 1 everywhere: nothing to rescale
 #pragma unroll
-                    for (int mt = 0; mt < KS; ++mt) {
-                        acc[mt][e] *= alpha;
-                        acc[mt][e + 2] *= alpha;
-                    }
+                for (int mt = 0; mt < KS; ++mt) {
+                    acc[mt][e] *= alpha;
+                    acc[mt][e + 2] *= alpha;
                 }
             }
             const uint32_t pb0 = movmatrix_t(pack_bf16(pr[0], pr[1]));

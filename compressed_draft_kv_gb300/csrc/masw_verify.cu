@@ -169,14 +169,10 @@ __global__ void __launch_bounds__(128) verify_kernel(const __grid_constant__ Ver
                     pr[e + 2] = exp2f(x[e + 2] - m_use);
                     l_run[nt][e] = l_run[nt][e] * alpha + pr[e] + pr[e + 2];
                     m_run[nt][e] = m_new;
-                    // rescale only when some column of the warp raised its max
-                    // (alpha is exactly 1 otherwise)
-                    if (__any_sync(0xffffffffu, alpha != 1.f)) {
 #pragma unroll
-                        for (int mt = 0; mt < 8; ++mt) {
-                            acc[mt][nt][e] *= alpha;
-                            acc[mt][nt][e + 2] *= alpha;
-                        }
+                    for (int mt = 0; mt < 8; ++mt) {
+                        acc[mt][nt][e] *= alpha;
+                        acc[mt][nt][e + 2] *= alpha;
                     }
                 }
                 pb[nt][0] = movmatrix_t(pack_bf16(pr[0], pr[1]));
