@@ -22,6 +22,12 @@ WORKLOADS = {
                            dtype="bf16", seed=2, steps=5),
     "verify8b_32k": dict(Hq=32, Hkv=8, D=128, layers=32, batch=4, prefix=32768, Lq=6,
                          dtype="bf16", seed=3),
+    # the pages' own memory configuration: S = W = 128 and nominal 4x / 8x
+    # compression (r = 4 / 8), on the 3B-draft attention shape at 32K
+    "paper_s128_w128_r4": dict(Hq=24, Hkv=8, D=128, layers=28, batch=8, prefix=32768, S=128, W=128, r=4,
+                               dtype="bf16", seed=5, steps=5),
+    "paper_s128_w128_r8": dict(Hq=24, Hkv=8, D=128, layers=28, batch=8, prefix=32768, S=128, W=128, r=8,
+                               dtype="bf16", seed=6, steps=5),
     "draft8b_b32_ragged": dict(Hq=32, Hkv=8, D=128, layers=32, batch=32, prefix_lo=16384, prefix_hi=32768,
                                S=4, W=2048, r=1024, dtype="bf16", seed=4, steps=8),
 }

@@ -311,6 +311,32 @@ def test_fused_full_step():
         p.close()
 
 
+@pytest.mark.parametrize("r", [4, 8])
+def test_paper_configuration_many_slots(r):
+    """The pages' configuration S = W = 128 with r = 4 / 8: the slot chain holds
+    most of the working set (hundreds of slots); boundaries every r steps."""
+    S = W = 128
+    p = Pair(S, W, r, 8, 128, 1, 2, "bf16", 24, max_seq_len=1400, reserve=8, full_kv=True, tag=f"paper{r}")
+    try:
+        p.load(0, 0, 1200, seed=1)
+        p.load(0, 1, 701, seed=2)
+        assert p.ref.m(0, 0) == (1200 - 256) // r
+        for step in range(1, 3 * r + 2):
+            p.step = step
+            due = [b for b in range(2) if orc.is_boundary(p.ref.t(0, b) + 1, S, W, r)
+                   and p.ref.m(0, b) == orc.slot_count(p.ref.t(0, b) + 1, S, W, r) - 1]
+            if due:
+                p.fstep_slot(0, due)
+            else:
+                p.fstep(0)
+            if step % 3 == 0:
+                p.draft(0, full=True)
+        p.check_state(0, 0)
+        p.check_state(0, 1)
+    finally:
+        p.close()
+
+
 def test_state_errors():
     p = Pair(2, 8, 4, 2, 64, 1, 1, "f32", 4, max_seq_len=18, tag="err")
     try:
