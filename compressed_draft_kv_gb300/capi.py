@@ -24,6 +24,7 @@ EXPORTS = [
     "masw_draft_step", "masw_full_step", "masw_draft_step_slot",
     "masw_verify_attn", "masw_verify_workspace_bytes", "masw_verify_attn_noalloc", "masw_mem_load", "masw_mem_export",
     "masw_query", "masw_sync", "masw_index", "masw_version",
+    "masw_greedy_accept", "masw_greedy_workspace_bytes", "masw_eq1_speedup",
 ]
 
 
@@ -76,6 +77,8 @@ def load() -> ctypes.CDLL:
         "masw_query": [P, I, I, ctypes.POINTER(masw_state_t)],
         "masw_sync": [P, P],
         "masw_index": [I, I, I, I, I, I],
+        "masw_greedy_accept": [P, P, I, I, I, I, P, P, P, Z, P],
+        "masw_greedy_workspace_bytes": [I, I, I, ctypes.POINTER(Z)],
     }
     for name, args in sig.items():
         fn = getattr(lib, name)
@@ -83,6 +86,8 @@ def load() -> ctypes.CDLL:
         fn.restype = I
     lib.masw_last_error.argtypes = [P]
     lib.masw_last_error.restype = ctypes.c_char_p
+    lib.masw_eq1_speedup.argtypes = [ctypes.c_double, I, ctypes.c_double, ctypes.c_double]
+    lib.masw_eq1_speedup.restype = ctypes.c_double
     lib.masw_version.argtypes = []
     lib.masw_version.restype = ctypes.c_char_p
     _lib = lib
@@ -224,6 +229,30 @@ def masw_verify_attn_noalloc(q, k_cache, v_cache, kv_len, o, lse=None, scale=0.0
     Hkv, Tmax = k_cache.shape[1], k_cache.shape[2]
     _check(load().masw_verify_attn_noalloc(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(kv_len), B, Lq, Hq, Hkv, D,
                                            Tmax, MASW_BF16, scale, _ptr(o), _ptr(lse), _stream(stream)))
+
+
+def masw_greedy_accept(logits, draft, tokens, n_emit, workspace=None, stream=None):
+    """logits [B, L+1, V] (bf16 or fp32), draft [B, L] int32 -> tokens [B, L+1], n_emit [B] (int32)."""
+    import torch
+    B, L1, V = logits.shape
+    L = L1 - 1
+    need = ctypes.c_size_t()
+    _check(load().masw_greedy_workspace_bytes(B, L, V, ctypes.byref(need)))
+    if workspace is None:
+        workspace = torch.empty(need.value, dtype=torch.uint8, device=logits.device)
+    dt = MASW_BF16 if logits.dtype == torch.bfloat16 else MASW_F32
+    _check(load().masw_greedy_accept(_ptr(logits), _ptr(draft), B, L, V, dt, _ptr(tokens), _ptr(n_emit),
+                                     _ptr(workspace), workspace.numel(), _stream(stream)))
+
+
+def masw_greedy_workspace_bytes(B, L, V) -> int:
+    out = ctypes.c_size_t()
+    _check(load().masw_greedy_workspace_bytes(B, L, V, ctypes.byref(out)))
+    return out.value
+
+
+def masw_eq1_speedup(l_acc, l_draft, t_draft, t_target) -> float:
+    return load().masw_eq1_speedup(l_acc, l_draft, t_draft, t_target)
 
 
 # ---------------------------------------------------------------- plumbing --

@@ -248,6 +248,32 @@ int masw_verify_attn_noalloc(const void* q, const void* k_cache, const void* v_c
                              int Tmax, int dtype, float scale, float* o, float* lse,
                              masw_stream_t stream);
 
+/* ---- speculative acceptance ------------------------------------------------------ */
+
+/* Greedy acceptance of a speculative block ([EN] §2.2 and §3.3 Algorithm 2
+ * step 5; the pages' experiments decode greedily, temperature 0).  For each
+ * sequence b: tokens[b][j] = argmax over v of logits[b][j][v] for j = 0..L (ties
+ * go to the smallest id; NaN entries are skipped); L_acc = the first j < L with
+ * draft[b][j] != tokens[b][j], or L when all drafts match; n_emit[b] = L_acc + 1,
+ * and the emitted tokens are tokens[b][0 .. L_acc] (accepted drafts, then the
+ * target's correction or bonus token).
+ * logits: device [B, L+1, V] (dtype MASW_BF16 or MASW_F32); draft: device int
+ * [B, L]; tokens: device int [B, L+1]; n_emit: device int [B]; workspace:
+ * device scratch of masw_greedy_workspace_bytes() bytes (16-byte aligned; no
+ * initialisation needed; not shared by overlapping calls). */
+int masw_greedy_accept(const void* logits, const int* draft, int B, int L, int V, int dtype,
+                       int* tokens, int* n_emit, void* workspace, size_t workspace_bytes,
+                       masw_stream_t stream);
+
+/* Bytes of workspace masw_greedy_accept needs for these sizes on the current device. */
+int masw_greedy_workspace_bytes(int B, int L, int V, size_t* bytes);
+
+/* Eq. 1 of [EN] §2.2: speedup over autoregressive decoding,
+ * (l_acc + 1) / (l_draft * t_draft / t_target + 1), from the mean accepted
+ * length and the per-token draft and target latencies.  Host only; returns -1
+ * for invalid arguments. */
+double masw_eq1_speedup(double l_acc, int l_draft, double t_draft, double t_target);
+
 /* ---- plumbing for set-up, tests and benchmarks --------------------------------- */
 
 /* Set (layer, seq) to the state after t raw tokens whose K/V are k_raw, v_raw

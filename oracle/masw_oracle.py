@@ -60,7 +60,7 @@ __all__ = [
     "local_window", "n_local", "slot_count", "boundary", "is_boundary",
     "slot_pos_id", "working_set_size", "draft_mask", "slot_write_mask",
     "full_mask", "verify_mask", "attention", "IndexSim", "MaswOracle",
-    "verify_attn",
+    "verify_attn", "greedy_accept", "eq1_speedup",
 ]
 
 
@@ -447,3 +447,34 @@ def verify_attn(q, k_cache, v_cache, kv_len, scale: float | None = None):
         for j in range(Lq):
             O[b, j], L[b, j] = attention(q[b, j], K, V, mask[j], scale)
     return O, L
+
+
+# --------------------------------------------------------------------------
+# Speculative acceptance and the speedup model.
+# --------------------------------------------------------------------------
+
+def greedy_accept(logits, draft):
+    """Greedy speculative acceptance ([EN] §2.2, §3.3 Algorithm 2 step 5; the
+    experiments use temperature 0).  logits [B, L+1, V], draft [B, L] ->
+    tokens [B, L+1] (target argmax per position, first index among ties) and
+    n_emit [B] = L_acc + 1, L_acc = number of leading drafts equal to the
+    target's tokens."""
+    logits = np.asarray(logits, dtype=np.float64)
+    draft = np.asarray(draft)
+    B, L1, V = logits.shape
+    L = L1 - 1
+    tokens = np.zeros((B, L1), dtype=np.int64)
+    n_emit = np.zeros(B, dtype=np.int64)
+    for b in range(B):
+        for j in range(L1):
+            tokens[b, j] = int(np.argmax(logits[b, j]))
+        l_acc = 0
+        while l_acc < L and draft[b, l_acc] == tokens[b, l_acc]:
+            l_acc += 1
+        n_emit[b] = l_acc + 1
+    return tokens, n_emit
+
+
+def eq1_speedup(l_acc: float, l_draft: int, t_draft: float, t_target: float) -> float:
+    """Eq. 1 of [EN] §2.2: (L_acc + 1) / (L_draft * t_d / t_t + 1)."""
+    return (l_acc + 1.0) / (l_draft * (t_draft / t_target) + 1.0)

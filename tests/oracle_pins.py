@@ -418,9 +418,50 @@ def pin_rollback(o):
         raise AssertionError("rollback by 4 > R=3 must be refused")
 
 
+def pin_greedy_accept(o):
+    """Greedy acceptance against a hand loop on tiny logits, with the special
+    cases: all drafts accepted (bonus token), first draft rejected, ties going
+    to the smallest id."""
+    rng = _rng(21)
+    B, L, V = 5, 4, 11
+    logits = rng.standard_normal((B, L + 1, V))
+    arg = logits.argmax(-1)
+    draft = arg[:, :L].copy()
+    draft[1, 0] = (arg[1, 0] + 1) % V           # first rejected
+    draft[2, 2] = (arg[2, 2] + 3) % V           # two accepted
+    draft[3, 3] = (arg[3, 3] + 1) % V           # three accepted
+    tokens, n_emit = o.greedy_accept(logits, draft)
+    for b in range(B):
+        want_tok = []
+        for j in range(L + 1):
+            best, bi = -math.inf, -1
+            for v in range(V):
+                if logits[b, j, v] > best:
+                    best, bi = logits[b, j, v], v
+            want_tok.append(bi)
+        k = 0
+        while k < L and draft[b, k] == want_tok[k]:
+            k += 1
+        assert list(tokens[b]) == want_tok
+        assert n_emit[b] == k + 1
+    assert list(n_emit) == [L + 1, 1, 3, 4, L + 1]
+    tied = np.zeros((1, 2, 6))
+    tied[0, 0, [2, 4]] = 1.0
+    tok, n = o.greedy_accept(tied, np.array([[2]]))
+    assert tok[0, 0] == 2 and n[0] == 2 and tok[0, 1] == 0
+
+
+def pin_eq1(o):
+    """Eq. 1 limits: a free draft gives L_acc + 1; with t_d = t_t and nothing
+    accepted the speedup is 1 / (L_draft + 1)."""
+    assert o.eq1_speedup(5, 5, 0.0, 1.0) == 6.0
+    assert abs(o.eq1_speedup(0, 5, 1.0, 1.0) - 1.0 / 6.0) < 1e-15
+    assert abs(o.eq1_speedup(3.0, 5, 0.1, 1.0) - 4.0 / 1.5) < 1e-15
+
+
 ALL_PINS = [
     pin_golden_trace, pin_sim_vs_closed_forms, pin_working_set_at_configs,
     pin_masw_equals_full_before_eviction, pin_segments_combine, pin_bruteforce_tiny,
     pin_q_zero_and_single, pin_one_hot_exclusion, pin_sdpa, pin_permutation,
-    pin_verify_rows_are_decodes, pin_rollback,
+    pin_verify_rows_are_decodes, pin_rollback, pin_greedy_accept, pin_eq1,
 ]

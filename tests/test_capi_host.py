@@ -95,3 +95,10 @@ def test_create_without_gpu_fails_cleanly():
     assert rc in (capi.MASW_ECUDA, capi.MASW_ENOMEM)
     assert h.value is None
     assert capi.masw_last_error(None)
+
+
+def test_eq1_speedup_matches_oracle():
+    ensure_built()
+    for args in [(5, 5, 0.0, 1.0), (0, 5, 1.0, 1.0), (3.65, 5, 13.94, 40.0), (4.72, 5, 0.2, 1.0)]:
+        assert abs(capi.masw_eq1_speedup(*args) - o.eq1_speedup(*args)) < 1e-12
+    assert capi.masw_eq1_speedup(1, 5, 1.0, 0.0) == -1.0

@@ -337,6 +337,37 @@ def test_paper_configuration_many_slots(r):
         p.close()
 
 
+@pytest.mark.parametrize("dtype,B,L,V", [("bf16", 4, 5, 128256), ("f32", 3, 5, 1000), ("bf16", 2, 0, 77),
+                                         ("f32", 7, 9, 32003)])
+def test_greedy_accept(dtype, B, L, V):
+    """Greedy acceptance on seeded synthetic logits, bit-exact against the
+    oracle: a mix of fully accepted, partly accepted and rejected blocks, ties."""
+    logits = synth.normal((B, L + 1, V), dtype, "accept", B, L, V)
+    lf = logits.float().numpy()
+    arg = lf.argmax(-1)
+    draft = arg[:, :L].copy()
+    for b in range(B):
+        if L and b % 3 == 1:
+            draft[b, (b * 7) % L] = (arg[b, (b * 7) % L] + 1) % V
+        if L and b % 3 == 2:
+            draft[b, 0] = (arg[b, 0] + 5) % V
+    if V > 10:   # a tie at the top of row (0, 0): the smaller id must win
+        top = int(arg[0, 0])
+        other = (top + 7) % V
+        logits[0, 0, other] = logits[0, 0, top]
+        lf = logits.float().numpy()
+    want_tok, want_n = orc.greedy_accept(lf, draft)
+    dl = logits.to(DEV)
+    dd = torch.from_numpy(np.ascontiguousarray(draft, dtype=np.int32)).to(DEV)
+    tok = torch.full((B, L + 1), -7, dtype=torch.int32, device=DEV)
+    n = torch.full((B,), -7, dtype=torch.int32, device=DEV)
+    capi.masw_greedy_accept(dl, dd, tok, n)
+    capi.masw_greedy_accept(dl, dd, tok, n)    # a second call reuses the reset tickets
+    torch.cuda.synchronize()
+    assert np.array_equal(tok.cpu().numpy(), want_tok)
+    assert np.array_equal(n.cpu().numpy(), want_n)
+
+
 def test_state_errors():
     p = Pair(2, 8, 4, 2, 64, 1, 1, "f32", 4, max_seq_len=18, tag="err")
     try:

@@ -63,7 +63,18 @@ MUTATIONS = {
                           lambda tau, m, S, W, self_attend=False: _slot_mask_self(tau, m, S, W)),
     "verify_causal_shift": ("verify_mask", lambda kv_len, Lq: _verify_shift(kv_len, Lq)),
     "sink_dropped": ("draft_mask", lambda t, n_slots, S, W: _draft_no_sink(t, n_slots, S, W)),
+    "accept_one_past_mismatch": ("greedy_accept", lambda logits, draft: _accept_off_by_one(logits, draft)),
+    "eq1_without_verify_cost": ("eq1_speedup", lambda l_acc, l_draft, t_d, t_t: (l_acc + 1.0) / (l_draft * t_d / t_t)
+                                if t_d else l_acc + 1.0),
 }
+
+_orig_accept = o.greedy_accept
+
+
+def _accept_off_by_one(logits, draft):
+    tokens, n = _orig_accept(logits, draft)
+    L = np.asarray(draft).shape[1]
+    return tokens, np.minimum(n + 1, L + 1)
 
 _orig = {name: getattr(o, name) for name in
          ("local_window", "slot_write_mask", "verify_mask", "draft_mask")}
