@@ -60,7 +60,7 @@ __all__ = [
     "local_window", "n_local", "slot_count", "boundary", "is_boundary",
     "slot_pos_id", "working_set_size", "draft_mask", "slot_write_mask",
     "full_mask", "verify_mask", "attention", "IndexSim", "MaswOracle",
-    "verify_attn", "greedy_accept", "eq1_speedup",
+    "verify_attn", "greedy_accept", "eq1_speedup", "prefill_attn",
 ]
 
 
@@ -478,3 +478,46 @@ def greedy_accept(logits, draft):
 def eq1_speedup(l_acc: float, l_draft: int, t_draft: float, t_target: float) -> float:
     """Eq. 1 of [EN] §2.2: (L_acc + 1) / (L_draft * t_d / t_t + 1)."""
     return (l_acc + 1.0) / (l_draft * (t_draft / t_target) + 1.0)
+
+
+# --------------------------------------------------------------------------
+# Draft prefill under the structured write mask.
+# --------------------------------------------------------------------------
+
+def prefill_attn(S, W, r, q_raw, k_raw, v_raw, q_slot, k_slot, v_slot, scale=None, self_attend=False):
+    """One layer of the draft prefill over T raw tokens with the M = m(T) slot
+    tokens interleaved ([EN] §3.3 Algorithm 2 step 2, with the structured mask of
+    §3.2 Algorithm 1 step 2): raw token i reads the sink, its local window and
+    the slots materialised before it (tau_m < i); slot g_m reads the sink, the
+    window at tau_m and slots 1..m-1.  Columns are [raw 1..T] ++ [slot 1..M].
+    q_raw [T, Hq, D], k_raw/v_raw [T, Hkv, D], q_slot [M, Hq, D],
+    k_slot/v_slot [M, Hkv, D].  Returns O_raw [T, Hq, D], LSE_raw [T, Hq],
+    O_slot [M, Hq, D], LSE_slot [M, Hq]."""
+    q_raw = np.asarray(q_raw, dtype=np.float64)
+    k_raw = np.asarray(k_raw, dtype=np.float64)
+    v_raw = np.asarray(v_raw, dtype=np.float64)
+    T, Hq, D = q_raw.shape
+    M = slot_count(T, S, W, r)
+    q_slot = np.asarray(q_slot, dtype=np.float64).reshape(M, Hq, D)
+    k_slot = np.asarray(k_slot, dtype=np.float64).reshape(M, -1, D)
+    v_slot = np.asarray(v_slot, dtype=np.float64).reshape(M, -1, D)
+    scale = (1.0 / math.sqrt(D)) if not scale else float(scale)
+    K = np.concatenate([k_raw, k_slot], 0)
+    V = np.concatenate([v_raw, v_slot], 0)
+    o_raw = np.zeros((T, Hq, D))
+    l_raw = np.full((T, Hq), -np.inf)
+    for i in range(1, T + 1):
+        mask = np.zeros(T + M, dtype=bool)
+        mask[:i] = draft_mask(i, 0, S, W)            # raw columns 1..i
+        mask[T:T + slot_count(i - 1, S, W, r)] = True   # slots with tau_m <= i-1
+        o_raw[i - 1], l_raw[i - 1] = attention(q_raw[i - 1], K, V, mask, scale)
+    o_slot = np.zeros((M, Hq, D))
+    l_slot = np.full((M, Hq), -np.inf)
+    for m in range(1, M + 1):
+        tau = boundary(m, S, W, r)
+        row = slot_write_mask(tau, m, S, W, self_attend)
+        mask = np.zeros(T + M, dtype=bool)
+        mask[:tau] = row[:tau]
+        mask[T:T + m] = row[tau:]
+        o_slot[m - 1], l_slot[m - 1] = attention(q_slot[m - 1], K, V, mask, scale)
+    return o_raw, l_raw, o_slot, l_slot

@@ -459,9 +459,34 @@ def pin_eq1(o):
     assert abs(o.eq1_speedup(3.0, 5, 0.1, 1.0) - 4.0 / 1.5) < 1e-15
 
 
+def pin_prefill_equals_incremental(o):
+    """Prefill under the structured mask == appending the same tokens one by one
+    with a draft query after each append and the slot write at each boundary
+    (the decode-time definitions); a plain causal prefill differs."""
+    S, W, r, Hkv, G, D, T = 2, 5, 3, 2, 2, 4, 26
+    rng = _rng(31)
+    M = o.slot_count(T, S, W, r)
+    qr, kr, vr = rng.standard_normal((T, G * Hkv, D)), rng.standard_normal((T, Hkv, D)), rng.standard_normal((T, Hkv, D))
+    qs, ks, vs = rng.standard_normal((M, G * Hkv, D)), rng.standard_normal((M, Hkv, D)), rng.standard_normal((M, Hkv, D))
+    o_raw, l_raw, o_slot, l_slot = o.prefill_attn(S, W, r, qr, kr, vr, qs, ks, vs)
+    mem = o.MaswOracle(S, W, r, Hkv, D, 1, 1)
+    m = 0
+    for i in range(T):
+        mem.append(0, kr[i][None], vr[i][None])
+        got, gl = mem.draft_attn(0, qr[i][None])
+        assert np.allclose(got[0], o_raw[i], rtol=0, atol=1e-12) and np.allclose(gl[0], l_raw[i], rtol=0, atol=1e-12)
+        if o.is_boundary(i + 1, S, W, r):
+            gs, gsl = mem.materialize_slot(0, [0], qs[m][None], ks[m][None], vs[m][None])
+            assert np.allclose(gs[0], o_slot[m], rtol=0, atol=1e-12)
+            m += 1
+    assert m == M
+    causal, _ = o.attention(qr[-1], kr, vr, np.ones(T, bool), 1 / math.sqrt(D))
+    assert not np.allclose(causal, o_raw[-1])
+
+
 ALL_PINS = [
     pin_golden_trace, pin_sim_vs_closed_forms, pin_working_set_at_configs,
     pin_masw_equals_full_before_eviction, pin_segments_combine, pin_bruteforce_tiny,
     pin_q_zero_and_single, pin_one_hot_exclusion, pin_sdpa, pin_permutation,
-    pin_verify_rows_are_decodes, pin_rollback, pin_greedy_accept, pin_eq1,
+    pin_verify_rows_are_decodes, pin_rollback, pin_greedy_accept, pin_eq1, pin_prefill_equals_incremental,
 ]
