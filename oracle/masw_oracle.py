@@ -499,8 +499,8 @@ def prefill_attn(S, W, r, q_raw, k_raw, v_raw, q_slot, k_slot, v_slot, scale=Non
     T, Hq, D = q_raw.shape
     M = slot_count(T, S, W, r)
     q_slot = np.asarray(q_slot, dtype=np.float64).reshape(M, Hq, D)
-    k_slot = np.asarray(k_slot, dtype=np.float64).reshape(M, -1, D)
-    v_slot = np.asarray(v_slot, dtype=np.float64).reshape(M, -1, D)
+    k_slot = np.asarray(k_slot, dtype=np.float64).reshape(M, k_raw.shape[1], D)
+    v_slot = np.asarray(v_slot, dtype=np.float64).reshape(M, k_raw.shape[1], D)
     scale = (1.0 / math.sqrt(D)) if not scale else float(scale)
     K = np.concatenate([k_raw, k_slot], 0)
     V = np.concatenate([v_raw, v_slot], 0)
