@@ -13,7 +13,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 OUT_DIR = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libmasw.so")
-SOURCES = ["masw_pool.cu", "masw_decode.cu", "masw_decode_mma.cu", "masw_verify.cu", "masw_accept.cu"]
+SOURCES = ["masw_pool.cu", "masw_decode.cu", "masw_decode_mma.cu", "masw_verify.cu", "masw_accept.cu", "masw_prefill.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

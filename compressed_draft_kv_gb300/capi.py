@@ -24,7 +24,7 @@ EXPORTS = [
     "masw_draft_step", "masw_full_step", "masw_draft_step_slot",
     "masw_verify_attn", "masw_verify_workspace_bytes", "masw_verify_attn_noalloc", "masw_mem_load", "masw_mem_export",
     "masw_query", "masw_sync", "masw_index", "masw_version",
-    "masw_greedy_accept", "masw_greedy_workspace_bytes", "masw_eq1_speedup",
+    "masw_greedy_accept", "masw_greedy_workspace_bytes", "masw_eq1_speedup", "masw_prefill",
 ]
 
 
@@ -69,6 +69,7 @@ def load() -> ctypes.CDLL:
         "masw_draft_step": [P, I, P, P, P, P, I, P, P, P],
         "masw_full_step": [P, I, P, P, P, P, I, P, P, P],
         "masw_draft_step_slot": [P, I, P, P, P, P, I, P, P, IP, I, P, P, P, P, P, P],
+        "masw_prefill": [P, I, I, I, P, P, P, P, P, P, I, P, P, P, P, P],
         "masw_verify_attn": [P, P, P, P, I, I, I, I, I, I, I, F, P, P, P, Z, P],
         "masw_verify_workspace_bytes": [I, I, I, I, I, I, ctypes.POINTER(Z)],
         "masw_verify_attn_noalloc": [P, P, P, P, I, I, I, I, I, I, I, F, P, P, P],
@@ -256,6 +257,16 @@ def masw_eq1_speedup(l_acc, l_draft, t_draft, t_target) -> float:
 
 
 # ---------------------------------------------------------------- plumbing --
+
+def masw_prefill(handle, layer, seq, q_raw, k_raw, v_raw, q_slot, k_slot, v_slot, o_raw, lse_raw=None,
+                 o_slot=None, lse_slot=None, stream=None):
+    """Prefill one (layer, seq): q_raw [T, Hq, D], k_raw/v_raw [T, Hkv, D], the slot
+    tokens' q/k/v [M, ...] (None when M = 0), outputs fp32 o [.., Hq, D], lse [.., Hq]."""
+    T, Hq = q_raw.shape[0], q_raw.shape[1]
+    _check(load().masw_prefill(handle, layer, seq, T, _ptr(q_raw), _ptr(k_raw), _ptr(v_raw), _ptr(q_slot),
+                               _ptr(k_slot), _ptr(v_slot), Hq, _ptr(o_raw), _ptr(lse_raw), _ptr(o_slot),
+                               _ptr(lse_slot), _stream(stream)), handle)
+
 
 def masw_mem_load(handle, layer, seq, k_raw, v_raw, k_slots=None, v_slots=None):
     """k_raw, v_raw: [t, Hkv, D] torch tensors (CPU or CUDA), contiguous."""

@@ -147,6 +147,30 @@ int masw_materialize_slot(masw_mem_t* mem, int layer, const int* seq_ids, int n,
                           const void* q_g, const void* k_g, const void* v_g,
                           float* o_g, float* lse_g, int n_q_heads, masw_stream_t stream);
 
+/* Draft prefill of one (layer, seq) under the structured write mask ([EN] §3.3
+ * Algorithm 2 step 2, mask of §3.2 Algorithm 1 step 2): one attention pass over
+ * a prefix of T raw tokens with the M = max(0, (T-S-W)/r) slot tokens
+ * interleaved, then M_0 is stored as the sequence's memory (sink rows, the last
+ * W+R raw tokens in their ring rows, slots 1..M with position ids tau_1..tau_M,
+ * and the full cache with full_kv), so that decoding continues at t = T.
+ *   raw token i (1-based) attends to sink tokens 1..min(S, i), raw tokens
+ *   max(S+1, i-W+1)..i and slots m with tau_m < i;
+ *   slot token g_m attends to the sink, raw tokens tau_m-W+1..tau_m and slots
+ *   1..m-1 (1..m with slot_self_attend).
+ * q_raw: device [T, n_q_heads, D]; k_raw, v_raw: device [T, Hkv, D];
+ * q_slot: device [M, n_q_heads, D]; k_slot, v_slot: device [M, Hkv, D] (the
+ * slot tokens' projections; may be NULL when M = 0); all bf16, 16-byte aligned.
+ * o_raw: device float [T, n_q_heads, D]; lse_raw: device float [T, n_q_heads]
+ * or NULL; o_slot, lse_slot likewise [M, ...].  bf16 pools with head_dim 128
+ * only (EINVAL otherwise); ECAPACITY when T > max_seq_len or M exceeds the slot
+ * chain.  The previous state of (layer, seq) is replaced; inputs must stay
+ * valid until the stream reaches the call. */
+int masw_prefill(masw_mem_t* mem, int layer, int seq, int T,
+                 const void* q_raw, const void* k_raw, const void* v_raw,
+                 const void* q_slot, const void* k_slot, const void* v_slot, int n_q_heads,
+                 float* o_raw, float* lse_raw, float* o_slot, float* lse_slot,
+                 masw_stream_t stream);
+
 /* Undo the last t[b] - t_new[i] raw tokens of the listed sequences in every
  * layer ([EN] §3.3 Algorithm 2 step 6): counters go back to t_new and slots
  * with tau_m > t_new are dropped.  Needs 0 <= t - t_new <= R in every layer

@@ -68,6 +68,30 @@ class Pair:
         capi.masw_mem_load(self.h, layer, seq, kr, vr, ks if n else None, vs if n else None)
         self.ref.load(layer, seq, kr.float().numpy(), vr.float().numpy(), ks.float().numpy(), vs.float().numpy())
 
+    def prefill(self, layer, seq, t, seed=0):
+        """masw_prefill of a t-token prefix; checks O/LSE of every raw and slot
+        row against the oracle's prefill and mirrors the resulting memory into it."""
+        n = orc.slot_count(t, self.S, self.W, self.r)
+        g = lambda shape, name: synth.normal(shape, self.dtype, self.tag, "prefill", seed, name, layer, seq)
+        qr, kr, vr = g((t, self.Hq, self.D), "q"), g((t, self.Hkv, self.D), "k"), g((t, self.Hkv, self.D), "v")
+        qs, ks, vs = g((n, self.Hq, self.D), "qs"), g((n, self.Hkv, self.D), "ks"), g((n, self.Hkv, self.D), "vs")
+        o_r = torch.empty(t, self.Hq, self.D, device=DEV)
+        l_r = torch.empty(t, self.Hq, device=DEV)
+        o_s = torch.empty(max(n, 1), self.Hq, self.D, device=DEV)
+        l_s = torch.empty(max(n, 1), self.Hq, device=DEV)
+        dev = [x.to(DEV) if x.numel() else None for x in (qr, kr, vr, qs, ks, vs)]
+        capi.masw_prefill(self.h, layer, seq, *dev, o_r, l_r, o_s if n else None, l_s if n else None)
+        want = orc.prefill_attn(self.S, self.W, self.r, qr.float().numpy(), kr.float().numpy(), vr.float().numpy(),
+                                qs.float().numpy(), ks.float().numpy(), vs.float().numpy(),
+                                scale=self.ref.scale, self_attend=self.ref.self_attend)
+        capi.masw_sync(self.h)
+        assert_close(o_r, want[0], self.dtype, f"prefill O_raw l={layer} b={seq}")
+        assert_close(l_r, want[1], self.dtype, "prefill LSE_raw")
+        if n:
+            assert_close(o_s[:n], want[2], self.dtype, f"prefill O_slot l={layer} b={seq}")
+            assert_close(l_s[:n], want[3], self.dtype, "prefill LSE_slot")
+        self.ref.load(layer, seq, kr.float().numpy(), vr.float().numpy(), ks.float().numpy(), vs.float().numpy())
+
     def rand(self, shape, *name, scale=1.0):
         return synth.normal(shape, self.dtype, self.tag, "io", self.step, *name, scale=scale)
 

@@ -1,0 +1,109 @@
+"""Draft prefill (masw_prefill) against the oracle's prefill under the structured
+write mask, then decoding continued from the stored memory M_0."""
+import pytest
+import torch
+
+import oracle.masw_oracle as orc
+from compressed_draft_kv_gb300 import capi
+
+from gpu_helpers import DEV, Pair
+
+pytestmark = pytest.mark.gpu
+
+# (S, W, r, Hkv, G, T): several 64-row tiles with ragged tails, slot tiles of
+# W/r + 1 rows, r > W (one slot per tile), no sink, prefixes inside the sink and
+# inside the first window, the paper's S = W = 128 with r = 4
+CASES = [
+    (4, 16, 4, 2, 4, 100),
+    (4, 16, 4, 1, 8, 257),
+    (0, 32, 8, 2, 2, 200),
+    (8, 16, 4, 2, 4, 5),
+    (4, 64, 16, 2, 4, 60),
+    (4, 8, 16, 1, 4, 150),
+    (2, 40, 3, 2, 1, 333),
+    (128, 128, 4, 2, 4, 1024),
+]
+
+
+@pytest.mark.parametrize("S,W,r,Hkv,G,T", CASES)
+def test_prefill_matches_oracle(S, W, r, Hkv, G, T):
+    p = Pair(S, W, r, Hkv, 128, layers=2, batch=3, dtype="bf16", Hq=Hkv * G, max_seq_len=T + 64,
+             tag=f"prefill{S}_{W}_{r}_{T}")
+    try:
+        p.prefill(1, 2, T)
+        p.check_state(1, 2)
+    finally:
+        p.close()
+
+
+def test_prefill_self_attend_and_scale():
+    p = Pair(4, 16, 4, 2, 128, layers=1, batch=1, dtype="bf16", Hq=8, max_seq_len=256, self_attend=True,
+             scale=0.05, tag="prefill_sa")
+    try:
+        p.prefill(0, 0, 130)
+        p.check_state(0, 0)
+    finally:
+        p.close()
+
+
+def test_decode_continues_after_prefill():
+    """Prefill every sequence to a different length, then fused draft steps (with
+    slot writes at the boundaries), a rollback and more steps, all against the
+    oracle; the full-KV cache written by the prefill is checked too."""
+    S, W, r, Hkv, G, R = 4, 24, 4, 2, 4, 6
+    B = 3
+    p = Pair(S, W, r, Hkv, 128, layers=1, batch=B, dtype="bf16", Hq=Hkv * G, max_seq_len=400, full_kv=True,
+             reserve=R, tag="prefill_cont")
+    try:
+        lens = [37, 64, 29]            # one mid-window, one on a boundary, one just past S+W
+        for b, t in enumerate(lens):
+            p.prefill(0, b, t, seed=b)
+            p.check_state(0, b)
+        for step in range(12):
+            p.step = step
+            due = [b for b in range(B) if orc.is_boundary(p.ref.t(0, b) + 1, S, W, r)]
+            if due:
+                p.fstep_slot(0, due)
+            else:
+                p.fstep(0)
+            p.draft(0, full=True)
+        for b in range(B):
+            p.check_state(0, b)
+        t_new = [p.ref.t(0, b) - k for b, k in enumerate((R, 1, 3))]
+        capi.masw_rollback(p.h, list(range(B)), t_new)
+        p.ref.rollback(list(range(B)), t_new)
+        for step in range(12, 20):
+            p.step = step
+            due = [b for b in range(B) if orc.is_boundary(p.ref.t(0, b) + 1, S, W, r)]
+            if due:
+                p.fstep_slot(0, due)
+            else:
+                p.fstep(0)
+        for b in range(B):
+            p.check_state(0, b)
+    finally:
+        p.close()
+
+
+def test_prefill_rejects_bad_calls():
+    p = Pair(4, 16, 4, 2, 128, layers=1, batch=1, dtype="bf16", Hq=8, max_seq_len=64, tag="prefill_bad")
+    q = torch.zeros(65, 8, 128, dtype=torch.bfloat16, device=DEV)
+    kv = torch.zeros(65, 2, 128, dtype=torch.bfloat16, device=DEV)
+    o = torch.empty(65, 8, 128, device=DEV)
+    try:
+        with pytest.raises(capi.MaswError):        # T > max_seq_len
+            capi.masw_prefill(p.h, 0, 0, q, kv, kv, q, kv, kv, o)
+        with pytest.raises(capi.MaswError):        # slots needed but none given
+            capi.masw_prefill(p.h, 0, 0, q[:40], kv[:40], kv[:40], None, None, None, o)
+        with pytest.raises(capi.MaswError):        # seq out of range
+            capi.masw_prefill(p.h, 0, 1, q[:8], kv[:8], kv[:8], None, None, None, o)
+    finally:
+        p.close()
+    f = Pair(4, 16, 4, 2, 64, layers=1, batch=1, dtype="f32", Hq=8, max_seq_len=64, tag="prefill_f32")
+    try:
+        q32 = torch.zeros(8, 8, 64, device=DEV)
+        kv32 = torch.zeros(8, 2, 64, device=DEV)
+        with pytest.raises(capi.MaswError):        # bf16 / head_dim 128 pools only
+            capi.masw_prefill(f.h, 0, 0, q32, kv32, kv32, None, None, None, torch.empty(8, 8, 64, device=DEV))
+    finally:
+        f.close()
