@@ -64,6 +64,7 @@ MUTATIONS = {
     "verify_causal_shift": ("verify_mask", lambda kv_len, Lq: _verify_shift(kv_len, Lq)),
     "sink_dropped": ("draft_mask", lambda t, n_slots, S, W: _draft_no_sink(t, n_slots, S, W)),
     "accept_one_past_mismatch": ("greedy_accept", lambda logits, draft: _accept_off_by_one(logits, draft)),
+    "prefill_raw_sees_slot_of_its_own_boundary": ("prefill_attn", lambda *a, **k: _prefill_slot_too_early(*a, **k)),
     "eq1_without_verify_cost": ("eq1_speedup", lambda l_acc, l_draft, t_d, t_t: (l_acc + 1.0) / (l_draft * t_d / t_t)
                                 if t_d else l_acc + 1.0),
 }
@@ -76,6 +77,25 @@ def _accept_off_by_one(logits, draft):
     L = np.asarray(draft).shape[1]
     return tokens, np.minimum(n + 1, L + 1)
 
+def _prefill_slot_too_early(S, W, r, q_raw, k_raw, v_raw, q_slot, k_slot, v_slot, scale=None, self_attend=False):
+    """Raw token tau_m also reads slot m (the slot written at its own step)."""
+    q_raw, k_raw, v_raw = (np.asarray(x, np.float64) for x in (q_raw, k_raw, v_raw))
+    T, Hq, D = q_raw.shape
+    M = o.slot_count(T, S, W, r)
+    k_slot = np.asarray(k_slot, np.float64).reshape(M, k_raw.shape[1], D)
+    v_slot = np.asarray(v_slot, np.float64).reshape(M, k_raw.shape[1], D)
+    out = list(_orig_prefill(S, W, r, q_raw, k_raw, v_raw, q_slot, k_slot, v_slot, scale, self_attend))
+    K, V = np.concatenate([k_raw, k_slot]), np.concatenate([v_raw, v_slot])
+    sc = (1.0 / math.sqrt(D)) if not scale else float(scale)
+    for i in range(1, T + 1):
+        mask = np.zeros(T + M, dtype=bool)
+        mask[:i] = o.draft_mask(i, 0, S, W)
+        mask[T:T + o.slot_count(i, S, W, r)] = True
+        out[0][i - 1], out[1][i - 1] = o.attention(q_raw[i - 1], K, V, mask, sc)
+    return tuple(out)
+
+
+_orig_prefill = o.prefill_attn
 _orig = {name: getattr(o, name) for name in
          ("local_window", "slot_write_mask", "verify_mask", "draft_mask")}
 
