@@ -68,6 +68,17 @@ def _peaks():
         return 6800.0, "fallback"
 
 
+def _peaks_tensor():
+    """Dense bf16 tensor peak: the measured cuBLAS burst figure (prefill launches
+    are timed in short bursts), else the fallback."""
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            d = json.load(f)
+        return float(d["bf16_tflops"]), "measured (burst)"
+    except Exception:
+        return 1900.0, "fallback"
+
+
 # ----------------------------------------------------------------- clocks --
 
 class ClockSampler:
@@ -418,6 +429,66 @@ def run_verify(torch, capi, synth, reps: int = 5):
             "launches": 2 * L}
 
 
+def prefill_flops(T, S, W, r, Hq, D, self_attend=False):
+    """Algorithmic flops of one (layer, sequence) prefill: 4 D flops (QK^T and PV)
+    per query head per visible (query, key) pair of the structured mask."""
+    def slots(t):
+        return max(0, (t - S - W) // r)
+    pairs = 0
+    for i in range(1, T + 1):
+        pairs += min(S, i) + (i - max(S + 1, i - W + 1) + 1 if i > S else 0) + slots(i - 1)
+    M = slots(T)
+    for m in range(1, M + 1):
+        pairs += S + W + (m if self_attend else m - 1)
+    return 4 * D * Hq * pairs, pairs
+
+
+def run_prefill(torch, capi, synth, workload: str, T: int, reps: int = 3):
+    """Draft prefill of a T-token prefix through every layer of the draft model
+    for one sequence (one masw_prefill per layer: attention of all raw and slot
+    rows under the structured mask, then M_0 stored), timed with CUDA events."""
+    w = synth.WORKLOADS[workload]
+    L, Hq, Hkv, D, S, W, r = w["layers"], w["Hq"], w["Hkv"], w["D"], w["S"], w["W"], w["r"]
+    M = max(0, (T - S - W) // r)
+    dev = torch.device("cuda", torch.cuda.current_device())
+    g = torch.Generator(device=dev)
+    g.manual_seed(7)
+    mk = lambda *shape: torch.randn(*shape, generator=g, device=dev).to(torch.bfloat16)
+    qr, kr, vr = mk(T, Hq, D), mk(T, Hkv, D), mk(T, Hkv, D)
+    qs, ks, vs = mk(max(M, 1), Hq, D), mk(max(M, 1), Hkv, D), mk(max(M, 1), Hkv, D)
+    o_r = torch.empty(T, Hq, D, device=dev)
+    l_r = torch.empty(T, Hq, device=dev)
+    o_s = torch.empty(max(M, 1), Hq, D, device=dev)
+    l_s = torch.empty(max(M, 1), Hq, device=dev)
+    h = capi.masw_mem_create(S, W, r, Hkv, D, L, batch=1, dtype=capi.MASW_BF16, max_seq_len=T + 64,
+                             rollback_reserve=16)
+    st = torch.cuda.Stream(device=dev)
+
+    def run():
+        for l in range(L):
+            capi.masw_prefill(h, l, 0, qr, kr, vr, qs, ks, vs, o_r, l_r, o_s, l_s, stream=st)
+    with torch.cuda.stream(st):
+        run()
+        run()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(st):
+        e0.record(st)
+        for _ in range(reps):
+            run()
+        e1.record(st)
+    torch.cuda.synchronize()
+    secs = e0.elapsed_time(e1) / 1e3 / reps
+    capi.masw_mem_destroy(h)
+    flops, pairs = prefill_flops(T, S, W, r, Hq, D)
+    per_launch = secs / L
+    return {"workload": workload, "prefix": T, "layers": L, "slots": M, "ms_per_prefill": secs * 1e3,
+            "ms_per_layer": per_launch * 1e3, "tokens_per_s": T / secs,
+            "tflops": flops / per_launch / 1e12, "flops_per_layer": flops, "visible_pairs_per_head": pairs,
+            "launches": 2 * L}
+
+
 # ------------------------------------------------------------ CPU oracle --
 
 def oracle_sample(seconds_budget: float = 12.0):
@@ -471,6 +542,18 @@ def profile_case(kind: str, prefix: int):
     dev = torch.device("cuda", 0)
     g = torch.Generator(device=dev)
     g.manual_seed(5)
+    if kind == "prefill":
+        T = prefix
+        M = max(0, (T - S - W) // r)
+        mk = lambda *shape: torch.randn(*shape, generator=g, device=dev).to(torch.bfloat16)
+        h = capi.masw_mem_create(S, W, r, Hkv, D, 1, batch=1, dtype=capi.MASW_BF16, max_seq_len=T + 64)
+        qr, kr, vr, qs, ks, vs = mk(T, Hq, D), mk(T, Hkv, D), mk(T, Hkv, D), mk(M, Hq, D), mk(M, Hkv, D), mk(M, Hkv, D)
+        o_r, o_s = torch.empty(T, Hq, D, device=dev), torch.empty(max(M, 1), Hq, D, device=dev)
+        for _ in range(3):
+            capi.masw_prefill(h, 0, 0, qr, kr, vr, qs, ks, vs, o_r, None, o_s, None)
+        torch.cuda.synchronize()
+        capi.masw_mem_destroy(h)
+        return
     if kind == "verify":
         vb, Lq, Hq8 = 4, 6, 32
         T = prefix + Lq
@@ -521,7 +604,10 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-verify", action="store_true")
     ap.add_argument("--e2e-iters", type=int, default=5)
-    ap.add_argument("--profile-case", choices=["draft", "step", "full", "verify"], default=None,
+    ap.add_argument("--no-prefill", action="store_true")
+    ap.add_argument("--prefill-only", action="store_true",
+                    help="only the draft prefill of one sequence through all layers (one JSON line)")
+    ap.add_argument("--profile-case", choices=["draft", "step", "full", "verify", "prefill"], default=None,
                     help="run a few launches of one kernel on a small state (4 layers) for an ncu capture")
     args = ap.parse_args()
     if args.warmup < 3:
@@ -565,6 +651,19 @@ def main():
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
         barrier = dist.barrier
+
+    if args.prefill_only:
+        with ClockSampler(local) as clk:
+            pf = run_prefill(torch, capi, synth, args.workload, prefix, reps=max(1, args.steps // 20))
+        peak = _peaks_tensor()
+        pf["roofline"] = {"bound": "tensor", "achieved": pf["tflops"], "peak": peak[0], "unit": "TFLOP/s",
+                          "frac": pf["tflops"] / peak[0], "peak_kind": peak[1]}
+        pf["clocks"] = clk.summary()
+        if rank == 0:
+            print(json.dumps({"metric": "draft prefill tokens/s (one sequence, all layers)", "value": pf["tokens_per_s"],
+                              "unit": "tokens/s", "higher_is_better": True, "dtype": "bf16", "data": "synthetic",
+                              "prefill": pf}))
+        return
 
     if args.sweep:
         rows = []
@@ -611,6 +710,12 @@ def main():
     verify = None
     if not args.no_verify and args.workload == WORKLOAD:
         verify = run_verify(torch, capi, synth)
+    prefill = None
+    if not args.no_prefill and args.workload == WORKLOAD:
+        prefill = run_prefill(torch, capi, synth, args.workload, prefix)
+        tp = _peaks_tensor()
+        prefill["tensor_frac"] = prefill["tflops"] / tp[0]
+        prefill["tensor_peak_kind"] = tp[1]
 
     if world > 1:
         import torch.distributed as dist
@@ -661,6 +766,8 @@ def main():
         verify["draft_over_verify_per_sequence"] = draft_per_seq / verify_per_seq
         verify["hbm_frac"] = verify["gbs"] / peak
         line["verify"] = verify
+    if prefill:
+        line["prefill"] = prefill
     if rank == 0 and world == 1 and not args.no_cpu_baseline and args.workload == WORKLOAD:
         line["cpu_baseline"] = oracle_sample()
     if rank == 0:

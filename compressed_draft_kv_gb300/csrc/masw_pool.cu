@@ -657,10 +657,11 @@ int masw_sync(masw_mem_t* mem, masw_stream_t stream) {
     MASW_CUDA_TRY(mem, cudaStreamSynchronize((cudaStream_t)stream));
     int err[4] = {0, 0, 0, 0};
     MASW_CUDA_TRY(mem, cudaMemcpy(err, mem->d_err, sizeof(err), cudaMemcpyDeviceToHost));
-    if (err[0] || err[1]) {
+    if (err[0] || err[1] || err[2]) {
         const int zero[4] = {0, 0, 0, 0};
         MASW_CUDA_TRY(mem, cudaMemcpy(mem->d_err, zero, sizeof(zero), cudaMemcpyHostToDevice));
         if (err[0]) return masw_set_error(mem, MASW_ETIMEOUT, "a device-side bounded wait ran out");
+        if (err[2]) return masw_set_error(mem, MASW_ECUDA, "a kernel's shared memory was not 1024-byte aligned");
         return masw_set_error(mem, MASW_ECAPACITY, "a device-side append exceeded max_seq_len");
     }
     return MASW_OK;

@@ -6,270 +6,410 @@
 // Query rows: raw token i (1-based) reads the sink, raw tokens of its window
 // [max(S+1, i-W+1), i], and the slots materialised before it (tau_m < i); slot
 // token g_m reads the sink, the window at tau_m and slots 1..m-1.  Key rows come
-// from the caller's raw and slot K/V arrays ([T, Hkv, D], [M, Hkv, D]); the
-// visible set of a 64-row query tile is a handful of contiguous key ranges
-// (sink, window band, slot prefix), walked in 64-key blocks with the exact
-// per-element mask.
+// from the caller's raw and slot K/V arrays ([T, Hkv, D], [M, Hkv, D]).  For one
+// tile of query rows the visible keys are a few contiguous ranges (sink, window
+// band, slot prefix), and for one row each range is a single interval, so the
+// mask is two compares per score.
 //
-// Tensor cores (mma.sync m16n8k16 bf16 -> fp32), FlashAttention-style: 4 warps,
-// 16 query rows each, Q as the A operand, K rows as B fragments (ldmatrix),
-// online softmax per row, P reused from the accumulator layout as the A operand
-// of P.V, V as B fragments (ldmatrix.trans), K/V blocks staged with cp.async in
-// XOR-swizzled shared memory (2 stages).  Grid (query tiles, Hq).
+// Fifth-generation tensor cores, one CTA per (128-row query tile, query head):
+//   * TMA tiled loads (128-byte swizzle) bring Q (resident), and K and V blocks
+//     of 64 keys into two stages each;
+//   * thread 0 issues S = Q K^T (tcgen05.mma, M = 128, N = 64, accumulator in
+//     tensor memory) and O += P V (M = 128, N = 128, V read MN-major);
+//   * thread t owns query row t (TMEM lane t): it reads its 64 scores with
+//     tcgen05.ld, applies the mask and the online softmax, and writes its row of
+//     P (bf16) into shared memory in the swizzled K-major layout the next MMA
+//     reads;
+//   * the running max only moves when a row's maximum grows by more than 2^8,
+//     so the O rescale (tcgen05.ld / st of the row) is rare; the final
+//     normalisation uses the same max, so the result is exact.
+// 112 KB of shared memory and 256 TMEM columns per CTA: two CTAs per SM, whose
+// softmax and MMA phases overlap.
 #include "masw_internal.cuh"
+
+#include <cuda.h>
+#include <cudaTypedefs.h>
 
 #include <algorithm>
 #include <cstring>
+#include <mutex>
 
 namespace masw {
 
+namespace tcp {
+
+constexpr int kBM = 128;                         // query rows per CTA = TMEM lanes
+constexpr int kBN = 64;                          // keys per block
+constexpr int kD = 128;                          // head_dim
+constexpr uint32_t kQBytes = kBM * kD * 2;       // 2 panels of 128 rows x 128 B
+constexpr uint32_t kKVBytes = kBN * kD * 2;      // 2 panels of 64 rows x 128 B
+constexpr uint32_t kPBytes = kBM * kBN * 2;      // 1 panel of 128 rows x 128 B
+constexpr uint32_t kOffQ = 0;
+constexpr uint32_t kOffK = kOffQ + kQBytes;
+constexpr uint32_t kOffV = kOffK + 2 * kKVBytes;
+constexpr uint32_t kOffP = kOffV + 2 * kKVBytes;
+constexpr uint32_t kOffBar = kOffP + kPBytes;    // 7 mbarriers + the TMEM address
+constexpr uint32_t kSmem = kOffBar + 64;
+constexpr uint32_t kTmemCols = 256;
+constexpr uint32_t kColO = 0;                    // O: columns [0, 128)
+constexpr uint32_t kColS = 128;                  // S: columns [128, 192)
+// instruction descriptors (kind::f16): f32 accumulator, bf16 A and B, M = 128;
+// S: N = 64, both operands K-major; O: N = 128, B (V) MN-major
+constexpr uint32_t kIdescBase = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(kBM >> 4) << 24);
+constexpr uint32_t kIdescS = kIdescBase | ((uint32_t)(kBN >> 3) << 17);
+constexpr uint32_t kIdescO = kIdescBase | (1u << 16) | ((uint32_t)(kD >> 3) << 17);
+
+// shared-memory matrix descriptor, 128-byte swizzle (atoms of 8 rows x 128 B)
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+    return (uint64_t)((saddr >> 4) & 0x3FFFu) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
+           ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (2ull << 61);
+}
+
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, int c0, int c1, int c2,
+                                            uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], "
+        "[%5];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(bar)
+        : "memory");
+}
+__device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(
+            d_tmem),
+        "l"(a), "l"(b), "r"(idesc), "r"(acc)
+        : "memory");
+}
+__device__ __forceinline__ void umma_commit(uint32_t bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+                 : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
+#define MASW_R8(i) "=r"(v[i]), "=r"(v[i + 1]), "=r"(v[i + 2]), "=r"(v[i + 3]), "=r"(v[i + 4]), "=r"(v[i + 5]), \
+                   "=r"(v[i + 6]), "=r"(v[i + 7])
+#define MASW_W8(i) "r"(v[i]), "r"(v[i + 1]), "r"(v[i + 2]), "r"(v[i + 3]), "r"(v[i + 4]), "r"(v[i + 5]), \
+                   "r"(v[i + 6]), "r"(v[i + 7])
+// 32 consecutive fp32 columns of this thread's TMEM lane
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&v)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+        "%15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+        : MASW_R8(0), MASW_R8(8), MASW_R8(16), MASW_R8(24)
+        : "r"(taddr)
+        : "memory");
+}
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&v)[32]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+        "%15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(taddr),
+        MASW_W8(0), MASW_W8(8), MASW_W8(16), MASW_W8(24)
+        : "memory");
+}
+#undef MASW_R8
+#undef MASW_W8
+__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d)
+                 : "memory");
+}
+
+}  // namespace tcp
+
 struct PrefillParams {
-    const __nv_bfloat16* q_raw;   // [T][Hq][D]
-    const __nv_bfloat16* k_raw;   // [T][Hkv][D]
-    const __nv_bfloat16* v_raw;
-    const __nv_bfloat16* q_slot;  // [M][Hq][D]
-    const __nv_bfloat16* k_slot;  // [M][Hkv][D]
-    const __nv_bfloat16* v_slot;
-    float* o_raw;                 // [T][Hq][D]
-    float* lse_raw;               // [T][Hq] or null
-    float* o_slot;                // [M][Hq][D]
-    float* lse_slot;              // [M][Hq] or null
+    CUtensorMap tm_q_raw;    // [T][Hq][128] bf16, box 64 x 1 x 128
+    CUtensorMap tm_k_raw;    // [T][Hkv][128] bf16, box 64 x 1 x 64
+    CUtensorMap tm_v_raw;
+    CUtensorMap tm_q_slot;   // [M][Hq][128] (unused when M = 0)
+    CUtensorMap tm_k_slot;   // [M][Hkv][128]
+    CUtensorMap tm_v_slot;
+    float* o_raw;            // [T][Hq][128]
+    float* lse_raw;          // [T][Hq] or null
+    float* o_slot;           // [M][Hq][128]
+    float* lse_slot;         // [M][Hq] or null
+    int* d_err;
     int T, M, S, W, r, Hq, Hkv, self_attend;
-    int raw_tiles;                // tiles of raw query rows (the rest are slot tiles)
-    int slot_rows;                // slot query rows per slot tile (SB)
+    int raw_tiles;           // tiles of raw query rows (the rest are slot tiles)
+    int slot_rows;           // slot query rows per slot tile
     float scale_log2;
 };
 
-constexpr int kPD = 128;            // head_dim
-constexpr int kPRowB = kPD * 2;
-constexpr int kPBM = 64;            // query rows per CTA
-constexpr int kPBN = 64;            // keys per block
-constexpr int kPStage = 2 * kPBN * kPRowB;
-constexpr int kPNst = 2;
-constexpr int kPSmem = kPBM * kPRowB + kPNst * kPStage;   // Q tile + K/V stages
-
-__device__ __forceinline__ uint32_t pswz(int row, int ch) { return (uint32_t)(row * kPRowB + ((ch ^ (row & 7)) << 4)); }
-
-// key range: rows [a, b) of either the raw (slot = 0) or the slot (slot = 1) arrays
+// key range: rows [a, b) of the raw (slot = 0) or the slot (slot = 1) arrays
 struct KRange {
     int a, b, slot;
 };
 
-__global__ void __launch_bounds__(128) prefill_kernel(const __grid_constant__ PrefillParams p) {
-    extern __shared__ __align__(128) uint8_t smem[];
-    pdl_wait();
-    pdl_trigger();
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+__global__ void __launch_bounds__(128, 2) prefill_kernel(const __grid_constant__ PrefillParams p) {
+    using namespace tcp;
+    extern __shared__ __align__(1024) uint8_t smem[];
+    const int tid = threadIdx.x, warp = tid >> 5;
+    const uint32_t sb = smem_u32(smem);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBar);   // q, k0, k1, v0, v1, s, o
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + kOffBar + 56);
+    const uint32_t bar_q = sb + kOffBar, bar_s = bar_q + 40, bar_o = bar_q + 48;
+
     const int hq = blockIdx.y, G = p.Hq / p.Hkv, kvh = hq / G;
     const bool slot_tile = (int)blockIdx.x >= p.raw_tiles;
-    // raw tiles hold 64 consecutive positions; slot tiles hold slot_rows slots, so
-    // that their windows (r apart) span at most about 2W raw keys
-    const int q0 = slot_tile ? ((int)blockIdx.x - p.raw_tiles) * p.slot_rows : (int)blockIdx.x * kPBM;
+    const int q0 = slot_tile ? ((int)blockIdx.x - p.raw_tiles) * p.slot_rows : (int)blockIdx.x * kBM;
     const int nq = slot_tile ? p.M : p.T;
-    const int q1 = imin(nq, q0 + (slot_tile ? p.slot_rows : kPBM));
-    const __nv_bfloat16* qsrc = slot_tile ? p.q_slot : p.q_raw;
-
-    // visible key ranges of the tile (0-based rows)
-    KRange rg[3];
-    int nr = 0;
+    const int q1 = imin(nq, q0 + (slot_tile ? p.slot_rows : kBM));
     const int S = p.S, W = p.W, r = p.r;
+
+    // visible key ranges of the tile, and this thread's interval in each
+    KRange rg[3];
+    int lo[3], hi[3];
+    int nr = 0;
+    const int qrow = q0 + tid;
+    const bool live = qrow < q1;
     if (!slot_tile) {
-        const int i0 = q0 + 1, i1 = q1;            // 1-based raw positions of the tile
-        if (S > 0) rg[nr++] = KRange{0, imin(S, i1), 0};
+        const int i0 = q0 + 1, i1 = q1, i = qrow + 1;   // 1-based raw positions
+        if (S > 0) {
+            rg[nr] = KRange{0, imin(S, i1), 0};
+            lo[nr] = 0;
+            hi[nr++] = live ? imin(S, i) : 0;
+        }
         const int wlo = imax(S + 1, i0 - W + 1);
-        if (i1 >= wlo) rg[nr++] = KRange{wlo - 1, i1, 0};
+        if (i1 >= wlo) {
+            rg[nr] = KRange{wlo - 1, i1, 0};
+            lo[nr] = imax(S + 1, i - W + 1) - 1;
+            hi[nr++] = live ? i : 0;
+        }
         const int ns = slot_count(i1 - 1, S, W, r);
-        if (ns > 0) rg[nr++] = KRange{0, ns, 1};
+        if (ns > 0) {
+            rg[nr] = KRange{0, ns, 1};
+            lo[nr] = 0;
+            hi[nr++] = live ? slot_count(i - 1, S, W, r) : 0;
+        }
     } else {
-        const int m0 = q0 + 1, m1 = q1;            // 1-based slot indices of the tile
-        const int tau0 = S + W + m0 * r, tau1 = S + W + m1 * r;
-        if (S > 0) rg[nr++] = KRange{0, S, 0};
-        rg[nr++] = KRange{imax(S, tau0 - W), tau1, 0};
+        const int m0 = q0 + 1, m1 = q1, m = qrow + 1;   // 1-based slot indices
+        const int tau0 = S + W + m0 * r, tau1 = S + W + m1 * r, tau = S + W + m * r;
+        if (S > 0) {
+            rg[nr] = KRange{0, S, 0};
+            lo[nr] = 0;
+            hi[nr++] = live ? S : 0;
+        }
+        rg[nr] = KRange{imax(S, tau0 - W), tau1, 0};
+        lo[nr] = tau - W;
+        hi[nr++] = live ? tau : 0;
         const int ns = p.self_attend ? m1 : m1 - 1;
-        if (ns > 0) rg[nr++] = KRange{0, ns, 1};
+        if (ns > 0) {
+            rg[nr] = KRange{0, ns, 1};
+            lo[nr] = 0;
+            hi[nr++] = live ? (p.self_attend ? m : m - 1) : 0;
+        }
     }
-    int nblk = 0, bstart[4];
+    int bstart[4];
+    int nblk = 0;
     for (int k = 0; k < nr; ++k) {
         bstart[k] = nblk;
-        nblk += (rg[k].b - rg[k].a + kPBN - 1) / kPBN;
+        nblk += (rg[k].b - rg[k].a + kBN - 1) / kBN;
     }
     bstart[nr] = nblk;
-
-    const uint32_t sq = smem_u32(smem);
-    const uint32_t sbase = sq + kPBM * kPRowB;
-    // Q tile (rows past q1 zero-filled)
-    for (int idx = tid; idx < kPBM * 16; idx += 128) {
-        const int row = idx >> 4, ch = idx & 15;
-        const int qr = q0 + row;
-        const bool in = qr < q1;
-        cp_async16(sq + pswz(row, ch), qsrc + ((size_t)(in ? qr : q0) * p.Hq + hq) * kPD + ch * 8, in ? 16 : 0);
-    }
-    auto load_block = [&](int blk, int stage) {
-        int k = 0;
+    auto block_of = [&](int blk, int& k, int& key0) {
+        k = 0;
         while (k + 1 < nr && blk >= bstart[k + 1]) ++k;
-        const int key0 = rg[k].a + (blk - bstart[k]) * kPBN;
-        const int kend = rg[k].b;
-        const __nv_bfloat16* ks = rg[k].slot ? p.k_slot : p.k_raw;
-        const __nv_bfloat16* vs = rg[k].slot ? p.v_slot : p.v_raw;
-        const uint32_t sk = sbase + (uint32_t)stage * kPStage;
-        const uint32_t sv = sk + kPBN * kPRowB;
-        for (int idx = tid; idx < kPBN * 16; idx += 128) {
-            const int row = idx >> 4, ch = idx & 15;
-            const int key = key0 + row;
-            const bool in = key < kend;
-            const size_t off = ((size_t)(in ? key : key0) * p.Hkv + kvh) * kPD + ch * 8;
-            cp_async16(sk + pswz(row, ch), ks + off, in ? 16 : 0);
-            cp_async16(sv + pswz(row, ch), vs + off, in ? 16 : 0);
-        }
+        key0 = rg[k].a + (blk - bstart[k]) * kBN;
     };
-    if (nblk > 0) load_block(0, 0);
-    cp_async_commit();
 
-    // per-lane query rows (0-based within the tile): lane/4 and lane/4 + 8 of this warp's 16
-    const int qa = q0 + warp * 16 + (lane >> 2), qb = qa + 8;
-    uint32_t qf[8][4];
-    float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f};
-    float acc[16][4];
-#pragma unroll
-    for (int nt = 0; nt < 16; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
+    pdl_wait();
+    pdl_trigger();
+    // the swizzled layouts need a 1024-byte aligned base; after a timed-out wait
+    // anywhere in the grid the remaining CTAs skip their work
+    const bool misaligned = (sb & 1023u) != 0u;
+    if (__syncthreads_or(tid == 0 && (misaligned || *reinterpret_cast<volatile int*>(p.d_err) == MASW_ETIMEOUT))) {
+        if (misaligned && tid == 0) atomicExch(p.d_err + 2, 1);
+        return;
+    }
+    if (warp == 0) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tslot)),
+                     "r"(kTmemCols)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    if (tid == 0) {
+        for (int b = 0; b < 7; ++b) mbar_init(bars + b, 1);
+        fence_mbar_init();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tslot;
+    const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+    const uint32_t t_o = tmem + kColO, t_s = tmem + kColS;
 
-    for (int blk = 0; blk < nblk; ++blk) {
-        if (blk + 1 < nblk) load_block(blk + 1, (blk + 1) & 1);
-        cp_async_commit();
-        cp_async_wait<1>();
-        __syncthreads();
-        if (blk == 0) {
-#pragma unroll
-            for (int ks = 0; ks < 8; ++ks)
-                ldsm_x4(sq + pswz(warp * 16 + (lane & 15), ks * 2 + (lane >> 4)), qf[ks][0], qf[ks][1], qf[ks][2],
-                        qf[ks][3]);
+    // thread 0: TMA producer and MMA issuer
+    int issued_k[2] = {0, 0}, issued_v[2] = {0, 0}, waited_k[2] = {0, 0}, waited_v[2] = {0, 0};
+    auto load_kv = [&](int blk, bool is_v) {
+        int k, key0;
+        block_of(blk, k, key0);
+        const CUtensorMap* m = rg[k].slot ? (is_v ? &p.tm_v_slot : &p.tm_k_slot) : (is_v ? &p.tm_v_raw : &p.tm_k_raw);
+        const int st = blk & 1;
+        const uint32_t dst = sb + (is_v ? kOffV : kOffK) + st * kKVBytes;
+        const uint32_t bar = sb + kOffBar + 8 * ((is_v ? 3 : 1) + st);
+        mbar_expect_tx(bars + (is_v ? 3 : 1) + st, kKVBytes);
+        tma_load_3d(dst, m, 0, kvh, key0, bar);
+        tma_load_3d(dst + kKVBytes / 2, m, 64, kvh, key0, bar);
+        ++(is_v ? issued_v : issued_k)[st];
+    };
+    bool ok = true;
+    if (tid == 0) {
+        const CUtensorMap* mq = slot_tile ? &p.tm_q_slot : &p.tm_q_raw;
+        mbar_expect_tx(bars + 0, kQBytes);
+        tma_load_3d(sb + kOffQ, mq, 0, hq, q0, bar_q);
+        tma_load_3d(sb + kOffQ + kQBytes / 2, mq, 64, hq, q0, bar_q);
+        for (int b = 0; b < imin(2, nblk); ++b) {
+            load_kv(b, false);
+            load_kv(b, true);
         }
-        int k = 0;
-        while (k + 1 < nr && blk >= bstart[k + 1]) ++k;
-        const int key0 = rg[k].a + (blk - bstart[k]) * kPBN;
-        const int kend = rg[k].b;
-        const bool kslot = rg[k].slot != 0;
-        const uint32_t sk = sbase + (uint32_t)(blk & 1) * kPStage;
-        const uint32_t sv = sk + kPBN * kPRowB;
+    }
 
-        // S = Q K^T for this warp's 16 rows x 64 keys (8 n-tiles of 8 keys)
-        float s[8][4];
-#pragma unroll
-        for (int nt = 0; nt < 8; ++nt) s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
-#pragma unroll
-        for (int ks = 0; ks < 8; ++ks) {
-#pragma unroll
-            for (int np = 0; np < 4; ++np) {   // two n-tiles per ldmatrix.x4
-                uint32_t b0, b1, b2, b3;
-                ldsm_x4(sk + pswz(np * 16 + (lane & 7) + ((lane >> 4) << 3), ks * 2 + ((lane >> 3) & 1)), b0, b1, b2,
-                        b3);
-                mma16816(s[2 * np], qf[ks][0], qf[ks][1], qf[ks][2], qf[ks][3], b0, b1);
-                mma16816(s[2 * np + 1], qf[ks][0], qf[ks][1], qf[ks][2], qf[ks][3], b2, b3);
+    float m_run = -INFINITY, l_run = 0.f;
+    bool aborted = false;
+    for (int j = 0; j < nblk; ++j) {
+        const int st = j & 1;
+        const uint32_t ph = (uint32_t)(j >> 1) & 1u;
+        if (tid == 0) {
+            if (j == 0) ok = ok && mbar_wait(bars + 0, 0, p.d_err);
+            if (ok) {
+                ok = mbar_wait(bars + 1 + st, ph, p.d_err);
+                waited_k[st] += ok ? 1 : 0;
             }
-        }
-        // structured mask, scale, online softmax per row
-        float rmax[2] = {-INFINITY, -INFINITY};
+            tc_fence_after();
+            if (ok) {
+                const uint32_t qa = sb + kOffQ, kb = sb + kOffK + st * kKVBytes;
 #pragma unroll
-        for (int nt = 0; nt < 8; ++nt)
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const int key = key0 + nt * 8 + (lane & 3) * 2 + (e & 1);
-                const int qrow = (e < 2) ? qa : qb;
-                bool vis = key < kend && qrow < q1;
-                if (vis) {
-                    if (!slot_tile) {
-                        const int i = qrow + 1;                      // raw query position
-                        if (!kslot) {
-                            const int j = key + 1;                   // raw key position
-                            vis = (j <= S) ? (j <= i) : (j >= imax(S + 1, i - W + 1) && j <= i);
-                        } else {
-                            vis = key < slot_count(i - 1, S, W, r);  // slot key+1 has tau <= i-1
-                        }
-                    } else {
-                        const int m = qrow + 1;                      // slot query index
-                        const int tau = S + W + m * r;
-                        if (!kslot) {
-                            const int j = key + 1;
-                            vis = (j <= S) || (j >= tau - W + 1 && j <= tau);
-                        } else {
-                            vis = p.self_attend ? key < m : key < m - 1;
-                        }
-                    }
+                for (int kk = 0; kk < kD / 16; ++kk) {
+                    const uint64_t a = sw128_desc(qa + (kk >> 2) * (kQBytes / 2) + (kk & 3) * 32, 16, 1024);
+                    const uint64_t b = sw128_desc(kb + (kk >> 2) * (kKVBytes / 2) + (kk & 3) * 32, 16, 1024);
+                    umma_bf16(t_s, a, b, kIdescS, kk > 0 ? 1u : 0u);
                 }
-                s[nt][e] = vis ? s[nt][e] * p.scale_log2 : -INFINITY;
-                rmax[e >> 1] = fmaxf(rmax[e >> 1], s[nt][e]);
             }
-        float alpha[2];
-#pragma unroll
-        for (int h2 = 0; h2 < 2; ++h2) {
-            float mx = rmax[h2];
-            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-            const float m_new = fmaxf(m_run[h2], mx);
-            const float m_use = m_new == -INFINITY ? 0.f : m_new;
-            alpha[h2] = exp2f(m_run[h2] - m_use);
-            m_run[h2] = m_new;
-            rmax[h2] = m_use;
+            umma_commit(bar_s);
         }
-        float rsum[2] = {0.f, 0.f};
-        uint32_t pa[4][4];
-#pragma unroll
-        for (int nt = 0; nt < 8; ++nt) {
-            const float p0 = exp2f(s[nt][0] - rmax[0]), p1 = exp2f(s[nt][1] - rmax[0]);
-            const float p2 = exp2f(s[nt][2] - rmax[1]), p3 = exp2f(s[nt][3] - rmax[1]);
-            rsum[0] += p0 + p1;
-            rsum[1] += p2 + p3;
-            // accumulator tile nt -> half of the A fragment of k-step nt/2
-            pa[nt >> 1][(nt & 1) * 2 + 0] = pack_bf16(p0, p1);
-            pa[nt >> 1][(nt & 1) * 2 + 1] = pack_bf16(p2, p3);
-        }
-#pragma unroll
-        for (int h2 = 0; h2 < 2; ++h2) l_run[h2] = l_run[h2] * alpha[h2] + rsum[h2];
-#pragma unroll
-        for (int nt = 0; nt < 16; ++nt) {
-            acc[nt][0] *= alpha[0];
-            acc[nt][1] *= alpha[0];
-            acc[nt][2] *= alpha[1];
-            acc[nt][3] *= alpha[1];
-        }
-        // O += P V: k-steps of 16 keys, 16 n-tiles of 8 head dims
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {
-#pragma unroll
-            for (int dp = 0; dp < 8; ++dp) {   // two d n-tiles per ldmatrix.x4.trans
-                uint32_t b0, b1, b2, b3;
-                ldsm_x4_t(sv + pswz(kk * 16 + (lane & 7) + (((lane >> 3) & 1) << 3), dp * 2 + (lane >> 4)), b0, b1,
-                          b2, b3);
-                mma16816(acc[2 * dp], pa[kk][0], pa[kk][1], pa[kk][2], pa[kk][3], b0, b1);
-                mma16816(acc[2 * dp + 1], pa[kk][0], pa[kk][1], pa[kk][2], pa[kk][3], b2, b3);
-            }
-        }
-        __syncthreads();   // the stage is refilled by the next iteration's prefetch
-    }
-    cp_async_wait<0>();
+        __syncwarp();
+        ok = mbar_wait(bars + 5, (uint32_t)j & 1u, p.d_err) && ok;
+        tc_fence_after();
+        uint32_t sv[2][32];
+        tmem_ld32(t_s + lane_off, sv[0]);
+        tmem_ld32(t_s + lane_off + 32, sv[1]);
+        tmem_wait_ld();
+        // S(j) is done with K stage st: refill it two blocks ahead
+        if (tid == 0 && ok && j + 2 < nblk) load_kv(j + 2, false);
 
-    // finish: row sums over the 4 lanes of a row, normalise, store
+        int k, key0;
+        block_of(j, k, key0);
+        const int lo_k = lo[k], hi_k = hi[k];
+        float s[64];
+        float mx = -INFINITY;
 #pragma unroll
-    for (int h2 = 0; h2 < 2; ++h2) {
-        l_run[h2] += __shfl_xor_sync(0xffffffffu, l_run[h2], 1);
-        l_run[h2] += __shfl_xor_sync(0xffffffffu, l_run[h2], 2);
+        for (int e = 0; e < 64; ++e) {
+            const int key = key0 + e;
+            const float x = __uint_as_float(sv[e >> 5][e & 31]) * p.scale_log2;
+            s[e] = (key >= lo_k && key < hi_k) ? x : -INFINITY;
+            mx = fmaxf(mx, s[e]);
+        }
+        float alpha = 1.f;
+        const float m_new = fmaxf(m_run, mx);
+        if (m_new > m_run + 8.f) {
+            alpha = exp2f(m_run - m_new);
+            m_run = m_new;
+        }
+        const float mref = m_run == -INFINITY ? 0.f : m_run;
+        uint32_t pk[32];
+        float sum = 0.f;
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+            const float p0 = exp2f(s[2 * e] - mref), p1 = exp2f(s[2 * e + 1] - mref);
+            sum += p0 + p1;
+            pk[e] = pack_bf16(p0, p1);
+        }
+        const bool resc = alpha != 1.f && l_run > 0.f;
+        l_run = l_run * alpha + sum;
+
+        // PV(j-1) must be complete before O is rescaled and P is overwritten
+        if (j > 0) ok = mbar_wait(bars + 6, (uint32_t)(j - 1) & 1u, p.d_err) && ok;
+        tc_fence_after();
+        // ... and it released V stage (j+1)&1
+        if (tid == 0 && ok && j >= 1 && j + 1 < nblk) load_kv(j + 1, true);
+        if (__any_sync(0xffffffffu, resc)) {
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                uint32_t ov[32];
+                tmem_ld32(t_o + lane_off + c * 32, ov);
+                tmem_wait_ld();
+#pragma unroll
+                for (int e = 0; e < 32; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * alpha);
+                tmem_st32(t_o + lane_off + c * 32, ov);
+            }
+            tmem_wait_st();
+        }
+        // row tid of P: 64 bf16 = one 128-byte swizzled row
+        const uint32_t prow = sb + kOffP + (uint32_t)tid * 128u;
+#pragma unroll
+        for (int c = 0; c < 8; ++c)
+            st_shared_v4(prow + ((uint32_t)(c ^ (tid & 7)) << 4), pk[4 * c], pk[4 * c + 1], pk[4 * c + 2],
+                         pk[4 * c + 3]);
+        fence_async_smem();
+        tc_fence_before();
+        if (__syncthreads_or(!ok)) {
+            aborted = true;   // PV(j) not issued; PV(j-1) was waited above
+            break;
+        }
+        if (tid == 0) {
+            tc_fence_after();
+            ok = mbar_wait(bars + 3 + st, ph, p.d_err);
+            waited_v[st] += ok ? 1 : 0;
+            if (ok) {
+                const uint32_t vb = sb + kOffV + st * kKVBytes;
+#pragma unroll
+                for (int kk = 0; kk < kBN / 16; ++kk) {
+                    const uint64_t a = sw128_desc(sb + kOffP + kk * 32, 16, 1024);
+                    const uint64_t b = sw128_desc(vb + kk * 2048, kKVBytes / 2, 1024);
+                    umma_bf16(t_o, a, b, kIdescO, (j > 0 || kk > 0) ? 1u : 0u);
+                }
+            }
+            umma_commit(bar_o);
+        }
+        __syncwarp();
     }
+    // last PV (every committed phase of bar_o is waited here or in the loop)
+    if (nblk > 0 && !aborted) ok = mbar_wait(bars + 6, (uint32_t)(nblk - 1) & 1u, p.d_err) && ok;
+    tc_fence_after();
     float* obase = slot_tile ? p.o_slot : p.o_raw;
     float* lbase = slot_tile ? p.lse_slot : p.lse_raw;
+    const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
+    float* orow = obase + ((size_t)(live ? qrow : q0) * p.Hq + hq) * kD;
 #pragma unroll
-    for (int h2 = 0; h2 < 2; ++h2) {
-        const int qrow = h2 ? qb : qa;
-        if (qrow >= q1) continue;
-        const float l = l_run[h2];
-        const float inv = l > 0.f ? 1.f / l : 0.f;
-        float* orow = obase + ((size_t)qrow * p.Hq + hq) * kPD;
+    for (int c = 0; c < 4; ++c) {
+        uint32_t ov[32];
+        tmem_ld32(t_o + lane_off + c * 32, ov);
+        tmem_wait_ld();
+        if (live && nblk > 0) {
 #pragma unroll
-        for (int nt = 0; nt < 16; ++nt) {
-            const int d = nt * 8 + (lane & 3) * 2;
-            *reinterpret_cast<float2*>(orow + d) = make_float2(acc[nt][2 * h2] * inv, acc[nt][2 * h2 + 1] * inv);
+            for (int e = 0; e < 32; e += 4)
+                *reinterpret_cast<float4*>(orow + c * 32 + e) =
+                    make_float4(__uint_as_float(ov[e]) * inv, __uint_as_float(ov[e + 1]) * inv,
+                                __uint_as_float(ov[e + 2]) * inv, __uint_as_float(ov[e + 3]) * inv);
         }
-        if (lbase && (lane & 3) == 0)
-            lbase[(size_t)qrow * p.Hq + hq] = l > 0.f ? (m_run[h2] + __log2f(l)) * 0.6931471805599453f : -INFINITY;
+    }
+    if (live && lbase)
+        lbase[(size_t)qrow * p.Hq + hq] = l_run > 0.f ? (m_run + __log2f(l_run)) * 0.6931471805599453f : -INFINITY;
+    // on an early exit, let the loads still in flight land before the CTA ends
+    if (tid == 0 && (aborted || !ok)) {
+        for (int st = 0; st < 2; ++st) {
+            for (int n = waited_k[st]; n < issued_k[st]; ++n) mbar_wait(bars + 1 + st, (uint32_t)n & 1u, nullptr);
+            for (int n = waited_v[st]; n < issued_v[st]; ++n) mbar_wait(bars + 3 + st, (uint32_t)n & 1u, nullptr);
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols) : "memory");
     }
 }
 
@@ -344,6 +484,35 @@ __global__ void prefill_store_kernel(const __grid_constant__ StoreParams p) {
 
 using namespace masw;
 
+// cuTensorMapEncodeTiled from the driver, looked up once through the runtime
+static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+        else
+            cudaGetLastError();
+    });
+    return fn;
+}
+
+// [rows][heads][128] bf16 as a 3-d tensor (head_dim innermost), boxes of
+// 64 x 1 x box_rows elements with the 128-byte swizzle the MMA descriptors use
+static bool make_map(CUtensorMap* map, const void* base, int rows, int heads, int box_rows) {
+    const cuuint64_t dims[3] = {128, (cuuint64_t)heads, (cuuint64_t)rows};
+    const cuuint64_t strides[2] = {256, (cuuint64_t)heads * 256};
+    const cuuint32_t box[3] = {64, 1, (cuuint32_t)box_rows};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    return encode_fn()(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+                       CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                       CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 extern "C" int masw_prefill(masw_mem_t* mem, int layer, int seq, int T, const void* q_raw, const void* k_raw,
                             const void* v_raw, const void* q_slot, const void* k_slot, const void* v_slot,
                             int n_q_heads, float* o_raw, float* lse_raw, float* o_slot, float* lse_slot,
@@ -351,7 +520,7 @@ extern "C" int masw_prefill(masw_mem_t* mem, int layer, int seq, int T, const vo
     if (!mem) return masw_set_error(nullptr, MASW_EINVAL, "prefill: NULL handle");
     if (layer < 0 || layer >= mem->L || seq < 0 || seq >= mem->B)
         return masw_set_error(mem, MASW_EINVAL, "prefill: layer or seq out of range");
-    if (mem->dtype != MASW_BF16 || mem->D != kPD)
+    if (mem->dtype != MASW_BF16 || mem->D != tcp::kD)
         return masw_set_error(mem, MASW_EINVAL, "prefill: bf16 pools with head_dim 128 only");
     if (n_q_heads < mem->Hkv || n_q_heads % mem->Hkv) return masw_set_error(mem, MASW_EINVAL, "prefill: bad n_q_heads");
     if (T < 1 || T > mem->max_seq_len) return masw_set_error(mem, MASW_ECAPACITY, "prefill: T out of range");
@@ -365,37 +534,44 @@ extern "C" int masw_prefill(masw_mem_t* mem, int layer, int seq, int T, const vo
     if (((uintptr_t)o_raw | (uintptr_t)o_slot) & 7 || ((uintptr_t)lse_raw | (uintptr_t)lse_slot) & 3)
         return masw_set_error(mem, MASW_EINVAL, "prefill: outputs must be 8-byte (O) / 4-byte (LSE) aligned");
     if (n_q_heads > 65535) return masw_set_error(mem, MASW_EINVAL, "prefill: too many heads");
+    if (!encode_fn()) return masw_set_error(mem, MASW_ECUDA, "prefill: cuTensorMapEncodeTiled is unavailable");
     PrefillParams p;
     std::memset(&p, 0, sizeof(p));
-    p.q_raw = (const __nv_bfloat16*)q_raw;
-    p.k_raw = (const __nv_bfloat16*)k_raw;
-    p.v_raw = (const __nv_bfloat16*)v_raw;
-    p.q_slot = (const __nv_bfloat16*)q_slot;
-    p.k_slot = (const __nv_bfloat16*)k_slot;
-    p.v_slot = (const __nv_bfloat16*)v_slot;
+    const int Hkv = mem->Hkv;
+    bool maps = make_map(&p.tm_q_raw, q_raw, T, n_q_heads, tcp::kBM) && make_map(&p.tm_k_raw, k_raw, T, Hkv, tcp::kBN) &&
+                make_map(&p.tm_v_raw, v_raw, T, Hkv, tcp::kBN);
+    if (M > 0)
+        maps = maps && make_map(&p.tm_q_slot, q_slot, M, n_q_heads, tcp::kBM) &&
+               make_map(&p.tm_k_slot, k_slot, M, Hkv, tcp::kBN) && make_map(&p.tm_v_slot, v_slot, M, Hkv, tcp::kBN);
+    if (!maps) return masw_set_error(mem, MASW_EINVAL, "prefill: cannot describe the inputs as TMA tensors");
     p.o_raw = o_raw;
     p.lse_raw = lse_raw;
     p.o_slot = o_slot;
     p.lse_slot = lse_slot;
+    p.d_err = mem->d_err;
     p.T = T;
     p.M = M;
     p.S = mem->S;
     p.W = mem->W;
     p.r = mem->r;
     p.Hq = n_q_heads;
-    p.Hkv = mem->Hkv;
+    p.Hkv = Hkv;
     p.self_attend = mem->self_attend;
-    p.raw_tiles = (T + kPBM - 1) / kPBM;
-    p.slot_rows = imin(kPBM, imax(1, mem->W / mem->r + 1));
+    p.raw_tiles = (T + tcp::kBM - 1) / tcp::kBM;
+    // slot rows per tile: extra rows widen the tile's window band by r keys
+    // each, worth it while that stays below the keys every slot row reads anyway
+    p.slot_rows = imin(tcp::kBM, imax(1, (mem->S + mem->W + M / 2) / mem->r + 1));
     p.scale_log2 = mem->scale * 1.4426950408889634f;
     const int tiles = p.raw_tiles + (M + p.slot_rows - 1) / p.slot_rows;
     cudaStream_t st = (cudaStream_t)stream;
     static bool configured[64] = {};
     if (!configured[mem->device & 63]) {
-        MASW_CUDA_TRY(mem, cudaFuncSetAttribute(prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kPSmem));
+        MASW_CUDA_TRY(mem, cudaFuncSetAttribute(prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, tcp::kSmem));
+        MASW_CUDA_TRY(mem, cudaFuncSetAttribute(prefill_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                                cudaSharedmemCarveoutMaxShared));
         configured[mem->device & 63] = true;
     }
-    MASW_CUDA_TRY(mem, masw_launch(prefill_kernel, dim3(tiles, n_q_heads), dim3(128), kPSmem, st, 1, p));
+    MASW_CUDA_TRY(mem, masw_launch(prefill_kernel, dim3(tiles, n_q_heads), dim3(128), tcp::kSmem, st, 1, p));
     StoreParams sp;
     std::memset(&sp, 0, sizeof(sp));
     sp.k_raw = (const uint8_t*)k_raw;
