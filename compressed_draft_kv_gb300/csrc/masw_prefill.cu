@@ -84,6 +84,12 @@ __device__ __forceinline__ void umma_commit(uint32_t bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
                  : "memory");
 }
+// 2^x by the MUFU instruction (inputs of -inf give 0)
+__device__ __forceinline__ float ex2_approx(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
@@ -138,11 +144,6 @@ struct PrefillParams {
     float scale_log2;
 };
 
-// key range: rows [a, b) of the raw (slot = 0) or the slot (slot = 1) arrays
-struct KRange {
-    int a, b, slot;
-};
-
 __global__ void __launch_bounds__(128, 2) prefill_kernel(const __grid_constant__ PrefillParams p) {
     using namespace tcp;
     extern __shared__ __align__(1024) uint8_t smem[];
@@ -159,60 +160,48 @@ __global__ void __launch_bounds__(128, 2) prefill_kernel(const __grid_constant__
     const int q1 = imin(nq, q0 + (slot_tile ? p.slot_rows : kBM));
     const int S = p.S, W = p.W, r = p.r;
 
-    // visible key ranges of the tile, and this thread's interval in each
-    KRange rg[3];
-    int lo[3], hi[3];
-    int nr = 0;
+    // visible key ranges of the tile: 0 = sink and 1 = window band (raw rows),
+    // 2 = slot prefix (slot rows), each [a_k, b_k) possibly empty; this thread's
+    // row sees the interval [lo_k, hi_k) of range k.  Kept in scalars (no
+    // dynamically indexed arrays) so that nothing spills to local memory.
     const int qrow = q0 + tid;
     const bool live = qrow < q1;
+    int a0 = 0, b0 = 0, a1 = 0, b1 = 0, b2 = 0;
+    int lo1 = 0, hi0 = 0, hi1 = 0, hi2 = 0;
     if (!slot_tile) {
         const int i0 = q0 + 1, i1 = q1, i = qrow + 1;   // 1-based raw positions
-        if (S > 0) {
-            rg[nr] = KRange{0, imin(S, i1), 0};
-            lo[nr] = 0;
-            hi[nr++] = live ? imin(S, i) : 0;
-        }
-        const int wlo = imax(S + 1, i0 - W + 1);
-        if (i1 >= wlo) {
-            rg[nr] = KRange{wlo - 1, i1, 0};
-            lo[nr] = imax(S + 1, i - W + 1) - 1;
-            hi[nr++] = live ? i : 0;
-        }
-        const int ns = slot_count(i1 - 1, S, W, r);
-        if (ns > 0) {
-            rg[nr] = KRange{0, ns, 1};
-            lo[nr] = 0;
-            hi[nr++] = live ? slot_count(i - 1, S, W, r) : 0;
+        b0 = imin(S, i1);
+        a1 = imax(S + 1, i0 - W + 1) - 1;
+        b1 = imax(a1, i1);
+        b2 = slot_count(i1 - 1, S, W, r);
+        lo1 = imax(S + 1, i - W + 1) - 1;
+        if (live) {
+            hi0 = imin(S, i);
+            hi1 = i;
+            hi2 = slot_count(i - 1, S, W, r);
         }
     } else {
         const int m0 = q0 + 1, m1 = q1, m = qrow + 1;   // 1-based slot indices
         const int tau0 = S + W + m0 * r, tau1 = S + W + m1 * r, tau = S + W + m * r;
-        if (S > 0) {
-            rg[nr] = KRange{0, S, 0};
-            lo[nr] = 0;
-            hi[nr++] = live ? S : 0;
-        }
-        rg[nr] = KRange{imax(S, tau0 - W), tau1, 0};
-        lo[nr] = tau - W;
-        hi[nr++] = live ? tau : 0;
-        const int ns = p.self_attend ? m1 : m1 - 1;
-        if (ns > 0) {
-            rg[nr] = KRange{0, ns, 1};
-            lo[nr] = 0;
-            hi[nr++] = live ? (p.self_attend ? m : m - 1) : 0;
+        b0 = S;
+        a1 = imax(S, tau0 - W);
+        b1 = tau1;
+        b2 = imax(0, p.self_attend ? m1 : m1 - 1);
+        lo1 = tau - W;
+        if (live) {
+            hi0 = S;
+            hi1 = tau;
+            hi2 = p.self_attend ? m : m - 1;
         }
     }
-    int bstart[4];
-    int nblk = 0;
-    for (int k = 0; k < nr; ++k) {
-        bstart[k] = nblk;
-        nblk += (rg[k].b - rg[k].a + kBN - 1) / kBN;
-    }
-    bstart[nr] = nblk;
+    (void)a0;
+    const int bs1 = (b0 + kBN - 1) / kBN;
+    const int bs2 = bs1 + (b1 - a1 + kBN - 1) / kBN;
+    const int nblk = bs2 + (b2 + kBN - 1) / kBN;
+    // range index and first key of block blk
     auto block_of = [&](int blk, int& k, int& key0) {
-        k = 0;
-        while (k + 1 < nr && blk >= bstart[k + 1]) ++k;
-        key0 = rg[k].a + (blk - bstart[k]) * kBN;
+        k = (blk >= bs1 ? 1 : 0) + (blk >= bs2 ? 1 : 0);
+        key0 = k == 0 ? blk * kBN : (k == 1 ? a1 + (blk - bs1) * kBN : (blk - bs2) * kBN);
     };
 
     pdl_wait();
@@ -242,18 +231,20 @@ __global__ void __launch_bounds__(128, 2) prefill_kernel(const __grid_constant__
     const uint32_t t_o = tmem + kColO, t_s = tmem + kColS;
 
     // thread 0: TMA producer and MMA issuer
-    int issued_k[2] = {0, 0}, issued_v[2] = {0, 0}, waited_k[2] = {0, 0}, waited_v[2] = {0, 0};
+    // per stage: loads issued and phases waited (thread 0's bookkeeping, for the
+    // drain on an early exit); bit-packed counters, stage st in bits 16*st
+    uint32_t issued_k = 0, issued_v = 0, waited_k = 0, waited_v = 0;
     auto load_kv = [&](int blk, bool is_v) {
         int k, key0;
         block_of(blk, k, key0);
-        const CUtensorMap* m = rg[k].slot ? (is_v ? &p.tm_v_slot : &p.tm_k_slot) : (is_v ? &p.tm_v_raw : &p.tm_k_raw);
+        const CUtensorMap* m = k == 2 ? (is_v ? &p.tm_v_slot : &p.tm_k_slot) : (is_v ? &p.tm_v_raw : &p.tm_k_raw);
         const int st = blk & 1;
         const uint32_t dst = sb + (is_v ? kOffV : kOffK) + st * kKVBytes;
         const uint32_t bar = sb + kOffBar + 8 * ((is_v ? 3 : 1) + st);
         mbar_expect_tx(bars + (is_v ? 3 : 1) + st, kKVBytes);
         tma_load_3d(dst, m, 0, kvh, key0, bar);
         tma_load_3d(dst + kKVBytes / 2, m, 64, kvh, key0, bar);
-        ++(is_v ? issued_v : issued_k)[st];
+        (is_v ? issued_v : issued_k) += 1u << (16 * st);
     };
     bool ok = true;
     if (tid == 0) {
@@ -276,7 +267,7 @@ __global__ void __launch_bounds__(128, 2) prefill_kernel(const __grid_constant__
             if (j == 0) ok = ok && mbar_wait(bars + 0, 0, p.d_err);
             if (ok) {
                 ok = mbar_wait(bars + 1 + st, ph, p.d_err);
-                waited_k[st] += ok ? 1 : 0;
+                waited_k += ok ? 1u << (16 * st) : 0u;
             }
             tc_fence_after();
             if (ok) {
@@ -302,31 +293,42 @@ __global__ void __launch_bounds__(128, 2) prefill_kernel(const __grid_constant__
 
         int k, key0;
         block_of(j, k, key0);
-        const int lo_k = lo[k], hi_k = hi[k];
-        float s[64];
-        float mx = -INFINITY;
+        const int lo_k = k == 1 ? lo1 : 0;
+        const int hi_k = k == 0 ? hi0 : (k == 1 ? hi1 : hi2);
+        // visible columns of this block for this row: [e_lo, e_hi)
+        const int e_lo = imin(kBN, imax(0, lo_k - key0)), e_hi = imin(kBN, imax(0, hi_k - key0));
+        float x[64];
 #pragma unroll
-        for (int e = 0; e < 64; ++e) {
-            const int key = key0 + e;
-            const float x = __uint_as_float(sv[e >> 5][e & 31]) * p.scale_log2;
-            s[e] = (key >= lo_k && key < hi_k) ? x : -INFINITY;
-            mx = fmaxf(mx, s[e]);
+        for (int e = 0; e < 64; ++e) x[e] = __uint_as_float(sv[e >> 5][e & 31]);
+        if (e_lo > 0 || e_hi < kBN) {
+#pragma unroll
+            for (int e = 0; e < 64; ++e) x[e] = (e >= e_lo && e < e_hi) ? x[e] : -INFINITY;
         }
+        // row max of the raw scores (scale > 0 commutes with max), 8 chains
+        float mx8[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) mx8[e] = x[e];
+#pragma unroll
+        for (int e = 8; e < 64; ++e) mx8[e & 7] = fmaxf(mx8[e & 7], x[e]);
+        const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                               fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
         float alpha = 1.f;
-        const float m_new = fmaxf(m_run, mx);
+        const float m_new = fmaxf(m_run, mx * p.scale_log2);
         if (m_new > m_run + 8.f) {
-            alpha = exp2f(m_run - m_new);
+            alpha = ex2_approx(m_run - m_new);
             m_run = m_new;
         }
-        const float mref = m_run == -INFINITY ? 0.f : m_run;
+        const float nmref = m_run == -INFINITY ? 0.f : -m_run;
         uint32_t pk[32];
-        float sum = 0.f;
+        float sum8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int e = 0; e < 32; ++e) {
-            const float p0 = exp2f(s[2 * e] - mref), p1 = exp2f(s[2 * e + 1] - mref);
-            sum += p0 + p1;
+            const float p0 = ex2_approx(fmaf(x[2 * e], p.scale_log2, nmref));
+            const float p1 = ex2_approx(fmaf(x[2 * e + 1], p.scale_log2, nmref));
+            sum8[e & 7] += p0 + p1;
             pk[e] = pack_bf16(p0, p1);
         }
+        const float sum = ((sum8[0] + sum8[1]) + (sum8[2] + sum8[3])) + ((sum8[4] + sum8[5]) + (sum8[6] + sum8[7]));
         const bool resc = alpha != 1.f && l_run > 0.f;
         l_run = l_run * alpha + sum;
 
@@ -362,7 +364,7 @@ __global__ void __launch_bounds__(128, 2) prefill_kernel(const __grid_constant__
         if (tid == 0) {
             tc_fence_after();
             ok = mbar_wait(bars + 3 + st, ph, p.d_err);
-            waited_v[st] += ok ? 1 : 0;
+            waited_v += ok ? 1u << (16 * st) : 0u;
             if (ok) {
                 const uint32_t vb = sb + kOffV + st * kKVBytes;
 #pragma unroll
@@ -401,8 +403,11 @@ __global__ void __launch_bounds__(128, 2) prefill_kernel(const __grid_constant__
     // on an early exit, let the loads still in flight land before the CTA ends
     if (tid == 0 && (aborted || !ok)) {
         for (int st = 0; st < 2; ++st) {
-            for (int n = waited_k[st]; n < issued_k[st]; ++n) mbar_wait(bars + 1 + st, (uint32_t)n & 1u, nullptr);
-            for (int n = waited_v[st]; n < issued_v[st]; ++n) mbar_wait(bars + 3 + st, (uint32_t)n & 1u, nullptr);
+            const uint32_t sh = 16 * st;
+            for (uint32_t n = (waited_k >> sh) & 0xFFFFu; n < ((issued_k >> sh) & 0xFFFFu); ++n)
+                mbar_wait(bars + 1 + st, n & 1u, nullptr);
+            for (uint32_t n = (waited_v >> sh) & 0xFFFFu; n < ((issued_v >> sh) & 0xFFFFu); ++n)
+                mbar_wait(bars + 3 + st, n & 1u, nullptr);
         }
     }
     tc_fence_before();
