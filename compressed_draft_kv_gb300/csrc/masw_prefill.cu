@@ -48,11 +48,11 @@ constexpr uint32_t kOffQ = 0;
 constexpr uint32_t kOffK = kOffQ + kQBytes;
 constexpr uint32_t kOffV = kOffK + 2 * kKVBytes;
 constexpr uint32_t kOffP = kOffV + 2 * kKVBytes;
-constexpr uint32_t kOffBar = kOffP + kPBytes;    // 7 mbarriers + the TMEM address
-constexpr uint32_t kSmem = kOffBar + 64;
+constexpr uint32_t kOffBar = kOffP + kPBytes;    // 9 mbarriers + the TMEM address
+constexpr uint32_t kSmem = kOffBar + 80;
 constexpr uint32_t kTmemCols = 256;
 constexpr uint32_t kColO = 0;                    // O: columns [0, 128)
-constexpr uint32_t kColS = 128;                  // S: columns [128, 192)
+constexpr uint32_t kColS = 128;                  // S: two buffers, columns [128, 192) and [192, 256)
 // instruction descriptors (kind::f16): f32 accumulator, bf16 A and B, M = 128;
 // S: N = 64, both operands K-major; O: N = 128, B (V) MN-major
 constexpr uint32_t kIdescBase = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(kBM >> 4) << 24);
@@ -149,9 +149,10 @@ __global__ void __launch_bounds__(128, 2) prefill_kernel(const __grid_constant__
     extern __shared__ __align__(1024) uint8_t smem[];
     const int tid = threadIdx.x, warp = tid >> 5;
     const uint32_t sb = smem_u32(smem);
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBar);   // q, k0, k1, v0, v1, s, o
-    uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + kOffBar + 56);
-    const uint32_t bar_q = sb + kOffBar, bar_s = bar_q + 40, bar_o = bar_q + 48;
+    // mbarriers: q, k0, k1, v0, v1, s0, s1, o, done
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBar);
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + kOffBar + 72);
+    const uint32_t bar_q = sb + kOffBar, bar_o = bar_q + 56, bar_done = bar_q + 64;
 
     const int hq = blockIdx.y, G = p.Hq / p.Hkv, kvh = hq / G;
     const bool slot_tile = (int)blockIdx.x >= p.raw_tiles;
@@ -220,7 +221,7 @@ __global__ void __launch_bounds__(128, 2) prefill_kernel(const __grid_constant__
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
     }
     if (tid == 0) {
-        for (int b = 0; b < 7; ++b) mbar_init(bars + b, 1);
+        for (int b = 0; b < 9; ++b) mbar_init(bars + b, 1);
         fence_mbar_init();
     }
     tc_fence_before();
@@ -228,7 +229,7 @@ __global__ void __launch_bounds__(128, 2) prefill_kernel(const __grid_constant__
     tc_fence_after();
     const uint32_t tmem = *tslot;
     const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
-    const uint32_t t_o = tmem + kColO, t_s = tmem + kColS;
+    const uint32_t t_o = tmem + kColO;
 
     // thread 0: TMA producer and MMA issuer
     // per stage: loads issued and phases waited (thread 0's bookkeeping, for the
@@ -247,6 +248,26 @@ __global__ void __launch_bounds__(128, 2) prefill_kernel(const __grid_constant__
         (is_v ? issued_v : issued_k) += 1u << (16 * st);
     };
     bool ok = true;
+    // S(blk) = Q K(blk)^T into TMEM buffer blk & 1 (thread 0; commits even when
+    // a wait failed so that the waiting threads move on)
+    auto issue_s = [&](int blk) {
+        const int st = blk & 1;
+        if (ok) {
+            ok = mbar_wait(bars + 1 + st, (uint32_t)(blk >> 1) & 1u, p.d_err);
+            waited_k += ok ? 1u << (16 * st) : 0u;
+        }
+        tc_fence_after();
+        if (ok) {
+            const uint32_t qa = sb + kOffQ, kb = sb + kOffK + st * kKVBytes;
+#pragma unroll
+            for (int kk = 0; kk < kD / 16; ++kk) {
+                const uint64_t a = sw128_desc(qa + (kk >> 2) * (kQBytes / 2) + (kk & 3) * 32, 16, 1024);
+                const uint64_t b = sw128_desc(kb + (kk >> 2) * (kKVBytes / 2) + (kk & 3) * 32, 16, 1024);
+                umma_bf16(tmem + kColS + 64 * st, a, b, kIdescS, kk > 0 ? 1u : 0u);
+            }
+        }
+        umma_commit(sb + kOffBar + 8 * (5 + st));
+    };
     if (tid == 0) {
         const CUtensorMap* mq = slot_tile ? &p.tm_q_slot : &p.tm_q_raw;
         mbar_expect_tx(bars + 0, kQBytes);
@@ -256,37 +277,23 @@ __global__ void __launch_bounds__(128, 2) prefill_kernel(const __grid_constant__
             load_kv(b, false);
             load_kv(b, true);
         }
+        if (nblk > 0) ok = mbar_wait(bars + 0, 0, p.d_err);
+        for (int b = 0; b < imin(2, nblk); ++b) issue_s(b);
     }
+    __syncwarp();
 
+    // Block j: S(j) was issued two blocks ahead.  While the threads run the
+    // softmax of block j the tensor cores run PV(j-1) and S(j+1).
     float m_run = -INFINITY, l_run = 0.f;
     bool aborted = false;
     for (int j = 0; j < nblk; ++j) {
         const int st = j & 1;
         const uint32_t ph = (uint32_t)(j >> 1) & 1u;
-        if (tid == 0) {
-            if (j == 0) ok = ok && mbar_wait(bars + 0, 0, p.d_err);
-            if (ok) {
-                ok = mbar_wait(bars + 1 + st, ph, p.d_err);
-                waited_k += ok ? 1u << (16 * st) : 0u;
-            }
-            tc_fence_after();
-            if (ok) {
-                const uint32_t qa = sb + kOffQ, kb = sb + kOffK + st * kKVBytes;
-#pragma unroll
-                for (int kk = 0; kk < kD / 16; ++kk) {
-                    const uint64_t a = sw128_desc(qa + (kk >> 2) * (kQBytes / 2) + (kk & 3) * 32, 16, 1024);
-                    const uint64_t b = sw128_desc(kb + (kk >> 2) * (kKVBytes / 2) + (kk & 3) * 32, 16, 1024);
-                    umma_bf16(t_s, a, b, kIdescS, kk > 0 ? 1u : 0u);
-                }
-            }
-            umma_commit(bar_s);
-        }
-        __syncwarp();
-        ok = mbar_wait(bars + 5, (uint32_t)j & 1u, p.d_err) && ok;
+        ok = mbar_wait(bars + 5 + st, ph, p.d_err) && ok;
         tc_fence_after();
         uint32_t sv[2][32];
-        tmem_ld32(t_s + lane_off, sv[0]);
-        tmem_ld32(t_s + lane_off + 32, sv[1]);
+        tmem_ld32(tmem + kColS + 64 * st + lane_off, sv[0]);
+        tmem_ld32(tmem + kColS + 64 * st + lane_off + 32, sv[1]);
         tmem_wait_ld();
         // S(j) is done with K stage st: refill it two blocks ahead
         if (tid == 0 && ok && j + 2 < nblk) load_kv(j + 2, false);
@@ -333,7 +340,7 @@ __global__ void __launch_bounds__(128, 2) prefill_kernel(const __grid_constant__
         l_run = l_run * alpha + sum;
 
         // PV(j-1) must be complete before O is rescaled and P is overwritten
-        if (j > 0) ok = mbar_wait(bars + 6, (uint32_t)(j - 1) & 1u, p.d_err) && ok;
+        if (j > 0) ok = mbar_wait(bars + 7, (uint32_t)(j - 1) & 1u, p.d_err) && ok;
         tc_fence_after();
         // ... and it released V stage (j+1)&1
         if (tid == 0 && ok && j >= 1 && j + 1 < nblk) load_kv(j + 1, true);
@@ -358,7 +365,7 @@ __global__ void __launch_bounds__(128, 2) prefill_kernel(const __grid_constant__
         fence_async_smem();
         tc_fence_before();
         if (__syncthreads_or(!ok)) {
-            aborted = true;   // PV(j) not issued; PV(j-1) was waited above
+            aborted = true;   // PV(j) not issued; S(j+1) may still be in flight
             break;
         }
         if (tid == 0) {
@@ -375,11 +382,13 @@ __global__ void __launch_bounds__(128, 2) prefill_kernel(const __grid_constant__
                 }
             }
             umma_commit(bar_o);
+            // every thread has read S(j): its buffer takes S(j+2)
+            if (j + 2 < nblk) issue_s(j + 2);
         }
         __syncwarp();
     }
     // last PV (every committed phase of bar_o is waited here or in the loop)
-    if (nblk > 0 && !aborted) ok = mbar_wait(bars + 6, (uint32_t)(nblk - 1) & 1u, p.d_err) && ok;
+    if (nblk > 0 && !aborted) ok = mbar_wait(bars + 7, (uint32_t)(nblk - 1) & 1u, p.d_err) && ok;
     tc_fence_after();
     float* obase = slot_tile ? p.o_slot : p.o_raw;
     float* lbase = slot_tile ? p.lse_slot : p.lse_raw;
@@ -400,8 +409,11 @@ __global__ void __launch_bounds__(128, 2) prefill_kernel(const __grid_constant__
     }
     if (live && lbase)
         lbase[(size_t)qrow * p.Hq + hq] = l_run > 0.f ? (m_run + __log2f(l_run)) * 0.6931471805599453f : -INFINITY;
-    // on an early exit, let the loads still in flight land before the CTA ends
+    // on an early exit, let the MMAs and loads still in flight finish before the
+    // CTA ends (one commit covers every MMA this thread issued)
     if (tid == 0 && (aborted || !ok)) {
+        umma_commit(bar_done);
+        mbar_wait(bars + 8, 0, nullptr);
         for (int st = 0; st < 2; ++st) {
             const uint32_t sh = 16 * st;
             for (uint32_t n = (waited_k >> sh) & 0xFFFFu; n < ((issued_k >> sh) & 0xFFFFu); ++n)
