@@ -11,20 +11,25 @@
 // band, slot prefix), and for one row each range is a single interval, so the
 // mask is two compares per score.
 //
-// Fifth-generation tensor cores, one CTA per (128-row query tile, query head):
-//   * TMA tiled loads (128-byte swizzle) bring Q (resident), and K and V blocks
-//     of 64 keys into two stages each;
-//   * thread 0 issues S = Q K^T (tcgen05.mma, M = 128, N = 64, accumulator in
-//     tensor memory) and O += P V (M = 128, N = 128, V read MN-major);
-//   * thread t owns query row t (TMEM lane t): it reads its 64 scores with
-//     tcgen05.ld, applies the mask and the online softmax, and writes its row of
-//     P (bf16) into shared memory in the swizzled K-major layout the next MMA
-//     reads;
+// Fifth-generation tensor cores, one CTA per (128-row query tile, query head),
+// two CTAs per SM:
+//   * the four softmax warps load their rows of Q once and store them in tensor
+//     memory, where S = Q K^T reads them as the A operand (no shared-memory
+//     re-reads of Q);
+//   * lane 0 of a fifth warp issues TMA tiled loads (128-byte swizzle) of K and
+//     V blocks of 64 keys into three stages each, two blocks ahead, and issues
+//     S = Q K^T (tcgen05.mma, M = 128, N = 64, accumulator in tensor memory) and
+//     O += P V (M = 128, N = 128, V read MN-major);
+//   * thread t of the softmax warps owns query row t (TMEM lane t): it reads its
+//     64 scores with tcgen05.ld, applies the mask and the online softmax, and
+//     writes its row of P (bf16) into shared memory in the swizzled K-major
+//     layout the PV MMA reads;
 //   * the running max only moves when a row's maximum grows by more than 2^8,
 //     so the O rescale (tcgen05.ld / st of the row) is rare; the final
-//     normalisation uses the same max, so the result is exact.
-// 112 KB of shared memory and 256 TMEM columns per CTA: two CTAs per SM, whose
-// softmax and MMA phases overlap.
+//     normalisation uses the same max, so the result is exact;
+//   * the roles hand off through mbarriers (S done, S read, P written, PV done),
+//     every wait is bounded and one timed-out wait stops the CTA and the grid.
+// 112 KB of shared memory and 256 TMEM columns (O, S, Q) per CTA.
 #include "masw_internal.cuh"
 
 #include <cuda.h>
@@ -41,20 +46,20 @@ namespace tcp {
 constexpr int kBM = 128;                         // query rows per CTA = TMEM lanes
 constexpr int kBN = 64;                          // keys per block
 constexpr int kD = 128;                          // head_dim
-constexpr uint32_t kQBytes = kBM * kD * 2;       // 2 panels of 128 rows x 128 B
+constexpr int kStages = 3;                       // K and V stages
 constexpr uint32_t kKVBytes = kBN * kD * 2;      // 2 panels of 64 rows x 128 B
 constexpr uint32_t kPBytes = kBM * kBN * 2;      // 1 panel of 128 rows x 128 B
-constexpr uint32_t kOffQ = 0;
-constexpr uint32_t kOffK = kOffQ + kQBytes;
-constexpr uint32_t kOffV = kOffK + 2 * kKVBytes;
-constexpr uint32_t kOffP = kOffV + 2 * kKVBytes;
-constexpr uint32_t kOffBar = kOffP + kPBytes;    // 9 mbarriers + the TMEM address
-constexpr uint32_t kSmem = kOffBar + 80;
+constexpr uint32_t kOffK = 0;
+constexpr uint32_t kOffV = kOffK + kStages * kKVBytes;
+constexpr uint32_t kOffP = kOffV + kStages * kKVBytes;
+constexpr uint32_t kOffBar = kOffP + kPBytes;    // mbarriers, the TMEM address, an abort flag
+constexpr uint32_t kSmem = kOffBar + 160;
 constexpr uint32_t kTmemCols = 256;
 constexpr uint32_t kColO = 0;                    // O: columns [0, 128)
-constexpr uint32_t kColS = 128;                  // S: two buffers, columns [128, 192) and [192, 256)
+constexpr uint32_t kColS = 128;                  // S: columns [128, 192)
+constexpr uint32_t kColQ = 192;                  // Q (bf16 pairs, the A operand of S): [192, 256)
 // instruction descriptors (kind::f16): f32 accumulator, bf16 A and B, M = 128;
-// S: N = 64, both operands K-major; O: N = 128, B (V) MN-major
+// S: N = 64, A (Q, tensor memory) and B (K) K-major; O: N = 128, B (V) MN-major
 constexpr uint32_t kIdescBase = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(kBM >> 4) << 24);
 constexpr uint32_t kIdescS = kIdescBase | ((uint32_t)(kBN >> 3) << 17);
 constexpr uint32_t kIdescO = kIdescBase | (1u << 16) | ((uint32_t)(kD >> 3) << 17);
@@ -80,6 +85,15 @@ __device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t a, uint64_t 
         "l"(a), "l"(b), "r"(idesc), "r"(acc)
         : "memory");
 }
+// A operand in tensor memory: row i in lane i, 2 bf16 per 32-bit column
+__device__ __forceinline__ void umma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t idesc,
+                                             uint32_t acc) {
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(
+            d_tmem),
+        "r"(a_tmem), "l"(b), "r"(idesc), "r"(acc)
+        : "memory");
+}
 __device__ __forceinline__ void umma_commit(uint32_t bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
                  : "memory");
@@ -89,6 +103,30 @@ __device__ __forceinline__ float ex2_approx(float x) {
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
+}
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+// packed pairs of f32 (low, high) for the f32x2 FMA / add instructions
+__device__ __forceinline__ uint64_t f2_pack(float lo, float hi) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ void f2_unpack(uint64_t v, float& lo, float& hi) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
 }
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
@@ -127,47 +165,79 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t
 }  // namespace tcp
 
 struct PrefillParams {
-    CUtensorMap tm_q_raw;    // [T][Hq][128] bf16, box 64 x 1 x 128
     CUtensorMap tm_k_raw;    // [T][Hkv][128] bf16, box 64 x 1 x 64
     CUtensorMap tm_v_raw;
-    CUtensorMap tm_q_slot;   // [M][Hq][128] (unused when M = 0)
     CUtensorMap tm_k_slot;   // [M][Hkv][128]
     CUtensorMap tm_v_slot;
+    const __nv_bfloat16* q_raw;    // [T][Hq][128]
+    const __nv_bfloat16* q_slot;   // [M][Hq][128]
     float* o_raw;            // [T][Hq][128]
     float* lse_raw;          // [T][Hq] or null
     float* o_slot;           // [M][Hq][128]
     float* lse_slot;         // [M][Hq] or null
     int* d_err;
     int T, M, S, W, r, Hq, Hkv, self_attend;
-    int raw_tiles;           // tiles of raw query rows (the rest are slot tiles)
-    int slot_rows;           // slot query rows per slot tile
+    int slot_ctas;           // CTAs of slot query rows (first in the grid: their key bands are longer)
+    int slot_rows;           // slot query rows per tile of a slot CTA
     float scale_log2;
 };
 
-__global__ void __launch_bounds__(128, 2) prefill_kernel(const __grid_constant__ PrefillParams p) {
+// mbarriers of one CTA
+__device__ __forceinline__ constexpr int bar_k(int s) { return s; }        // K stage landed (TMA)
+__device__ __forceinline__ constexpr int bar_v(int s) { return 3 + s; }    // V stage landed (TMA)
+constexpr int kBarS = 6;       // S = Q K^T done (MMA commit)
+constexpr int kBarSFree = 7;   // the four softmax warps have read S (4 arrivals)
+constexpr int kBarP = 8;       // the four softmax warps have written P and rescaled O (4 arrivals)
+constexpr int kBarO = 9;       // O += P V done (MMA commit)
+constexpr int kBarQ = 10;      // the four softmax warps have stored Q in tensor memory (4 arrivals)
+constexpr int kBarDone = 11;   // every MMA of the CTA done (early exit only)
+constexpr int kNumBars = 12;
+
+// Bounded wait that also gives up as soon as another thread of the CTA has
+// given up (shared abort flag), so that one timed-out wait ends the CTA quickly.
+__device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, volatile int* abort_flag, int* err) {
+    for (uint32_t i = 0; i < kWaitPolls; ++i) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (*abort_flag) return false;
+        if (i > 256) __nanosleep(64);
+    }
+    *abort_flag = 1;
+    atomicExch(err, MASW_ETIMEOUT);
+    return false;
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+// Warp roles: warps 0-3 own query rows 0-127 (TMEM lanes), stage Q into tensor
+// memory and run the softmax; lane 0 of warp 4 issues every TMA load and every
+// MMA.  They hand off through mbarriers only.  Two CTAs per SM.
+__global__ void __launch_bounds__(160, 2) prefill_kernel(const __grid_constant__ PrefillParams p) {
     using namespace tcp;
     extern __shared__ __align__(1024) uint8_t smem[];
-    const int tid = threadIdx.x, warp = tid >> 5;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const uint32_t sb = smem_u32(smem);
-    // mbarriers: q, k0, k1, v0, v1, s0, s1, o, done
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBar);
-    uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + kOffBar + 72);
-    const uint32_t bar_q = sb + kOffBar, bar_o = bar_q + 56, bar_done = bar_q + 64;
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + kOffBar + 8 * kNumBars);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffBar + 8 * kNumBars + 4);
+    auto bar_at = [&](int i) { return sb + kOffBar + 8u * (uint32_t)i; };
 
     const int hq = blockIdx.y, G = p.Hq / p.Hkv, kvh = hq / G;
-    const bool slot_tile = (int)blockIdx.x >= p.raw_tiles;
-    const int q0 = slot_tile ? ((int)blockIdx.x - p.raw_tiles) * p.slot_rows : (int)blockIdx.x * kBM;
+    const bool slot_tile = (int)blockIdx.x < p.slot_ctas;
+    const int rpt = slot_tile ? p.slot_rows : kBM;               // rows of this CTA
+    const int q0 = ((int)blockIdx.x - (slot_tile ? 0 : p.slot_ctas)) * rpt;
     const int nq = slot_tile ? p.M : p.T;
-    const int q1 = imin(nq, q0 + (slot_tile ? p.slot_rows : kBM));
+    const int q1 = imin(nq, q0 + rpt);                           // the CTA's rows [q0, q1)
     const int S = p.S, W = p.W, r = p.r;
 
-    // visible key ranges of the tile: 0 = sink and 1 = window band (raw rows),
+    const int qrow = q0 + tid;
+    const bool live = tid < kBM && qrow < q1;
+
+    // visible key ranges of the CTA: 0 = sink and 1 = window band (raw rows),
     // 2 = slot prefix (slot rows), each [a_k, b_k) possibly empty; this thread's
     // row sees the interval [lo_k, hi_k) of range k.  Kept in scalars (no
     // dynamically indexed arrays) so that nothing spills to local memory.
-    const int qrow = q0 + tid;
-    const bool live = qrow < q1;
-    int a0 = 0, b0 = 0, a1 = 0, b1 = 0, b2 = 0;
+    int b0 = 0, a1 = 0, b1 = 0, b2 = 0;
     int lo1 = 0, hi0 = 0, hi1 = 0, hi2 = 0;
     if (!slot_tile) {
         const int i0 = q0 + 1, i1 = q1, i = qrow + 1;   // 1-based raw positions
@@ -195,7 +265,6 @@ __global__ void __launch_bounds__(128, 2) prefill_kernel(const __grid_constant__
             hi2 = p.self_attend ? m : m - 1;
         }
     }
-    (void)a0;
     const int bs1 = (b0 + kBN - 1) / kBN;
     const int bs2 = bs1 + (b1 - a1 + kBN - 1) / kBN;
     const int nblk = bs2 + (b2 + kBN - 1) / kBN;
@@ -221,206 +290,241 @@ __global__ void __launch_bounds__(128, 2) prefill_kernel(const __grid_constant__
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
     }
     if (tid == 0) {
-        for (int b = 0; b < 9; ++b) mbar_init(bars + b, 1);
+        for (int b = 0; b < kNumBars; ++b)
+            mbar_init(bars + b, (b == kBarSFree || b == kBarP || b == kBarQ) ? 4 : 1);
+        *abort_flag = 0;
         fence_mbar_init();
     }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tslot;
-    const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
-    const uint32_t t_o = tmem + kColO;
 
-    // thread 0: TMA producer and MMA issuer
-    // per stage: loads issued and phases waited (thread 0's bookkeeping, for the
-    // drain on an early exit); bit-packed counters, stage st in bits 16*st
-    uint32_t issued_k = 0, issued_v = 0, waited_k = 0, waited_v = 0;
-    auto load_kv = [&](int blk, bool is_v) {
-        int k, key0;
-        block_of(blk, k, key0);
-        const CUtensorMap* m = k == 2 ? (is_v ? &p.tm_v_slot : &p.tm_k_slot) : (is_v ? &p.tm_v_raw : &p.tm_k_raw);
-        const int st = blk & 1;
-        const uint32_t dst = sb + (is_v ? kOffV : kOffK) + st * kKVBytes;
-        const uint32_t bar = sb + kOffBar + 8 * ((is_v ? 3 : 1) + st);
-        mbar_expect_tx(bars + (is_v ? 3 : 1) + st, kKVBytes);
-        tma_load_3d(dst, m, 0, kvh, key0, bar);
-        tma_load_3d(dst + kKVBytes / 2, m, 64, kvh, key0, bar);
-        (is_v ? issued_v : issued_k) += 1u << (16 * st);
-    };
-    bool ok = true;
-    // S(blk) = Q K(blk)^T into TMEM buffer blk & 1 (thread 0; commits even when
-    // a wait failed so that the waiting threads move on)
-    auto issue_s = [&](int blk) {
-        const int st = blk & 1;
-        if (ok) {
-            ok = mbar_wait(bars + 1 + st, (uint32_t)(blk >> 1) & 1u, p.d_err);
-            waited_k += ok ? 1u << (16 * st) : 0u;
-        }
-        tc_fence_after();
-        if (ok) {
-            const uint32_t qa = sb + kOffQ, kb = sb + kOffK + st * kKVBytes;
-#pragma unroll
-            for (int kk = 0; kk < kD / 16; ++kk) {
-                const uint64_t a = sw128_desc(qa + (kk >> 2) * (kQBytes / 2) + (kk & 3) * 32, 16, 1024);
-                const uint64_t b = sw128_desc(kb + (kk >> 2) * (kKVBytes / 2) + (kk & 3) * 32, 16, 1024);
-                umma_bf16(tmem + kColS + 64 * st, a, b, kIdescS, kk > 0 ? 1u : 0u);
+    if (warp == 4) {
+        // ---------------- producer / MMA issuer (one lane) ----------------
+        if (lane == 0 && nblk > 0) {
+            // blocks whose K (V) load was issued / waited: [0, ki) / [0, kw)
+            int ki = 0, kw = 0, vi = 0, vw = 0;
+            auto load_kv = [&](int blk, bool is_v) {
+                int k, key0;
+                block_of(blk, k, key0);
+                const CUtensorMap* m =
+                    k == 2 ? (is_v ? &p.tm_v_slot : &p.tm_k_slot) : (is_v ? &p.tm_v_raw : &p.tm_k_raw);
+                const int st = blk % kStages;
+                const int bi = is_v ? bar_v(st) : bar_k(st);
+                const uint32_t dst = sb + (is_v ? kOffV : kOffK) + st * kKVBytes;
+                mbar_expect_tx(bars + bi, kKVBytes);
+                tma_load_3d(dst, m, 0, kvh, key0, bar_at(bi));
+                tma_load_3d(dst + kKVBytes / 2, m, 64, kvh, key0, bar_at(bi));
+                (is_v ? vi : ki) = blk + 1;
+            };
+            for (int b = 0; b < imin(2, nblk); ++b) {
+                load_kv(b, false);
+                load_kv(b, true);
             }
-        }
-        umma_commit(sb + kOffBar + 8 * (5 + st));
-    };
-    if (tid == 0) {
-        const CUtensorMap* mq = slot_tile ? &p.tm_q_slot : &p.tm_q_raw;
-        mbar_expect_tx(bars + 0, kQBytes);
-        tma_load_3d(sb + kOffQ, mq, 0, hq, q0, bar_q);
-        tma_load_3d(sb + kOffQ + kQBytes / 2, mq, 64, hq, q0, bar_q);
-        for (int b = 0; b < imin(2, nblk); ++b) {
-            load_kv(b, false);
-            load_kv(b, true);
-        }
-        if (nblk > 0) ok = mbar_wait(bars + 0, 0, p.d_err);
-        for (int b = 0; b < imin(2, nblk); ++b) issue_s(b);
-    }
-    __syncwarp();
-
-    // Block j: S(j) was issued two blocks ahead.  While the threads run the
-    // softmax of block j the tensor cores run PV(j-1) and S(j+1).
-    float m_run = -INFINITY, l_run = 0.f;
-    bool aborted = false;
-    for (int j = 0; j < nblk; ++j) {
-        const int st = j & 1;
-        const uint32_t ph = (uint32_t)(j >> 1) & 1u;
-        ok = mbar_wait(bars + 5 + st, ph, p.d_err) && ok;
-        tc_fence_after();
-        uint32_t sv[2][32];
-        tmem_ld32(tmem + kColS + 64 * st + lane_off, sv[0]);
-        tmem_ld32(tmem + kColS + 64 * st + lane_off + 32, sv[1]);
-        tmem_wait_ld();
-        // S(j) is done with K stage st: refill it two blocks ahead
-        if (tid == 0 && ok && j + 2 < nblk) load_kv(j + 2, false);
-
-        int k, key0;
-        block_of(j, k, key0);
-        const int lo_k = k == 1 ? lo1 : 0;
-        const int hi_k = k == 0 ? hi0 : (k == 1 ? hi1 : hi2);
-        // visible columns of this block for this row: [e_lo, e_hi)
-        const int e_lo = imin(kBN, imax(0, lo_k - key0)), e_hi = imin(kBN, imax(0, hi_k - key0));
-        float x[64];
+            bool ok = wait_or_abort(bars + kBarQ, 0, abort_flag, p.d_err);
+            // iteration j: S(j) as soon as the softmax has read S(j-1), the K
+            // load two blocks ahead, then PV(j-1) and the V load two blocks ahead
+            for (int j = 0; ok && j <= nblk; ++j) {
+                if (j < nblk) {
+                    const int st = j % kStages;
+                    ok = wait_or_abort(bars + bar_k(st), (uint32_t)(j / kStages) & 1u, abort_flag, p.d_err);
+                    if (ok) kw = j + 1;
+                    if (ok && j >= 1) ok = wait_or_abort(bars + kBarSFree, (uint32_t)(j - 1) & 1u, abort_flag, p.d_err);
+                    if (!ok) break;
+                    tc_fence_after();
+                    const uint32_t kb = sb + kOffK + st * kKVBytes;
 #pragma unroll
-        for (int e = 0; e < 64; ++e) x[e] = __uint_as_float(sv[e >> 5][e & 31]);
-        if (e_lo > 0 || e_hi < kBN) {
+                    for (int kk = 0; kk < kD / 16; ++kk) {
+                        const uint64_t bd = sw128_desc(kb + (kk >> 2) * (kKVBytes / 2) + (kk & 3) * 32, 16, 1024);
+                        umma_bf16_ts(tmem + kColS, tmem + kColQ + kk * 8, bd, kIdescS, kk > 0 ? 1u : 0u);
+                    }
+                    umma_commit(bar_at(kBarS));
+                    // K(j+2) takes the stage of K(j-1), whose S the softmax has read
+                    if (j + 2 < nblk) load_kv(j + 2, false);
+                }
+                if (j >= 1) {
+                    const int pj = j - 1, ps = pj % kStages;
+                    ok = wait_or_abort(bars + kBarP, (uint32_t)pj & 1u, abort_flag, p.d_err);
+                    if (ok) {
+                        ok = wait_or_abort(bars + bar_v(ps), (uint32_t)(pj / kStages) & 1u, abort_flag, p.d_err);
+                        if (ok) vw = pj + 1;
+                    }
+                    if (!ok) break;
+                    tc_fence_after();
+                    const uint32_t vb = sb + kOffV + ps * kKVBytes;
 #pragma unroll
-            for (int e = 0; e < 64; ++e) x[e] = (e >= e_lo && e < e_hi) ? x[e] : -INFINITY;
-        }
-        // row max of the raw scores (scale > 0 commutes with max), 8 chains
-        float mx8[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) mx8[e] = x[e];
-#pragma unroll
-        for (int e = 8; e < 64; ++e) mx8[e & 7] = fmaxf(mx8[e & 7], x[e]);
-        const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                               fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
-        float alpha = 1.f;
-        const float m_new = fmaxf(m_run, mx * p.scale_log2);
-        if (m_new > m_run + 8.f) {
-            alpha = ex2_approx(m_run - m_new);
-            m_run = m_new;
-        }
-        const float nmref = m_run == -INFINITY ? 0.f : -m_run;
-        uint32_t pk[32];
-        float sum8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-        for (int e = 0; e < 32; ++e) {
-            const float p0 = ex2_approx(fmaf(x[2 * e], p.scale_log2, nmref));
-            const float p1 = ex2_approx(fmaf(x[2 * e + 1], p.scale_log2, nmref));
-            sum8[e & 7] += p0 + p1;
-            pk[e] = pack_bf16(p0, p1);
-        }
-        const float sum = ((sum8[0] + sum8[1]) + (sum8[2] + sum8[3])) + ((sum8[4] + sum8[5]) + (sum8[6] + sum8[7]));
-        const bool resc = alpha != 1.f && l_run > 0.f;
-        l_run = l_run * alpha + sum;
-
-        // PV(j-1) must be complete before O is rescaled and P is overwritten
-        if (j > 0) ok = mbar_wait(bars + 7, (uint32_t)(j - 1) & 1u, p.d_err) && ok;
-        tc_fence_after();
-        // ... and it released V stage (j+1)&1
-        if (tid == 0 && ok && j >= 1 && j + 1 < nblk) load_kv(j + 1, true);
-        if (__any_sync(0xffffffffu, resc)) {
-#pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                uint32_t ov[32];
-                tmem_ld32(t_o + lane_off + c * 32, ov);
-                tmem_wait_ld();
-#pragma unroll
-                for (int e = 0; e < 32; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * alpha);
-                tmem_st32(t_o + lane_off + c * 32, ov);
-            }
-            tmem_wait_st();
-        }
-        // row tid of P: 64 bf16 = one 128-byte swizzled row
-        const uint32_t prow = sb + kOffP + (uint32_t)tid * 128u;
-#pragma unroll
-        for (int c = 0; c < 8; ++c)
-            st_shared_v4(prow + ((uint32_t)(c ^ (tid & 7)) << 4), pk[4 * c], pk[4 * c + 1], pk[4 * c + 2],
-                         pk[4 * c + 3]);
-        fence_async_smem();
-        tc_fence_before();
-        if (__syncthreads_or(!ok)) {
-            aborted = true;   // PV(j) not issued; S(j+1) may still be in flight
-            break;
-        }
-        if (tid == 0) {
-            tc_fence_after();
-            ok = mbar_wait(bars + 3 + st, ph, p.d_err);
-            waited_v += ok ? 1u << (16 * st) : 0u;
-            if (ok) {
-                const uint32_t vb = sb + kOffV + st * kKVBytes;
-#pragma unroll
-                for (int kk = 0; kk < kBN / 16; ++kk) {
-                    const uint64_t a = sw128_desc(sb + kOffP + kk * 32, 16, 1024);
-                    const uint64_t b = sw128_desc(vb + kk * 2048, kKVBytes / 2, 1024);
-                    umma_bf16(t_o, a, b, kIdescO, (j > 0 || kk > 0) ? 1u : 0u);
+                    for (int kk = 0; kk < kBN / 16; ++kk) {
+                        const uint64_t a = sw128_desc(sb + kOffP + kk * 32, 16, 1024);
+                        const uint64_t bd = sw128_desc(vb + kk * 2048, kKVBytes / 2, 1024);
+                        umma_bf16(tmem + kColO, a, bd, kIdescO, (pj > 0 || kk > 0) ? 1u : 0u);
+                    }
+                    umma_commit(bar_at(kBarO));
+                    // P(j-1) written means the softmax saw PV(j-2) complete:
+                    // V(j+1) takes the stage of V(j-2)
+                    if (j + 1 < nblk && j + 1 >= 2) load_kv(j + 1, true);
                 }
             }
-            umma_commit(bar_o);
-            // every thread has read S(j): its buffer takes S(j+2)
-            if (j + 2 < nblk) issue_s(j + 2);
+            if (!ok) {
+                // early exit: let every MMA and load in flight finish before the
+                // CTA releases its tensor and shared memory
+                *abort_flag = 1;
+                umma_commit(bar_at(kBarDone));
+                mbar_wait(bars + kBarDone, 0, nullptr);
+                for (int blk = kw; blk < ki; ++blk)
+                    mbar_wait(bars + bar_k(blk % kStages), (uint32_t)(blk / kStages) & 1u, nullptr);
+                for (int blk = vw; blk < vi; ++blk)
+                    mbar_wait(bars + bar_v(blk % kStages), (uint32_t)(blk / kStages) & 1u, nullptr);
+            }
         }
         __syncwarp();
-    }
-    // last PV (every committed phase of bar_o is waited here or in the loop)
-    if (nblk > 0 && !aborted) ok = mbar_wait(bars + 7, (uint32_t)(nblk - 1) & 1u, p.d_err) && ok;
-    tc_fence_after();
-    float* obase = slot_tile ? p.o_slot : p.o_raw;
-    float* lbase = slot_tile ? p.lse_slot : p.lse_raw;
-    const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
-    float* orow = obase + ((size_t)(live ? qrow : q0) * p.Hq + hq) * kD;
+    } else {
+        // ---------------- softmax warps: thread tid owns query row tid ----------------
+        const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+        const uint32_t t_o = tmem + kColO + lane_off;
+        // Q row -> tensor memory (zeros past the last row), the A operand of S
+        {
+            const __nv_bfloat16* qsrc = slot_tile ? p.q_slot : p.q_raw;
+            const uint4* qp = reinterpret_cast<const uint4*>(qsrc + ((size_t)(live ? qrow : 0) * p.Hq + hq) * kD);
 #pragma unroll
-    for (int c = 0; c < 4; ++c) {
-        uint32_t ov[32];
-        tmem_ld32(t_o + lane_off + c * 32, ov);
-        tmem_wait_ld();
-        if (live && nblk > 0) {
+            for (int h = 0; h < 2; ++h) {
+                uint32_t qv[32];
 #pragma unroll
-            for (int e = 0; e < 32; e += 4)
-                *reinterpret_cast<float4*>(orow + c * 32 + e) =
-                    make_float4(__uint_as_float(ov[e]) * inv, __uint_as_float(ov[e + 1]) * inv,
-                                __uint_as_float(ov[e + 2]) * inv, __uint_as_float(ov[e + 3]) * inv);
+                for (int c = 0; c < 8; ++c) {
+                    const uint4 w = live ? __ldg(qp + h * 8 + c) : make_uint4(0u, 0u, 0u, 0u);
+                    qv[4 * c] = w.x;
+                    qv[4 * c + 1] = w.y;
+                    qv[4 * c + 2] = w.z;
+                    qv[4 * c + 3] = w.w;
+                }
+                tmem_st32(tmem + kColQ + lane_off + h * 32, qv);
+            }
+            tmem_wait_st();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar_at(kBarQ));
         }
-    }
-    if (live && lbase)
-        lbase[(size_t)qrow * p.Hq + hq] = l_run > 0.f ? (m_run + __log2f(l_run)) * 0.6931471805599453f : -INFINITY;
-    // on an early exit, let the MMAs and loads still in flight finish before the
-    // CTA ends (one commit covers every MMA this thread issued)
-    if (tid == 0 && (aborted || !ok)) {
-        umma_commit(bar_done);
-        mbar_wait(bars + 8, 0, nullptr);
-        for (int st = 0; st < 2; ++st) {
-            const uint32_t sh = 16 * st;
-            for (uint32_t n = (waited_k >> sh) & 0xFFFFu; n < ((issued_k >> sh) & 0xFFFFu); ++n)
-                mbar_wait(bars + 1 + st, n & 1u, nullptr);
-            for (uint32_t n = (waited_v >> sh) & 0xFFFFu; n < ((issued_v >> sh) & 0xFFFFu); ++n)
-                mbar_wait(bars + 3 + st, n & 1u, nullptr);
+        float m_run = -INFINITY, l_run = 0.f;
+        bool ok = true;
+        for (int j = 0; j < nblk; ++j) {
+            if (!__all_sync(0xffffffffu, wait_or_abort(bars + kBarS, (uint32_t)j & 1u, abort_flag, p.d_err))) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            uint32_t sv[2][32];
+            tmem_ld32(tmem + kColS + lane_off, sv[0]);
+            tmem_ld32(tmem + kColS + lane_off + 32, sv[1]);
+            tmem_wait_ld();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar_at(kBarSFree));
+
+            int k, key0;
+            block_of(j, k, key0);
+            const int lo_k = k == 1 ? lo1 : 0;
+            const int hi_k = k == 0 ? hi0 : (k == 1 ? hi1 : hi2);
+            // visible columns of this block for this row: [e_lo, e_hi)
+            const int e_lo = imin(kBN, imax(0, lo_k - key0)), e_hi = imin(kBN, imax(0, hi_k - key0));
+            float x[64];
+#pragma unroll
+            for (int e = 0; e < 64; ++e) x[e] = __uint_as_float(sv[e >> 5][e & 31]);
+            if (e_lo > 0 || e_hi < kBN) {
+#pragma unroll
+                for (int e = 0; e < 64; ++e) x[e] = (e >= e_lo && e < e_hi) ? x[e] : -INFINITY;
+            }
+            // row max of the raw scores (scale > 0 commutes with max): 3-input
+            // max in four chains
+            float mx4[4] = {x[0], x[1], x[2], x[3]};
+#pragma unroll
+            for (int e = 4; e < 64; e += 8) {
+#pragma unroll
+                for (int c = 0; c < 4; ++c) mx4[c] = fmax3(mx4[c], x[e + 2 * c], x[e + 2 * c + 1]);
+            }
+            const float mx = fmax3(fmax3(mx4[0], mx4[1], mx4[2]), mx4[3], mx4[3]);
+            float alpha = 1.f;
+            const float m_new = fmaxf(m_run, mx * p.scale_log2);
+            if (m_new > m_run + 8.f) {
+                alpha = ex2_approx(m_run - m_new);
+                m_run = m_new;
+            }
+            const float nmref = m_run == -INFINITY ? 0.f : -m_run;
+            // p = 2^(x * scale_log2 - m): packed FMA for the arguments, packed
+            // adds for the row sum (four f32x2 chains)
+            const uint64_t sc2 = f2_pack(p.scale_log2, p.scale_log2), nm2 = f2_pack(nmref, nmref);
+            uint32_t pk[32];
+            uint64_t sum2[4] = {0, 0, 0, 0};
+#pragma unroll
+            for (int e = 0; e < 32; ++e) {
+                float a0, a1v;
+                f2_unpack(f2_fma(f2_pack(x[2 * e], x[2 * e + 1]), sc2, nm2), a0, a1v);
+                const float p0 = ex2_approx(a0), p1 = ex2_approx(a1v);
+                sum2[e & 3] = f2_add(sum2[e & 3], f2_pack(p0, p1));
+                pk[e] = pack_bf16(p0, p1);
+            }
+            float sum_lo, sum_hi;
+            f2_unpack(f2_add(f2_add(sum2[0], sum2[1]), f2_add(sum2[2], sum2[3])), sum_lo, sum_hi);
+            const float sum = sum_lo + sum_hi;
+            const bool resc = alpha != 1.f && l_run > 0.f;
+            l_run = l_run * alpha + sum;
+
+            // PV(j-1) must be complete before O is rescaled and P is overwritten
+            if (j > 0) {
+                if (!__all_sync(0xffffffffu,
+                                wait_or_abort(bars + kBarO, (uint32_t)(j - 1) & 1u, abort_flag, p.d_err))) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+            }
+            if (__any_sync(0xffffffffu, resc)) {
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    uint32_t ov[32];
+                    tmem_ld32(t_o + c * 32, ov);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * alpha);
+                    tmem_st32(t_o + c * 32, ov);
+                }
+                tmem_wait_st();
+            }
+            // row tid of P: 64 bf16 = one 128-byte swizzled row
+            const uint32_t prow = sb + kOffP + (uint32_t)tid * 128u;
+#pragma unroll
+            for (int c = 0; c < 8; ++c)
+                st_shared_v4(prow + ((uint32_t)(c ^ (tid & 7)) << 4), pk[4 * c], pk[4 * c + 1], pk[4 * c + 2],
+                             pk[4 * c + 3]);
+            fence_async_smem();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar_at(kBarP));
         }
+        // last PV, then O / l for this row
+        if (ok && nblk > 0)
+            ok = __all_sync(0xffffffffu,
+                            wait_or_abort(bars + kBarO, (uint32_t)(nblk - 1) & 1u, abort_flag, p.d_err));
+        tc_fence_after();
+        float* obase = slot_tile ? p.o_slot : p.o_raw;
+        float* lbase = slot_tile ? p.lse_slot : p.lse_raw;
+        const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
+        float* orow = obase + ((size_t)(live ? qrow : q0) * p.Hq + hq) * kD;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            uint32_t ov[32];
+            tmem_ld32(t_o + c * 32, ov);
+            tmem_wait_ld();
+            if (live && nblk > 0) {
+#pragma unroll
+                for (int e = 0; e < 32; e += 4)
+                    *reinterpret_cast<float4*>(orow + c * 32 + e) =
+                        make_float4(__uint_as_float(ov[e]) * inv, __uint_as_float(ov[e + 1]) * inv,
+                                    __uint_as_float(ov[e + 2]) * inv, __uint_as_float(ov[e + 3]) * inv);
+            }
+        }
+        if (live && lbase)
+            lbase[(size_t)qrow * p.Hq + hq] =
+                l_run > 0.f ? (m_run + __log2f(l_run)) * 0.6931471805599453f : -INFINITY;
     }
     tc_fence_before();
     __syncthreads();
@@ -555,12 +659,13 @@ extern "C" int masw_prefill(masw_mem_t* mem, int layer, int seq, int T, const vo
     PrefillParams p;
     std::memset(&p, 0, sizeof(p));
     const int Hkv = mem->Hkv;
-    bool maps = make_map(&p.tm_q_raw, q_raw, T, n_q_heads, tcp::kBM) && make_map(&p.tm_k_raw, k_raw, T, Hkv, tcp::kBN) &&
+    bool maps = make_map(&p.tm_k_raw, k_raw, T, Hkv, tcp::kBN) &&
                 make_map(&p.tm_v_raw, v_raw, T, Hkv, tcp::kBN);
     if (M > 0)
-        maps = maps && make_map(&p.tm_q_slot, q_slot, M, n_q_heads, tcp::kBM) &&
-               make_map(&p.tm_k_slot, k_slot, M, Hkv, tcp::kBN) && make_map(&p.tm_v_slot, v_slot, M, Hkv, tcp::kBN);
+        maps = maps && make_map(&p.tm_k_slot, k_slot, M, Hkv, tcp::kBN) && make_map(&p.tm_v_slot, v_slot, M, Hkv, tcp::kBN);
     if (!maps) return masw_set_error(mem, MASW_EINVAL, "prefill: cannot describe the inputs as TMA tensors");
+    p.q_raw = (const __nv_bfloat16*)q_raw;
+    p.q_slot = (const __nv_bfloat16*)q_slot;
     p.o_raw = o_raw;
     p.lse_raw = lse_raw;
     p.o_slot = o_slot;
@@ -574,12 +679,13 @@ extern "C" int masw_prefill(masw_mem_t* mem, int layer, int seq, int T, const vo
     p.Hq = n_q_heads;
     p.Hkv = Hkv;
     p.self_attend = mem->self_attend;
-    p.raw_tiles = (T + tcp::kBM - 1) / tcp::kBM;
+    const int raw_ctas = (T + tcp::kBM - 1) / tcp::kBM;
     // slot rows per tile: extra rows widen the tile's window band by r keys
     // each, worth it while that stays below the keys every slot row reads anyway
     p.slot_rows = imin(tcp::kBM, imax(1, (mem->S + mem->W + M / 2) / mem->r + 1));
     p.scale_log2 = mem->scale * 1.4426950408889634f;
-    const int tiles = p.raw_tiles + (M + p.slot_rows - 1) / p.slot_rows;
+    p.slot_ctas = (M + p.slot_rows - 1) / p.slot_rows;
+    const int tiles = p.slot_ctas + raw_ctas;
     cudaStream_t st = (cudaStream_t)stream;
     static bool configured[64] = {};
     if (!configured[mem->device & 63]) {
@@ -588,7 +694,7 @@ extern "C" int masw_prefill(masw_mem_t* mem, int layer, int seq, int T, const vo
                                                 cudaSharedmemCarveoutMaxShared));
         configured[mem->device & 63] = true;
     }
-    MASW_CUDA_TRY(mem, masw_launch(prefill_kernel, dim3(tiles, n_q_heads), dim3(128), tcp::kSmem, st, 1, p));
+    MASW_CUDA_TRY(mem, masw_launch(prefill_kernel, dim3(tiles, n_q_heads), dim3(160), tcp::kSmem, st, 1, p));
     StoreParams sp;
     std::memset(&sp, 0, sizeof(sp));
     sp.k_raw = (const uint8_t*)k_raw;
