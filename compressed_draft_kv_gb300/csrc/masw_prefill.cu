@@ -16,10 +16,12 @@
 //   * the four softmax warps load their rows of Q once and store them in tensor
 //     memory, where S = Q K^T reads them as the A operand (no shared-memory
 //     re-reads of Q);
-//   * lane 0 of a fifth warp issues TMA tiled loads (128-byte swizzle) of K and
-//     V blocks of 64 keys into three stages each, two blocks ahead, and issues
-//     S = Q K^T (tcgen05.mma, M = 128, N = 64, accumulator in tensor memory) and
-//     O += P V (M = 128, N = 128, V read MN-major);
+//   * lane 0 of a fifth warp issues TMA tiled loads (128-byte swizzle) of K
+//     blocks of 64 keys into three stages, two blocks ahead, and S = Q K^T
+//     (tcgen05.mma, M = 128, N = 64, accumulator in tensor memory); lane 0 of a
+//     sixth warp does the same for V and O += P V (M = 128, N = 128, V read
+//     MN-major).  Two issuing threads keep both MMA streams moving: a single
+//     thread spends most of its time on MMA issue and commit round trips;
 //   * thread t of the softmax warps owns query row t (TMEM lane t): it reads its
 //     64 scores with tcgen05.ld, applies the mask and the online softmax, and
 //     writes its row of P (bf16) into shared memory in the swizzled K-major
@@ -190,8 +192,9 @@ constexpr int kBarSFree = 7;   // the four softmax warps have read S (4 arrivals
 constexpr int kBarP = 8;       // the four softmax warps have written P and rescaled O (4 arrivals)
 constexpr int kBarO = 9;       // O += P V done (MMA commit)
 constexpr int kBarQ = 10;      // the four softmax warps have stored Q in tensor memory (4 arrivals)
-constexpr int kBarDone = 11;   // every MMA of the CTA done (early exit only)
-constexpr int kNumBars = 12;
+constexpr int kBarDone = 11;   // every S MMA done (early exit only)
+constexpr int kBarDoneV = 12;  // every PV MMA done (early exit only)
+constexpr int kNumBars = 13;
 
 // Bounded wait that also gives up as soon as another thread of the CTA has
 // given up (shared abort flag), so that one timed-out wait ends the CTA quickly.
@@ -210,9 +213,10 @@ __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
 }
 
 // Warp roles: warps 0-3 own query rows 0-127 (TMEM lanes), stage Q into tensor
-// memory and run the softmax; lane 0 of warp 4 issues every TMA load and every
-// MMA.  They hand off through mbarriers only.  Two CTAs per SM.
-__global__ void __launch_bounds__(160, 2) prefill_kernel(const __grid_constant__ PrefillParams p) {
+// memory and run the softmax; lane 0 of warp 4 loads K and issues S = Q K^T,
+// lane 0 of warp 5 loads V and issues O += P V.  They hand off through mbarriers
+// only.  Two CTAs per SM.
+__global__ void __launch_bounds__(192, 2) prefill_kernel(const __grid_constant__ PrefillParams p) {
     using namespace tcp;
     extern __shared__ __align__(1024) uint8_t smem[];
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -300,12 +304,15 @@ __global__ void __launch_bounds__(160, 2) prefill_kernel(const __grid_constant__
     tc_fence_after();
     const uint32_t tmem = *tslot;
 
-    if (warp == 4) {
-        // ---------------- producer / MMA issuer (one lane) ----------------
+    if (warp >= 4) {
+        // ------- warp 4 lane 0: K loads and S = Q K^T; warp 5 lane 0: V loads and O += P V -------
+        // (two issuing threads: each waits on its own inputs, so neither MMA
+        // stream stalls behind the other's waits)
         if (lane == 0 && nblk > 0) {
-            // blocks whose K (V) load was issued / waited: [0, ki) / [0, kw)
-            int ki = 0, kw = 0, vi = 0, vw = 0;
-            auto load_kv = [&](int blk, bool is_v) {
+            const bool is_v = warp == 5;
+            // blocks whose load was issued / waited: [0, li) / [0, lw)
+            int li = 0, lw = 0;
+            auto load = [&](int blk) {
                 int k, key0;
                 block_of(blk, k, key0);
                 const CUtensorMap* m =
@@ -316,20 +323,17 @@ __global__ void __launch_bounds__(160, 2) prefill_kernel(const __grid_constant__
                 mbar_expect_tx(bars + bi, kKVBytes);
                 tma_load_3d(dst, m, 0, kvh, key0, bar_at(bi));
                 tma_load_3d(dst + kKVBytes / 2, m, 64, kvh, key0, bar_at(bi));
-                (is_v ? vi : ki) = blk + 1;
+                li = blk + 1;
             };
-            for (int b = 0; b < imin(2, nblk); ++b) {
-                load_kv(b, false);
-                load_kv(b, true);
-            }
-            bool ok = wait_or_abort(bars + kBarQ, 0, abort_flag, p.d_err);
-            // iteration j: S(j) as soon as the softmax has read S(j-1), the K
-            // load two blocks ahead, then PV(j-1) and the V load two blocks ahead
-            for (int j = 0; ok && j <= nblk; ++j) {
-                if (j < nblk) {
+            for (int b = 0; b < imin(2, nblk); ++b) load(b);
+            bool ok = true;
+            if (!is_v) {
+                ok = wait_or_abort(bars + kBarQ, 0, abort_flag, p.d_err);
+                for (int j = 0; ok && j < nblk; ++j) {
                     const int st = j % kStages;
                     ok = wait_or_abort(bars + bar_k(st), (uint32_t)(j / kStages) & 1u, abort_flag, p.d_err);
-                    if (ok) kw = j + 1;
+                    if (ok) lw = j + 1;
+                    // single S buffer: the softmax must have read S(j-1)
                     if (ok && j >= 1) ok = wait_or_abort(bars + kBarSFree, (uint32_t)(j - 1) & 1u, abort_flag, p.d_err);
                     if (!ok) break;
                     tc_fence_after();
@@ -341,40 +345,41 @@ __global__ void __launch_bounds__(160, 2) prefill_kernel(const __grid_constant__
                     }
                     umma_commit(bar_at(kBarS));
                     // K(j+2) takes the stage of K(j-1), whose S the softmax has read
-                    if (j + 2 < nblk) load_kv(j + 2, false);
+                    if (j + 2 < nblk) load(j + 2);
                 }
-                if (j >= 1) {
-                    const int pj = j - 1, ps = pj % kStages;
-                    ok = wait_or_abort(bars + kBarP, (uint32_t)pj & 1u, abort_flag, p.d_err);
+            } else {
+                for (int j = 0; ok && j < nblk; ++j) {
+                    const int st = j % kStages;
+                    ok = wait_or_abort(bars + kBarP, (uint32_t)j & 1u, abort_flag, p.d_err);
                     if (ok) {
-                        ok = wait_or_abort(bars + bar_v(ps), (uint32_t)(pj / kStages) & 1u, abort_flag, p.d_err);
-                        if (ok) vw = pj + 1;
+                        ok = wait_or_abort(bars + bar_v(st), (uint32_t)(j / kStages) & 1u, abort_flag, p.d_err);
+                        if (ok) lw = j + 1;
                     }
                     if (!ok) break;
                     tc_fence_after();
-                    const uint32_t vb = sb + kOffV + ps * kKVBytes;
+                    const uint32_t vb = sb + kOffV + st * kKVBytes;
 #pragma unroll
                     for (int kk = 0; kk < kBN / 16; ++kk) {
                         const uint64_t a = sw128_desc(sb + kOffP + kk * 32, 16, 1024);
                         const uint64_t bd = sw128_desc(vb + kk * 2048, kKVBytes / 2, 1024);
-                        umma_bf16(tmem + kColO, a, bd, kIdescO, (pj > 0 || kk > 0) ? 1u : 0u);
+                        umma_bf16(tmem + kColO, a, bd, kIdescO, (j > 0 || kk > 0) ? 1u : 0u);
                     }
                     umma_commit(bar_at(kBarO));
-                    // P(j-1) written means the softmax saw PV(j-2) complete:
-                    // V(j+1) takes the stage of V(j-2)
-                    if (j + 1 < nblk && j + 1 >= 2) load_kv(j + 1, true);
+                    // P(j) written means the softmax saw PV(j-1) complete:
+                    // V(j+2) takes the stage of V(j-1)
+                    if (j + 2 < nblk) load(j + 2);
                 }
             }
             if (!ok) {
-                // early exit: let every MMA and load in flight finish before the
-                // CTA releases its tensor and shared memory
+                // early exit: let this thread's MMAs and loads in flight finish
+                // before the CTA releases its tensor and shared memory
                 *abort_flag = 1;
-                umma_commit(bar_at(kBarDone));
-                mbar_wait(bars + kBarDone, 0, nullptr);
-                for (int blk = kw; blk < ki; ++blk)
-                    mbar_wait(bars + bar_k(blk % kStages), (uint32_t)(blk / kStages) & 1u, nullptr);
-                for (int blk = vw; blk < vi; ++blk)
-                    mbar_wait(bars + bar_v(blk % kStages), (uint32_t)(blk / kStages) & 1u, nullptr);
+                const int done = is_v ? kBarDoneV : kBarDone;
+                umma_commit(bar_at(done));
+                mbar_wait(bars + done, 0, nullptr);
+                for (int blk = lw; blk < li; ++blk)
+                    mbar_wait(bars + (is_v ? bar_v(blk % kStages) : bar_k(blk % kStages)),
+                              (uint32_t)(blk / kStages) & 1u, nullptr);
             }
         }
         __syncwarp();
@@ -694,7 +699,7 @@ extern "C" int masw_prefill(masw_mem_t* mem, int layer, int seq, int T, const vo
                                                 cudaSharedmemCarveoutMaxShared));
         configured[mem->device & 63] = true;
     }
-    MASW_CUDA_TRY(mem, masw_launch(prefill_kernel, dim3(tiles, n_q_heads), dim3(160), tcp::kSmem, st, 1, p));
+    MASW_CUDA_TRY(mem, masw_launch(prefill_kernel, dim3(tiles, n_q_heads), dim3(192), tcp::kSmem, st, 1, p));
     StoreParams sp;
     std::memset(&sp, 0, sizeof(sp));
     sp.k_raw = (const uint8_t*)k_raw;
