@@ -484,7 +484,29 @@ def eq1_speedup(l_acc: float, l_draft: int, t_draft: float, t_target: float) -> 
 # Draft prefill under the structured write mask.
 # --------------------------------------------------------------------------
 
-def prefill_attn(S, W, r, q_raw, k_raw, v_raw, q_slot, k_slot, v_slot, scale=None, self_attend=False):
+def prefill_row_mask(kind, idx, T, S, W, r, self_attend=False):
+    """Mask row of one prefill query over the columns [raw 1..T] ++ [slot 1..M]
+    ([EN] §3.3 Algorithm 2 step 2 with the structured mask of §3.2 Algorithm 1
+    step 2).  kind "raw": raw token idx (1-based) reads the sink, its local
+    window and the slots with tau_m < idx; kind "slot": slot g_idx reads what the
+    slot write at tau_idx reads (sink, window at tau_idx, slots 1..idx-1)."""
+    M = slot_count(T, S, W, r)
+    mask = np.zeros(T + M, dtype=bool)
+    if kind == "raw":
+        i = idx
+        mask[:i] = draft_mask(i, 0, S, W)            # raw columns 1..i
+        mask[T:T + slot_count(i - 1, S, W, r)] = True   # slots with tau_m <= i-1
+    else:
+        m = idx
+        tau = boundary(m, S, W, r)
+        row = slot_write_mask(tau, m, S, W, self_attend)
+        mask[:tau] = row[:tau]
+        mask[T:T + m] = row[tau:]
+    return mask
+
+
+def prefill_attn(S, W, r, q_raw, k_raw, v_raw, q_slot, k_slot, v_slot, scale=None, self_attend=False,
+                 raw_rows=None, slot_rows=None):
     """One layer of the draft prefill over T raw tokens with the M = m(T) slot
     tokens interleaved ([EN] §3.3 Algorithm 2 step 2, with the structured mask of
     §3.2 Algorithm 1 step 2): raw token i reads the sink, its local window and
@@ -492,7 +514,8 @@ def prefill_attn(S, W, r, q_raw, k_raw, v_raw, q_slot, k_slot, v_slot, scale=Non
     window at tau_m and slots 1..m-1.  Columns are [raw 1..T] ++ [slot 1..M].
     q_raw [T, Hq, D], k_raw/v_raw [T, Hkv, D], q_slot [M, Hq, D],
     k_slot/v_slot [M, Hkv, D].  Returns O_raw [T, Hq, D], LSE_raw [T, Hq],
-    O_slot [M, Hq, D], LSE_slot [M, Hq]."""
+    O_slot [M, Hq, D], LSE_slot [M, Hq].  raw_rows / slot_rows (1-based lists)
+    restrict the evaluation to those rows (the others stay 0 / -inf)."""
     q_raw = np.asarray(q_raw, dtype=np.float64)
     k_raw = np.asarray(k_raw, dtype=np.float64)
     v_raw = np.asarray(v_raw, dtype=np.float64)
@@ -506,18 +529,12 @@ def prefill_attn(S, W, r, q_raw, k_raw, v_raw, q_slot, k_slot, v_slot, scale=Non
     V = np.concatenate([v_raw, v_slot], 0)
     o_raw = np.zeros((T, Hq, D))
     l_raw = np.full((T, Hq), -np.inf)
-    for i in range(1, T + 1):
-        mask = np.zeros(T + M, dtype=bool)
-        mask[:i] = draft_mask(i, 0, S, W)            # raw columns 1..i
-        mask[T:T + slot_count(i - 1, S, W, r)] = True   # slots with tau_m <= i-1
+    for i in (range(1, T + 1) if raw_rows is None else raw_rows):
+        mask = prefill_row_mask("raw", i, T, S, W, r)
         o_raw[i - 1], l_raw[i - 1] = attention(q_raw[i - 1], K, V, mask, scale)
     o_slot = np.zeros((M, Hq, D))
     l_slot = np.full((M, Hq), -np.inf)
-    for m in range(1, M + 1):
-        tau = boundary(m, S, W, r)
-        row = slot_write_mask(tau, m, S, W, self_attend)
-        mask = np.zeros(T + M, dtype=bool)
-        mask[:tau] = row[:tau]
-        mask[T:T + m] = row[tau:]
+    for m in (range(1, M + 1) if slot_rows is None else slot_rows):
+        mask = prefill_row_mask("slot", m, T, S, W, r, self_attend)
         o_slot[m - 1], l_slot[m - 1] = attention(q_slot[m - 1], K, V, mask, scale)
     return o_raw, l_raw, o_slot, l_slot
