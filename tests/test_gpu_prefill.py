@@ -107,3 +107,48 @@ def test_prefill_rejects_bad_calls():
             capi.masw_prefill(f.h, 0, 0, q32, kv32, kv32, None, None, None, torch.empty(8, 8, 64, device=DEV))
     finally:
         f.close()
+
+
+def test_prefill_full_size_sampled_rows():
+    """The benchmark's launch configuration (3B-draft attention shape, 32K prefix,
+    S = 4, W = 1024, r = 512, 61 slots): sampled raw rows (sink, first window,
+    first boundaries, middle, last) and slot rows against the oracle's per-row
+    evaluation, and the stored memory bit for bit."""
+    import numpy as np
+    from compressed_draft_kv_gb300 import synth
+    S, W, r, Hkv, G, T, D = 4, 1024, 512, 8, 3, 32768, 128
+    Hq = Hkv * G
+    p = Pair(S, W, r, Hkv, D, layers=1, batch=1, dtype="bf16", Hq=Hq, max_seq_len=T + 64, reserve=16,
+             tag="prefill_full")
+    try:
+        M = orc.slot_count(T, S, W, r)
+        g = lambda shape, name: synth.normal(shape, "bf16", "prefill_full", name)
+        qr, kr, vr = g((T, Hq, D), "q"), g((T, Hkv, D), "k"), g((T, Hkv, D), "v")
+        qs, ks, vs = g((M, Hq, D), "qs"), g((M, Hkv, D), "ks"), g((M, Hkv, D), "vs")
+        o_r = torch.empty(T, Hq, D, device=DEV)
+        l_r = torch.empty(T, Hq, device=DEV)
+        o_s = torch.empty(M, Hq, D, device=DEV)
+        l_s = torch.empty(M, Hq, device=DEV)
+        capi.masw_prefill(p.h, 0, 0, qr.to(DEV), kr.to(DEV), vr.to(DEV), qs.to(DEV), ks.to(DEV), vs.to(DEV),
+                          o_r, l_r, o_s, l_s)
+        capi.masw_sync(p.h)
+        rng = np.random.default_rng(17)
+        raw_rows = sorted(set([1, 3, 4, 5, 64, 129, S + W, S + W + 1, S + W + r, S + W + r + 1, 16384, T - 1, T]
+                              + rng.integers(1, T + 1, 8).tolist()))
+        slot_rows = sorted(set([1, 2, M // 2, M - 1, M]))
+        want = orc.prefill_attn(S, W, r, qr.float().numpy(), kr.float().numpy(), vr.float().numpy(),
+                                qs.float().numpy(), ks.float().numpy(), vs.float().numpy(),
+                                raw_rows=raw_rows, slot_rows=slot_rows)
+        ri = [i - 1 for i in raw_rows]
+        si = [m - 1 for m in slot_rows]
+        from gpu_helpers import assert_close
+        assert_close(o_r[ri], want[0][ri], "bf16", "full-size prefill O_raw")
+        assert_close(l_r[ri], want[1][ri], "bf16", "full-size prefill LSE_raw")
+        assert_close(o_s[si], want[2][si], "bf16", "full-size prefill O_slot")
+        assert_close(l_s[si], want[3][si], "bf16", "full-size prefill LSE_slot")
+        # every row of the launch, not only the sampled ones, is finite
+        assert torch.isfinite(o_r).all() and torch.isfinite(l_r).all() and torch.isfinite(o_s).all()
+        p.ref.load(0, 0, kr.float().numpy(), vr.float().numpy(), ks.float().numpy(), vs.float().numpy())
+        p.check_state(0, 0)
+    finally:
+        p.close()
