@@ -392,6 +392,7 @@ int masw_launch_decode(masw_mem_t* mem, int mode, int layer, const void* q, int 
     prm.Tmax = mem->max_seq_len;
     prm.M_max = mem->M_max;
     prm.self_attend = mem->self_attend;
+    prm.early = mem->last_write_layer != layer ? 1 : 0;
     if (step_active) {
         prm.step = 1;
         for (int i = 0; i < MASW_MAX_BATCH / 32; ++i) prm.active[i] = step_active[i];
@@ -422,7 +423,14 @@ int masw_launch_decode(masw_mem_t* mem, int mode, int layer, const void* q, int 
     while (n_split > 1 && masw_decode_part_floats(n_rows, mem->Hkv, G, mem->D, n_split) > mem->part_floats)
         --n_split;
     prm.n_split = n_split;
-    if (mem->dtype == MASW_BF16) return masw_launch_decode_mma(mem, prm, G, n_rows, kmax, stream);
-    if (mem->D == 128) return launch_g<float, 128>(mem, prm, G, n_rows, stream);
-    return launch_g<float, 64>(mem, prm, G, n_rows, stream);
+    int rc;
+    if (mem->dtype == MASW_BF16)
+        rc = masw_launch_decode_mma(mem, prm, G, n_rows, kmax, stream);
+    else if (mem->D == 128)
+        rc = launch_g<float, 128>(mem, prm, G, n_rows, stream);
+    else
+        rc = launch_g<float, 64>(mem, prm, G, n_rows, stream);
+    // a fused step stores the new token's row, a slot write stores the slot's rows
+    if (prm.step || mode == kModeSlot || fuse) mem->last_write_layer = layer;
+    return rc;
 }

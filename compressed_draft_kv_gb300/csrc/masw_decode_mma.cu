@@ -29,10 +29,13 @@ namespace cg = cooperative_groups;
 
 namespace masw {
 
-template <int D>
+// NST stages of K/V in shared memory: 2 (64 KB, three CTAs fit on an SM, so the
+// next launch's CTAs start copying while this one merges) or 3 (96 KB, more
+// bytes in flight for CTAs that each stream a long run of keys)
+template <int D, int NST_>
 struct MmaCfg {
     static constexpr int KPS = 64;               // keys per stage (16 per warp)
-    static constexpr int NST = 3;                // stages in flight
+    static constexpr int NST = NST_;
     static constexpr int CH = D / 8;             // 16-byte chunks per row
     static constexpr int ROWB = D * 2;           // bytes per bf16 row
     static constexpr int STAGE = 2 * KPS * ROWB; // K then V
@@ -47,9 +50,9 @@ __device__ __forceinline__ uint32_t swz_off(int row, int ch) {
     return (uint32_t)(row * ROWB + ((ch ^ (row & 7)) << 4));
 }
 
-template <int D>
+template <int D, int NST_>
 __global__ void __launch_bounds__(128) decode_mma_kernel(const __grid_constant__ DecodeParams p) {
-    using C = MmaCfg<D>;
+    using C = MmaCfg<D, NST_>;
     constexpr int KPS = C::KPS, NST = C::NST, CH = C::CH, ROWB = C::ROWB, KS = C::KS;
     extern __shared__ __align__(128) uint8_t smem[];
     __shared__ Seg segs[5];
@@ -92,27 +95,8 @@ __global__ void __launch_bounds__(128) decode_mma_kernel(const __grid_constant__
         s_nseg = n;
     };
     if (tid == 0) build(*(volatile const int*)(p.d_t + ci), *(volatile const int*)(p.d_m + ci));
-    pdl_wait();
-    pdl_trigger();
-
-    // Q^T as B fragments: column n < G is query head h*G + n of row z; columns
-    // G..2G-1 are the fused slot query's heads; the rest are zero
-    uint32_t qb[KS][2];
-    {
-        const int n = lane >> 2;
-        const bool real = n < NR;
-        const __nv_bfloat16* qrow =
-            n < G ? (const __nv_bfloat16*)p.q + ((size_t)z * p.Hq + (size_t)h * G + n) * D
-                  : (real ? (const __nv_bfloat16*)p.q_slot + ((size_t)si * p.Hq + (size_t)h * G + (n - G)) * D
-                          : (const __nv_bfloat16*)p.q);
-#pragma unroll
-        for (int ks = 0; ks < KS; ++ks) {
-            const int d = ks * 16 + (lane & 3) * 2;
-            qb[ks][0] = real ? *reinterpret_cast<const uint32_t*>(qrow + d) : 0u;
-            qb[ks][1] = real ? *reinterpret_cast<const uint32_t*>(qrow + d + 8) : 0u;
-        }
-    }
     __syncthreads();
+
     int nseg = s_nseg;
     int total = s_start[nseg];
     const bool fresh = p.step && ((p.active[z >> 5] >> (z & 31)) & 1u);
@@ -155,13 +139,49 @@ __global__ void __launch_bounds__(128) decode_mma_kernel(const __grid_constant__
             cp_async16(sv + swz_off<ROWB>(row, my_ch), vs, bytes);
         }
     };
+    // The first stages are copied before the dependency wait when the previous
+    // launch wrote no pool row of this layer (p.early) and they hold pool rows
+    // only (the new token's row and a self-attended slot come from the caller's
+    // buffers, which the previous kernel may still be writing).
+    const int n_input = ((p.step && ((p.active[z >> 5] >> (z & 31)) & 1u)) ? 1 : 0) +
+                        ((p.mode == kDevModeSlot && p.self_attend) ? 1 : 0);
+    const bool early = p.early && imin(r1, r0 + (NST - 1) * KPS) <= total - n_input;
+    if (early) {
 #pragma unroll
-    for (int c = 0; c < NST - 1; ++c) {
-        if (c < nstage) load_stage(c);
-        cp_async_commit();
+        for (int c = 0; c < NST - 1; ++c) {
+            if (c < nstage) load_stage(c);
+            cp_async_commit();
+        }
+    }
+    pdl_wait();
+    pdl_trigger();
+
+    // Q^T as B fragments: column n < G is query head h*G + n of row z; columns
+    // G..2G-1 are the fused slot query's heads; the rest are zero
+    uint32_t qb[KS][2];
+    {
+        const int n = lane >> 2;
+        const bool real = n < NR;
+        const __nv_bfloat16* qrow =
+            n < G ? (const __nv_bfloat16*)p.q + ((size_t)z * p.Hq + (size_t)h * G + n) * D
+                  : (real ? (const __nv_bfloat16*)p.q_slot + ((size_t)si * p.Hq + (size_t)h * G + (n - G)) * D
+                          : (const __nv_bfloat16*)p.q);
+#pragma unroll
+        for (int ks = 0; ks < KS; ++ks) {
+            const int d = ks * 16 + (lane & 3) * 2;
+            qb[ks][0] = real ? *reinterpret_cast<const uint32_t*>(qrow + d) : 0u;
+            qb[ks][1] = real ? *reinterpret_cast<const uint32_t*>(qrow + d + 8) : 0u;
+        }
     }
     if (tid == 0) s_respec = (p.d_t[ci] != s_t || p.d_m[ci] != s_m_before) ? 1 : 0;
     __syncthreads();
+    if (!s_respec && !early) {
+#pragma unroll
+        for (int c = 0; c < NST - 1; ++c) {
+            if (c < nstage) load_stage(c);
+            cp_async_commit();
+        }
+    }
     if (s_respec) {   // the previous kernel changed the counters: drop the speculative stages
         cp_async_wait<0>();
         __syncthreads();
@@ -388,7 +408,7 @@ __global__ void __launch_bounds__(128) decode_mma_kernel(const __grid_constant__
 }
 
 // Clusters of `cs` CTAs of the decode kernel that can be resident at once (cached per device).
-template <int D>
+template <int D, int NST>
 static int max_clusters(masw_mem_t* mem, int dev, int cs) {
     static int cache[64][9] = {};
     if (cs < 2 || cs > 8) return 0;
@@ -396,7 +416,7 @@ static int max_clusters(masw_mem_t* mem, int dev, int cs) {
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3(cs * 64, 1, 1);
         cfg.blockDim = dim3(128, 1, 1);
-        cfg.dynamicSmemBytes = MmaCfg<D>::SMEM;
+        cfg.dynamicSmemBytes = MmaCfg<D, NST>::SMEM;
         cudaLaunchAttribute a;
         a.id = cudaLaunchAttributeClusterDimension;
         a.val.clusterDim.x = cs;
@@ -405,7 +425,7 @@ static int max_clusters(masw_mem_t* mem, int dev, int cs) {
         cfg.attrs = &a;
         cfg.numAttrs = 1;
         int n = 0;
-        if (cudaOccupancyMaxActiveClusters(&n, decode_mma_kernel<D>, &cfg) != cudaSuccess) {
+        if (cudaOccupancyMaxActiveClusters(&n, decode_mma_kernel<D, NST>, &cfg) != cudaSuccess) {
             cudaGetLastError();
             n = 0;
         }
@@ -415,47 +435,72 @@ static int max_clusters(masw_mem_t* mem, int dev, int cs) {
     return cache[dev][cs];
 }
 
+struct MmaPlan {
+    int n_split;
+    bool cluster;
+};
+
+// One wave of the NST-stage kernel.  Splits of a pair are merged inside a
+// thread-block cluster (distributed shared memory, no global round trip) when
+// clusters of that size can all be resident at once; otherwise (few pairs, many
+// splits) the ticketed global merge is used.
+template <int D, int NST>
+static int plan_mma(masw_mem_t* mem, int rows, int GR, int kmax, MmaPlan& pl) {
+    using C = MmaCfg<D, NST>;
+    static int occ[64] = {};
+    const int dev = mem->device & 63;
+    if (!occ[dev]) {
+        MASW_CUDA_TRY(mem, cudaFuncSetAttribute(decode_mma_kernel<D, NST>,
+                                                cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM));
+        int n = 0;
+        MASW_CUDA_TRY(mem, cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_mma_kernel<D, NST>, 128, C::SMEM));
+        occ[dev] = n > 0 ? n : 1;
+    }
+    const int pairs = rows * mem->Hkv;
+    const int slots = occ[dev] * mem->num_sms;
+    const int max_useful = imax(1, (kmax + 63) / 64);
+    pl.n_split = 1;
+    pl.cluster = false;
+    for (int cs = imin(8, imin(max_useful, slots / imax(1, pairs))); cs >= 2; --cs) {
+        if (cs * pairs * 2 >= slots && max_clusters<D, NST>(mem, dev, cs) >= pairs) {
+            pl.n_split = cs;
+            pl.cluster = true;
+            break;
+        }
+    }
+    if (!pl.cluster) {
+        int n_split = imax(1, slots / pairs);
+        n_split = imin(n_split, max_useful);
+        n_split = imin(n_split, kMaxSplit);
+        while (n_split > 1 && masw_decode_part_floats(rows, mem->Hkv, GR, D, n_split) > mem->part_floats) --n_split;
+        pl.n_split = n_split;
+    }
+    return MASW_OK;
+}
+
+template <int D, int NST>
+static int launch_plan(masw_mem_t* mem, DecodeParams& prm, int rows, const MmaPlan& pl, cudaStream_t stream) {
+    prm.n_split = pl.n_split;
+    prm.cluster = pl.cluster ? 1 : 0;
+    MASW_CUDA_TRY(mem, masw_launch(decode_mma_kernel<D, NST>, dim3(pl.n_split, mem->Hkv, rows), dim3(128),
+                                   MmaCfg<D, NST>::SMEM, stream, pl.cluster ? pl.n_split : 1, prm));
+    return MASW_OK;
+}
+
+// Two stages unless each CTA would stream a long run of keys (e.g. one split
+// per pair at batch 32): then three stages keep more bytes in flight, which
+// matters more than an early start of the next launch.
+constexpr int kLongRunKeys = 1536;
+
 template <int D>
 static int launch_mma(masw_mem_t* mem, DecodeParams& prm, int G, int rows, int kmax, cudaStream_t stream) {
     const int GR = prm.q_slot ? 2 * G : G;   // partial rows per pair
     prm.rows_per_pair = GR;
-    using C = MmaCfg<D>;
-    static int occ[64] = {};
-    const int dev = mem->device & 63;
-    if (!occ[dev]) {
-        MASW_CUDA_TRY(mem, cudaFuncSetAttribute(decode_mma_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                C::SMEM));
-        int n = 0;
-        MASW_CUDA_TRY(mem, cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_mma_kernel<D>, 128, C::SMEM));
-        occ[dev] = n > 0 ? n : 1;
-    }
-    // One wave.  Splits of a pair are merged inside a thread-block cluster
-    // (distributed shared memory, no global round trip) when clusters of that
-    // size can all be resident at once; otherwise (few pairs, many splits) the
-    // ticketed global merge is used.
-    const int pairs = rows * mem->Hkv;
-    const int slots = occ[dev] * mem->num_sms;
-    const int max_useful = imax(1, (kmax + 63) / 64);
-    int n_split = 1;
-    bool cluster = false;
-    for (int cs = imin(8, imin(max_useful, slots / imax(1, pairs))); cs >= 2; --cs) {
-        if (cs * pairs * 2 >= slots && max_clusters<D>(mem, dev, cs) >= pairs) {
-            n_split = cs;
-            cluster = true;
-            break;
-        }
-    }
-    if (!cluster) {
-        n_split = imax(1, slots / pairs);
-        n_split = imin(n_split, max_useful);
-        n_split = imin(n_split, kMaxSplit);
-        while (n_split > 1 && masw_decode_part_floats(rows, mem->Hkv, GR, D, n_split) > mem->part_floats) --n_split;
-    }
-    prm.n_split = n_split;
-    prm.cluster = cluster ? 1 : 0;
-    MASW_CUDA_TRY(mem, masw_launch(decode_mma_kernel<D>, dim3(n_split, mem->Hkv, rows), dim3(128), C::SMEM, stream,
-                                   cluster ? n_split : 1, prm));
-    return MASW_OK;
+    MmaPlan pl;
+    if (int rc = plan_mma<D, 2>(mem, rows, GR, kmax, pl)) return rc;
+    if (kmax / pl.n_split <= kLongRunKeys) return launch_plan<D, 2>(mem, prm, rows, pl, stream);
+    if (int rc = plan_mma<D, 3>(mem, rows, GR, kmax, pl)) return rc;
+    return launch_plan<D, 3>(mem, prm, rows, pl, stream);
 }
 
 }  // namespace masw

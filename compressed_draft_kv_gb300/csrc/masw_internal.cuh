@@ -60,6 +60,11 @@ struct masw_mem {
     unsigned* tickets = nullptr;      // [B*Hkv] per-(row, head) split tickets
     std::vector<int> h_t, h_m;
     int device = 0, num_sms = 0;
+    // layer whose pool rows the last launch of this handle wrote (-2: unknown,
+    // e.g. after set-up).  A decode launch of another layer may copy its first
+    // K/V stages before its programmatic-launch dependency wait: the kernel it
+    // overlaps with cannot have written those rows.
+    int last_write_layer = -2;
     std::string err;
 };
 
@@ -334,6 +339,8 @@ struct DecodeParams {
     int mode, layer, B, Hkv, Hq, S, W, Wc, C, Tmax, M_max, n_split, self_attend;
     int step;             // 1: append the new token (k_g/v_g) of every active row first (fused step)
     int cluster;          // 1: the n_split CTAs of a pair form a cluster and merge in shared memory
+    int early;            // 1: the previous launch wrote no pool row of this layer; pool rows may be
+                          // copied before the dependency wait (counters are re-checked after it)
     // fused boundary step: slot query / K / V / outputs for the listed rows
     // (slot_of[z] = index into them, -1 for rows not at a boundary)
     const void* q_slot;
