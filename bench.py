@@ -436,6 +436,50 @@ def run_verify(torch, capi, synth, reps: int = 5):
             "launches": 2 * L}
 
 
+def run_accept(torch, capi, reps: int = 20):
+    """Greedy acceptance of verified blocks: batch 8, L_draft = 5 (6 logit rows
+    per sequence), a 128,256-token vocabulary (Llama-3), bf16 logits.  24
+    distinct logit buffers (295 MB, larger than L2) are cycled inside a graph so
+    every call reads its logits from HBM."""
+    B, L, V, nbuf = 8, 5, 128256, 24
+    dev = torch.device("cuda", torch.cuda.current_device())
+    g = torch.Generator(device=dev)
+    g.manual_seed(11)
+    logits = [torch.randn(B, L + 1, V, generator=g, device=dev).to(torch.bfloat16) for _ in range(nbuf)]
+    draft = torch.randint(0, V, (B, L), generator=g, device=dev, dtype=torch.int32)
+    tokens = torch.empty(B, L + 1, dtype=torch.int32, device=dev)
+    n_emit = torch.empty(B, dtype=torch.int32, device=dev)
+    ws = torch.zeros(capi.masw_greedy_workspace_bytes(B, L, V), dtype=torch.uint8, device=dev)
+    st = torch.cuda.Stream(device=dev)
+
+    def run():
+        for x in logits:
+            capi.masw_greedy_accept(x, draft, tokens, n_emit, workspace=ws, stream=st.cuda_stream)
+    with torch.cuda.stream(st):
+        run()
+    torch.cuda.synchronize()
+    gr = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(gr, stream=st):
+        run()
+    for _ in range(3):
+        gr.replay()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(st):
+        e0.record(st)
+        for _ in range(reps):
+            gr.replay()
+        e1.record(st)
+    torch.cuda.synchronize()
+    per_call = e0.elapsed_time(e1) / 1e3 / (reps * nbuf)
+    nbytes = B * (L + 1) * V * 2
+    del logits
+    torch.cuda.empty_cache()
+    return {"batch": B, "l_draft": L, "vocab": V, "dtype": "bf16", "us_per_call": per_call * 1e6,
+            "bytes_per_call": nbytes, "gbs": nbytes / per_call / 1e9, "launches": 1}
+
+
 def prefill_flops(T, S, W, r, Hq, D, self_attend=False):
     """Algorithmic flops of one (layer, sequence) prefill: 4 D flops (QK^T and PV)
     per query head per visible (query, key) pair of the structured mask."""
@@ -717,6 +761,10 @@ def main():
     verify = None
     if not args.no_verify and args.workload == WORKLOAD:
         verify = run_verify(torch, capi, synth)
+    accept = None
+    if not args.no_verify and args.workload == WORKLOAD:
+        accept = run_accept(torch, capi)
+        accept["hbm_frac"] = accept["gbs"] / _peaks()[0]
     prefill = None
     if not args.no_prefill and args.workload == WORKLOAD:
         prefill = run_prefill(torch, capi, synth, args.workload, prefix)
@@ -774,6 +822,23 @@ def main():
         verify["draft_over_verify_per_sequence"] = draft_per_seq / verify_per_seq
         verify["hbm_frac"] = verify["gbs"] / peak
         line["verify"] = verify
+        # Eq. 1 of the pages with this run's attention-only latencies: t_d = one
+        # draft decode step per sequence, t_t = one verify per sequence, and the
+        # pages' tokens per iteration (3B draft, 32K; [EN] §5 draft-cost table)
+        t_d = (secs / args.steps) / dsteps / wl["batch"]
+        t_t = verify["ms_per_verify"] / 1e3 / verify["batch"]
+        t_d_full = (secs_full / full_iters) / dsteps / wl["batch"]
+        line["eq1_illustration"] = {
+            "note": "attention-only latencies measured here (draft memory S=4, W=1024, r=512) with the pages' "
+                    "Tok./Iter; an illustration of Eq. 1, not a measured model speedup",
+            "l_draft": dsteps, "t_draft_over_t_target": t_d / t_t, "t_full_draft_over_t_target": t_d_full / t_t,
+            "tok_per_iter_pages": {"full_kv_draft": 4.05, "masw_4x": 3.65, "masw_8x": 3.43},
+            "speedup_masw_4x": capi.masw_eq1_speedup(3.65 - 1.0, dsteps, t_d, t_t),
+            "speedup_masw_8x": capi.masw_eq1_speedup(3.43 - 1.0, dsteps, t_d, t_t),
+            "speedup_full_kv_draft": capi.masw_eq1_speedup(4.05 - 1.0, dsteps, t_d_full, t_t),
+        }
+    if accept:
+        line["greedy_accept"] = accept
     if prefill:
         line["prefill"] = prefill
     if rank == 0 and world == 1 and not args.no_cpu_baseline and args.workload == WORKLOAD:

@@ -239,8 +239,8 @@ def masw_greedy_accept(logits, draft, tokens, n_emit, workspace=None, stream=Non
     L = L1 - 1
     need = ctypes.c_size_t()
     _check(load().masw_greedy_workspace_bytes(B, L, V, ctypes.byref(need)))
-    if workspace is None:
-        workspace = torch.empty(need.value, dtype=torch.uint8, device=logits.device)
+    if workspace is None:   # zero-filled once; every call leaves it zero-filled
+        workspace = torch.zeros(need.value, dtype=torch.uint8, device=logits.device)
     dt = MASW_BF16 if logits.dtype == torch.bfloat16 else MASW_F32
     _check(load().masw_greedy_accept(_ptr(logits), _ptr(draft), B, L, V, dt, _ptr(tokens), _ptr(n_emit),
                                      _ptr(workspace), workspace.numel(), _stream(stream)))

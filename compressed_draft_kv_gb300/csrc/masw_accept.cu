@@ -9,8 +9,9 @@
 //
 // Grid (chunks, L+1, B): each CTA reduces one vocabulary chunk of one row with
 // 16-byte loads to a (max, id) pair; the last CTA of a sequence (ticket) merges
-// the chunks of its L+1 rows and computes L_acc.  HBM-bound: the logits are read
-// once.
+// the chunks of its L+1 rows, computes L_acc and resets its ticket, so the
+// workspace is zero-filled again when the call completes.  HBM-bound: the
+// logits are read once.
 #include "masw_internal.cuh"
 
 #include <cstring>
@@ -51,13 +52,24 @@ __global__ void __launch_bounds__(256) accept_kernel(const __grid_constant__ Acc
                 const float f = __bfloat162float(x[i]);
                 if (better(f, i, bv, bi)) { bv = f; bi = i; }
             }
-            for (int i = vv0 + tid * 8; i < vv1; i += 256 * 8) {
-                const uint4 w = *reinterpret_cast<const uint4*>(x + i);
-                float f[8];
-                Elem<__nv_bfloat16>::unpack(w, f);
+            // four independent 16-byte loads in flight per thread per round
+            for (int i0 = vv0 + tid * 8; i0 < vv1; i0 += 4 * 256 * 8) {
+                uint4 w[4];
 #pragma unroll
-                for (int k = 0; k < 8; ++k)
-                    if (better(f[k], i + k, bv, bi)) { bv = f[k]; bi = i + k; }
+                for (int u = 0; u < 4; ++u) {
+                    const int i = i0 + u * 256 * 8;
+                    w[u] = i < vv1 ? __ldcs(reinterpret_cast<const uint4*>(x + i)) : make_uint4(0u, 0u, 0u, 0u);
+                }
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const int i = i0 + u * 256 * 8;
+                    if (i >= vv1) break;
+                    float f[8];
+                    Elem<__nv_bfloat16>::unpack(w[u], f);
+#pragma unroll
+                    for (int k = 0; k < 8; ++k)
+                        if (better(f[k], i + k, bv, bi)) { bv = f[k]; bi = i + k; }
+                }
             }
             v = imax(vv0, vv1);
         }
@@ -204,8 +216,9 @@ extern "C" int masw_greedy_accept(const void* logits, const int* draft, int B, i
     const size_t es = p.bf16 ? 2 : 4;
     p.vec = (((uintptr_t)logits & 15) == 0 && ((size_t)V * es) % 16 == 0) ? 1 : 0;
     cudaStream_t st = (cudaStream_t)stream;
-    cudaError_t e = cudaMemsetAsync(p.tickets, 0, (size_t)B * sizeof(unsigned), st);
-    if (e == cudaSuccess) e = masw_launch(accept_kernel, dim3(chunks, L + 1, B), dim3(256), 0, st, 1, p);
+    // the tickets are zero on entry (zero-filled workspace, reset by the last
+    // CTA of every call): no memset node between calls
+    const cudaError_t e = masw_launch(accept_kernel, dim3(chunks, L + 1, B), dim3(256), 0, st, 1, p);
     if (e != cudaSuccess) return masw_set_error(nullptr, MASW_ECUDA, std::string("greedy: ") + cudaGetErrorString(e));
     return MASW_OK;
 }

@@ -283,8 +283,10 @@ int masw_verify_attn_noalloc(const void* q, const void* k_cache, const void* v_c
  * target's correction or bonus token).
  * logits: device [B, L+1, V] (dtype MASW_BF16 or MASW_F32); draft: device int
  * [B, L]; tokens: device int [B, L+1]; n_emit: device int [B]; workspace:
- * device scratch of masw_greedy_workspace_bytes() bytes (16-byte aligned; no
- * initialisation needed; not shared by overlapping calls). */
+ * device scratch of masw_greedy_workspace_bytes() bytes (16-byte aligned; zero-filled
+ * by the caller before its first use, e.g. with cudaMemset; every completed call
+ * leaves it zero-filled again, so it is cleared once per allocation; not shared by
+ * overlapping calls). */
 int masw_greedy_accept(const void* logits, const int* draft, int B, int L, int V, int dtype,
                        int* tokens, int* n_emit, void* workspace, size_t workspace_bytes,
                        masw_stream_t stream);

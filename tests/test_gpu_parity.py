@@ -361,11 +361,15 @@ def test_greedy_accept(dtype, B, L, V):
     dd = torch.from_numpy(np.ascontiguousarray(draft, dtype=np.int32)).to(DEV)
     tok = torch.full((B, L + 1), -7, dtype=torch.int32, device=DEV)
     n = torch.full((B,), -7, dtype=torch.int32, device=DEV)
-    capi.masw_greedy_accept(dl, dd, tok, n)
-    capi.masw_greedy_accept(dl, dd, tok, n)    # a second call reuses the reset tickets
-    torch.cuda.synchronize()
-    assert np.array_equal(tok.cpu().numpy(), want_tok)
-    assert np.array_equal(n.cpu().numpy(), want_n)
+    ws = torch.zeros(capi.masw_greedy_workspace_bytes(B, L, V), dtype=torch.uint8, device=DEV)
+    for call in range(3):   # one zero-filled workspace, reused: every call leaves its tickets at zero
+        tok.fill_(-7)
+        n.fill_(-7)
+        capi.masw_greedy_accept(dl, dd, tok, n, workspace=ws)
+        torch.cuda.synchronize()
+        assert np.array_equal(tok.cpu().numpy(), want_tok), call
+        assert np.array_equal(n.cpu().numpy(), want_n), call
+    assert not ws[-4 * B:].any()   # the per-sequence tickets (the workspace's last B words) are zero again
 
 
 def test_state_errors():
