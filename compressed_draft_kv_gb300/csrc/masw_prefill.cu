@@ -337,12 +337,14 @@ __global__ void __launch_bounds__(192, 2) prefill_kernel(const __grid_constant__
                     if (ok && j >= 1) ok = wait_or_abort(bars + kBarSFree, (uint32_t)(j - 1) & 1u, abort_flag, p.d_err);
                     if (!ok) break;
                     tc_fence_after();
-                    const uint32_t kb = sb + kOffK + st * kKVBytes;
+                    // descriptor of the stage once; k-step kk adds a compile-time
+                    // offset to the start-address field (addresses stay < 256 KB)
+                    const uint64_t bd0 = sw128_desc(sb + kOffK + st * kKVBytes, 16, 1024);
 #pragma unroll
-                    for (int kk = 0; kk < kD / 16; ++kk) {
-                        const uint64_t bd = sw128_desc(kb + (kk >> 2) * (kKVBytes / 2) + (kk & 3) * 32, 16, 1024);
-                        umma_bf16_ts(tmem + kColS, tmem + kColQ + kk * 8, bd, kIdescS, kk > 0 ? 1u : 0u);
-                    }
+                    for (int kk = 0; kk < kD / 16; ++kk)
+                        umma_bf16_ts(tmem + kColS, tmem + kColQ + kk * 8,
+                                     bd0 + (uint64_t)(((kk >> 2) * (kKVBytes / 2) + (kk & 3) * 32) >> 4), kIdescS,
+                                     kk > 0 ? 1u : 0u);
                     umma_commit(bar_at(kBarS));
                     // K(j+2) takes the stage of K(j-1), whose S the softmax has read
                     if (j + 2 < nblk) load(j + 2);
@@ -357,13 +359,12 @@ __global__ void __launch_bounds__(192, 2) prefill_kernel(const __grid_constant__
                     }
                     if (!ok) break;
                     tc_fence_after();
-                    const uint32_t vb = sb + kOffV + st * kKVBytes;
+                    const uint64_t a0 = sw128_desc(sb + kOffP, 16, 1024);
+                    const uint64_t v0 = sw128_desc(sb + kOffV + st * kKVBytes, kKVBytes / 2, 1024);
 #pragma unroll
-                    for (int kk = 0; kk < kBN / 16; ++kk) {
-                        const uint64_t a = sw128_desc(sb + kOffP + kk * 32, 16, 1024);
-                        const uint64_t bd = sw128_desc(vb + kk * 2048, kKVBytes / 2, 1024);
-                        umma_bf16(tmem + kColO, a, bd, kIdescO, (j > 0 || kk > 0) ? 1u : 0u);
-                    }
+                    for (int kk = 0; kk < kBN / 16; ++kk)
+                        umma_bf16(tmem + kColO, a0 + (uint64_t)((kk * 32) >> 4), v0 + (uint64_t)((kk * 2048) >> 4),
+                                  kIdescO, (j > 0 || kk > 0) ? 1u : 0u);
                     umma_commit(bar_at(kBarO));
                     // P(j) written means the softmax saw PV(j-1) complete:
                     // V(j+2) takes the stage of V(j-1)
