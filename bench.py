@@ -804,7 +804,7 @@ def main():
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": _recorded_traffic() if args.workload == WORKLOAD else None,
                      "peak_kind": peak_kind,
-                     "kernel": "decode_mma_kernel<128, 2> (masw_draft_step: fused append + draft attention)",
+                     "kernel": "decode_mma_kernel<128, NST> (masw_draft_step: fused append + draft attention; NST = 2 stages, 3 when each CTA streams a long run of keys)",
                      "bytes_per_launch": total_b, "kv_bytes_per_launch": kv_b,
                      "us_per_launch": kern_s * 1e6, "frac_of_8tbs": achieved / 8000.0},
         "gpu_launches": launches * args.steps,
