@@ -392,7 +392,7 @@ int masw_launch_decode(masw_mem_t* mem, int mode, int layer, const void* q, int 
     prm.Tmax = mem->max_seq_len;
     prm.M_max = mem->M_max;
     prm.self_attend = mem->self_attend;
-    prm.early = mem->last_write_layer != layer ? 1 : 0;
+    prm.early = masw_may_copy_early(mem, stream, layer) ? 1 : 0;
     if (step_active) {
         prm.step = 1;
         for (int i = 0; i < MASW_MAX_BATCH / 32; ++i) prm.active[i] = step_active[i];
@@ -431,6 +431,6 @@ int masw_launch_decode(masw_mem_t* mem, int mode, int layer, const void* q, int 
     else
         rc = launch_g<float, 64>(mem, prm, G, n_rows, stream);
     // a fused step stores the new token's row, a slot write stores the slot's rows
-    if (prm.step || mode == kModeSlot || fuse) mem->last_write_layer = layer;
+    masw_note_launch(mem, stream, (prm.step || mode == kModeSlot || fuse) ? layer : -1);
     return rc;
 }

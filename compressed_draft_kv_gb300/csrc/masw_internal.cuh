@@ -60,10 +60,12 @@ struct masw_mem {
     unsigned* tickets = nullptr;      // [B*Hkv] per-(row, head) split tickets
     std::vector<int> h_t, h_m;
     int device = 0, num_sms = 0;
-    // layer whose pool rows the last launch of this handle wrote (-2: unknown,
-    // e.g. after set-up).  A decode launch of another layer may copy its first
-    // K/V stages before its programmatic-launch dependency wait: the kernel it
-    // overlaps with cannot have written those rows.
+    // The handle's last launch: its stream and the layer whose pool rows it
+    // wrote (-1: none; -2: unknown, e.g. after set-up).  A decode launch on the
+    // same stream for another layer may copy its first K/V stages before its
+    // programmatic-launch dependency wait: the only kernel it can overlap with is
+    // the previous one on that stream, which wrote none of those rows.
+    void* last_stream = nullptr;
     int last_write_layer = -2;
     std::string err;
 };
@@ -466,6 +468,14 @@ __device__ void pair_tail(const DecodeParams& p, int lb, int h, int t, int m_bef
 // Host helpers shared by the translation units.
 // ---------------------------------------------------------------------------
 int masw_set_error(masw_mem_t* mem, int code, const std::string& msg);
+// record a launch of the handle (see masw_mem::last_stream)
+inline void masw_note_launch(masw_mem_t* mem, void* stream, int wrote_layer) {
+    mem->last_stream = stream;
+    mem->last_write_layer = wrote_layer;
+}
+inline bool masw_may_copy_early(const masw_mem_t* mem, void* stream, int layer) {
+    return mem->last_write_layer != -2 && mem->last_stream == stream && mem->last_write_layer != layer;
+}
 #define MASW_CUDA_TRY(mem, call)                                                        \
     do {                                                                                \
         cudaError_t e_ = (call);                                                        \

@@ -330,7 +330,7 @@ int masw_append_kv(masw_mem_t* mem, int layer, const void* k, const void* v, con
         p.Wc = mem->Wc;
         p.C = mem->C;
         p.Tmax = mem->max_seq_len;
-        mem->last_write_layer = layer;
+        masw_note_launch(mem, (void*)stream, layer);
         MASW_CUDA_TRY(mem, masw_launch(append_kernel, dim3(mem->B), dim3(128), 0, (cudaStream_t)stream, 1, p));
         for (int b = 0; b < mem->B; ++b)
             if (!active || active[b]) mem->h_t[(size_t)layer * mem->B + b] += 1;
@@ -404,6 +404,7 @@ int masw_rollback(masw_mem_t* mem, const int* seq_ids, const int* t_new, int n, 
     p.W = mem->W;
     p.r = mem->r;
     p.n = n;
+    masw_note_launch(mem, (void*)stream, -1);   // counters only (re-checked by every decode launch)
     MASW_CUDA_TRY(mem, masw_launch(rollback_kernel, dim3(n), dim3(32), 0, (cudaStream_t)stream, 1, p));
     for (int i = 0; i < n; ++i)
         for (int l = 0; l < mem->L; ++l) {
@@ -557,7 +558,7 @@ int masw_mem_load(masw_mem_t* mem, int layer, int seq, int t, const void* k_raw,
             return masw_set_error(mem, MASW_EINVAL, "load: n_slots must equal max(0, (t-S-W)/r)");
         if (n_slots > 0 && (!k_slots || !v_slots)) return masw_set_error(mem, MASW_EINVAL, "load: NULL slot K/V");
         if (n_slots > mem->M_max) return masw_set_error(mem, MASW_ECAPACITY, "load: slot chain is full");
-        mem->last_write_layer = layer;
+        masw_note_launch(mem, nullptr, -2);   // set-up: no early copies right after a load
         MASW_CUDA_TRY(mem, cudaDeviceSynchronize());
         const size_t rowb = (size_t)mem->D * mem->esize;
         const size_t lb = (size_t)layer * mem->B + seq;

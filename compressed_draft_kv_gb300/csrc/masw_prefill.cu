@@ -700,7 +700,7 @@ extern "C" int masw_prefill(masw_mem_t* mem, int layer, int seq, int T, const vo
                                                 cudaSharedmemCarveoutMaxShared));
         configured[mem->device & 63] = true;
     }
-    mem->last_write_layer = layer;   // the store kernel below writes this layer's rows
+    masw_note_launch(mem, (void*)st, layer);   // the store kernel below writes this layer's rows
     MASW_CUDA_TRY(mem, masw_launch(prefill_kernel, dim3(tiles, n_q_heads), dim3(192), tcp::kSmem, st, 1, p));
     StoreParams sp;
     std::memset(&sp, 0, sizeof(sp));
