@@ -180,7 +180,9 @@ struct PrefillParams {
     int* d_err;
     int T, M, S, W, r, Hq, Hkv, self_attend;
     int slot_ctas;           // CTAs of slot query rows (first in the grid: their key bands are longer)
-    int slot_rows;           // slot query rows per tile of a slot CTA
+    int slot_rows;           // slots per slot CTA
+    int slot_pack;           // G: a slot CTA holds the rows of all G query heads of one kv head
+                             // (row = slot * G + head), 1: one query head per slot CTA
     float scale_log2;
 };
 
@@ -226,16 +228,22 @@ __global__ void __launch_bounds__(192, 2) prefill_kernel(const __grid_constant__
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffBar + 8 * kNumBars + 4);
     auto bar_at = [&](int i) { return sb + kOffBar + 8u * (uint32_t)i; };
 
-    const int hq = blockIdx.y, G = p.Hq / p.Hkv, kvh = hq / G;
+    const int G = p.Hq / p.Hkv;
     const bool slot_tile = (int)blockIdx.x < p.slot_ctas;
-    const int rpt = slot_tile ? p.slot_rows : kBM;               // rows of this CTA
+    // packed slot CTAs: blockIdx.y is the kv head and the rows are (slot, head)
+    // pairs of its G query heads, which share the slot's mask and K/V
+    const int pack = slot_tile ? p.slot_pack : 1;
+    if (pack > 1 && (int)blockIdx.y >= p.Hkv) return;           // no work: uniform exit before any sync
+    const int kvh = pack > 1 ? (int)blockIdx.y : (int)blockIdx.y / G;
+    const int rpt = slot_tile ? p.slot_rows : kBM;               // positions (slots) of this CTA
     const int q0 = ((int)blockIdx.x - (slot_tile ? 0 : p.slot_ctas)) * rpt;
     const int nq = slot_tile ? p.M : p.T;
-    const int q1 = imin(nq, q0 + rpt);                           // the CTA's rows [q0, q1)
+    const int q1 = imin(nq, q0 + rpt);                           // the CTA's positions [q0, q1)
     const int S = p.S, W = p.W, r = p.r;
 
-    const int qrow = q0 + tid;
-    const bool live = tid < kBM && qrow < q1;
+    const int qrow = q0 + (pack > 1 ? tid / pack : tid);         // this thread's position
+    const int hq = pack > 1 ? kvh * G + tid % pack : (int)blockIdx.y;   // and query head
+    const bool live = tid < kBM && (pack == 1 || tid < rpt * pack) && qrow < q1;
 
     // visible key ranges of the CTA: 0 = sink and 1 = window band (raw rows),
     // 2 = slot prefix (slot rows), each [a_k, b_k) possibly empty; this thread's
@@ -690,6 +698,7 @@ extern "C" int masw_prefill(masw_mem_t* mem, int layer, int seq, int T, const vo
     // each, worth it while that stays below the keys every slot row reads anyway
     p.slot_rows = imin(tcp::kBM, imax(1, (mem->S + mem->W + M / 2) / mem->r + 1));
     p.scale_log2 = mem->scale * 1.4426950408889634f;
+    p.slot_pack = p.slot_rows * (n_q_heads / Hkv) <= tcp::kBM ? n_q_heads / Hkv : 1;
     p.slot_ctas = (M + p.slot_rows - 1) / p.slot_rows;
     const int tiles = p.slot_ctas + raw_ctas;
     cudaStream_t st = (cudaStream_t)stream;
