@@ -509,6 +509,73 @@ def test_draft3b_full_size_sampled():
         p.close()
 
 
+def test_draft8b_large_batch_long_runs_sampled():
+    """The large-batch launch shape (batch 32, 32q/8kv, W = 2048, r = 1024,
+    ragged prefixes 16K..32K): one split per (sequence, head) streams ~2080 keys,
+    which selects the three-stage kernel.  Eight fused steps with per-sequence
+    slot writes at each sequence's own boundary; two sequences carry CPU-seeded
+    data checked against the oracle, the rest are filled on the device."""
+    S, W, r = 4, 2048, 1024
+    B, Hkv, D, G = 32, 8, 128, 4
+    Hq = Hkv * G
+    prefixes = synth.ragged_prefixes(B, 16384, 32768, "long-runs")
+    # two checked sequences, one of them two steps before its boundary
+    prefixes[5] = S + W + 20 * r - 2
+    sampled = [5, 17]
+    p = Pair(S, W, r, Hkv, D, 1, B, "bf16", Hq, max_seq_len=32768 + 64, reserve=16, tag="cfg5")
+    try:
+        g = torch.Generator(device=DEV)
+        g.manual_seed(99)
+        for b in range(B):
+            t = prefixes[b]
+            if b in sampled:
+                p.load(0, b, t, seed=3)
+            else:
+                n = orc.slot_count(t, S, W, r)
+                kr = torch.randn(t, Hkv, D, generator=g, device=DEV).to(torch.bfloat16)
+                ks = torch.randn(max(n, 1), Hkv, D, generator=g, device=DEV).to(torch.bfloat16)
+                capi.masw_mem_load(p.h, 0, b, kr, kr, ks[:n] if n else None, ks[:n] if n else None)
+                del kr, ks
+        tcur = list(prefixes)
+        crossed = False
+        for step in range(8):
+            p.step = step
+            due = [b for b in range(B) if orc.is_boundary(tcur[b] + 1, S, W, r)]
+            k = p.rand((B, Hkv, D), "k")
+            v = p.rand((B, Hkv, D), "v")
+            q = p.rand((B, Hq, D), "q")
+            o = torch.empty(B, Hq, D, device=DEV)
+            lse = torch.empty(B, Hq, device=DEV)
+            if due:
+                n = len(due)
+                qg, kg, vg = p.rand((n, Hq, D), "qg"), p.rand((n, Hkv, D), "kg"), p.rand((n, Hkv, D), "vg")
+                og = torch.empty(n, Hq, D, device=DEV)
+                capi.masw_draft_step_slot(p.h, 0, q.to(DEV), k.to(DEV), v.to(DEV), o, due, qg.to(DEV), kg.to(DEV),
+                                          vg.to(DEV), og, lse=lse)
+            else:
+                capi.masw_draft_step(p.h, 0, q.to(DEV), k.to(DEV), v.to(DEV), o, lse)
+            tcur = [t + 1 for t in tcur]
+            p.ref.append(0, k.float().numpy(), v.float().numpy(), active=[b in sampled for b in range(B)])
+            for sb in sampled:
+                Kc, Vc = p.ref._columns(0, sb)
+                mask = orc.draft_mask(p.ref.t(0, sb), p.ref.m(0, sb), S, W)
+                wo, wl = orc.attention(q.float().numpy()[sb], Kc, Vc, mask, p.ref.scale)
+                assert_close(o[sb], wo, "bf16", f"cfg5 draft b={sb} step={step}")
+                assert_close(lse[sb], wl, "bf16", "cfg5 draft LSE")
+                if sb in due:
+                    crossed = True
+                    i = due.index(sb)
+                    w, _ = p.ref.materialize_slot(0, [sb], qg.float().numpy()[i:i + 1], kg.float().numpy()[i:i + 1],
+                                                  vg.float().numpy()[i:i + 1])
+                    assert_close(og[i:i + 1], w, "bf16", f"cfg5 slot b={sb} step={step}")
+        assert crossed and p.ref.m(0, 5) == orc.slot_count(prefixes[5] + 8, S, W, r)
+        capi.masw_sync(p.h)
+        for sb in sampled:
+            p.check_state(0, sb)
+    finally:
+        p.close()
+
+
 def test_graph_replay_matches_eager():
     """A captured speculative iteration (appends, draft attention, a slot
     write at the boundary, rollback) replays with the same results: the
