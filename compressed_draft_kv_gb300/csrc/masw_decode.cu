@@ -18,6 +18,8 @@
 // the last CTA of each pair (split_epilogue).
 #include "masw_internal.cuh"
 
+#include <atomic>
+
 #include <cstring>
 
 namespace masw {
@@ -316,12 +318,12 @@ decode_kernel(const __grid_constant__ DecodeParams p) {
 template <typename T, int D, int G>
 static int launch_t(masw_mem_t* mem, const DecodeParams& prm, int rows, cudaStream_t stream) {
     using Cfg = DecodeCfg<T, D>;
-    static bool configured[64] = {};
+    static std::atomic<bool> configured[64];   // per device, set once (idempotent)
     const int dev = mem->device & 63;
-    if (!configured[dev]) {
+    if (!configured[dev].load(std::memory_order_acquire)) {
         MASW_CUDA_TRY(mem, cudaFuncSetAttribute(decode_kernel<T, D, G>,
                                                 cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES));
-        configured[dev] = true;
+        configured[dev].store(true, std::memory_order_release);
     }
     MASW_CUDA_TRY(mem, masw_launch(decode_kernel<T, D, G>, dim3(prm.n_split, mem->Hkv, rows), dim3(Cfg::THREADS),
                                    Cfg::SMEM_BYTES, stream, 1, prm));

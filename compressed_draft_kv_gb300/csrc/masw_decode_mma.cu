@@ -22,6 +22,8 @@
 // never gathered in HBM.  Split partials are merged by split_epilogue.
 #include "masw_internal.cuh"
 
+#include <atomic>
+
 #include <cooperative_groups.h>
 #include <cstring>
 
@@ -410,9 +412,9 @@ __global__ void __launch_bounds__(128) decode_mma_kernel(const __grid_constant__
 // Clusters of `cs` CTAs of the decode kernel that can be resident at once (cached per device).
 template <int D, int NST>
 static int max_clusters(masw_mem_t* mem, int dev, int cs) {
-    static int cache[64][9] = {};
+    static std::atomic<int> cache[64][9];   // per device and cluster size (idempotent fill)
     if (cs < 2 || cs > 8) return 0;
-    if (!cache[dev][cs]) {
+    if (!cache[dev][cs].load(std::memory_order_acquire)) {
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3(cs * 64, 1, 1);
         cfg.blockDim = dim3(128, 1, 1);
@@ -429,10 +431,10 @@ static int max_clusters(masw_mem_t* mem, int dev, int cs) {
             cudaGetLastError();
             n = 0;
         }
-        cache[dev][cs] = n > 0 ? n : -1;
+        cache[dev][cs].store(n > 0 ? n : -1, std::memory_order_release);
     }
     (void)mem;
-    return cache[dev][cs];
+    return cache[dev][cs].load(std::memory_order_acquire);
 }
 
 struct MmaPlan {
@@ -447,17 +449,17 @@ struct MmaPlan {
 template <int D, int NST>
 static int plan_mma(masw_mem_t* mem, int rows, int GR, int kmax, MmaPlan& pl) {
     using C = MmaCfg<D, NST>;
-    static int occ[64] = {};
+    static std::atomic<int> occ[64];   // resident CTAs per SM, per device (idempotent fill)
     const int dev = mem->device & 63;
-    if (!occ[dev]) {
+    if (!occ[dev].load(std::memory_order_acquire)) {
         MASW_CUDA_TRY(mem, cudaFuncSetAttribute(decode_mma_kernel<D, NST>,
                                                 cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM));
         int n = 0;
         MASW_CUDA_TRY(mem, cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_mma_kernel<D, NST>, 128, C::SMEM));
-        occ[dev] = n > 0 ? n : 1;
+        occ[dev].store(n > 0 ? n : 1, std::memory_order_release);
     }
     const int pairs = rows * mem->Hkv;
-    const int slots = occ[dev] * mem->num_sms;
+    const int slots = occ[dev].load(std::memory_order_acquire) * mem->num_sms;
     const int max_useful = imax(1, (kmax + 63) / 64);
     pl.n_split = 1;
     pl.cluster = false;

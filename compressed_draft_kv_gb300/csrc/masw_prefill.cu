@@ -34,6 +34,8 @@
 // 112 KB of shared memory and 256 TMEM columns (O, S, Q) per CTA.
 #include "masw_internal.cuh"
 
+#include <atomic>
+
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -702,12 +704,12 @@ extern "C" int masw_prefill(masw_mem_t* mem, int layer, int seq, int T, const vo
     p.slot_ctas = (M + p.slot_rows - 1) / p.slot_rows;
     const int tiles = p.slot_ctas + raw_ctas;
     cudaStream_t st = (cudaStream_t)stream;
-    static bool configured[64] = {};
-    if (!configured[mem->device & 63]) {
+    static std::atomic<bool> configured[64];   // per device, set once (idempotent)
+    if (!configured[mem->device & 63].load(std::memory_order_acquire)) {
         MASW_CUDA_TRY(mem, cudaFuncSetAttribute(prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, tcp::kSmem));
         MASW_CUDA_TRY(mem, cudaFuncSetAttribute(prefill_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
                                                 cudaSharedmemCarveoutMaxShared));
-        configured[mem->device & 63] = true;
+        configured[mem->device & 63].store(true, std::memory_order_release);
     }
     masw_note_launch(mem, (void*)st, layer);   // the store kernel below writes this layer's rows
     MASW_CUDA_TRY(mem, masw_launch(prefill_kernel, dim3(tiles, n_q_heads), dim3(192), tcp::kSmem, st, 1, p));

@@ -13,6 +13,8 @@
 // split_epilogue.
 #include "masw_internal.cuh"
 
+#include <atomic>
+
 #include <cstring>
 
 namespace masw {
@@ -259,10 +261,10 @@ __global__ void __launch_bounds__(128) verify_kernel(const __grid_constant__ Ver
 
 // Resident verify CTAs per SM for NT query tiles (cached per device).
 static int verify_occupancy(int NT) {
-    static int cache[64][5] = {};
+    static std::atomic<int> cache[64][5];   // per device and tile count (idempotent fill)
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64 || NT < 1 || NT > 4) return 1;
-    if (!cache[dev][NT]) {
+    if (!cache[dev][NT].load(std::memory_order_acquire)) {
         int n = 0;
         cudaError_t e = cudaSuccess;
         switch (NT) {
@@ -276,9 +278,9 @@ static int verify_occupancy(int NT) {
                     if (!e) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, verify_kernel<4>, 128, kVSmem); break;
         }
         if (e != cudaSuccess) cudaGetLastError();
-        cache[dev][NT] = n > 0 ? n : 1;
+        cache[dev][NT].store(n > 0 ? n : 1, std::memory_order_release);
     }
-    return cache[dev][NT];
+    return cache[dev][NT].load(std::memory_order_acquire);
 }
 
 // Split count shared by the launcher and the workspace query: one wave of the
@@ -330,13 +332,13 @@ extern "C" int masw_verify_workspace_bytes(int B, int Lq, int Hq, int Hkv, int D
 
 template <int NT>
 static cudaError_t launch_verify(const VerifyParams& prm, cudaStream_t stream) {
-    static bool configured[64] = {};
+    static std::atomic<bool> configured[64];   // per device, set once (idempotent)
     int dev = 0;
     cudaGetDevice(&dev);
-    if (!configured[dev & 63]) {
+    if (!configured[dev & 63].load(std::memory_order_acquire)) {
         cudaError_t e = cudaFuncSetAttribute(verify_kernel<NT>, cudaFuncAttributeMaxDynamicSharedMemorySize, kVSmem);
         if (e != cudaSuccess) return e;
-        configured[dev & 63] = true;
+        configured[dev & 63].store(true, std::memory_order_release);
     }
     return masw_launch(verify_kernel<NT>, dim3(prm.n_split, prm.Hkv, prm.B), dim3(128), kVSmem, stream, 1, prm);
 }
