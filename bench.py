@@ -540,6 +540,26 @@ def run_prefill(torch, capi, synth, workload: str, T: int, reps: int = 3):
             "launches": 2 * L}
 
 
+# ------------------------------------------------------ ranks (replicas) --
+
+def max_over_ranks(timings, world: int, device: str = "cpu"):
+    """Each timing's maximum over the ranks of the job (the slowest replica sets
+    the job's time); a single process returns its own timings."""
+    if world <= 1:
+        return list(timings)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(x) for x in timings], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.tolist()
+
+
+def whole_job_rate(world: int, units_per_rank: float, secs: float) -> float:
+    """Units processed by all ranks (weak scaling: every replica does the same
+    work) per second of the slowest rank."""
+    return world * units_per_rank / secs
+
+
 # ------------------------------------------------------------ CPU oracle --
 
 def oracle_sample(seconds_budget: float = 12.0):
@@ -772,16 +792,10 @@ def main():
         prefill["tensor_frac"] = prefill["tflops"] / tp[0]
         prefill["tensor_peak_kind"] = tp[1]
 
-    if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([secs, secs_full, e2e_s / args.e2e_iters], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        secs, secs_full, e2e_per = t.tolist()
-    else:
-        e2e_per = e2e_s / args.e2e_iters
+    secs, secs_full, e2e_per = max_over_ranks([secs, secs_full, e2e_s / args.e2e_iters], world, "cuda")
     dsteps = wl["steps"]
-    value = world * args.steps * dsteps / secs
-    full_value = world * full_iters * dsteps / secs_full
+    value = whole_job_rate(world, args.steps * dsteps, secs)
+    full_value = whole_job_rate(world, full_iters * dsteps, secs_full)
     peak, peak_kind = _peaks()
     achieved = total_b / kern_s / 1e9
     line = {
