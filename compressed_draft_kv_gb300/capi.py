@@ -25,6 +25,7 @@ EXPORTS = [
     "masw_verify_attn", "masw_verify_workspace_bytes", "masw_verify_attn_noalloc", "masw_mem_load", "masw_mem_export",
     "masw_query", "masw_sync", "masw_index", "masw_version",
     "masw_greedy_accept", "masw_greedy_workspace_bytes", "masw_eq1_speedup", "masw_prefill",
+    "masw_selftest_timeout",
 ]
 
 
@@ -70,6 +71,7 @@ def load() -> ctypes.CDLL:
         "masw_full_step": [P, I, P, P, P, P, I, P, P, P],
         "masw_draft_step_slot": [P, I, P, P, P, P, I, P, P, IP, I, P, P, P, P, P, P],
         "masw_prefill": [P, I, I, I, P, P, P, P, P, P, I, P, P, P, P, P],
+        "masw_selftest_timeout": [P, I, P],
         "masw_verify_attn": [P, P, P, P, I, I, I, I, I, I, I, F, P, P, P, Z, P],
         "masw_verify_workspace_bytes": [I, I, I, I, I, I, ctypes.POINTER(Z)],
         "masw_verify_attn_noalloc": [P, P, P, P, I, I, I, I, I, I, I, F, P, P, P],
@@ -266,6 +268,12 @@ def masw_prefill(handle, layer, seq, q_raw, k_raw, v_raw, q_slot, k_slot, v_slot
     _check(load().masw_prefill(handle, layer, seq, T, _ptr(q_raw), _ptr(k_raw), _ptr(v_raw), _ptr(q_slot),
                                _ptr(k_slot), _ptr(v_slot), Hq, _ptr(o_raw), _ptr(lse_raw), _ptr(o_slot),
                                _ptr(lse_slot), _stream(stream)), handle)
+
+
+def masw_selftest_timeout(handle, polls=1000, stream=None):
+    """Launch the failure-detection self-test (a bounded wait that runs out);
+    the next masw_sync raises MaswError with MASW_ETIMEOUT."""
+    _check(load().masw_selftest_timeout(handle, polls, _stream(stream)), handle)
 
 
 def masw_mem_load(handle, layer, seq, k_raw, v_raw, k_slots=None, v_slots=None):

@@ -113,13 +113,16 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 }
 // Bounded wait on a phase of `bar`.  Returns false (and records the failure in
 // *err) if the phase did not complete within the poll budget.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* err) {
-    for (uint32_t i = 0; i < kWaitPolls; ++i) {
+__device__ __forceinline__ bool mbar_wait_polls(uint64_t* bar, uint32_t parity, int* err, uint32_t polls) {
+    for (uint32_t i = 0; i < polls; ++i) {
         if (mbar_try_wait(bar, parity)) return true;
         if (i > 64) __nanosleep(128);
     }
     if (err) atomicExch(err, MASW_ETIMEOUT);
     return false;
+}
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* err) {
+    return mbar_wait_polls(bar, parity, err, kWaitPolls);
 }
 
 // Programmatic dependent launch.  Every library kernel is launched with the

@@ -102,6 +102,22 @@ __global__ void rollback_kernel(const __grid_constant__ RollbackParams p) {
 
 // Copy rows [0, n) of src [n][Hkv][rowb] into dst head blocks:
 // dst + h * head_stride + (row0 + j) * rowb.
+// Failure-detection self-test: thread 0 waits, with the given poll budget, on
+// an mbarrier that nothing ever arrives on.  The bounded wait runs out and
+// records MASW_ETIMEOUT exactly as a stalled copy would in the attention
+// kernels; no copy is in flight and nothing else is held, so the context stays
+// usable.
+__global__ void wait_timeout_probe(int* d_err, unsigned polls) {
+    __shared__ uint64_t bar;
+    pdl_wait();
+    pdl_trigger();
+    if (threadIdx.x == 0) {
+        mbar_init(&bar, 1);
+        fence_mbar_init();
+        mbar_wait_polls(&bar, 0, d_err, polls);
+    }
+}
+
 __global__ void scatter_rows_kernel(const uint8_t* src, int n, int Hkv, int rowb, uint8_t* dst,
                                     size_t head_stride, int row0) {
     const int vpr = rowb / 16;
@@ -652,6 +668,14 @@ int masw_query(masw_mem_t* mem, int layer, int seq, masw_state_t* out) {
     out->dev_m = mv[0];
     for (int h = 1; h < mem->Hkv; ++h)   // every kv head's copy must agree
         if (tv[h] != tv[0] || mv[h] != mv[0]) out->dev_t = out->dev_m = -1;
+    return MASW_OK;
+}
+
+int masw_selftest_timeout(masw_mem_t* mem, int polls, masw_stream_t stream) {
+    if (!mem) return masw_set_error(nullptr, MASW_EINVAL, "selftest: NULL handle");
+    if (polls < 1 || polls > (1 << 20)) return masw_set_error(mem, MASW_EINVAL, "selftest: polls must be in [1, 2^20]");
+    MASW_CUDA_TRY(mem, masw_launch(wait_timeout_probe, dim3(1), dim3(32), 0, (cudaStream_t)stream, 1, mem->d_err,
+                                   (unsigned)polls));
     return MASW_OK;
 }
 

@@ -324,6 +324,13 @@ int masw_query(masw_mem_t* mem, int layer, int seq, masw_state_t* out);
  * last masw_sync (MASW_ETIMEOUT) or by the CUDA runtime (MASW_ECUDA). */
 int masw_sync(masw_mem_t* mem, masw_stream_t stream);
 
+/* Failure-detection self-test: launch a kernel whose bounded wait (the helper
+ * every TMA/MMA wait of the library uses) waits `polls` polls, in [1, 2^20], on
+ * a barrier nothing arrives on, runs out and records MASW_ETIMEOUT; the next
+ * masw_sync returns MASW_ETIMEOUT and clears it.  Nothing is in flight when the
+ * wait gives up, so the handle and the context stay usable. */
+int masw_selftest_timeout(masw_mem_t* mem, int polls, masw_stream_t stream);
+
 /* Host-side index model, exported so it can be checked without a GPU.
  * which: 0 = local-window lo (1-based), 1 = n_local, 2 = slot count m(t),
  * 3 = is_boundary(t), 4 = ring row of token t ((t-S-1) mod (W+R), -1 for a

@@ -628,3 +628,23 @@ def test_graph_replay_matches_eager():
         assert st["dev_t"] == st["t"] == t0 and st["dev_m"] == st["m"] == orc.slot_count(t0, S, W, r)
     finally:
         p.close()
+
+
+def test_bounded_wait_timeout_is_reported_and_the_context_survives():
+    """Failure detection without a fault: a bounded wait on a barrier nothing
+    arrives on runs out, masw_sync reports MASW_ETIMEOUT (once), and the same
+    handle keeps working afterwards."""
+    p = Pair(4, 16, 4, 2, 64, 1, 1, "f32", 8, max_seq_len=64, tag="timeout")
+    try:
+        p.load(0, 0, 30, seed=1)
+        capi.masw_selftest_timeout(p.h, polls=1000)
+        with pytest.raises(capi.MaswError) as ei:
+            capi.masw_sync(p.h)
+        assert ei.value.code == capi.MASW_ETIMEOUT
+        capi.masw_sync(p.h)          # reported once, then cleared
+        p.step = 0
+        p.append(0)
+        p.draft(0)                   # attention still matches the oracle
+        p.check_state(0, 0)
+    finally:
+        p.close()
