@@ -319,28 +319,39 @@ __global__ void __launch_bounds__(128) decode_mma_kernel(const __grid_constant__
         cg::cluster_group cluster = cg::this_cluster();
         const int nc = (int)cluster.num_blocks(), rank = (int)cluster.block_rank();
         const int per = (NR * D + nc - 1) / nc;
-        // merge this CTA's 4 warps per element (one pass, no further block
-        // barrier) and push the CTA partial to the rank that finalises it
-        for (int i = tid; i < NR * D; i += 128) {
-            const int n = i / D, d = i % D;
+        // this CTA's 4 warps per row: max, weights and sum (one thread per
+        // row), then every element of the CTA partial is pushed to the rank
+        // that finalises it, and the rows' (max, sum) to every rank -- spread
+        // over the threads, so no thread serialises the remote stores
+        float* ew = scratch + 96;                     // [8 rows][4 warps], clear of the post-sync scratch
+        if (tid < NR) {
             float M = -INFINITY;
 #pragma unroll
-            for (int w = 0; w < 4; ++w) M = fmaxf(M, wm[w * 8 + n]);
-            float l = 0.f, a = 0.f;
+            for (int w = 0; w < 4; ++w) M = fmaxf(M, wm[w * 8 + tid]);
+            float l = 0.f;
 #pragma unroll
             for (int w = 0; w < 4; ++w) {
-                const float mw = wm[w * 8 + n];
-                const float ew = mw == -INFINITY ? 0.f : exp2f(mw - M);
-                l += ew * wl[w * 8 + n];
-                a += ew * wo[(w * 8 + n) * WS + d];
+                const float mw = wm[w * 8 + tid];
+                const float e = mw == -INFINITY ? 0.f : exp2f(mw - M);
+                ew[tid * 4 + w] = e;
+                l += e * wl[w * 8 + tid];
             }
+            cm[tid] = M;
+            cl[tid] = l;
+        }
+        __syncthreads();
+        for (int i = tid; i < NR * D; i += 128) {
+            const int n = i / D, d = i % D;
+            float a = 0.f;
+#pragma unroll
+            for (int w = 0; w < 4; ++w) a += ew[n * 4 + w] * wo[(w * 8 + n) * WS + d];
             const int k = i / per;
             cluster.map_shared_rank(r_o, k)[rank * per + (i - k * per)] = a;
-            if (d == 0)
-                for (int kk = 0; kk < nc; ++kk) {
-                    cluster.map_shared_rank(r_m, kk)[rank * 8 + n] = M;
-                    cluster.map_shared_rank(r_l, kk)[rank * 8 + n] = l;
-                }
+        }
+        for (int t = tid; t < NR * nc; t += 128) {
+            const int n = t / nc, kk = t % nc;
+            cluster.map_shared_rank(r_m, kk)[rank * 8 + n] = cm[n];
+            cluster.map_shared_rank(r_l, kk)[rank * 8 + n] = cl[n];
         }
         cluster.sync();                               // every peer's pushes have landed here
         float* w = scratch;                           // [8 rows][8 ranks] merge weights
