@@ -47,6 +47,13 @@ struct MmaCfg {
                   "merge does not fit in the stage buffers");
 };
 
+// 2^x by the MUFU instruction (an input of -inf gives 0)
+__device__ __forceinline__ float fast_ex2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
 template <int ROWB>
 __device__ __forceinline__ uint32_t swz_off(int row, int ch) {
     return (uint32_t)(row * ROWB + ((ch ^ (row & 7)) << 4));
@@ -324,20 +331,22 @@ __global__ void __launch_bounds__(128) decode_mma_kernel(const __grid_constant__
         // that finalises it, and the rows' (max, sum) to every rank -- spread
         // over the threads, so no thread serialises the remote stores
         float* ew = scratch + 96;                     // [8 rows][4 warps], clear of the post-sync scratch
-        if (tid < NR) {
-            float M = -INFINITY;
-#pragma unroll
-            for (int w = 0; w < 4; ++w) M = fmaxf(M, wm[w * 8 + tid]);
-            float l = 0.f;
-#pragma unroll
-            for (int w = 0; w < 4; ++w) {
-                const float mw = wm[w * 8 + tid];
-                const float e = mw == -INFINITY ? 0.f : exp2f(mw - M);
-                ew[tid * 4 + w] = e;
-                l += e * wl[w * 8 + tid];
+        if (tid < 32) {                               // lane = row * 4 + warp: groups of 4 lanes per row
+            const int n = tid >> 2, w = tid & 3;
+            const float mw = n < NR ? wm[w * 8 + n] : -INFINITY;
+            float M = fmaxf(mw, __shfl_xor_sync(0xffffffffu, mw, 1));
+            M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, 2));
+            const float e = mw == -INFINITY ? 0.f : fast_ex2(mw - M);
+            float l = e * (n < NR ? wl[w * 8 + n] : 0.f);
+            l += __shfl_xor_sync(0xffffffffu, l, 1);
+            l += __shfl_xor_sync(0xffffffffu, l, 2);
+            if (n < NR) {
+                ew[n * 4 + w] = e;
+                if (w == 0) {
+                    cm[n] = M;
+                    cl[n] = l;
+                }
             }
-            cm[tid] = M;
-            cl[tid] = l;
         }
         __syncthreads();
         for (int i = tid; i < NR * D; i += 128) {
@@ -357,18 +366,25 @@ __global__ void __launch_bounds__(128) decode_mma_kernel(const __grid_constant__
         float* w = scratch;                           // [8 rows][8 ranks] merge weights
         float* den = w + 64;                          // [8]
         float* Mx = den + 8;                          // [8]
-        if (tid < NR) {
-            float M = -INFINITY;
-            for (int r = 0; r < nc; ++r) M = fmaxf(M, r_m[r * 8 + tid]);
-            float dn = 0.f;
-            for (int r = 0; r < nc; ++r) {
-                const float mr = r_m[r * 8 + tid];
-                const float wr = mr == -INFINITY ? 0.f : exp2f(mr - M);
-                w[tid * 8 + r] = wr;
-                dn += wr * r_l[r * 8 + tid];
+        if (tid < 64) {                               // thread = row * 8 + rank: groups of 8 lanes per row
+            const int n = tid >> 3, r = tid & 7;
+            const bool real = n < NR && r < nc;
+            const float mr = real ? r_m[r * 8 + n] : -INFINITY;
+            float M = fmaxf(mr, __shfl_xor_sync(0xffffffffu, mr, 1));
+            M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, 2));
+            M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, 4));
+            const float wr = mr == -INFINITY ? 0.f : fast_ex2(mr - M);
+            float dn = wr * (real ? r_l[r * 8 + n] : 0.f);
+            dn += __shfl_xor_sync(0xffffffffu, dn, 1);
+            dn += __shfl_xor_sync(0xffffffffu, dn, 2);
+            dn += __shfl_xor_sync(0xffffffffu, dn, 4);
+            if (n < NR) {
+                w[n * 8 + r] = wr;
+                if (r == 0) {
+                    den[n] = dn;
+                    Mx[n] = M;
+                }
             }
-            den[tid] = dn;
-            Mx[tid] = M;
         }
         __syncthreads();
         const int lo = rank * per, hi = imin(NR * D, lo + per);
