@@ -209,7 +209,6 @@ __global__ void __launch_bounds__(128) decode_mma_kernel(const __grid_constant__
         }
     }
 
-    if (fresh && split == 0) step_store_row<ROWB>(p, lb, h, z, s_t);
     const float sl2 = p.scale_log2;
     float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f};
     float acc[KS][4];
@@ -275,6 +274,10 @@ __global__ void __launch_bounds__(128) decode_mma_kernel(const __grid_constant__
     }
     cp_async_wait<0>();
     __syncthreads();
+    // the new token's row into its pool row (no CTA of this launch reads the row
+    // it overwrites), by the last split, whose share of the keys is the
+    // smallest: its global read stays off the other splits' critical path
+    if (fresh && split == p.n_split - 1) step_store_row<ROWB>(p, lb, h, z, s_t);
 
     // ---- warp results -> shared (8 columns), merge the 4 warps over the G real ones ----
     constexpr int WS = D + 8;                       // padded row stride of wo

@@ -409,7 +409,7 @@ __device__ __forceinline__ int build_segments(const DecodeParams& p, int lb, int
     return n;
 }
 
-// Fused step, split 0 of each (row, head): store the new token's K/V row of
+// Fused step, the last split of each (row, head): store the new token's K/V row of
 // head h in its sink or ring row (the ring write evicts token t+1-W-R, which no
 // CTA of this launch reads) and in the full-KV cache.
 template <int ROWB>
