@@ -5,7 +5,8 @@
 // K/V row, 24 flop per byte at Lq = 6, G = 4), so it runs on tensor cores:
 // mma.sync m16n8k16 bf16 -> fp32 with KEYS as the M dimension and the Lq*G
 // query rows as N (8 per tile), so 24 query rows fill three N tiles without
-// padding.  S^T = K Q^T is accumulated per 16-key tile from ldmatrix fragments
+// padding.  Each warp owns one N tile of one 16-key group (4 NT warps per CTA),
+// which keeps its accumulators at about 80 registers.  S^T = K Q^T is accumulated per 16-key tile from ldmatrix fragments
 // of an XOR-swizzled shared-memory stage (cp.async, 3 stages), softmax runs
 // online per query column in the log2 domain, P^T is turned from the
 // accumulator layout into a B operand with movmatrix, and O^T += V^T P^T uses
@@ -47,10 +48,23 @@ static_assert((2 * 4 * kVMaxNQ + 4 * kVMaxNQ * (kVD + 8) + 2 * kVMaxNQ + kVMaxNQ
 __device__ __forceinline__ uint32_t swz(int row, int chunk) {  // byte offset of a 16-B chunk
     return (uint32_t)(row * kVRowB + ((chunk ^ (row & 7)) << 4));
 }
+// three stages for every tile count (two CTAs per SM at three tiles; six stages
+// on one CTA per SM measured slower)
 template <int NT>
-__global__ void __launch_bounds__(128) verify_kernel(const __grid_constant__ VerifyParams p) {
+__host__ __device__ constexpr int verify_stages() { return kVNst; }
+template <int NT>
+__host__ __device__ constexpr int verify_smem() { return verify_stages<NT>() * kVStage; }
+
+// NT tiles of 8 query columns; warp w handles keys 16 (w % 4) .. +15 of each
+// stage for column tile w / 4, so a warp keeps one tile's accumulators (about
+// 96 registers) and a CTA has 4 NT warps: more warps in flight than one warp
+// holding every tile.
+template <int NT>
+__global__ void __launch_bounds__(128 * NT) verify_kernel(const __grid_constant__ VerifyParams p) {
+    constexpr int NSTV = verify_stages<NT>();
     extern __shared__ __align__(128) uint8_t smem[];
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nthr = blockDim.x;
+    const int kg = warp & 3, ct = warp >> 2;   // key group, column tile
     const int split = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
     const int G = p.G, NQ = p.NQ;
     pdl_wait();
@@ -69,12 +83,10 @@ __global__ void __launch_bounds__(128) verify_kernel(const __grid_constant__ Ver
     // one stage = 64 keys of K and V, 16-byte chunks XOR-swizzled by row;
     // rows past k1 are zero-filled (src-size 0 reads nothing)
     auto load_stage = [&](int c) {
-        const uint32_t sk = sbase + (uint32_t)(c % kVNst) * kVStage;
+        const uint32_t sk = sbase + (uint32_t)(c % NSTV) * kVStage;
         const uint32_t sv = sk + kVKeys * kVRowB;
         const int key0 = k0 + c * kVKeys;
-#pragma unroll
-        for (int i = 0; i < (kVKeys * 16) / 128; ++i) {
-            const int idx = tid + i * 128;
+        for (int idx = tid; idx < kVKeys * 16; idx += nthr) {
             const int row = idx >> 4, ch = idx & 15;
             const int key = key0 + row;
             const bool in = key < k1;
@@ -84,116 +96,101 @@ __global__ void __launch_bounds__(128) verify_kernel(const __grid_constant__ Ver
         }
     };
 #pragma unroll
-    for (int c = 0; c < kVNst - 1; ++c) {
+    for (int c = 0; c < NSTV - 1; ++c) {
         if (c < nstage) load_stage(c);
         cp_async_commit();
     }
 
-    // Q^T as B fragments: column n = query row (j = n / G, gi = n % G)
-    uint32_t qb[8][NT][2];
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt) {
-        const int n = nt * 8 + (lane >> 2);
+    // Q^T as B fragments of this warp's column tile: column n = query row
+    // (j = n / G, gi = n % G)
+    uint32_t qb[8][2];
+    {
+        const int n = ct * 8 + (lane >> 2);
         const bool real = n < NQ;
         const int j = real ? n / G : 0, gi = real ? n % G : 0;
         const __nv_bfloat16* qrow = p.q + (((size_t)b * p.Lq + j) * p.Hq + (size_t)h * G + gi) * kVD;
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks) {
             const int d = ks * 16 + (lane & 3) * 2;
-            qb[ks][nt][0] = real ? *reinterpret_cast<const uint32_t*>(qrow + d) : 0u;
-            qb[ks][nt][1] = real ? *reinterpret_cast<const uint32_t*>(qrow + d + 8) : 0u;
+            qb[ks][0] = real ? *reinterpret_cast<const uint32_t*>(qrow + d) : 0u;
+            qb[ks][1] = real ? *reinterpret_cast<const uint32_t*>(qrow + d + 8) : 0u;
         }
     }
-    // causal limit of this lane's two columns per N tile: key < lim
-    int lim[NT][2];
+    // causal limit of this lane's two columns: key < lim
+    int lim[2];
 #pragma unroll
-    for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-            const int n = nt * 8 + (lane & 3) * 2 + e;
-            lim[nt][e] = n < NQ ? imin(k1, n_keys - p.Lq + 1 + n / G) : k1;
-        }
+    for (int e = 0; e < 2; ++e) {
+        const int n = ct * 8 + (lane & 3) * 2 + e;
+        lim[e] = n < NQ ? imin(k1, n_keys - p.Lq + 1 + n / G) : k1;
+    }
 
-    float m_run[NT][2], l_run[NT][2];
-    float acc[8][NT][4];
+    float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f};
+    float acc[8][4];
 #pragma unroll
-    for (int nt = 0; nt < NT; ++nt) {
-        m_run[nt][0] = m_run[nt][1] = -INFINITY;
-        l_run[nt][0] = l_run[nt][1] = 0.f;
-#pragma unroll
-        for (int mt = 0; mt < 8; ++mt) acc[mt][nt][0] = acc[mt][nt][1] = acc[mt][nt][2] = acc[mt][nt][3] = 0.f;
-    }
+    for (int mt = 0; mt < 8; ++mt) acc[mt][0] = acc[mt][1] = acc[mt][2] = acc[mt][3] = 0.f;
 
     for (int c = 0; c < nstage; ++c) {
-        cp_async_wait<kVNst - 2>();
+        cp_async_wait<NSTV - 2>();
         __syncthreads();
         {   // refill the stage consumed in the previous iteration
-            const int cn = c + kVNst - 1;
+            const int cn = c + NSTV - 1;
             if (cn < nstage) load_stage(cn);
             cp_async_commit();
         }
-        const uint32_t sk = sbase + (uint32_t)(c % kVNst) * kVStage;
+        const uint32_t sk = sbase + (uint32_t)(c % NSTV) * kVStage;
         const uint32_t sv = sk + kVKeys * kVRowB;
-        const int kw = warp * 16;
+        const int kw = kg * 16;
         const int key_tile = k0 + c * kVKeys + kw;
         if (key_tile < k1) {
-            float s[NT][4];
-#pragma unroll
-            for (int nt = 0; nt < NT; ++nt) s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
+            float s[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
             for (int ks = 0; ks < 8; ++ks) {
                 uint32_t a0, a1, a2, a3;
                 const int row = kw + (lane & 7) + ((lane >> 3) & 1) * 8;
                 ldsm_x4(sk + swz(row, ks * 2 + (lane >> 4)), a0, a1, a2, a3);
-#pragma unroll
-                for (int nt = 0; nt < NT; ++nt) mma16816(s[nt], a0, a1, a2, a3, qb[ks][nt][0], qb[ks][nt][1]);
+                mma16816(s, a0, a1, a2, a3, qb[ks][0], qb[ks][1]);
             }
             const int key_a = key_tile + (lane >> 2), key_b = key_a + 8;
-            uint32_t pb[NT][2];
+            float x[4];
+            x[0] = key_a < lim[0] ? s[0] * p.scale_log2 : -INFINITY;
+            x[1] = key_a < lim[1] ? s[1] * p.scale_log2 : -INFINITY;
+            x[2] = key_b < lim[0] ? s[2] * p.scale_log2 : -INFINITY;
+            x[3] = key_b < lim[1] ? s[3] * p.scale_log2 : -INFINITY;
+            float pr[4];
 #pragma unroll
-            for (int nt = 0; nt < NT; ++nt) {
-                float x[4];
-                x[0] = key_a < lim[nt][0] ? s[nt][0] * p.scale_log2 : -INFINITY;
-                x[1] = key_a < lim[nt][1] ? s[nt][1] * p.scale_log2 : -INFINITY;
-                x[2] = key_b < lim[nt][0] ? s[nt][2] * p.scale_log2 : -INFINITY;
-                x[3] = key_b < lim[nt][1] ? s[nt][3] * p.scale_log2 : -INFINITY;
-                float pr[4];
+            for (int e = 0; e < 2; ++e) {
+                float mx = fmaxf(x[e], x[e + 2]);
+                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+                const float m_new = fmaxf(m_run[e], mx);
+                const float m_use = m_new == -INFINITY ? 0.f : m_new;   // column fully masked so far
+                const float alpha = exp2f(m_run[e] - m_use);
+                pr[e] = exp2f(x[e] - m_use);
+                pr[e + 2] = exp2f(x[e + 2] - m_use);
+                l_run[e] = l_run[e] * alpha + pr[e] + pr[e + 2];
+                m_run[e] = m_new;
 #pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                    float mx = fmaxf(x[e], x[e + 2]);
-                    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
-                    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
-                    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
-                    const float m_new = fmaxf(m_run[nt][e], mx);
-                    const float m_use = m_new == -INFINITY ? 0.f : m_new;   // column fully masked so far
-                    const float alpha = exp2f(m_run[nt][e] - m_use);
-                    pr[e] = exp2f(x[e] - m_use);
-                    pr[e + 2] = exp2f(x[e + 2] - m_use);
-                    l_run[nt][e] = l_run[nt][e] * alpha + pr[e] + pr[e + 2];
-                    m_run[nt][e] = m_new;
-#pragma unroll
-                    for (int mt = 0; mt < 8; ++mt) {
-                        acc[mt][nt][e] *= alpha;
-                        acc[mt][nt][e + 2] *= alpha;
-                    }
+                for (int mt = 0; mt < 8; ++mt) {
+                    acc[mt][e] *= alpha;
+                    acc[mt][e + 2] *= alpha;
                 }
-                pb[nt][0] = movmatrix_t(pack_bf16(pr[0], pr[1]));
-                pb[nt][1] = movmatrix_t(pack_bf16(pr[2], pr[3]));
             }
+            const uint32_t pb0 = movmatrix_t(pack_bf16(pr[0], pr[1]));
+            const uint32_t pb1 = movmatrix_t(pack_bf16(pr[2], pr[3]));
 #pragma unroll
             for (int mt = 0; mt < 8; ++mt) {
                 uint32_t a0, a1, a2, a3;
                 const int row = kw + (lane & 7) + (lane >> 4) * 8;
                 ldsm_x4_t(sv + swz(row, mt * 2 + ((lane >> 3) & 1)), a0, a1, a2, a3);
-#pragma unroll
-                for (int nt = 0; nt < NT; ++nt) mma16816(acc[mt][nt], a0, a1, a2, a3, pb[nt][0], pb[nt][1]);
+                mma16816(acc[mt], a0, a1, a2, a3, pb0, pb1);
             }
         }
     }
     cp_async_wait<0>();
     __syncthreads();
 
-    // ---- warp results -> shared, then merge the 4 warps ----
+    // ---- warp results -> shared, then merge the 4 key groups ----
     constexpr int NQM = NT * 8;
     constexpr int WS = kVD + 8;                     // padded row stride: conflict-free stores
     float* wm = reinterpret_cast<float*>(smem);    // [4][NQM]
@@ -204,25 +201,23 @@ __global__ void __launch_bounds__(128) verify_kernel(const __grid_constant__ Ver
     float* co = cl + NQM;                           // [NQM][D]
     float* scratch = co + NQM * kVD;
 #pragma unroll
-    for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-            float l = l_run[nt][e];
-            l += __shfl_xor_sync(0xffffffffu, l, 4);
-            l += __shfl_xor_sync(0xffffffffu, l, 8);
-            l += __shfl_xor_sync(0xffffffffu, l, 16);
-            const int n = nt * 8 + (lane & 3) * 2 + e;
-            if (lane < 4) {
-                wm[warp * NQM + n] = m_run[nt][e];
-                wl[warp * NQM + n] = l;
-            }
-#pragma unroll
-            for (int mt = 0; mt < 8; ++mt) {
-                const int d = mt * 16 + (lane >> 2);
-                wo[(warp * NQM + n) * WS + d] = acc[mt][nt][e];
-                wo[(warp * NQM + n) * WS + d + 8] = acc[mt][nt][e + 2];
-            }
+    for (int e = 0; e < 2; ++e) {
+        float l = l_run[e];
+        l += __shfl_xor_sync(0xffffffffu, l, 4);
+        l += __shfl_xor_sync(0xffffffffu, l, 8);
+        l += __shfl_xor_sync(0xffffffffu, l, 16);
+        const int n = ct * 8 + (lane & 3) * 2 + e;
+        if (lane < 4) {
+            wm[kg * NQM + n] = m_run[e];
+            wl[kg * NQM + n] = l;
         }
+#pragma unroll
+        for (int mt = 0; mt < 8; ++mt) {
+            const int d = mt * 16 + (lane >> 2);
+            wo[(kg * NQM + n) * WS + d] = acc[mt][e];
+            wo[(kg * NQM + n) * WS + d + 8] = acc[mt][e + 2];
+        }
+    }
     __syncthreads();
     if (tid < NQ) {
         float M = -INFINITY;
@@ -234,7 +229,7 @@ __global__ void __launch_bounds__(128) verify_kernel(const __grid_constant__ Ver
         cl[tid] = l;
     }
     __syncthreads();
-    for (int i = tid; i < NQ * kVD; i += 128) {
+    for (int i = tid; i < NQ * kVD; i += nthr) {
         const int n = i / kVD;
         const float M = cm[n];
         float a = 0.f;
@@ -259,6 +254,15 @@ __global__ void __launch_bounds__(128) verify_kernel(const __grid_constant__ Ver
     split_epilogue<kVD>(NQ, cm, cl, co, out, part, p.tickets + b * p.Hkv + h, split, p.n_split, scratch);
 }
 
+template <int NT>
+static cudaError_t verify_configure(int* n) {
+    cudaError_t e = cudaFuncSetAttribute(verify_kernel<NT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         verify_smem<NT>());
+    if (e == cudaSuccess)
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(n, verify_kernel<NT>, 128 * NT, verify_smem<NT>());
+    return e;
+}
+
 // Resident verify CTAs per SM for NT query tiles (cached per device).
 static int verify_occupancy(int NT) {
     static std::atomic<int> cache[64][5];   // per device and tile count (idempotent fill)
@@ -268,14 +272,10 @@ static int verify_occupancy(int NT) {
         int n = 0;
         cudaError_t e = cudaSuccess;
         switch (NT) {
-            case 1: e = cudaFuncSetAttribute(verify_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, kVSmem);
-                    if (!e) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, verify_kernel<1>, 128, kVSmem); break;
-            case 2: e = cudaFuncSetAttribute(verify_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, kVSmem);
-                    if (!e) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, verify_kernel<2>, 128, kVSmem); break;
-            case 3: e = cudaFuncSetAttribute(verify_kernel<3>, cudaFuncAttributeMaxDynamicSharedMemorySize, kVSmem);
-                    if (!e) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, verify_kernel<3>, 128, kVSmem); break;
-            default: e = cudaFuncSetAttribute(verify_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize, kVSmem);
-                    if (!e) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, verify_kernel<4>, 128, kVSmem); break;
+            case 1: e = verify_configure<1>(&n); break;
+            case 2: e = verify_configure<2>(&n); break;
+            case 3: e = verify_configure<3>(&n); break;
+            default: e = verify_configure<4>(&n); break;
         }
         if (e != cudaSuccess) cudaGetLastError();
         cache[dev][NT].store(n > 0 ? n : 1, std::memory_order_release);
@@ -336,11 +336,13 @@ static cudaError_t launch_verify(const VerifyParams& prm, cudaStream_t stream) {
     int dev = 0;
     cudaGetDevice(&dev);
     if (!configured[dev & 63].load(std::memory_order_acquire)) {
-        cudaError_t e = cudaFuncSetAttribute(verify_kernel<NT>, cudaFuncAttributeMaxDynamicSharedMemorySize, kVSmem);
+        cudaError_t e = cudaFuncSetAttribute(verify_kernel<NT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             verify_smem<NT>());
         if (e != cudaSuccess) return e;
         configured[dev & 63].store(true, std::memory_order_release);
     }
-    return masw_launch(verify_kernel<NT>, dim3(prm.n_split, prm.Hkv, prm.B), dim3(128), kVSmem, stream, 1, prm);
+    return masw_launch(verify_kernel<NT>, dim3(prm.n_split, prm.Hkv, prm.B), dim3(128 * NT), verify_smem<NT>(),
+                       stream, 1, prm);
 }
 
 extern "C" int masw_verify_attn(const void* q, const void* k_cache, const void* v_cache, const int* kv_len, int B,
