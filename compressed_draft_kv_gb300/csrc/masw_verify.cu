@@ -142,14 +142,17 @@ __global__ void __launch_bounds__(128 * NT) verify_kernel(const __grid_constant_
         const int kw = kg * 16;
         const int key_tile = k0 + c * kVKeys + kw;
         if (key_tile < k1) {
-            float s[4] = {0.f, 0.f, 0.f, 0.f};
+            // two accumulators (even and odd k-steps) halve the dependent MMA chain
+            float s[4] = {0.f, 0.f, 0.f, 0.f}, s2[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
             for (int ks = 0; ks < 8; ++ks) {
                 uint32_t a0, a1, a2, a3;
                 const int row = kw + (lane & 7) + ((lane >> 3) & 1) * 8;
                 ldsm_x4(sk + swz(row, ks * 2 + (lane >> 4)), a0, a1, a2, a3);
-                mma16816(s, a0, a1, a2, a3, qb[ks][0], qb[ks][1]);
+                mma16816((ks & 1) ? s2 : s, a0, a1, a2, a3, qb[ks][0], qb[ks][1]);
             }
+#pragma unroll
+            for (int e = 0; e < 4; ++e) s[e] += s2[e];
             const int key_a = key_tile + (lane >> 2), key_b = key_a + 8;
             float x[4];
             x[0] = key_a < lim[0] ? s[0] * p.scale_log2 : -INFINITY;
