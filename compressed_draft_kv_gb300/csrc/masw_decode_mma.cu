@@ -54,9 +54,74 @@ __device__ __forceinline__ float fast_ex2(float x) {
     return y;
 }
 
+// Distributed shared memory hand-off of the cluster merge: a CTA writes into a
+// peer's shared memory with st.async, whose bytes count down the peer's mbarrier
+// (complete_tx), so each receiver waits only for the bytes it needs -- no
+// cluster-wide barrier after the main loop.
+__device__ __forceinline__ uint32_t mapa_rank(uint32_t saddr, int rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
+    return r;
+}
+__device__ __forceinline__ void st_async_v4(uint32_t raddr, float4 v, uint32_t rbar) {
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(
+                     raddr),
+                 "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w), "r"(rbar)
+                 : "memory");
+}
+__device__ __forceinline__ void st_async_v2(uint32_t raddr, float a, float b, uint32_t rbar) {
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v2.f32 [%0], {%1, %2}, [%3];" ::"r"(raddr),
+                 "f"(a), "f"(b), "r"(rbar)
+                 : "memory");
+}
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+    asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.aligned;" ::: "memory"); }
+// bounded wait on phase 0 of a receive mbarrier, acquiring the peers' writes
+__device__ __forceinline__ bool recv_wait(uint64_t* bar, int* err) {
+    for (uint32_t i = 0; i < kWaitPolls; ++i) {
+        uint32_t ok;
+        asm volatile(
+            "{\n .reg .pred p;\n mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], 0;\n"
+            " selp.u32 %0, 1, 0, p;\n}\n"
+            : "=r"(ok)
+            : "r"(smem_u32(bar))
+            : "memory");
+        if (ok) return true;
+        if (i > 64) __nanosleep(64);
+    }
+    atomicExch(err, MASW_ETIMEOUT);
+    return false;
+}
+
 template <int ROWB>
 __device__ __forceinline__ uint32_t swz_off(int row, int ch) {
     return (uint32_t)(row * ROWB + ((ch ^ (row & 7)) << 4));
+}
+
+// Fused step: store the new token's K/V row of head h, held in shared memory as
+// row `row` of a stage (swizzled 16-byte chunks), in its sink or ring row (the
+// ring write evicts token t+1-W-R, which no CTA of this launch reads) and in the
+// full-KV cache.
+template <int ROWB>
+__device__ void step_store_row_smem(const DecodeParams& p, int lb, int h, int t, const uint8_t* stage_k,
+                                    const uint8_t* stage_v, int row) {
+    const int i = t + 1;
+    const int prow = i <= p.S ? i - 1 : p.S + ring_row(i, p.S, p.Wc);
+    const size_t dst = (((size_t)lb * p.Hkv + h) * p.C + prow) * ROWB;
+    const bool to_full = p.full_k != nullptr && i <= p.Tmax;
+    const size_t fdst = (((size_t)lb * p.Hkv + h) * p.Tmax + (i - 1)) * (size_t)ROWB;
+    for (int c = threadIdx.x; c < ROWB / 16; c += blockDim.x) {
+        const uint4 kv = *reinterpret_cast<const uint4*>(stage_k + swz_off<ROWB>(row, c));
+        const uint4 vv = *reinterpret_cast<const uint4*>(stage_v + swz_off<ROWB>(row, c));
+        *reinterpret_cast<uint4*>((uint8_t*)p.pool_k + dst + c * 16) = kv;
+        *reinterpret_cast<uint4*>((uint8_t*)p.pool_v + dst + c * 16) = vv;
+        if (to_full) {
+            *reinterpret_cast<uint4*>((uint8_t*)p.full_k + fdst + c * 16) = kv;
+            *reinterpret_cast<uint4*>((uint8_t*)p.full_v + fdst + c * 16) = vv;
+        }
+    }
 }
 
 template <int D, int NST_>
@@ -69,9 +134,12 @@ __global__ void __launch_bounds__(128) decode_mma_kernel(const __grid_constant__
     __shared__ const uint8_t* s_vk[5];
     __shared__ const uint8_t* s_vv[5];
     __shared__ int s_nseg, s_m_before, s_t, s_respec;
-    // cluster merge receive buffers (written by peer CTAs; never aliased with the stages)
-    __shared__ float r_m[64], r_l[64];
-    __shared__ float r_o[8 * D + 8];
+    // cluster merge receive buffers (written by peer CTAs with st.async; never
+    // aliased with the stages): (max, sum) per (rank, row), the o slices, and the
+    // mbarrier their bytes count down
+    __shared__ __align__(16) float2 r_ml[64];
+    __shared__ __align__(16) float r_o[8 * D + 32];
+    __shared__ uint64_t r_bar;
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int split = blockIdx.x, h = blockIdx.y, z = blockIdx.z;
@@ -80,6 +148,22 @@ __global__ void __launch_bounds__(128) decode_mma_kernel(const __grid_constant__
     const int G = p.Hq / p.Hkv;
     const int si = p.q_slot ? (int)p.slot_of[z] : -1;   // fused slot query of this row, if any
     const int NR = si >= 0 ? 2 * G : G;                  // query columns of this pair
+    // cluster merge: rank k finalises elements [k*per, (k+1)*per) of the pair's
+    // NR x D output (per a multiple of 4, so 16-byte pushes never straddle two
+    // ranks) and receives, from each of the n_split ranks, that slice and the
+    // (max, sum) of the NR rows.  The receive mbarrier is initialised here and
+    // made visible to the peers by a cluster arrive whose wait comes just before
+    // the first push.
+    const int per = ((NR * D + p.n_split - 1) / p.n_split + 3) & ~3;
+    if (p.cluster) {
+        if (tid == 0) {
+            const int slice = imax(0, imin(per, NR * D - split * per));
+            mbar_init(&r_bar, 1);
+            mbar_expect_tx(&r_bar, (uint32_t)(p.n_split * (slice * 4 + NR * 8)));
+            fence_mbar_init();
+        }
+        cluster_arrive_relaxed();
+    }
     // Segment table, built speculatively before the PDL wait (the counters are
     // read while the previous kernel drains) and verified after it; the copies
     // of the first stages are issued on the speculative table, and rebuilt and
@@ -278,9 +362,19 @@ __global__ void __launch_bounds__(128) decode_mma_kernel(const __grid_constant__
     cp_async_wait<0>();
     __syncthreads();
     // the new token's row into its pool row (no CTA of this launch reads the row
-    // it overwrites), by the last split, whose share of the keys is the
-    // smallest: its global read stays off the other splits' critical path
-    if (fresh && split == p.n_split - 1) step_store_row<ROWB>(p, lb, h, z, s_t);
+    // it overwrites), by the split whose keys include it: that split streamed the
+    // row from the caller's buffer into its last stage or the one before, and no
+    // later stage overwrote it, so the row is stored from shared memory with no
+    // global read on the way to the merge
+    if (fresh) {
+        const int jf = total - n_input;             // logical index of the new token's row
+        if (jf >= r0 && jf < r1) {
+            const int cf = (jf - r0) / KPS;
+            step_store_row_smem<ROWB>(p, lb, h, s_t, smem + (cf % NST) * C::STAGE, smem + (cf % NST) * C::STAGE + KPS * ROWB,
+                                      jf - r0 - cf * KPS);
+            __syncthreads();   // the merge below reuses the stage buffers (uniform: one condition per CTA)
+        }
+    }
 
     // ---- warp results -> shared (8 columns), merge the 4 warps over the G real ones ----
     constexpr int WS = D + 8;                       // padded row stride of wo
@@ -325,88 +419,83 @@ __global__ void __launch_bounds__(128) decode_mma_kernel(const __grid_constant__
     bool final_cta;
     if (p.cluster) {
         // The n_split CTAs of this (row, head) pair form one thread-block
-        // cluster.  Each pushes its (m, l) to every rank and the slice of its o
-        // that rank k finalises into rank k's receive buffers (remote shared
-        // memory stores, no waiting), one cluster barrier makes them visible,
-        // and each rank merges its slice from its own shared memory.
-        cg::cluster_group cluster = cg::this_cluster();
-        const int nc = (int)cluster.num_blocks(), rank = (int)cluster.block_rank();
-        const int per = (NR * D + nc - 1) / nc;
-        // this CTA's 4 warps per row: max, weights and sum (one thread per
-        // row), then every element of the CTA partial is pushed to the rank
-        // that finalises it, and the rows' (max, sum) to every rank -- spread
-        // over the threads, so no thread serialises the remote stores
-        float* ew = scratch + 96;                     // [8 rows][4 warps], clear of the post-sync scratch
-        if (tid < 32) {                               // lane = row * 4 + warp: groups of 4 lanes per row
-            const int n = tid >> 2, w = tid & 3;
-            const float mw = n < NR ? wm[w * 8 + n] : -INFINITY;
-            float M = fmaxf(mw, __shfl_xor_sync(0xffffffffu, mw, 1));
-            M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, 2));
-            const float e = mw == -INFINITY ? 0.f : fast_ex2(mw - M);
-            float l = e * (n < NR ? wl[w * 8 + n] : 0.f);
-            l += __shfl_xor_sync(0xffffffffu, l, 1);
-            l += __shfl_xor_sync(0xffffffffu, l, 2);
-            if (n < NR) {
-                ew[n * 4 + w] = e;
-                if (w == 0) {
-                    cm[n] = M;
-                    cl[n] = l;
-                }
-            }
-        }
-        __syncthreads();
-        for (int i = tid; i < NR * D; i += 128) {
-            const int n = i / D, d = i % D;
-            float a = 0.f;
+        // cluster (rank = split).  Each merges its 4 warps per element and pushes
+        // the slice of its partial that rank k finalises, and its rows' (max,
+        // sum), into rank k's receive buffers; each rank waits for its own bytes
+        // only and merges its slice.  Merge weights are computed where they are
+        // used (no extra block barrier).
+        const int nc = p.n_split, rank = split;
+        cluster_wait();                               // every peer's receive mbarrier is initialised
+        for (int i4 = tid * 4; i4 < NR * D; i4 += 512) {
+            const int n = i4 / D, d = i4 % D;
+            float mw[4], M = -INFINITY;
 #pragma unroll
-            for (int w = 0; w < 4; ++w) a += ew[n * 4 + w] * wo[(w * 8 + n) * WS + d];
-            const int k = i / per;
-            cluster.map_shared_rank(r_o, k)[rank * per + (i - k * per)] = a;
+            for (int w = 0; w < 4; ++w) {
+                mw[w] = wm[w * 8 + n];
+                M = fmaxf(M, mw[w]);
+            }
+            float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+            for (int w = 0; w < 4; ++w) {
+                const float e = mw[w] == -INFINITY ? 0.f : fast_ex2(mw[w] - M);
+                const float4 x = *reinterpret_cast<const float4*>(wo + (w * 8 + n) * WS + d);
+                a.x += e * x.x;
+                a.y += e * x.y;
+                a.z += e * x.z;
+                a.w += e * x.w;
+            }
+            const int k = i4 / per;
+            st_async_v4(mapa_rank(smem_u32(r_o + rank * per + (i4 - k * per)), k), a, mapa_rank(smem_u32(&r_bar), k));
         }
         for (int t = tid; t < NR * nc; t += 128) {
             const int n = t / nc, kk = t % nc;
-            cluster.map_shared_rank(r_m, kk)[rank * 8 + n] = cm[n];
-            cluster.map_shared_rank(r_l, kk)[rank * 8 + n] = cl[n];
+            float M = -INFINITY;
+#pragma unroll
+            for (int w = 0; w < 4; ++w) M = fmaxf(M, wm[w * 8 + n]);
+            float l = 0.f;
+#pragma unroll
+            for (int w = 0; w < 4; ++w) {
+                const float mv = wm[w * 8 + n];
+                if (mv != -INFINITY) l += fast_ex2(mv - M) * wl[w * 8 + n];
+            }
+            st_async_v2(mapa_rank(smem_u32(&r_ml[rank * 8 + n]), kk), M, l, mapa_rank(smem_u32(&r_bar), kk));
         }
-        cluster.sync();                               // every peer's pushes have landed here
-        float* w = scratch;                           // [8 rows][8 ranks] merge weights
-        float* den = w + 64;                          // [8]
-        float* Mx = den + 8;                          // [8]
-        if (tid < 64) {                               // thread = row * 8 + rank: groups of 8 lanes per row
-            const int n = tid >> 3, r = tid & 7;
-            const bool real = n < NR && r < nc;
-            const float mr = real ? r_m[r * 8 + n] : -INFINITY;
-            float M = fmaxf(mr, __shfl_xor_sync(0xffffffffu, mr, 1));
-            M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, 2));
-            M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, 4));
-            const float wr = mr == -INFINITY ? 0.f : fast_ex2(mr - M);
-            float dn = wr * (real ? r_l[r * 8 + n] : 0.f);
-            dn += __shfl_xor_sync(0xffffffffu, dn, 1);
-            dn += __shfl_xor_sync(0xffffffffu, dn, 2);
-            dn += __shfl_xor_sync(0xffffffffu, dn, 4);
-            if (n < NR) {
-                w[n * 8 + r] = wr;
-                if (r == 0) {
-                    den[n] = dn;
-                    Mx[n] = M;
+        // this rank's slice from every rank (its own pushes included)
+        const bool got = __syncthreads_and(tid != 0 || recv_wait(&r_bar, p.d_err));
+        const int lo = rank * per, hi = imin(NR * D, lo + per);
+        if (got) {
+            for (int i = lo + tid; i < hi; i += 128) {
+                const int n = i / D;
+                float M = -INFINITY;
+#pragma unroll
+                for (int r = 0; r < 8; ++r)
+                    if (r < nc) M = fmaxf(M, r_ml[r * 8 + n].x);
+                float a = 0.f, dn = 0.f;
+#pragma unroll
+                for (int r = 0; r < 8; ++r) {
+                    if (r < nc) {
+                        const float2 ml = r_ml[r * 8 + n];
+                        const float wr = ml.x == -INFINITY ? 0.f : fast_ex2(ml.x - M);
+                        dn += wr * ml.y;
+                        a += wr * r_o[r * per + (i - lo)];
+                    }
+                }
+                out.optr(n)[i % D] = dn > 0.f ? a / dn : 0.f;
+            }
+            if (rank == 0 && tid < NR) {
+                float* lp = out.lptr(tid);
+                if (lp) {
+                    float M = -INFINITY, dn = 0.f;
+                    for (int r = 0; r < nc; ++r) M = fmaxf(M, r_ml[r * 8 + tid].x);
+                    for (int r = 0; r < nc; ++r) {
+                        const float2 ml = r_ml[r * 8 + tid];
+                        if (ml.x != -INFINITY) dn += fast_ex2(ml.x - M) * ml.y;
+                    }
+                    *lp = dn > 0.f ? (M + __log2f(dn)) * 0.6931471805599453f : -INFINITY;
                 }
             }
         }
-        __syncthreads();
-        const int lo = rank * per, hi = imin(NR * D, lo + per);
-        for (int i = lo + tid; i < hi; i += 128) {
-            const int n = i / D;
-            float a = 0.f;
-            for (int r = 0; r < nc; ++r) a += w[n * 8 + r] * r_o[r * per + (i - lo)];
-            const float dn = den[n];
-            out.optr(n)[i % D] = dn > 0.f ? a / dn : 0.f;
-        }
-        if (rank == 0 && tid < NR) {
-            float* lp = out.lptr(tid);
-            const float dn = den[tid];
-            if (lp) *lp = dn > 0.f ? (Mx[tid] + __log2f(dn)) * 0.6931471805599453f : -INFINITY;
-        }
-        final_cta = rank == 0;
+        final_cta = got && rank == 0;
     } else {
         if (tid < NR) {
             float M = -INFINITY;

@@ -409,29 +409,6 @@ __device__ __forceinline__ int build_segments(const DecodeParams& p, int lb, int
     return n;
 }
 
-// Fused step, the last split of each (row, head): store the new token's K/V row of
-// head h in its sink or ring row (the ring write evicts token t+1-W-R, which no
-// CTA of this launch reads) and in the full-KV cache.
-template <int ROWB>
-__device__ void step_store_row(const DecodeParams& p, int lb, int h, int z, int t) {
-    const int i = t + 1;
-    const int row = i <= p.S ? i - 1 : p.S + ring_row(i, p.S, p.Wc);
-    const size_t src = ((size_t)z * p.Hkv + h) * ROWB;
-    const size_t dst = (((size_t)lb * p.Hkv + h) * p.C + row) * ROWB;
-    const bool to_full = p.full_k != nullptr && i <= p.Tmax;
-    const size_t fdst = (((size_t)lb * p.Hkv + h) * p.Tmax + (i - 1)) * (size_t)ROWB;
-    for (int c = threadIdx.x; c < ROWB / 16; c += blockDim.x) {
-        const uint4 kv = *reinterpret_cast<const uint4*>((const uint8_t*)p.k_g + src + c * 16);
-        const uint4 vv = *reinterpret_cast<const uint4*>((const uint8_t*)p.v_g + src + c * 16);
-        *reinterpret_cast<uint4*>((uint8_t*)p.pool_k + dst + c * 16) = kv;
-        *reinterpret_cast<uint4*>((uint8_t*)p.pool_v + dst + c * 16) = vv;
-        if (to_full) {
-            *reinterpret_cast<uint4*>((uint8_t*)p.full_k + fdst + c * 16) = kv;
-            *reinterpret_cast<uint4*>((uint8_t*)p.full_v + fdst + c * 16) = vv;
-        }
-    }
-}
-
 // After the attention of pair (row z, head h) is final -- its last split, or
 // rank 0 of its cluster -- every CTA of the pair has read this head's copy of
 // the counters, so the pair updates them on its own, with no cross-head
