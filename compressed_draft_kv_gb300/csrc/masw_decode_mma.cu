@@ -304,6 +304,10 @@ __global__ void __launch_bounds__(128, NST_ == 2 ? 3 : 2) decode_mma_kernel(cons
         }
     }
 
+    // every peer arrived at its start, so this wait is free here and keeps the
+    // cluster barrier off the merge's critical path
+    if (p.cluster) cluster_wait();                   // every peer's receive mbarrier is initialised
+
     const float sl2 = p.scale_log2;
     float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f};
     float acc[KS][4];
@@ -440,7 +444,6 @@ __global__ void __launch_bounds__(128, NST_ == 2 ? 3 : 2) decode_mma_kernel(cons
         // only and merges its slice.  Merge weights are computed where they are
         // used (no extra block barrier).
         const int nc = p.n_split, rank = split;
-        cluster_wait();                               // every peer's receive mbarrier is initialised
         for (int i4 = tid * 4; i4 < NR * D; i4 += 512) {
             const int n = i4 / D, d = i4 % D;
             float mw[4], M = -INFINITY;
@@ -462,7 +465,8 @@ __global__ void __launch_bounds__(128, NST_ == 2 ? 3 : 2) decode_mma_kernel(cons
             const int k = i4 / per;
             st_async_v4(mapa_rank(smem_u32(r_o + rank * per + (i4 - k * per)), k), a, mapa_rank(smem_u32(&r_bar), k));
         }
-        for (int t = tid; t < NR * nc; t += 128) {
+        // the rows' (max, sum) from the highest threads, beside the slice pushes
+        for (int t = 127 - tid; t < NR * nc; t += 128) {
             const int n = t / nc, kk = t % nc;
             float M = -INFINITY;
 #pragma unroll
@@ -495,7 +499,7 @@ __global__ void __launch_bounds__(128, NST_ == 2 ? 3 : 2) decode_mma_kernel(cons
                         a += wr * r_o[r * per + (i - lo)];
                     }
                 }
-                out.optr(n)[i % D] = dn > 0.f ? a / dn : 0.f;
+                out.optr(n)[i % D] = dn > 0.f ? __fdividef(a, dn) : 0.f;
             }
             if (rank == 0 && tid < NR) {
                 float* lp = out.lptr(tid);
