@@ -342,12 +342,14 @@ __global__ void __launch_bounds__(128, NST_ == 2 ? 3 : 2) decode_mma_kernel(cons
             }
 #pragma unroll
             for (int e = 0; e < 4; ++e) s[e] += s2[e];
-            const int key_a = key_tile + (lane >> 2), key_b = key_a + 8;
             float x[4];
-            x[0] = key_a < r1 ? s[0] * sl2 : -INFINITY;
-            x[1] = key_a < r1 ? s[1] * sl2 : -INFINITY;
-            x[2] = key_b < r1 ? s[2] * sl2 : -INFINITY;
-            x[3] = key_b < r1 ? s[3] * sl2 : -INFINITY;
+#pragma unroll
+            for (int e = 0; e < 4; ++e) x[e] = s[e] * sl2;
+            if (key_tile + 16 > r1) {                   // the split's last, partial tile (warp-uniform)
+                const int key_a = key_tile + (lane >> 2), key_b = key_a + 8;
+                if (key_a >= r1) x[0] = x[1] = -INFINITY;
+                if (key_b >= r1) x[2] = x[3] = -INFINITY;
+            }
             float pr[4];
 #pragma unroll
             for (int e = 0; e < 2; ++e) {
@@ -356,9 +358,9 @@ __global__ void __launch_bounds__(128, NST_ == 2 ? 3 : 2) decode_mma_kernel(cons
                 mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
                 mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
                 const float m_new = fmaxf(m_run[e], mx);   // finite: key_tile < r1
-                const float alpha = exp2f(m_run[e] - m_new);
-                pr[e] = exp2f(x[e] - m_new);
-                pr[e + 2] = exp2f(x[e + 2] - m_new);
+                const float alpha = fast_ex2(m_run[e] - m_new);
+                pr[e] = fast_ex2(x[e] - m_new);
+                pr[e + 2] = fast_ex2(x[e + 2] - m_new);
                 l_run[e] = l_run[e] * alpha + pr[e] + pr[e + 2];
                 m_run[e] = m_new;
 #pragma unroll

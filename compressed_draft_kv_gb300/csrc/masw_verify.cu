@@ -45,6 +45,12 @@ static_assert((2 * 4 * kVMaxNQ + 4 * kVMaxNQ * (kVD + 8) + 2 * kVMaxNQ + kVMaxNQ
                epilogue_scratch_floats(kVMaxNQ, kVMaxSplit)) * 4 <= kVSmem,
               "verify merge does not fit in the stage buffers");
 
+// 2^x by the MUFU instruction (an input of -inf gives 0)
+__device__ __forceinline__ float ex2_ftz(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
 __device__ __forceinline__ uint32_t swz(int row, int chunk) {  // byte offset of a 16-B chunk
     return (uint32_t)(row * kVRowB + ((chunk ^ (row & 7)) << 4));
 }
@@ -153,12 +159,19 @@ __global__ void __launch_bounds__(128 * NT) verify_kernel(const __grid_constant_
             }
 #pragma unroll
             for (int e = 0; e < 4; ++e) s[e] += s2[e];
-            const int key_a = key_tile + (lane >> 2), key_b = key_a + 8;
             float x[4];
-            x[0] = key_a < lim[0] ? s[0] * p.scale_log2 : -INFINITY;
-            x[1] = key_a < lim[1] ? s[1] * p.scale_log2 : -INFINITY;
-            x[2] = key_b < lim[0] ? s[2] * p.scale_log2 : -INFINITY;
-            x[3] = key_b < lim[1] ? s[3] * p.scale_log2 : -INFINITY;
+#pragma unroll
+            for (int e = 0; e < 4; ++e) x[e] = s[e] * p.scale_log2;
+            // the causal mask only bites in the tile that crosses the block's
+            // diagonal (warp-uniform test: every key of the tile below every
+            // column's limit)
+            if (!__all_sync(0xffffffffu, key_tile + 16 <= imin(lim[0], lim[1]))) {
+                const int key_a = key_tile + (lane >> 2), key_b = key_a + 8;
+                if (key_a >= lim[0]) x[0] = -INFINITY;
+                if (key_a >= lim[1]) x[1] = -INFINITY;
+                if (key_b >= lim[0]) x[2] = -INFINITY;
+                if (key_b >= lim[1]) x[3] = -INFINITY;
+            }
             float pr[4];
 #pragma unroll
             for (int e = 0; e < 2; ++e) {
@@ -168,9 +181,9 @@ __global__ void __launch_bounds__(128 * NT) verify_kernel(const __grid_constant_
                 mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
                 const float m_new = fmaxf(m_run[e], mx);
                 const float m_use = m_new == -INFINITY ? 0.f : m_new;   // column fully masked so far
-                const float alpha = exp2f(m_run[e] - m_use);
-                pr[e] = exp2f(x[e] - m_use);
-                pr[e + 2] = exp2f(x[e + 2] - m_use);
+                const float alpha = ex2_ftz(m_run[e] - m_use);
+                pr[e] = ex2_ftz(x[e] - m_use);
+                pr[e + 2] = ex2_ftz(x[e + 2] - m_use);
                 l_run[e] = l_run[e] * alpha + pr[e] + pr[e + 2];
                 m_run[e] = m_new;
 #pragma unroll
