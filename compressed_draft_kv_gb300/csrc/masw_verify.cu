@@ -7,7 +7,7 @@
 // query rows as N (8 per tile), so 24 query rows fill three N tiles without
 // padding.  Each warp owns one N tile of one 16-key group (4 NT warps per CTA),
 // which keeps its accumulators at about 80 registers.  S^T = K Q^T is accumulated per 16-key tile from ldmatrix fragments
-// of an XOR-swizzled shared-memory stage (cp.async, 3 stages), softmax runs
+// of a padded-row shared-memory stage (cp.async, 3 stages), softmax runs
 // online per query column in the log2 domain, P^T is turned from the
 // accumulator layout into a B operand with movmatrix, and O^T += V^T P^T uses
 // ldmatrix.trans on the same V stage.  Splits over the key axis are merged by
@@ -36,7 +36,10 @@ struct VerifyParams {
 constexpr int kVD = 128;             // head_dim
 constexpr int kVKeys = 64;           // keys per stage (16 per warp)
 constexpr int kVRowB = kVD * 2;      // bytes per K/V row
-constexpr int kVStage = 2 * kVKeys * kVRowB;
+constexpr int kVRowP = kVRowB + 16;  // padded row stride in shared memory: the 8 row addresses of an
+                                     // ldmatrix phase fall in distinct banks, and every k-step's offset
+                                     // is a compile-time immediate (no per-access swizzle arithmetic)
+constexpr int kVStage = 2 * kVKeys * kVRowP;
 constexpr int kVNst = 3;
 constexpr int kVSmem = kVNst * kVStage;
 constexpr int kVMaxSplit = 64;       // bounds the merge scratch kept in shared memory
@@ -51,8 +54,8 @@ __device__ __forceinline__ float ex2_ftz(float x) {
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
 }
-__device__ __forceinline__ uint32_t swz(int row, int chunk) {  // byte offset of a 16-B chunk
-    return (uint32_t)(row * kVRowB + ((chunk ^ (row & 7)) << 4));
+__device__ __forceinline__ uint32_t pad_off(int row, int chunk) {  // byte offset of a 16-B chunk
+    return (uint32_t)(row * kVRowP + (chunk << 4));
 }
 // three stages for every tile count (two CTAs per SM at three tiles; six stages
 // on one CTA per SM measured slower)
@@ -86,19 +89,19 @@ __global__ void __launch_bounds__(128 * NT) verify_kernel(const __grid_constant_
     const __nv_bfloat16* vbase = p.v + ((size_t)b * p.Hkv + h) * (size_t)p.Tmax * kVD;
     const uint32_t sbase = smem_u32(smem);
 
-    // one stage = 64 keys of K and V, 16-byte chunks XOR-swizzled by row;
-    // rows past k1 are zero-filled (src-size 0 reads nothing)
+    // one stage = 64 keys of K and V in padded rows; rows past k1 are
+    // zero-filled (src-size 0 reads nothing)
     auto load_stage = [&](int c) {
         const uint32_t sk = sbase + (uint32_t)(c % NSTV) * kVStage;
-        const uint32_t sv = sk + kVKeys * kVRowB;
+        const uint32_t sv = sk + kVKeys * kVRowP;
         const int key0 = k0 + c * kVKeys;
         for (int idx = tid; idx < kVKeys * 16; idx += nthr) {
             const int row = idx >> 4, ch = idx & 15;
             const int key = key0 + row;
             const bool in = key < k1;
             const size_t goff = (size_t)(in ? key : k0) * kVD + ch * 8;
-            cp_async16(sk + swz(row, ch), kbase + goff, in ? 16 : 0);
-            cp_async16(sv + swz(row, ch), vbase + goff, in ? 16 : 0);
+            cp_async16(sk + pad_off(row, ch), kbase + goff, in ? 16 : 0);
+            cp_async16(sv + pad_off(row, ch), vbase + goff, in ? 16 : 0);
         }
     };
 #pragma unroll
@@ -130,6 +133,9 @@ __global__ void __launch_bounds__(128 * NT) verify_kernel(const __grid_constant_
         lim[e] = n < NQ ? imin(k1, n_keys - p.Lq + 1 + n / G) : k1;
     }
 
+    // this lane's ldmatrix row addresses within a stage (k-step / m-tile add 32 bytes)
+    const uint32_t k_off = pad_off(kg * 16 + (lane & 7) + ((lane >> 3) & 1) * 8, lane >> 4);
+    const uint32_t v_off = pad_off(kg * 16 + (lane & 7) + (lane >> 4) * 8, (lane >> 3) & 1);
     float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f};
     float acc[8][4];
 #pragma unroll
@@ -144,7 +150,7 @@ __global__ void __launch_bounds__(128 * NT) verify_kernel(const __grid_constant_
             cp_async_commit();
         }
         const uint32_t sk = sbase + (uint32_t)(c % NSTV) * kVStage;
-        const uint32_t sv = sk + kVKeys * kVRowB;
+        const uint32_t sv = sk + kVKeys * kVRowP;
         const int kw = kg * 16;
         const int key_tile = k0 + c * kVKeys + kw;
         if (key_tile < k1) {
@@ -153,8 +159,7 @@ __global__ void __launch_bounds__(128 * NT) verify_kernel(const __grid_constant_
 #pragma unroll
             for (int ks = 0; ks < 8; ++ks) {
                 uint32_t a0, a1, a2, a3;
-                const int row = kw + (lane & 7) + ((lane >> 3) & 1) * 8;
-                ldsm_x4(sk + swz(row, ks * 2 + (lane >> 4)), a0, a1, a2, a3);
+                ldsm_x4(sk + k_off + ks * 32, a0, a1, a2, a3);
                 mma16816((ks & 1) ? s2 : s, a0, a1, a2, a3, qb[ks][0], qb[ks][1]);
             }
 #pragma unroll
@@ -197,8 +202,7 @@ __global__ void __launch_bounds__(128 * NT) verify_kernel(const __grid_constant_
 #pragma unroll
             for (int mt = 0; mt < 8; ++mt) {
                 uint32_t a0, a1, a2, a3;
-                const int row = kw + (lane & 7) + (lane >> 4) * 8;
-                ldsm_x4_t(sv + swz(row, mt * 2 + ((lane >> 3) & 1)), a0, a1, a2, a3);
+                ldsm_x4_t(sv + v_off + mt * 32, a0, a1, a2, a3);
                 mma16816(acc[mt], a0, a1, a2, a3, pb0, pb1);
             }
         }
