@@ -161,6 +161,12 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&v)[32
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
+__device__ __forceinline__ float4 ld_shared_v4f(uint32_t addr) {
+    float4 v;
+    asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(addr)
+                 : "memory");
+    return v;
+}
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
     asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d)
                  : "memory");
@@ -290,6 +296,15 @@ __global__ void __launch_bounds__(192, 2) prefill_kernel(const __grid_constant__
 
     pdl_wait();
     pdl_trigger();
+    // this thread's Q row (softmax threads): all 16 loads in flight while the
+    // CTA allocates tensor memory and initialises its barriers
+    uint4 qreg[16];
+    if (warp < 4) {
+        const __nv_bfloat16* qsrc = slot_tile ? p.q_slot : p.q_raw;
+        const uint4* qp = reinterpret_cast<const uint4*>(qsrc + ((size_t)(live ? qrow : 0) * p.Hq + hq) * kD);
+#pragma unroll
+        for (int c = 0; c < 16; ++c) qreg[c] = live ? __ldg(qp + c) : make_uint4(0u, 0u, 0u, 0u);
+    }
     // the swizzled layouts need a 1024-byte aligned base; after a timed-out wait
     // anywhere in the grid the remaining CTAs skip their work
     const bool misaligned = (sb & 1023u) != 0u;
@@ -400,14 +415,12 @@ __global__ void __launch_bounds__(192, 2) prefill_kernel(const __grid_constant__
         const uint32_t t_o = tmem + kColO + lane_off;
         // Q row -> tensor memory (zeros past the last row), the A operand of S
         {
-            const __nv_bfloat16* qsrc = slot_tile ? p.q_slot : p.q_raw;
-            const uint4* qp = reinterpret_cast<const uint4*>(qsrc + ((size_t)(live ? qrow : 0) * p.Hq + hq) * kD);
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
                 uint32_t qv[32];
 #pragma unroll
                 for (int c = 0; c < 8; ++c) {
-                    const uint4 w = live ? __ldg(qp + h * 8 + c) : make_uint4(0u, 0u, 0u, 0u);
+                    const uint4 w = qreg[h * 8 + c];
                     qv[4 * c] = w.x;
                     qv[4 * c + 1] = w.y;
                     qv[4 * c + 2] = w.z;
@@ -524,18 +537,41 @@ __global__ void __launch_bounds__(192, 2) prefill_kernel(const __grid_constant__
         float* obase = slot_tile ? p.o_slot : p.o_raw;
         float* lbase = slot_tile ? p.lse_slot : p.lse_raw;
         const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
-        float* orow = obase + ((size_t)(live ? qrow : q0) * p.Hq + hq) * kD;
+        // O / l through a swizzled 32 x 32 tile per warp in the (now idle) K
+        // stages: thread `lane` writes 32 columns of its row, then each store
+        // instruction writes 128-byte pieces of 4 rows (the rows are Hq*512
+        // bytes apart in global memory, so one row per thread would scatter)
+        if (ok && nblk > 0) {
+            const uint32_t tile = sb + kOffK + (uint32_t)warp * 4096u;
+            float* rowp[8];                              // global row of tile row 4 i + lane / 8, or null
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-            uint32_t ov[32];
-            tmem_ld32(t_o + c * 32, ov);
-            tmem_wait_ld();
-            if (live && nblk > 0) {
+            for (int i = 0; i < 8; ++i) {
+                const int t = warp * 32 + i * 4 + (lane >> 3);
+                const int qr = q0 + (pack > 1 ? t / pack : t);
+                const int hh = pack > 1 ? kvh * G + t % pack : (int)blockIdx.y;
+                const bool lv = (pack == 1 || t < rpt * pack) && qr < q1;
+                rowp[i] = lv ? obase + ((size_t)qr * p.Hq + hh) * kD : nullptr;
+            }
 #pragma unroll
-                for (int e = 0; e < 32; e += 4)
-                    *reinterpret_cast<float4*>(orow + c * 32 + e) =
-                        make_float4(__uint_as_float(ov[e]) * inv, __uint_as_float(ov[e + 1]) * inv,
-                                    __uint_as_float(ov[e + 2]) * inv, __uint_as_float(ov[e + 3]) * inv);
+            for (int c = 0; c < 4; ++c) {
+                uint32_t ov[32];
+                tmem_ld32(t_o + c * 32, ov);
+                tmem_wait_ld();
+#pragma unroll
+                for (int e4 = 0; e4 < 8; ++e4)
+                    st_shared_v4(tile + (uint32_t)lane * 128u + ((uint32_t)(e4 ^ (lane & 7)) << 4),
+                                 __float_as_uint(__uint_as_float(ov[4 * e4]) * inv),
+                                 __float_as_uint(__uint_as_float(ov[4 * e4 + 1]) * inv),
+                                 __float_as_uint(__uint_as_float(ov[4 * e4 + 2]) * inv),
+                                 __float_as_uint(__uint_as_float(ov[4 * e4 + 3]) * inv));
+                __syncwarp();
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const int rr = i * 4 + (lane >> 3), e4 = lane & 7;
+                    const float4 v = ld_shared_v4f(tile + (uint32_t)rr * 128u + ((uint32_t)(e4 ^ (rr & 7)) << 4));
+                    if (rowp[i]) *reinterpret_cast<float4*>(rowp[i] + c * 32 + e4 * 4) = v;
+                }
+                __syncwarp();
             }
         }
         if (live && lbase)
