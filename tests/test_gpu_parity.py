@@ -509,6 +509,74 @@ def test_draft3b_full_size_sampled():
         p.close()
 
 
+@pytest.mark.parametrize("Hq", [24, 32])
+def test_fused_steps_full_size_sampled(Hq):
+    """The fused step and the fused boundary step at the benchmark's launch
+    shape (batch 8, 8 kv heads, 32K prefix, S=4, W=1024, r=512): every split of
+    a (row, head) pair is a CTA of one thread-block cluster, so the shared-memory
+    merge runs with G = 3 or 4 query columns per pair, and with 2G = 6 or 8 at the
+    boundary step, where the slot queries of all eight sequences ride in the same
+    launch.  The new token's row is stored by the split whose keys include it.
+    Two (layer, row) pairs carry CPU-seeded data and are checked against the
+    oracle; the other rows are filled on the device."""
+    S, W, r, t0 = 4, 1024, 512, 32768
+    B, L, Hkv, D = 8, 2, 8, 128
+    p = Pair(S, W, r, Hkv, D, L, B, "bf16", Hq, max_seq_len=t0 + 16, tag=f"fsz{Hq}")
+    sampled = {(0, 2), (1, 6)}
+    try:
+        g = torch.Generator(device=DEV)
+        g.manual_seed(4321)
+        n = orc.slot_count(t0, S, W, r)
+        for l in range(L):
+            for b in range(B):
+                if (l, b) in sampled:
+                    p.load(l, b, t0, seed=3)
+                else:
+                    kr = torch.randn(t0, Hkv, D, generator=g, device=DEV).to(torch.bfloat16)
+                    ks = torch.randn(n, Hkv, D, generator=g, device=DEV).to(torch.bfloat16)
+                    capi.masw_mem_load(p.h, l, b, kr, kr, ks, ks)
+                    del kr, ks
+        for step in range(1, 7):
+            p.step = step
+            boundary = step == 4          # tau_62 = 4 + 1024 + 62*512 = 32772 for every sequence
+            for l in range(L):
+                k = p.rand((B, Hkv, D), "k", l)
+                v = p.rand((B, Hkv, D), "v", l)
+                q = p.rand((B, Hq, D), "q", l)
+                o = torch.empty(B, Hq, D, device=DEV)
+                lse = torch.empty(B, Hq, device=DEV)
+                if boundary:
+                    assert orc.is_boundary(t0 + 4, S, W, r)
+                    qg = p.rand((B, Hq, D), "qg", l)
+                    kg = p.rand((B, Hkv, D), "kg", l)
+                    vg = p.rand((B, Hkv, D), "vg", l)
+                    og = torch.empty(B, Hq, D, device=DEV)
+                    lg = torch.empty(B, Hq, device=DEV)
+                    capi.masw_draft_step_slot(p.h, l, q.to(DEV), k.to(DEV), v.to(DEV), o, list(range(B)),
+                                              qg.to(DEV), kg.to(DEV), vg.to(DEV), og, lse, lg)
+                else:
+                    capi.masw_draft_step(p.h, l, q.to(DEV), k.to(DEV), v.to(DEV), o, lse)
+                for (sl, sb) in sampled:
+                    if sl != l:
+                        continue
+                    p.ref.append(l, k.float().numpy(), v.float().numpy(), active=[bb == sb for bb in range(B)])
+                    Kc, Vc = p.ref._columns(l, sb)
+                    mask = orc.draft_mask(p.ref.t(l, sb), p.ref.m(l, sb), S, W)
+                    wo, wl = orc.attention(q.float().numpy()[sb], Kc, Vc, mask, p.ref.scale)
+                    assert_close(o[sb], wo, "bf16", f"fused step Hq={Hq} l={l} b={sb} step={step}")
+                    assert_close(lse[sb], wl, "bf16", "fused step LSE")
+                    if boundary:
+                        w, wlg = p.ref.materialize_slot(l, [sb], qg.float().numpy()[sb:sb + 1],
+                                                        kg.float().numpy()[sb:sb + 1], vg.float().numpy()[sb:sb + 1])
+                        assert_close(og[sb:sb + 1], w, "bf16", f"fused slot Hq={Hq} l={l} b={sb}")
+                        assert_close(lg[sb:sb + 1], wlg, "bf16", "fused slot LSE")
+        capi.masw_sync(p.h)
+        for (sl, sb) in sampled:
+            p.check_state(sl, sb)
+    finally:
+        p.close()
+
+
 def test_draft8b_large_batch_long_runs_sampled():
     """The large-batch launch shape (batch 32, 32q/8kv, W = 2048, r = 1024,
     ragged prefixes 16K..32K): one split per (sequence, head) streams ~2080 keys,
