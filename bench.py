@@ -403,7 +403,7 @@ def run_verify(torch, capi, synth, reps: int = 5):
     q = [torch.randn(B, Lq, Hq, D, generator=g, device=dev).to(torch.bfloat16) for _ in range(L)]
     kl = torch.full((B,), T, dtype=torch.int32, device=dev)
     o = torch.empty(B, Lq, Hq, D, device=dev)
-    ws = torch.empty(capi.masw_verify_workspace_bytes(B, Lq, Hq, Hkv, D, T), dtype=torch.uint8, device=dev)
+    ws = torch.zeros(capi.masw_verify_workspace_bytes(B, Lq, Hq, Hkv, D, T), dtype=torch.uint8, device=dev)
     st = torch.cuda.Stream(device=dev)
 
     def run():
@@ -433,7 +433,7 @@ def run_verify(torch, capi, synth, reps: int = 5):
     torch.cuda.empty_cache()
     return {"ms_per_verify": secs * 1e3, "layers": L, "batch": B, "lq": Lq, "keys": T,
             "kv_bytes": kv_bytes, "gbs": kv_bytes / secs / 1e9, "tflops": flops / secs / 1e12,
-            "launches": 2 * L}
+            "launches": L}
 
 
 def run_accept(torch, capi, reps: int = 20):

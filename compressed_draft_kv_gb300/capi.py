@@ -219,7 +219,7 @@ def masw_verify_attn(q, k_cache, v_cache, kv_len, o, lse=None, workspace=None, s
     need = masw_verify_workspace_bytes(B, Lq, Hq, Hkv, D, Tmax)
     if workspace is None:
         import torch
-        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+        workspace = torch.zeros(need, dtype=torch.uint8, device=q.device)   # zero-filled before first use
     _check(load().masw_verify_attn(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(kv_len), B, Lq, Hq, Hkv, D, Tmax,
                                    MASW_BF16, scale, _ptr(o), _ptr(lse), _ptr(workspace), workspace.numel(),
                                    _stream(stream)))

@@ -239,8 +239,12 @@ int masw_full_step(masw_mem_t* mem, int layer, const void* q, const void* k, con
  * q: device [B, Lq, Hq, D]; k_cache, v_cache: device [B, Hkv, Tmax, D];
  * kv_len: device int [B], each in [Lq, Tmax]; o: device float [B, Lq, Hq, D];
  * lse: device float [B, Lq, Hq] or NULL; workspace: device scratch of at least
- * masw_verify_workspace_bytes() bytes (contents need no initialisation; it
- * must not be shared by calls that overlap on the GPU).  scale 0 -> 1/sqrt(D).
+ * masw_verify_workspace_bytes() bytes, zero-filled by the caller before its
+ * first use; every completed call leaves it zero-filled again (the last CTA of
+ * each (sequence, kv head) resets its ticket), so a workspace is reused without
+ * a memset between calls.  A call that ended with an error (for example
+ * MASW_ETIMEOUT from masw_sync) may leave it dirty: zero-fill it before reuse.
+ * It must not be shared by calls that overlap on the GPU.  scale 0 -> 1/sqrt(D).
  * D must be 128 and (Hq/Hkv) * Lq <= 32. */
 int masw_verify_attn(const void* q, const void* k_cache, const void* v_cache,
                      const int* kv_len, int B, int Lq, int Hq, int Hkv, int D,

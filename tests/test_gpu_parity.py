@@ -427,6 +427,28 @@ def test_verify_against_oracle(B, Lq, Hq, Hkv, Tmax, kv_len):
     _verify_case(B, Lq, Hq, Hkv, Tmax, kv_len, seed=B * 100 + Lq)
 
 
+def test_verify_workspace_reuse_leaves_tickets_zero():
+    """A zero-filled workspace is reused across calls with no memset between
+    them: every call leaves its (sequence, kv head) tickets at zero, and the
+    results of each call match the oracle."""
+    B, Lq, Hq, Hkv, Tmax, D = 2, 6, 32, 8, 1500, 128
+    need = capi.masw_verify_workspace_bytes(B, Lq, Hq, Hkv, D, Tmax)
+    ws = torch.zeros(need, dtype=torch.uint8, device=DEV)
+    for call, kv_len in enumerate([[1500, 900], [1200, 1500], [64, 700]]):
+        seed = 900 + call
+        q = synth.normal((B, Lq, Hq, D), "bf16", "verify", seed, "q")
+        k = synth.normal((B, Hkv, Tmax, D), "bf16", "verify", seed, "k")
+        v = synth.normal((B, Hkv, Tmax, D), "bf16", "verify", seed, "v")
+        kl = torch.tensor(kv_len, dtype=torch.int32)
+        o = torch.empty(B, Lq, Hq, D, device=DEV)
+        capi.masw_verify_attn(q.to(DEV), k.to(DEV), v.to(DEV), kl.to(DEV), o, workspace=ws)
+        torch.cuda.synchronize()
+        want, _ = orc.verify_attn(q.float().numpy(), k.float().numpy(), v.float().numpy(), kv_len, None)
+        assert_close(o, want, "bf16", f"verify call {call}")
+        tickets = ws[need - B * Hkv * 4:].view(torch.int32)
+        assert int(tickets.abs().sum()) == 0, f"call {call} left tickets {tickets.tolist()}"
+
+
 def test_verify_peaky_softmax_and_scale():
     _verify_case(2, 6, 32, 8, 512, [512, 200], seed=7, qscale=4.0)
     _verify_case(1, 6, 32, 8, 256, [250], seed=8, scale=0.2)
