@@ -33,6 +33,7 @@
 //     every wait is bounded and one timed-out wait stops the CTA and the grid.
 // 112 KB of shared memory and 256 TMEM columns (O, S, Q) per CTA.
 #include "masw_internal.cuh"
+#include "masw_tc.cuh"
 
 #include <atomic>
 
@@ -46,6 +47,8 @@
 namespace masw {
 
 namespace tcp {
+
+using namespace tc;
 
 constexpr int kBM = 128;                         // query rows per CTA = TMEM lanes
 constexpr int kBN = 64;                          // keys per block
@@ -67,110 +70,6 @@ constexpr uint32_t kColQ = 192;                  // Q (bf16 pairs, the A operand
 constexpr uint32_t kIdescBase = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(kBM >> 4) << 24);
 constexpr uint32_t kIdescS = kIdescBase | ((uint32_t)(kBN >> 3) << 17);
 constexpr uint32_t kIdescO = kIdescBase | (1u << 16) | ((uint32_t)(kD >> 3) << 17);
-
-// shared-memory matrix descriptor, 128-byte swizzle (atoms of 8 rows x 128 B)
-__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
-    return (uint64_t)((saddr >> 4) & 0x3FFFu) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
-           ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (2ull << 61);
-}
-
-__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, int c0, int c1, int c2,
-                                            uint32_t bar) {
-    asm volatile(
-        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], "
-        "[%5];" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(bar)
-        : "memory");
-}
-__device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
-    asm volatile(
-        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(
-            d_tmem),
-        "l"(a), "l"(b), "r"(idesc), "r"(acc)
-        : "memory");
-}
-// A operand in tensor memory: row i in lane i, 2 bf16 per 32-bit column
-__device__ __forceinline__ void umma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t idesc,
-                                             uint32_t acc) {
-    asm volatile(
-        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(
-            d_tmem),
-        "r"(a_tmem), "l"(b), "r"(idesc), "r"(acc)
-        : "memory");
-}
-__device__ __forceinline__ void umma_commit(uint32_t bar) {
-    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
-                 : "memory");
-}
-// 2^x by the MUFU instruction (inputs of -inf give 0)
-__device__ __forceinline__ float ex2_approx(float x) {
-    float y;
-    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-    return y;
-}
-__device__ __forceinline__ float fmax3(float a, float b, float c) {
-    float d;
-    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
-    return d;
-}
-// packed pairs of f32 (low, high) for the f32x2 FMA / add instructions
-__device__ __forceinline__ uint64_t f2_pack(float lo, float hi) {
-    uint64_t r;
-    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
-    return r;
-}
-__device__ __forceinline__ void f2_unpack(uint64_t v, float& lo, float& hi) {
-    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
-}
-__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
-    uint64_t d;
-    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
-    return d;
-}
-__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
-    uint64_t d;
-    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
-    return d;
-}
-__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
-__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
-__device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
-
-#define MASW_R8(i) "=r"(v[i]), "=r"(v[i + 1]), "=r"(v[i + 2]), "=r"(v[i + 3]), "=r"(v[i + 4]), "=r"(v[i + 5]), \
-                   "=r"(v[i + 6]), "=r"(v[i + 7])
-#define MASW_W8(i) "r"(v[i]), "r"(v[i + 1]), "r"(v[i + 2]), "r"(v[i + 3]), "r"(v[i + 4]), "r"(v[i + 5]), \
-                   "r"(v[i + 6]), "r"(v[i + 7])
-// 32 consecutive fp32 columns of this thread's TMEM lane
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&v)[32]) {
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
-        "%15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
-        : MASW_R8(0), MASW_R8(8), MASW_R8(16), MASW_R8(24)
-        : "r"(taddr)
-        : "memory");
-}
-__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&v)[32]) {
-    asm volatile(
-        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
-        "%15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(taddr),
-        MASW_W8(0), MASW_W8(8), MASW_W8(16), MASW_W8(24)
-        : "memory");
-}
-#undef MASW_R8
-#undef MASW_W8
-__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
-__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
-
-__device__ __forceinline__ float4 ld_shared_v4f(uint32_t addr) {
-    float4 v;
-    asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(addr)
-                 : "memory");
-    return v;
-}
-__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
-    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d)
-                 : "memory");
-}
 
 }  // namespace tcp
 
@@ -205,22 +104,6 @@ constexpr int kBarQ = 10;      // the four softmax warps have stored Q in tensor
 constexpr int kBarDone = 11;   // every S MMA done (early exit only)
 constexpr int kBarDoneV = 12;  // every PV MMA done (early exit only)
 constexpr int kNumBars = 13;
-
-// Bounded wait that also gives up as soon as another thread of the CTA has
-// given up (shared abort flag), so that one timed-out wait ends the CTA quickly.
-__device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, volatile int* abort_flag, int* err) {
-    for (uint32_t i = 0; i < kWaitPolls; ++i) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if (*abort_flag) return false;
-        if (i > 256) __nanosleep(64);
-    }
-    *abort_flag = 1;
-    atomicExch(err, MASW_ETIMEOUT);
-    return false;
-}
-__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
-}
 
 // Warp roles: warps 0-3 own query rows 0-127 (TMEM lanes), stage Q into tensor
 // memory and run the softmax; lane 0 of warp 4 loads K and issues S = Q K^T,
@@ -657,23 +540,6 @@ __global__ void prefill_store_kernel(const __grid_constant__ StoreParams p) {
 
 using namespace masw;
 
-// cuTensorMapEncodeTiled from the driver, looked up once through the runtime
-static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    static std::once_flag once;
-    std::call_once(once, [] {
-        void* f = nullptr;
-        cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
-                cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
-        else
-            cudaGetLastError();
-    });
-    return fn;
-}
-
 // [rows][heads][128] bf16 as a 3-d tensor (head_dim innermost), boxes of
 // 64 x 1 x box_rows elements with the 128-byte swizzle the MMA descriptors use
 static bool make_map(CUtensorMap* map, const void* base, int rows, int heads, int box_rows) {
@@ -681,7 +547,7 @@ static bool make_map(CUtensorMap* map, const void* base, int rows, int heads, in
     const cuuint64_t strides[2] = {256, (cuuint64_t)heads * 256};
     const cuuint32_t box[3] = {64, 1, (cuuint32_t)box_rows};
     const cuuint32_t estr[3] = {1, 1, 1};
-    return encode_fn()(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+    return tma_encode_fn()(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -707,7 +573,7 @@ extern "C" int masw_prefill(masw_mem_t* mem, int layer, int seq, int T, const vo
     if (((uintptr_t)o_raw | (uintptr_t)o_slot) & 7 || ((uintptr_t)lse_raw | (uintptr_t)lse_slot) & 3)
         return masw_set_error(mem, MASW_EINVAL, "prefill: outputs must be 8-byte (O) / 4-byte (LSE) aligned");
     if (n_q_heads > 65535) return masw_set_error(mem, MASW_EINVAL, "prefill: too many heads");
-    if (!encode_fn()) return masw_set_error(mem, MASW_ECUDA, "prefill: cuTensorMapEncodeTiled is unavailable");
+    if (!tma_encode_fn()) return masw_set_error(mem, MASW_ECUDA, "prefill: cuTensorMapEncodeTiled is unavailable");
     PrefillParams p;
     std::memset(&p, 0, sizeof(p));
     const int Hkv = mem->Hkv;

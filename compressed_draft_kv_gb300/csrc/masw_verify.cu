@@ -1,18 +1,14 @@
 // Target verify attention over an uncompressed cache ([EN] §3.3 Algorithm 2
 // step 5): Lq query positions per sequence, causal inside the block, GQA.
 //
-// This is the one dense contraction on the path (Lq*G query rows share every
-// K/V row, 24 flop per byte at Lq = 6, G = 4), so it runs on tensor cores:
-// mma.sync m16n8k16 bf16 -> fp32 with KEYS as the M dimension and the Lq*G
-// query rows as N (8 per tile), so 24 query rows fill three N tiles without
-// padding.  Each warp owns one N tile of one 16-key group (4 NT warps per CTA),
-// which keeps its accumulators at about 80 registers.  S^T = K Q^T is accumulated per 16-key tile from ldmatrix fragments
-// of a padded-row shared-memory stage (cp.async, 3 stages), softmax runs
-// online per query column in the log2 domain, P^T is turned from the
-// accumulator layout into a B operand with movmatrix, and O^T += V^T P^T uses
-// ldmatrix.trans on the same V stage.  Splits over the key axis are merged by
-// split_epilogue.
+// This is the one dense contraction on the path (the Lq*G query rows of a kv
+// head share every K/V row: 24 flop per byte at Lq = 6, G = 4), so it runs on
+// the fifth-generation tensor cores with TMA and tensor memory (the machinery
+// of the draft prefill): per (key split, kv head, sequence) one CTA streams its
+// keys in blocks of 64 and keeps S, O and Q in tensor memory; splits over the
+// key axis are merged by split_epilogue.
 #include "masw_internal.cuh"
+#include "masw_tc.cuh"
 
 #include <atomic>
 
@@ -20,294 +16,424 @@
 
 namespace masw {
 
-struct VerifyParams {
-    const __nv_bfloat16* q;   // [B][Lq][Hq][D]
-    const __nv_bfloat16* k;   // [B][Hkv][Tmax][D]
-    const __nv_bfloat16* v;
+constexpr int kVD = 128;             // head_dim
+constexpr int kVMaxSplit = 64;       // key splits per (sequence, kv head) at most
+constexpr int kVMaxNQ = 32;          // query rows (Lq * G) per (sequence, kv head) at most
+
+// ---------------------------------------------------------------------------
+// Verify on fifth-generation tensor cores.  One CTA per (key split, kv head,
+// sequence), 192 threads.  The pair's NQ = Lq * G <= 32 query rows (row n is
+// position n / G, head h * G + n % G) are stored four times in tensor memory,
+// at lanes 32 w + n for w = 0..3, so S = Q K^T (M = 128, N = 64 keys) yields
+// every score four times, once in each warp's lane quarter.  Softmax warp w
+// handles only columns 16 w .. 16 w + 15 of each block: its rows of P are zero
+// elsewhere, so the one O += P V MMA (N = 128) accumulates four partial
+// outputs over disjoint keys, each with its own running max and sum, merged
+// at the end.  This spreads the exponentials over the four SM sub-partitions
+// (a single softmax warp holding all 64 columns left three of them idle).
+// Lane 0 of warp 4 loads K (TMA) and issues S; lane 0 of warp 5 loads V and
+// issues P V.  The split partials are merged by split_epilogue.  Two CTAs per
+// SM (256 tensor-memory columns and 112 KB of shared memory each).
+// ---------------------------------------------------------------------------
+namespace vtc {
+using namespace tc;
+constexpr int kBM = 128;                         // MMA rows = tensor-memory lanes
+constexpr int kBN = 64;                          // keys per block
+constexpr int kD = 128;                          // head_dim
+constexpr int kStages = 3;                       // K and V stages
+constexpr uint32_t kKVBytes = kBN * kD * 2;      // 2 panels of 64 rows x 128 B
+constexpr uint32_t kPBytes = kBM * kBN * 2;      // 1 panel of 128 rows x 128 B
+constexpr uint32_t kOffK = 0;
+constexpr uint32_t kOffV = kOffK + kStages * kKVBytes;
+constexpr uint32_t kOffP = kOffV + kStages * kKVBytes;
+constexpr uint32_t kSmem = kOffP + kPBytes;      // the barriers are static shared memory
+constexpr uint32_t kTmemCols = 256;
+constexpr uint32_t kColO = 0;                    // O: columns [0, 128)
+constexpr uint32_t kColS = 128;                  // S: columns [128, 192)
+constexpr uint32_t kColQ = 192;                  // Q (bf16 pairs, the A operand of S): [192, 256)
+// instruction descriptors (kind::f16): f32 accumulator, bf16 A and B, M = 128;
+// S: N = 64, A (Q, tensor memory) and B (K) K-major; O: N = 128, B (V) MN-major
+constexpr uint32_t kIdescBase = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(kBM >> 4) << 24);
+constexpr uint32_t kIdescS = kIdescBase | ((uint32_t)(kBN >> 3) << 17);
+constexpr uint32_t kIdescO = kIdescBase | (1u << 16) | ((uint32_t)(kD >> 3) << 17);
+__device__ __forceinline__ constexpr int bar_k(int s) { return s; }        // K stage landed (TMA)
+__device__ __forceinline__ constexpr int bar_v(int s) { return 3 + s; }    // V stage landed (TMA)
+constexpr int kBarS = 6;       // S = Q K^T done (MMA commit)
+constexpr int kBarSFree = 7;   // the four softmax warps have read S (4 arrivals)
+constexpr int kBarP = 8;       // the four softmax warps have written P and rescaled O (4 arrivals)
+constexpr int kBarO = 9;       // O += P V done (MMA commit)
+constexpr int kBarQ = 10;      // the four softmax warps have stored Q in tensor memory (4 arrivals)
+constexpr int kBarDone = 11;   // every S MMA done (early exit only)
+constexpr int kBarDoneV = 12;  // every PV MMA done (early exit only)
+constexpr int kNumBars = 13;
+// merge layout in the idle stage buffers after the loop: four partial O rows
+// per query row, their (max, sum), the merged rows and (max, sum)
+constexpr uint32_t kOffPartO = 0;                                  // [4][kVMaxNQ][128] f32
+constexpr uint32_t kOffPartML = kOffPartO + 4 * kVMaxNQ * kD * 4;  // [2][4][kVMaxNQ] f32
+constexpr uint32_t kOffML = kOffPartML + 2 * 4 * kVMaxNQ * 4;      // [2][kVMaxNQ] f32
+constexpr uint32_t kOffCO = kOffP;                                 // [kVMaxNQ][128] f32
+static_assert(kOffML + 2 * kVMaxNQ * 4 <= kOffP && kVMaxNQ * kD * 4 <= kPBytes, "merge does not fit");
+}  // namespace vtc
+
+struct VerifyTcParams {
+    CUtensorMap tm_k;         // K cache as [B*Hkv][Tmax][128] bf16, boxes of 64 x 64 x 1
+    CUtensorMap tm_v;
+    const __nv_bfloat16* q;   // [B][Lq][Hq][128]
     const int* kv_len;        // [B]
-    float* o;                 // [B][Lq][Hq][D]
+    float* o;                 // [B][Lq][Hq][128]
     float* lse;               // [B][Lq][Hq] or null
     float* part;              // [B*Hkv][n_split][NQ][D+2]
     unsigned* tickets;        // [B*Hkv]
+    int* status;              // MASW_ETIMEOUT if a bounded wait gave up
     int B, Lq, Hq, Hkv, G, NQ, Tmax, n_split;
     float scale_log2;
 };
 
-constexpr int kVD = 128;             // head_dim
-constexpr int kVKeys = 64;           // keys per stage (16 per warp)
-constexpr int kVRowB = kVD * 2;      // bytes per K/V row
-constexpr int kVRowP = kVRowB + 16;  // padded row stride in shared memory: the 8 row addresses of an
-                                     // ldmatrix phase fall in distinct banks, and every k-step's offset
-                                     // is a compile-time immediate (no per-access swizzle arithmetic)
-constexpr int kVStage = 2 * kVKeys * kVRowP;
-constexpr int kVNst = 3;
-constexpr int kVSmem = kVNst * kVStage;
-constexpr int kVMaxSplit = 64;       // bounds the merge scratch kept in shared memory
-constexpr int kVMaxNQ = 32;
-static_assert((2 * 4 * kVMaxNQ + 4 * kVMaxNQ * (kVD + 8) + 2 * kVMaxNQ + kVMaxNQ * kVD +
-               epilogue_scratch_floats(kVMaxNQ, kVMaxSplit)) * 4 <= kVSmem,
-              "verify merge does not fit in the stage buffers");
-
-// 2^x by the MUFU instruction (an input of -inf gives 0)
-__device__ __forceinline__ float ex2_ftz(float x) {
-    float y;
-    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-    return y;
-}
-__device__ __forceinline__ uint32_t pad_off(int row, int chunk) {  // byte offset of a 16-B chunk
-    return (uint32_t)(row * kVRowP + (chunk << 4));
-}
-// three stages for every tile count (two CTAs per SM at three tiles; six stages
-// on one CTA per SM measured slower)
-template <int NT>
-__host__ __device__ constexpr int verify_stages() { return kVNst; }
-template <int NT>
-__host__ __device__ constexpr int verify_smem() { return verify_stages<NT>() * kVStage; }
-
-// NT tiles of 8 query columns; warp w handles keys 16 (w % 4) .. +15 of each
-// stage for column tile w / 4, so a warp keeps one tile's accumulators (about
-// 96 registers) and a CTA has 4 NT warps: more warps in flight than one warp
-// holding every tile.
-template <int NT>
-__global__ void __launch_bounds__(128 * NT) verify_kernel(const __grid_constant__ VerifyParams p) {
-    constexpr int NSTV = verify_stages<NT>();
-    extern __shared__ __align__(128) uint8_t smem[];
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nthr = blockDim.x;
-    const int kg = warp & 3, ct = warp >> 2;   // key group, column tile
+__global__ void __launch_bounds__(192, 2) verify_tc_kernel(const __grid_constant__ VerifyTcParams p) {
+    using namespace vtc;
+    extern __shared__ __align__(1024) uint8_t vsmem[];
+    __shared__ uint64_t bars[kNumBars];
+    __shared__ uint32_t tslot;
+    __shared__ int abort_store;
+    volatile int* abort_flag = &abort_store;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const uint32_t sb = smem_u32(vsmem);
+    auto bar_at = [&](int i) { return smem_u32(bars + i); };
     const int split = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
     const int G = p.G, NQ = p.NQ;
+
     pdl_wait();
     pdl_trigger();
-
     const int n_keys = p.kv_len[b];
-    const int chunk = (((n_keys + p.n_split - 1) / p.n_split) + kVKeys - 1) / kVKeys * kVKeys;
+    const int chunk = ((n_keys + p.n_split - 1) / p.n_split + kBN - 1) / kBN * kBN;
     const int k0 = imin(n_keys, split * chunk);
     const int k1 = imin(n_keys, k0 + chunk);
-    const int nstage = (k1 - k0 + kVKeys - 1) / kVKeys;
+    const int nblk = (k1 - k0 + kBN - 1) / kBN;
+    const int head_row = b * p.Hkv + h;          // third coordinate of the cache tensor maps
 
-    const __nv_bfloat16* kbase = p.k + ((size_t)b * p.Hkv + h) * (size_t)p.Tmax * kVD;
-    const __nv_bfloat16* vbase = p.v + ((size_t)b * p.Hkv + h) * (size_t)p.Tmax * kVD;
-    const uint32_t sbase = smem_u32(smem);
-
-    // one stage = 64 keys of K and V in padded rows; rows past k1 are
-    // zero-filled (src-size 0 reads nothing)
-    auto load_stage = [&](int c) {
-        const uint32_t sk = sbase + (uint32_t)(c % NSTV) * kVStage;
-        const uint32_t sv = sk + kVKeys * kVRowP;
-        const int key0 = k0 + c * kVKeys;
-        for (int idx = tid; idx < kVKeys * 16; idx += nthr) {
-            const int row = idx >> 4, ch = idx & 15;
-            const int key = key0 + row;
-            const bool in = key < k1;
-            const size_t goff = (size_t)(in ? key : k0) * kVD + ch * 8;
-            cp_async16(sk + pad_off(row, ch), kbase + goff, in ? 16 : 0);
-            cp_async16(sv + pad_off(row, ch), vbase + goff, in ? 16 : 0);
-        }
-    };
+    // softmax warps 0-3: this lane's query row (copy `warp`) and the first key
+    // it may not see
+    const bool live = warp < 4 && lane < NQ;
+    const int jpos = lane / G;
+    const int lim = live ? imin(k1, n_keys - p.Lq + 1 + jpos) : k0;
+    uint4 qreg[16];
+    if (warp < 4) {
+        const uint4* qp = reinterpret_cast<const uint4*>(
+            p.q + (((size_t)b * p.Lq + (live ? jpos : 0)) * p.Hq + (size_t)h * G + (live ? lane % G : 0)) * kD);
 #pragma unroll
-    for (int c = 0; c < NSTV - 1; ++c) {
-        if (c < nstage) load_stage(c);
-        cp_async_commit();
+        for (int c = 0; c < 16; ++c) qreg[c] = live ? __ldg(qp + c) : make_uint4(0u, 0u, 0u, 0u);
     }
-
-    // Q^T as B fragments of this warp's column tile: column n = query row
-    // (j = n / G, gi = n % G)
-    uint32_t qb[8][2];
-    {
-        const int n = ct * 8 + (lane >> 2);
-        const bool real = n < NQ;
-        const int j = real ? n / G : 0, gi = real ? n % G : 0;
-        const __nv_bfloat16* qrow = p.q + (((size_t)b * p.Lq + j) * p.Hq + (size_t)h * G + gi) * kVD;
-#pragma unroll
-        for (int ks = 0; ks < 8; ++ks) {
-            const int d = ks * 16 + (lane & 3) * 2;
-            qb[ks][0] = real ? *reinterpret_cast<const uint32_t*>(qrow + d) : 0u;
-            qb[ks][1] = real ? *reinterpret_cast<const uint32_t*>(qrow + d + 8) : 0u;
-        }
+    const bool misaligned = (sb & 1023u) != 0u;
+    if (__syncthreads_or(tid == 0 && misaligned)) {
+        if (tid == 0) atomicExch(p.status, MASW_EINVAL);
+        return;
     }
-    // causal limit of this lane's two columns: key < lim
-    int lim[2];
-#pragma unroll
-    for (int e = 0; e < 2; ++e) {
-        const int n = ct * 8 + (lane & 3) * 2 + e;
-        lim[e] = n < NQ ? imin(k1, n_keys - p.Lq + 1 + n / G) : k1;
+    if (warp == 0) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&tslot)),
+                     "r"(kTmemCols)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
     }
+    if (tid == 0) {
+        for (int i = 0; i < kNumBars; ++i)
+            mbar_init(bars + i, (i == kBarSFree || i == kBarP || i == kBarQ) ? 4 : 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = tslot;
 
-    // this lane's ldmatrix row addresses within a stage (k-step / m-tile add 32 bytes)
-    const uint32_t k_off = pad_off(kg * 16 + (lane & 7) + ((lane >> 3) & 1) * 8, lane >> 4);
-    const uint32_t v_off = pad_off(kg * 16 + (lane & 7) + (lane >> 4) * 8, (lane >> 3) & 1);
-    float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f};
-    float acc[8][4];
+    if (warp >= 4) {
+        if (lane == 0 && nblk > 0) {
+            const bool is_v = warp == 5;
+            int li = 0, lw = 0;   // blocks whose load was issued / waited
+            auto load = [&](int blk) {
+                const int st = blk % kStages;
+                const int bi = is_v ? bar_v(st) : bar_k(st);
+                const uint32_t dst = sb + (is_v ? kOffV : kOffK) + st * kKVBytes;
+                const CUtensorMap* m = is_v ? &p.tm_v : &p.tm_k;
+                mbar_expect_tx(bars + bi, kKVBytes);
+                tma_load_3d(dst, m, 0, k0 + blk * kBN, head_row, bar_at(bi));
+                tma_load_3d(dst + kKVBytes / 2, m, 64, k0 + blk * kBN, head_row, bar_at(bi));
+                li = blk + 1;
+            };
+            for (int blk = 0; blk < imin(2, nblk); ++blk) load(blk);
+            bool ok = true;
+            if (!is_v) {
+                ok = wait_or_abort(bars + kBarQ, 0, abort_flag, p.status);
+                for (int j = 0; ok && j < nblk; ++j) {
+                    const int st = j % kStages;
+                    ok = wait_or_abort(bars + bar_k(st), (uint32_t)(j / kStages) & 1u, abort_flag, p.status);
+                    if (ok) lw = j + 1;
+                    // single S buffer: the softmax must have read S(j-1)
+                    if (ok && j >= 1) ok = wait_or_abort(bars + kBarSFree, (uint32_t)(j - 1) & 1u, abort_flag, p.status);
+                    if (!ok) break;
+                    tc_fence_after();
+                    const uint64_t bd0 = sw128_desc(sb + kOffK + st * kKVBytes, 16, 1024);
 #pragma unroll
-    for (int mt = 0; mt < 8; ++mt) acc[mt][0] = acc[mt][1] = acc[mt][2] = acc[mt][3] = 0.f;
-
-    for (int c = 0; c < nstage; ++c) {
-        cp_async_wait<NSTV - 2>();
-        __syncthreads();
-        {   // refill the stage consumed in the previous iteration
-            const int cn = c + NSTV - 1;
-            if (cn < nstage) load_stage(cn);
-            cp_async_commit();
-        }
-        const uint32_t sk = sbase + (uint32_t)(c % NSTV) * kVStage;
-        const uint32_t sv = sk + kVKeys * kVRowP;
-        const int kw = kg * 16;
-        const int key_tile = k0 + c * kVKeys + kw;
-        if (key_tile < k1) {
-            // two accumulators (even and odd k-steps) halve the dependent MMA chain
-            float s[4] = {0.f, 0.f, 0.f, 0.f}, s2[4] = {0.f, 0.f, 0.f, 0.f};
+                    for (int kk = 0; kk < kD / 16; ++kk)
+                        umma_bf16_ts(tmem + kColS, tmem + kColQ + kk * 8,
+                                     bd0 + (uint64_t)(((kk >> 2) * (kKVBytes / 2) + (kk & 3) * 32) >> 4), kIdescS,
+                                     kk > 0 ? 1u : 0u);
+                    umma_commit(bar_at(kBarS));
+                    // K(j+2) takes the stage of K(j-1), whose S the softmax has read
+                    if (j + 2 < nblk) load(j + 2);
+                }
+            } else {
+                for (int j = 0; ok && j < nblk; ++j) {
+                    const int st = j % kStages;
+                    ok = wait_or_abort(bars + kBarP, (uint32_t)j & 1u, abort_flag, p.status);
+                    if (ok) {
+                        ok = wait_or_abort(bars + bar_v(st), (uint32_t)(j / kStages) & 1u, abort_flag, p.status);
+                        if (ok) lw = j + 1;
+                    }
+                    if (!ok) break;
+                    tc_fence_after();
+                    const uint64_t a0 = sw128_desc(sb + kOffP, 16, 1024);
+                    const uint64_t v0 = sw128_desc(sb + kOffV + st * kKVBytes, kKVBytes / 2, 1024);
 #pragma unroll
-            for (int ks = 0; ks < 8; ++ks) {
-                uint32_t a0, a1, a2, a3;
-                ldsm_x4(sk + k_off + ks * 32, a0, a1, a2, a3);
-                mma16816((ks & 1) ? s2 : s, a0, a1, a2, a3, qb[ks][0], qb[ks][1]);
-            }
-#pragma unroll
-            for (int e = 0; e < 4; ++e) s[e] += s2[e];
-            float x[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) x[e] = s[e] * p.scale_log2;
-            // the causal mask only bites in the tile that crosses the block's
-            // diagonal (warp-uniform test: every key of the tile below every
-            // column's limit)
-            if (!__all_sync(0xffffffffu, key_tile + 16 <= imin(lim[0], lim[1]))) {
-                const int key_a = key_tile + (lane >> 2), key_b = key_a + 8;
-                if (key_a >= lim[0]) x[0] = -INFINITY;
-                if (key_a >= lim[1]) x[1] = -INFINITY;
-                if (key_b >= lim[0]) x[2] = -INFINITY;
-                if (key_b >= lim[1]) x[3] = -INFINITY;
-            }
-            float pr[4];
-#pragma unroll
-            for (int e = 0; e < 2; ++e) {
-                float mx = fmaxf(x[e], x[e + 2]);
-                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
-                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
-                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
-                const float m_new = fmaxf(m_run[e], mx);
-                const float m_use = m_new == -INFINITY ? 0.f : m_new;   // column fully masked so far
-                const float alpha = ex2_ftz(m_run[e] - m_use);
-                pr[e] = ex2_ftz(x[e] - m_use);
-                pr[e + 2] = ex2_ftz(x[e + 2] - m_use);
-                l_run[e] = l_run[e] * alpha + pr[e] + pr[e + 2];
-                m_run[e] = m_new;
-#pragma unroll
-                for (int mt = 0; mt < 8; ++mt) {
-                    acc[mt][e] *= alpha;
-                    acc[mt][e + 2] *= alpha;
+                    for (int kk = 0; kk < kBN / 16; ++kk)
+                        umma_bf16(tmem + kColO, a0 + (uint64_t)((kk * 32) >> 4), v0 + (uint64_t)((kk * 2048) >> 4),
+                                  kIdescO, (j > 0 || kk > 0) ? 1u : 0u);
+                    umma_commit(bar_at(kBarO));
+                    // P(j) written means the softmax saw PV(j-1) complete:
+                    // V(j+2) takes the stage of V(j-1)
+                    if (j + 2 < nblk) load(j + 2);
                 }
             }
-            const uint32_t pb0 = movmatrix_t(pack_bf16(pr[0], pr[1]));
-            const uint32_t pb1 = movmatrix_t(pack_bf16(pr[2], pr[3]));
-#pragma unroll
-            for (int mt = 0; mt < 8; ++mt) {
-                uint32_t a0, a1, a2, a3;
-                ldsm_x4_t(sv + v_off + mt * 32, a0, a1, a2, a3);
-                mma16816(acc[mt], a0, a1, a2, a3, pb0, pb1);
+            if (!ok) {
+                // early exit: let this thread's MMAs and loads in flight finish
+                // before the CTA releases its tensor and shared memory
+                *abort_flag = 1;
+                const int done = is_v ? kBarDoneV : kBarDone;
+                umma_commit(bar_at(done));
+                mbar_wait(bars + done, 0, nullptr);
+                for (int blk = lw; blk < li; ++blk)
+                    mbar_wait(bars + (is_v ? bar_v(blk % kStages) : bar_k(blk % kStages)),
+                              (uint32_t)(blk / kStages) & 1u, nullptr);
             }
         }
-    }
-    cp_async_wait<0>();
-    __syncthreads();
+        __syncwarp();
+    } else {
+        // ------- softmax warp w: lane n owns copy w of query row n, columns 16 w .. 16 w + 15 -------
+        const int w = warp;
+        const uint32_t lane_off = (uint32_t)(w * 32) << 16;
+        const uint32_t t_o = tmem + kColO + lane_off;
+        // Q row -> tensor memory (zeros for lanes past NQ), the A operand of S
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+            uint32_t qv[32];
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+                const uint4 x = qreg[hh * 8 + c];
+                qv[4 * c] = x.x;
+                qv[4 * c + 1] = x.y;
+                qv[4 * c + 2] = x.z;
+                qv[4 * c + 3] = x.w;
+            }
+            tmem_st32(tmem + kColQ + lane_off + hh * 32, qv);
+        }
+        // this row's P outside the warp's 16 columns stays zero: written once
+        const uint32_t prow = sb + kOffP + (uint32_t)(w * 32 + lane) * 128u;
+#pragma unroll
+        for (int c = 0; c < 8; ++c)
+            if ((c >> 1) != w) st_shared_v4(prow + ((uint32_t)(c ^ (lane & 7)) << 4), 0u, 0u, 0u, 0u);
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar_at(kBarQ));
+        float m_run = -INFINITY, l_run = 0.f;
+        bool ok = true;
+        for (int j = 0; j < nblk; ++j) {
+            if (!__all_sync(0xffffffffu, wait_or_abort(bars + kBarS, (uint32_t)j & 1u, abort_flag, p.status))) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            uint32_t sv[16];
+            tmem_ld16(tmem + kColS + lane_off + w * 16, sv);
+            tmem_wait_ld();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar_at(kBarSFree));
 
-    // ---- warp results -> shared, then merge the 4 key groups ----
-    constexpr int NQM = NT * 8;
-    constexpr int WS = kVD + 8;                     // padded row stride: conflict-free stores
-    float* wm = reinterpret_cast<float*>(smem);    // [4][NQM]
-    float* wl = wm + 4 * NQM;                       // [4][NQM]
-    float* wo = wl + 4 * NQM;                       // [4][NQM][WS]
-    float* cm = wo + 4 * NQM * WS;                  // [NQM]
-    float* cl = cm + NQM;
-    float* co = cl + NQM;                           // [NQM][D]
-    float* scratch = co + NQM * kVD;
+            // visible columns of this warp's 16 for this row: [0, e_hi) (causal limit)
+            const int key0 = k0 + j * kBN + w * 16;
+            const int e_hi = imin(16, imax(0, lim - key0));
+            float x[16];
 #pragma unroll
-    for (int e = 0; e < 2; ++e) {
-        float l = l_run[e];
-        l += __shfl_xor_sync(0xffffffffu, l, 4);
-        l += __shfl_xor_sync(0xffffffffu, l, 8);
-        l += __shfl_xor_sync(0xffffffffu, l, 16);
-        const int n = ct * 8 + (lane & 3) * 2 + e;
-        if (lane < 4) {
-            wm[kg * NQM + n] = m_run[e];
-            wl[kg * NQM + n] = l;
+            for (int e = 0; e < 16; ++e) x[e] = e < e_hi ? __uint_as_float(sv[e]) : -INFINITY;
+            const float mx = fmax3(fmax3(fmax3(x[0], x[1], x[2]), fmax3(x[3], x[4], x[5]), fmax3(x[6], x[7], x[8])),
+                                   fmax3(x[9], x[10], x[11]), fmax3(fmax3(x[12], x[13], x[14]), x[15], x[15]));
+            // the running max moves only when it grows by more than 2^8, so the O
+            // rescale is rare (exact: the partial is relative to m_run)
+            float alpha = 1.f;
+            const float m_new = fmaxf(m_run, mx * p.scale_log2);
+            if (m_new > m_run + 8.f) {
+                alpha = ex2_approx(m_run - m_new);
+                m_run = m_new;
+            }
+            const float nmref = m_run == -INFINITY ? 0.f : -m_run;
+            const uint64_t sc2 = f2_pack(p.scale_log2, p.scale_log2), nm2 = f2_pack(nmref, nmref);
+            uint32_t pk[8];
+            uint64_t sum2[2] = {0, 0};
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                float a0, a1v;
+                f2_unpack(f2_fma(f2_pack(x[2 * e], x[2 * e + 1]), sc2, nm2), a0, a1v);
+                const float p0 = ex2_approx(a0), p1 = ex2_approx(a1v);
+                sum2[e & 1] = f2_add(sum2[e & 1], f2_pack(p0, p1));
+                pk[e] = pack_bf16(p0, p1);
+            }
+            float sum_lo, sum_hi;
+            f2_unpack(f2_add(sum2[0], sum2[1]), sum_lo, sum_hi);
+            const bool resc = alpha != 1.f && l_run > 0.f;
+            l_run = l_run * alpha + (sum_lo + sum_hi);
+
+            // PV(j-1) must be complete before O is rescaled and P is overwritten
+            if (j > 0) {
+                if (!__all_sync(0xffffffffu,
+                                wait_or_abort(bars + kBarO, (uint32_t)(j - 1) & 1u, abort_flag, p.status))) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+            }
+            if (__any_sync(0xffffffffu, resc)) {
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    uint32_t ov[32];
+                    tmem_ld32(t_o + c * 32, ov);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * alpha);
+                    tmem_st32(t_o + c * 32, ov);
+                }
+                tmem_wait_st();
+            }
+            // this warp's two 16-byte chunks of the row (128-byte swizzle)
+            st_shared_v4(prow + ((uint32_t)((2 * w) ^ (lane & 7)) << 4), pk[0], pk[1], pk[2], pk[3]);
+            st_shared_v4(prow + ((uint32_t)((2 * w + 1) ^ (lane & 7)) << 4), pk[4], pk[5], pk[6], pk[7]);
+            fence_async_smem();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar_at(kBarP));
         }
+        if (ok && nblk > 0)
+            ok = __all_sync(0xffffffffu, wait_or_abort(bars + kBarO, (uint32_t)(nblk - 1) & 1u, abort_flag, p.status));
+        tc_fence_after();
+        // this copy's partial O row and (max, sum) -> the stage buffers (idle now)
+        float* po = reinterpret_cast<float*>(vsmem + kOffPartO) + ((size_t)w * kVMaxNQ + lane) * kD;
+        float* pml = reinterpret_cast<float*>(vsmem + kOffPartML);
 #pragma unroll
-        for (int mt = 0; mt < 8; ++mt) {
-            const int d = mt * 16 + (lane >> 2);
-            wo[(kg * NQM + n) * WS + d] = acc[mt][e];
-            wo[(kg * NQM + n) * WS + d + 8] = acc[mt][e + 2];
+        for (int c = 0; c < 4; ++c) {
+            uint32_t ov[32];
+            if (nblk > 0) {
+                tmem_ld32(t_o + c * 32, ov);
+                tmem_wait_ld();
+            }
+            if (live) {
+#pragma unroll
+                for (int e = 0; e < 32; e += 4)
+                    *reinterpret_cast<float4*>(po + c * 32 + e) =
+                        nblk > 0 ? make_float4(__uint_as_float(ov[e]), __uint_as_float(ov[e + 1]),
+                                               __uint_as_float(ov[e + 2]), __uint_as_float(ov[e + 3]))
+                                 : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+        }
+        if (live) {
+            pml[w * kVMaxNQ + lane] = m_run;
+            pml[(4 + w) * kVMaxNQ + lane] = l_run;
         }
     }
-    __syncthreads();
-    if (tid < NQ) {
+    tc_fence_before();
+    const bool aborted = __syncthreads_or(tid == 0 && *abort_flag != 0);
+    if (warp == 0) {
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols) : "memory");
+    }
+    if (aborted) return;   // outputs of this call are undefined; p.status says why
+    // merge the four copies of each row: M = max_w m_w, weights 2^(m_w - M)
+    const float* pml = reinterpret_cast<const float*>(vsmem + kOffPartML);
+    const float* po = reinterpret_cast<const float*>(vsmem + kOffPartO);
+    float* cm = reinterpret_cast<float*>(vsmem + kOffML);
+    float* cl = cm + kVMaxNQ;
+    float* co = reinterpret_cast<float*>(vsmem + kOffCO);
+    for (int i = tid; i < NQ * kD; i += blockDim.x) {
+        const int n = i / kD, d = i % kD;
         float M = -INFINITY;
-        for (int w = 0; w < 4; ++w) M = fmaxf(M, wm[w * NQM + tid]);
-        float l = 0.f;
-        for (int w = 0; w < 4; ++w)
-            if (wm[w * NQM + tid] != -INFINITY) l += exp2f(wm[w * NQM + tid] - M) * wl[w * NQM + tid];
-        cm[tid] = M;
-        cl[tid] = l;
-    }
-    __syncthreads();
-    for (int i = tid; i < NQ * kVD; i += nthr) {
-        const int n = i / kVD;
-        const float M = cm[n];
-        float a = 0.f;
-        for (int w = 0; w < 4; ++w)
-            if (wm[w * NQM + n] != -INFINITY) a += exp2f(wm[w * NQM + n] - M) * wo[(w * NQM + n) * WS + (i % kVD)];
+#pragma unroll
+        for (int w = 0; w < 4; ++w) M = fmaxf(M, pml[w * kVMaxNQ + n]);
+        float a = 0.f, l = 0.f;
+#pragma unroll
+        for (int w = 0; w < 4; ++w) {
+            const float mw = pml[w * kVMaxNQ + n];
+            const float e = mw == -INFINITY ? 0.f : ex2_approx(mw - M);
+            a += e * po[((size_t)w * kVMaxNQ + n) * kD + d];
+            l += e * pml[(4 + w) * kVMaxNQ + n];
+        }
         co[i] = a;
+        if (d == 0) {
+            cm[n] = M;
+            cl[n] = l;
+        }
     }
     __syncthreads();
-
     EpiOut out;
-    out.o = p.o + ((size_t)b * p.Lq * p.Hq + (size_t)h * G) * kVD;
+    out.o = p.o + ((size_t)b * p.Lq * p.Hq + (size_t)h * G) * kD;
     out.lse = p.lse ? p.lse + (size_t)b * p.Lq * p.Hq + (size_t)h * G : nullptr;
     out.rows_per_group = G;
-    out.o_row_stride = kVD;
-    out.o_group_stride = p.Hq * kVD;
+    out.o_row_stride = kD;
+    out.o_group_stride = p.Hq * kD;
     out.lse_row_stride = 1;
     out.lse_group_stride = p.Hq;
     out.o_alt = nullptr;
     out.lse_alt = nullptr;
     out.alt_from = -1;
-    float* part = p.part + (size_t)(b * p.Hkv + h) * p.n_split * NQ * (kVD + 2);
-    split_epilogue<kVD>(NQ, cm, cl, co, out, part, p.tickets + b * p.Hkv + h, split, p.n_split, scratch);
+    float* part = p.part + (size_t)head_row * p.n_split * NQ * (kD + 2);
+    split_epilogue<kD>(NQ, cm, cl, co, out, part, p.tickets + head_row, split, p.n_split, nullptr);
 }
 
-template <int NT>
-static cudaError_t verify_configure(int* n) {
-    cudaError_t e = cudaFuncSetAttribute(verify_kernel<NT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         verify_smem<NT>());
-    if (e == cudaSuccess)
-        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(n, verify_kernel<NT>, 128 * NT, verify_smem<NT>());
-    return e;
-}
-
-// Resident verify CTAs per SM for NT query tiles (cached per device).
-static int verify_occupancy(int NT) {
-    static std::atomic<int> cache[64][5];   // per device and tile count (idempotent fill)
+// Resident tensor-core verify CTAs per SM: the occupancy query, and the bound
+// from the kernel's attributes (shared memory with the per-block reserve), at
+// most two (256 tensor-memory columns each).
+static int verify_tc_occupancy() {
+    static std::atomic<int> cache[64];
     int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64 || NT < 1 || NT > 4) return 1;
-    if (!cache[dev][NT].load(std::memory_order_acquire)) {
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 1;
+    if (!cache[dev].load(std::memory_order_acquire)) {
         int n = 0;
-        cudaError_t e = cudaSuccess;
-        switch (NT) {
-            case 1: e = verify_configure<1>(&n); break;
-            case 2: e = verify_configure<2>(&n); break;
-            case 3: e = verify_configure<3>(&n); break;
-            default: e = verify_configure<4>(&n); break;
+        if (cudaFuncSetAttribute(verify_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, vtc::kSmem) !=
+                cudaSuccess ||
+            cudaFuncSetAttribute(verify_tc_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                 cudaSharedmemCarveoutMaxShared) != cudaSuccess ||
+            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, verify_tc_kernel, 192, vtc::kSmem) != cudaSuccess) {
+            cudaGetLastError();
+            n = 1;
         }
-        if (e != cudaSuccess) cudaGetLastError();
-        cache[dev][NT].store(n > 0 ? n : 1, std::memory_order_release);
+        cudaFuncAttributes fa;
+        int smem_sm = 0, smem_rsv = 0;
+        if (cudaFuncGetAttributes(&fa, verify_tc_kernel) == cudaSuccess &&
+            cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) == cudaSuccess &&
+            cudaDeviceGetAttribute(&smem_rsv, cudaDevAttrReservedSharedMemoryPerBlock, dev) == cudaSuccess) {
+            const long long per = (long long)vtc::kSmem + fa.sharedSizeBytes + smem_rsv;
+            n = imax(n, (int)(smem_sm / per));
+        } else {
+            cudaGetLastError();
+        }
+        cache[dev].store(imax(1, imin(n, 2)), std::memory_order_release);
     }
-    return cache[dev][NT].load(std::memory_order_acquire);
+    return cache[dev].load(std::memory_order_acquire);
 }
 
 // Split count shared by the launcher and the workspace query: one wave of the
 // resident CTA slots, at least 256 keys per split.
 static int verify_splits(int B, int Hkv, int Tmax, int num_sms, int NT) {
+    (void)NT;
     const int pairs = B * Hkv;
-    const int slots = verify_occupancy(NT) * num_sms;
+    const int slots = verify_tc_occupancy() * num_sms;
     int n = imax(1, slots / pairs);
     n = imin(n, imax(1, (Tmax + 255) / 256));
     return imin(n, kVMaxSplit);
@@ -346,23 +472,56 @@ extern "C" int masw_verify_workspace_bytes(int B, int Lq, int Hq, int Hkv, int D
     if (num_sms_current(&sms)) return masw_set_error(nullptr, MASW_ECUDA, "cannot query the current device");
     const int NQ = (Hq / Hkv) * Lq;
     const int n_split = verify_splits(B, Hkv, Tmax, sms, (NQ + 7) / 8);
-    *bytes = verify_part_bytes(B, Hkv, NQ, n_split) + (size_t)B * Hkv * sizeof(unsigned);
+    *bytes = verify_part_bytes(B, Hkv, NQ, n_split) + (size_t)B * Hkv * sizeof(unsigned) + 16;
     return MASW_OK;
 }
 
-template <int NT>
-static cudaError_t launch_verify(const VerifyParams& prm, cudaStream_t stream) {
-    static std::atomic<bool> configured[64];   // per device, set once (idempotent)
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (!configured[dev & 63].load(std::memory_order_acquire)) {
-        cudaError_t e = cudaFuncSetAttribute(verify_kernel<NT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             verify_smem<NT>());
-        if (e != cudaSuccess) return e;
-        configured[dev & 63].store(true, std::memory_order_release);
-    }
-    return masw_launch(verify_kernel<NT>, dim3(prm.n_split, prm.Hkv, prm.B), dim3(128 * NT), verify_smem<NT>(),
-                       stream, 1, prm);
+// K or V cache [B][Hkv][Tmax][128] bf16 as a 3-d tensor [B*Hkv][Tmax][128]
+// (head_dim innermost), boxes of 64 x 64 x 1 with the 128-byte swizzle the MMA
+// descriptors use; rows past Tmax read as zeros
+static bool make_cache_map(CUtensorMap* map, const void* base, int Tmax, int heads_total) {
+    const cuuint64_t dims[3] = {128, (cuuint64_t)Tmax, (cuuint64_t)heads_total};
+    const cuuint64_t strides[2] = {256, (cuuint64_t)Tmax * 256};
+    const cuuint32_t box[3] = {64, 64, 1};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    return tma_encode_fn()(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// The tensor-core verify kernel on (q, caches, scratch); scratch = [partials
+// (part_bytes)][tickets, one per (sequence, kv head)][status word].
+static int launch_verify_tc(const void* q, const void* k_cache, const void* v_cache, const int* kv_len, int B,
+                            int Lq, int Hq, int Hkv, int Tmax, float scale_log2, float* o, float* lse, void* scratch,
+                            size_t part_bytes, int n_split, cudaStream_t st, const char* who) {
+    if (!tma_encode_fn()) return masw_set_error(nullptr, MASW_ECUDA, std::string(who) + ": cuTensorMapEncodeTiled is unavailable");
+    if ((long long)B * Hkv > 0x7fffffff || (long long)Tmax * 256 >= (1ll << 40))
+        return masw_set_error(nullptr, MASW_EINVAL, std::string(who) + ": cache too large for a tensor map");
+    VerifyTcParams prm;
+    std::memset(&prm, 0, sizeof(prm));
+    if (!make_cache_map(&prm.tm_k, k_cache, Tmax, B * Hkv) || !make_cache_map(&prm.tm_v, v_cache, Tmax, B * Hkv))
+        return masw_set_error(nullptr, MASW_EINVAL, std::string(who) + ": cannot describe the caches as TMA tensors");
+    prm.q = (const __nv_bfloat16*)q;
+    prm.kv_len = kv_len;
+    prm.o = o;
+    prm.lse = lse;
+    prm.part = (float*)scratch;
+    prm.tickets = (unsigned*)((uint8_t*)scratch + part_bytes);
+    prm.status = (int*)(prm.tickets + (size_t)B * Hkv);
+    prm.B = B;
+    prm.Lq = Lq;
+    prm.Hq = Hq;
+    prm.Hkv = Hkv;
+    prm.G = Hq / Hkv;
+    prm.NQ = prm.G * Lq;
+    prm.Tmax = Tmax;
+    prm.n_split = n_split;
+    prm.scale_log2 = scale_log2;
+    verify_tc_occupancy();   // sets the kernel's shared-memory attributes once per device
+    const cudaError_t e =
+        masw_launch(verify_tc_kernel, dim3(n_split, Hkv, B), dim3(192), vtc::kSmem, st, 1, prm);
+    if (e != cudaSuccess) return masw_set_error(nullptr, MASW_ECUDA, std::string(who) + ": " + cudaGetErrorString(e));
+    return MASW_OK;
 }
 
 extern "C" int masw_verify_attn(const void* q, const void* k_cache, const void* v_cache, const int* kv_len, int B,
@@ -382,41 +541,14 @@ extern "C" int masw_verify_attn(const void* q, const void* k_cache, const void* 
     const int G = Hq / Hkv, NQ = G * Lq;
     const int n_split = verify_splits(B, Hkv, Tmax, sms, (NQ + 7) / 8);
     const size_t partb = verify_part_bytes(B, Hkv, NQ, n_split);
-    if (workspace_bytes < partb + (size_t)B * Hkv * sizeof(unsigned))
+    if (workspace_bytes < partb + (size_t)B * Hkv * sizeof(unsigned) + 16)
         return masw_set_error(nullptr, MASW_EINVAL, "verify: workspace too small");
-    VerifyParams prm;
-    std::memset(&prm, 0, sizeof(prm));
-    prm.q = (const __nv_bfloat16*)q;
-    prm.k = (const __nv_bfloat16*)k_cache;
-    prm.v = (const __nv_bfloat16*)v_cache;
-    prm.kv_len = kv_len;
-    prm.o = o;
-    prm.lse = lse;
-    prm.part = (float*)workspace;
-    prm.tickets = (unsigned*)((uint8_t*)workspace + partb);
-    prm.B = B;
-    prm.Lq = Lq;
-    prm.Hq = Hq;
-    prm.Hkv = Hkv;
-    prm.G = G;
-    prm.NQ = NQ;
-    prm.Tmax = Tmax;
-    prm.n_split = n_split;
-    prm.scale_log2 = (scale > 0.f ? scale : 1.0f / sqrtf((float)D)) * 1.4426950408889634f;
-    cudaStream_t st = (cudaStream_t)stream;
     // the tickets are zero on entry (zero-filled workspace, reset by the last
     // CTA of each pair in every call): no memset node between calls, so
     // consecutive verify launches keep their programmatic overlap
-    cudaError_t e = cudaSuccess;
-    const int NT = (NQ + 7) / 8;
-    switch (NT) {
-        case 1: e = launch_verify<1>(prm, st); break;
-        case 2: e = launch_verify<2>(prm, st); break;
-        case 3: e = launch_verify<3>(prm, st); break;
-        default: e = launch_verify<4>(prm, st); break;
-    }
-    if (e != cudaSuccess) return masw_set_error(nullptr, MASW_ECUDA, std::string("verify: ") + cudaGetErrorString(e));
-    return MASW_OK;
+    const float sl2 = (scale > 0.f ? scale : 1.0f / sqrtf((float)D)) * 1.4426950408889634f;
+    return launch_verify_tc(q, k_cache, v_cache, kv_len, B, Lq, Hq, Hkv, Tmax, sl2, o, lse, workspace, partb, n_split,
+                            (cudaStream_t)stream, "verify");
 }
 
 // ---------------------------------------------------------------------------
@@ -444,7 +576,7 @@ extern "C" int masw_verify_attn(const void* q, const void* k_cache, const void* 
 namespace masw {
 constexpr size_t kNoAllocPartBytes = (size_t)4 << 20;
 constexpr int kNoAllocMaxPairs = 4096;
-constexpr size_t kNoAllocBytes = kNoAllocPartBytes + (size_t)kNoAllocMaxPairs * sizeof(unsigned);
+constexpr size_t kNoAllocBytes = kNoAllocPartBytes + (size_t)kNoAllocMaxPairs * sizeof(unsigned) + 16;
 }  // namespace masw
 
 static __device__ __align__(256) uint8_t g_noalloc_scratch[masw::kNoAllocBytes];
@@ -497,36 +629,15 @@ extern "C" int masw_verify_attn_noalloc(const void* q, const void* k_cache, cons
     const int G = Hq / Hkv, NQ = G * Lq;
     int n_split = verify_splits(B, Hkv, Tmax, sms, (NQ + 7) / 8);
     while (n_split > 1 && verify_part_bytes(B, Hkv, NQ, n_split) > kNoAllocPartBytes) --n_split;
-    VerifyParams prm;
-    std::memset(&prm, 0, sizeof(prm));
-    prm.q = (const __nv_bfloat16*)q;
-    prm.k = (const __nv_bfloat16*)k_cache;
-    prm.v = (const __nv_bfloat16*)v_cache;
-    prm.kv_len = kv_len;
-    prm.o = o;
-    prm.lse = lse;
-    prm.part = (float*)scratch;
-    prm.tickets = (unsigned*)((uint8_t*)scratch + kNoAllocPartBytes);
-    prm.B = B;
-    prm.Lq = Lq;
-    prm.Hq = Hq;
-    prm.Hkv = Hkv;
-    prm.G = G;
-    prm.NQ = NQ;
-    prm.Tmax = Tmax;
-    prm.n_split = n_split;
-    prm.scale_log2 = (scale > 0.f ? scale : 1.0f / sqrtf((float)D)) * 1.4426950408889634f;
     cudaStream_t st = (cudaStream_t)stream;
-    cudaError_t e = cudaMemsetAsync(prm.tickets, 0, (size_t)B * Hkv * sizeof(unsigned), st);
+    // the library's static array cannot be re-zeroed by the caller after a
+    // failed call, so this variant clears the tickets and the status word on
+    // the stream at the start of every call
+    cudaError_t e = cudaMemsetAsync((uint8_t*)scratch + kNoAllocPartBytes, 0,
+                                    (size_t)kNoAllocMaxPairs * sizeof(unsigned) + 16, st);
     if (e != cudaSuccess)
         return masw_set_error(nullptr, MASW_ECUDA, std::string("verify_noalloc: ") + cudaGetErrorString(e));
-    switch ((NQ + 7) / 8) {
-        case 1: e = launch_verify<1>(prm, st); break;
-        case 2: e = launch_verify<2>(prm, st); break;
-        case 3: e = launch_verify<3>(prm, st); break;
-        default: e = launch_verify<4>(prm, st); break;
-    }
-    if (e != cudaSuccess)
-        return masw_set_error(nullptr, MASW_ECUDA, std::string("verify_noalloc: ") + cudaGetErrorString(e));
-    return MASW_OK;
+    const float sl2 = (scale > 0.f ? scale : 1.0f / sqrtf((float)D)) * 1.4426950408889634f;
+    return launch_verify_tc(q, k_cache, v_cache, kv_len, B, Lq, Hq, Hkv, Tmax, sl2, o, lse, scratch, kNoAllocPartBytes,
+                            n_split, st, "verify_noalloc");
 }

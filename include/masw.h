@@ -242,8 +242,10 @@ int masw_full_step(masw_mem_t* mem, int layer, const void* q, const void* k, con
  * masw_verify_workspace_bytes() bytes, zero-filled by the caller before its
  * first use; every completed call leaves it zero-filled again (the last CTA of
  * each (sequence, kv head) resets its ticket), so a workspace is reused without
- * a memset between calls.  A call that ended with an error (for example
- * MASW_ETIMEOUT from masw_sync) may leave it dirty: zero-fill it before reuse.
+ * a memset between calls.  The int at byte offset
+ * masw_verify_workspace_bytes() - 16 is a status word: 0, or MASW_ETIMEOUT
+ * when a bounded wait inside the kernel gave up (that call's outputs are then
+ * undefined, and the workspace must be zero-filled again before reuse).
  * It must not be shared by calls that overlap on the GPU.  scale 0 -> 1/sqrt(D).
  * D must be 128 and (Hq/Hkv) * Lq <= 32. */
 int masw_verify_attn(const void* q, const void* k_cache, const void* v_cache,

@@ -445,8 +445,8 @@ def test_verify_workspace_reuse_leaves_tickets_zero():
         torch.cuda.synchronize()
         want, _ = orc.verify_attn(q.float().numpy(), k.float().numpy(), v.float().numpy(), kv_len, None)
         assert_close(o, want, "bf16", f"verify call {call}")
-        tickets = ws[need - B * Hkv * 4:].view(torch.int32)
-        assert int(tickets.abs().sum()) == 0, f"call {call} left tickets {tickets.tolist()}"
+        tail = ws[need - 16 - B * Hkv * 4:].view(torch.int32)   # tickets, then the status word
+        assert int(tail.abs().sum()) == 0, f"call {call} left tickets/status {tail.tolist()}"
 
 
 def test_verify_peaky_softmax_and_scale():
