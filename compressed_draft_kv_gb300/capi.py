@@ -214,6 +214,9 @@ def masw_verify_workspace_bytes(B, Lq, Hq, Hkv, D, Tmax) -> int:
 
 
 def masw_verify_attn(q, k_cache, v_cache, kv_len, o, lse=None, workspace=None, scale=0.0, stream=None):
+    """q [B, Lq, Hq, D] bf16, caches [B, Hkv, Tmax, D] bf16, kv_len [B] int32 -> o [B, Lq, Hq, D] fp32.
+    A caller's workspace (uint8, at least masw_verify_workspace_bytes) must be zero-filled before its first
+    use; every completed call leaves it zero-filled.  Without one, a zero-filled workspace is allocated."""
     B, Lq, Hq, D = q.shape
     Hkv, Tmax = k_cache.shape[1], k_cache.shape[2]
     need = masw_verify_workspace_bytes(B, Lq, Hq, Hkv, D, Tmax)
