@@ -1,10 +1,10 @@
 // Target verify attention over an uncompressed cache ([EN] §3.3 Algorithm 2
 // step 5): Lq query positions per sequence, causal inside the block, GQA.
 //
-// This is the one dense contraction on the path (the Lq*G query rows of a kv
-// head share every K/V row: 24 flop per byte at Lq = 6, G = 4), so it runs on
-// the fifth-generation tensor cores with TMA and tensor memory (the machinery
-// of the draft prefill): per (key split, kv head, sequence) one CTA streams its
+// Like the draft prefill this is a dense contraction (the Lq*G query rows of a
+// kv head share every K/V row: 24 flop per byte at Lq = 6, G = 4), so it runs
+// on the fifth-generation tensor cores with TMA and tensor memory (the
+// prefill's machinery): per (key split, kv head, sequence) one CTA streams its
 // keys in blocks of 64 and keeps S, O and Q in tensor memory; splits over the
 // key axis are merged by split_epilogue.
 #include "masw_internal.cuh"
