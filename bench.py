@@ -667,7 +667,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="masw", choices=["masw", "reference"])
     ap.add_argument("--workload", default=WORKLOAD,
-                    choices=["draft3b_28l_b8", "draft8b_b32_ragged", "draft3b_1layer_8k", "paper_s128_w128_r4",
+                    choices=["draft3b_28l_b8", "draft3b_28l_b1", "draft8b_b32_ragged", "draft3b_1layer_8k", "paper_s128_w128_r4",
                              "paper_s128_w128_r8"])
     ap.add_argument("--prefix", type=int, default=None, help="override the prefix (all sequences)")
     ap.add_argument("--sweep", action="store_true",

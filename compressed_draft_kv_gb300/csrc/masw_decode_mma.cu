@@ -95,6 +95,10 @@ __device__ __forceinline__ bool recv_wait(uint64_t* bar, int* err) {
     return false;
 }
 
+// largest thread-block cluster of the split merge (16 needs the non-portable
+// cluster-size attribute; larger sizes fall back to the ticket merge)
+constexpr int kMaxClusterSize = 16;
+
 template <int ROWB>
 __device__ __forceinline__ uint32_t swz_off(int row, int ch) {
     return (uint32_t)(row * ROWB + ((ch ^ (row & 7)) << 4));
@@ -140,8 +144,8 @@ __global__ void __launch_bounds__(128, NST_ == 2 ? 3 : 2) decode_mma_kernel(cons
     // cluster merge receive buffers (written by peer CTAs with st.async; never
     // aliased with the stages): (max, sum) per (rank, row), the o slices, and the
     // mbarrier their bytes count down
-    __shared__ __align__(16) float2 r_ml[64];
-    __shared__ __align__(16) float r_o[8 * D + 32];
+    __shared__ __align__(16) float2 r_ml[kMaxClusterSize * 8];
+    __shared__ __align__(16) float r_o[8 * D + 4 * kMaxClusterSize];
     __shared__ uint64_t r_bar;
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -488,18 +492,16 @@ __global__ void __launch_bounds__(128, NST_ == 2 ? 3 : 2) decode_mma_kernel(cons
             for (int i = lo + tid; i < hi; i += 128) {
                 const int n = i / D;
                 float M = -INFINITY;
-#pragma unroll
-                for (int r = 0; r < 8; ++r)
-                    if (r < nc) M = fmaxf(M, r_ml[r * 8 + n].x);
+                for (int r = 0; r < nc; ++r) M = fmaxf(M, r_ml[r * 8 + n].x);
                 float a = 0.f, dn = 0.f;
-#pragma unroll
-                for (int r = 0; r < 8; ++r) {
-                    if (r < nc) {
-                        const float2 ml = r_ml[r * 8 + n];
-                        const float wr = ml.x == -INFINITY ? 0.f : fast_ex2(ml.x - M);
-                        dn += wr * ml.y;
-                        a += wr * r_o[r * per + (i - lo)];
-                    }
+                // runtime bound: unrolled over 16 predicated ranks this loop cost
+                // 2% of a launch at 6 ranks
+#pragma unroll 4
+                for (int r = 0; r < nc; ++r) {
+                    const float2 ml = r_ml[r * 8 + n];
+                    const float wr = ml.x == -INFINITY ? 0.f : fast_ex2(ml.x - M);
+                    dn += wr * ml.y;
+                    a += wr * r_o[r * per + (i - lo)];
                 }
                 out.optr(n)[i % D] = dn > 0.f ? __fdividef(a, dn) : 0.f;
             }
@@ -555,8 +557,8 @@ __global__ void __launch_bounds__(128, NST_ == 2 ? 3 : 2) decode_mma_kernel(cons
 // Clusters of `cs` CTAs of the decode kernel that can be resident at once (cached per device).
 template <int D, int NST>
 static int max_clusters(masw_mem_t* mem, int dev, int cs) {
-    static std::atomic<int> cache[64][9];   // per device and cluster size (idempotent fill)
-    if (cs < 2 || cs > 8) return 0;
+    static std::atomic<int> cache[64][kMaxClusterSize + 1];   // per device and cluster size (idempotent fill)
+    if (cs < 2 || cs > kMaxClusterSize) return 0;
     if (!cache[dev][cs].load(std::memory_order_acquire)) {
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3(cs * 64, 1, 1);
@@ -597,6 +599,10 @@ static int plan_mma(masw_mem_t* mem, int rows, int GR, int kmax, MmaPlan& pl) {
     if (!occ[dev].load(std::memory_order_acquire)) {
         MASW_CUDA_TRY(mem, cudaFuncSetAttribute(decode_mma_kernel<D, NST>,
                                                 cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM));
+        // clusters of up to 16 CTAs (beyond the portable 8) for few long pairs
+        if (cudaFuncSetAttribute(decode_mma_kernel<D, NST>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) !=
+            cudaSuccess)
+            cudaGetLastError();
         int n = 0;
         MASW_CUDA_TRY(mem, cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_mma_kernel<D, NST>, 128, C::SMEM));
         occ[dev].store(n > 0 ? n : 1, std::memory_order_release);
@@ -606,8 +612,12 @@ static int plan_mma(masw_mem_t* mem, int rows, int GR, int kmax, MmaPlan& pl) {
     const int max_useful = imax(1, (kmax + 63) / 64);
     pl.n_split = 1;
     pl.cluster = false;
-    for (int cs = imin(8, imin(max_useful, slots / imax(1, pairs))); cs >= 2; --cs) {
-        if (cs * pairs * 2 >= slots && max_clusters<D, NST>(mem, dev, cs) >= pairs) {
+    // a cluster size is taken when its grid fills at least half the resident
+    // slots, or when it already covers every useful split of a pair (few
+    // sequences: the shared-memory merge replaces the global ticket merge)
+    for (int cs = imin(kMaxClusterSize, imin(max_useful, slots / imax(1, pairs))); cs >= 2; --cs) {
+        if ((cs * pairs * 2 >= slots || cs >= imin(kMaxClusterSize, max_useful)) &&
+            max_clusters<D, NST>(mem, dev, cs) >= pairs) {
             pl.n_split = cs;
             pl.cluster = true;
             break;

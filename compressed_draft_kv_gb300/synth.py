@@ -20,6 +20,9 @@ WORKLOADS = {
                               dtype="bf16", seed=1, steps=5),
     "draft3b_28l_b8": dict(Hq=24, Hkv=8, D=128, layers=28, batch=8, prefix=32768, S=4, W=1024, r=512,
                            dtype="bf16", seed=2, steps=5),
+    # the pages' decoding setting: one sequence at a time
+    "draft3b_28l_b1": dict(Hq=24, Hkv=8, D=128, layers=28, batch=1, prefix=32768, S=4, W=1024, r=512,
+                           dtype="bf16", seed=7, steps=5),
     "verify8b_32k": dict(Hq=32, Hkv=8, D=128, layers=32, batch=4, prefix=32768, Lq=6,
                          dtype="bf16", seed=3),
     # the pages' own memory configuration: S = W = 128 and nominal 4x / 8x
