@@ -612,24 +612,22 @@ static int plan_mma(masw_mem_t* mem, int rows, int GR, int kmax, MmaPlan& pl) {
     const int max_useful = imax(1, (kmax + 63) / 64);
     pl.n_split = 1;
     pl.cluster = false;
+    // the ticket-merged plan's split count, for comparison
+    int ticket_split = imin(imin(imax(1, slots / pairs), max_useful), kMaxSplit);
+    while (ticket_split > 1 && masw_decode_part_floats(rows, mem->Hkv, GR, D, ticket_split) > mem->part_floats)
+        --ticket_split;
     // a cluster size is taken when its grid fills at least half the resident
-    // slots, or when it already covers every useful split of a pair (few
-    // sequences: the shared-memory merge replaces the global ticket merge)
+    // slots, or when it has at least half the ticket plan's splits (few
+    // sequences with short working sets: the shared-memory merge replaces the
+    // global ticket merge; long runs keep the ticket plan's many splits)
     for (int cs = imin(kMaxClusterSize, imin(max_useful, slots / imax(1, pairs))); cs >= 2; --cs) {
-        if ((cs * pairs * 2 >= slots || cs >= imin(kMaxClusterSize, max_useful)) &&
-            max_clusters<D, NST>(mem, dev, cs) >= pairs) {
+        if ((cs * pairs * 2 >= slots || 2 * cs >= ticket_split) && max_clusters<D, NST>(mem, dev, cs) >= pairs) {
             pl.n_split = cs;
             pl.cluster = true;
             break;
         }
     }
-    if (!pl.cluster) {
-        int n_split = imax(1, slots / pairs);
-        n_split = imin(n_split, max_useful);
-        n_split = imin(n_split, kMaxSplit);
-        while (n_split > 1 && masw_decode_part_floats(rows, mem->Hkv, GR, D, n_split) > mem->part_floats) --n_split;
-        pl.n_split = n_split;
-    }
+    if (!pl.cluster) pl.n_split = ticket_split;
     return MASW_OK;
 }
 
