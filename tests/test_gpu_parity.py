@@ -599,6 +599,32 @@ def test_fused_steps_full_size_sampled(Hq):
         p.close()
 
 
+@pytest.mark.parametrize("Hq", [24, 32])
+def test_fused_steps_one_sequence(Hq):
+    """One sequence (8 kv heads, 8K prefix, S=4, W=1024, r=512): each (sequence,
+    head) pair runs as a cluster of 16 CTAs merging in shared memory; fused
+    steps, and at tau_14 = 8196 the fused boundary step (2G = 6 or 8 query
+    columns per pair), across two layers, all rows checked against the oracle."""
+    S, W, r, t0 = 4, 1024, 512, 8192
+    B, L, Hkv, D = 1, 2, 8, 128
+    p = Pair(S, W, r, Hkv, D, L, B, "bf16", Hq, max_seq_len=t0 + 16, tag=f"fs1_{Hq}")
+    try:
+        for l in range(L):
+            p.load(l, 0, t0, seed=4 + l)
+        for step in range(1, 7):
+            p.step = step
+            for l in range(L):
+                if orc.is_boundary(p.ref.t(l, 0) + 1, S, W, r):
+                    p.fstep_slot(l, [0])
+                else:
+                    p.fstep(l)
+        for l in range(L):
+            p.check_state(l, 0)
+            assert p.ref.m(l, 0) == 14
+    finally:
+        p.close()
+
+
 def test_draft8b_large_batch_long_runs_sampled():
     """The large-batch launch shape (batch 32, 32q/8kv, W = 2048, r = 1024,
     ragged prefixes 16K..32K): one split per (sequence, head) streams ~2080 keys,
