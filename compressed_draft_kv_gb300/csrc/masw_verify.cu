@@ -349,7 +349,8 @@ __global__ void __launch_bounds__(192, 2) verify_tc_kernel(const __grid_constant
         }
     }
     tc_fence_before();
-    const bool aborted = __syncthreads_or(tid == 0 && *abort_flag != 0);
+    // every thread reads the flag: one that set it counts itself in
+    const bool aborted = __syncthreads_or(*abort_flag != 0);
     if (warp == 0) {
         tc_fence_after();
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols) : "memory");
