@@ -160,12 +160,14 @@ def workload_prefixes(w: dict, synth) -> list[int]:
 class DraftBench:
     """One speculative draft iteration of a workload, captured as a CUDA graph."""
 
-    def __init__(self, torch, capi, synth, workload: str, prefix: int | None = None):
+    def __init__(self, torch, capi, synth, workload: str, prefix: int | None = None, batch: int | None = None):
         self.torch, self.capi = torch, capi
         w = dict(synth.WORKLOADS[workload])
         if prefix is not None:
             w["prefix"] = prefix
             w.pop("prefix_lo", None)
+        if batch is not None:
+            w["batch"] = batch
         self.w = w
         self.L, self.B, self.Hq, self.Hkv, self.D = w["layers"], w["batch"], w["Hq"], w["Hkv"], w["D"]
         self.S, self.W, self.r = w["S"], w["W"], w["r"]
@@ -670,6 +672,7 @@ def main():
                     choices=["draft3b_28l_b8", "draft3b_28l_b1", "draft8b_b32_ragged", "draft3b_1layer_8k", "paper_s128_w128_r4",
                              "paper_s128_w128_r8"])
     ap.add_argument("--prefix", type=int, default=None, help="override the prefix (all sequences)")
+    ap.add_argument("--batch", type=int, default=None, help="override the number of sequences")
     ap.add_argument("--sweep", action="store_true",
                     help="MASW vs full-KV decode steps/s at prefixes 4K..32K (one JSON line)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -689,7 +692,11 @@ def main():
     local = int(os.environ.get("LOCAL_RANK", "0"))
 
     from compressed_draft_kv_gb300 import synth
-    wl = synth.WORKLOADS[args.workload]
+    wl = dict(synth.WORKLOADS[args.workload])
+    if args.batch is not None:
+        if args.batch < 1:
+            raise SystemExit("--batch must be at least 1")
+        wl["batch"] = args.batch
     prefix = args.prefix or wl.get("prefix", 32768)
 
     if args.profile_case:
@@ -760,7 +767,7 @@ def main():
                               "sweep": rows}))
         return
 
-    bench = DraftBench(torch, capi, synth, args.workload, args.prefix)
+    bench = DraftBench(torch, capi, synth, args.workload, args.prefix, args.batch)
     g_draft, launches = bench.capture(bench.iteration)
     g_full, launches_full = bench.capture(lambda: bench.iteration(full=True))
     full_iters = max(3, args.steps // 5)
@@ -799,7 +806,8 @@ def main():
     peak, peak_kind = _peaks()
     achieved = total_b / kern_s / 1e9
     line = {
-        "metric": METRIC if args.workload == WORKLOAD else f"MASW draft-attn decode steps/s ({args.workload})",
+        "metric": (METRIC if args.workload == WORKLOAD and args.batch is None and args.prefix is None
+                   else f"MASW draft-attn decode steps/s ({args.workload}, batch {wl['batch']}, prefix {prefix})"),
         "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": secs / args.steps * 1e3, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
@@ -816,7 +824,8 @@ def main():
                     "gbs": kv_step_full * full_iters * dsteps / secs_full / 1e9},
         "speedup_vs_full_kv": value / full_value,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                     "frac": achieved / peak, "traffic": _recorded_traffic() if args.workload == WORKLOAD else None,
+                     "frac": achieved / peak, "traffic": (_recorded_traffic() if args.workload == WORKLOAD and args.batch is None
+                                 and args.prefix is None else None),
                      "peak_kind": peak_kind,
                      "kernel": "decode_mma_kernel<128, NST> (masw_draft_step: fused append + draft attention; NST = 2 stages, 3 when each CTA streams a long run of keys)",
                      "bytes_per_launch": total_b, "kv_bytes_per_launch": kv_b,
