@@ -23,6 +23,7 @@
 #include "masw_internal.cuh"
 
 #include <atomic>
+#include <climits>
 
 #include <cooperative_groups.h>
 #include <cstring>
@@ -95,9 +96,10 @@ __device__ __forceinline__ bool recv_wait(uint64_t* bar, int* err) {
     return false;
 }
 
-// largest thread-block cluster of the split merge (16 needs the non-portable
-// cluster-size attribute; larger sizes fall back to the ticket merge)
-constexpr int kMaxClusterSize = 16;
+// largest thread-block cluster of the split merge (above 8 needs the
+// non-portable cluster-size attribute).  Sizes 14 and 16 were measured slower
+// than 12 even where they shorten every CTA's key run, so the plan stops at 12.
+constexpr int kMaxClusterSize = 12;
 
 template <int ROWB>
 __device__ __forceinline__ uint32_t swz_off(int row, int ch) {
@@ -585,6 +587,7 @@ static int max_clusters(masw_mem_t* mem, int dev, int cs) {
 struct MmaPlan {
     int n_split;
     bool cluster;
+    bool sparse;   // the grid leaves more than a third of the resident slots empty
 };
 
 // One wave of the NST-stage kernel.  Splits of a pair are merged inside a
@@ -599,7 +602,7 @@ static int plan_mma(masw_mem_t* mem, int rows, int GR, int kmax, MmaPlan& pl) {
     if (!occ[dev].load(std::memory_order_acquire)) {
         MASW_CUDA_TRY(mem, cudaFuncSetAttribute(decode_mma_kernel<D, NST>,
                                                 cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM));
-        // clusters of up to 16 CTAs (beyond the portable 8) for few long pairs
+        // clusters of up to 12 CTAs (beyond the portable 8) for few long pairs
         if (cudaFuncSetAttribute(decode_mma_kernel<D, NST>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) !=
             cudaSuccess)
             cudaGetLastError();
@@ -616,18 +619,32 @@ static int plan_mma(masw_mem_t* mem, int rows, int GR, int kmax, MmaPlan& pl) {
     int ticket_split = imin(imin(imax(1, slots / pairs), max_useful), kMaxSplit);
     while (ticket_split > 1 && masw_decode_part_floats(rows, mem->Hkv, GR, D, ticket_split) > mem->part_floats)
         --ticket_split;
-    // a cluster size is taken when its grid fills at least half the resident
-    // slots, or when it has at least half the ticket plan's splits (few
-    // sequences with short working sets: the shared-memory merge replaces the
-    // global ticket merge; long runs keep the ticket plan's many splits)
+    // A cluster size qualifies when all its clusters are resident at once and
+    // its grid fills at least half the resident slots, or has at least half the
+    // ticket plan's splits (few sequences with short working sets: the
+    // shared-memory merge replaces the global ticket merge; long runs keep the
+    // ticket plan's many splits).  Of those, take the fewest key stages per CTA;
+    // on a tie, a grid whose clusters take at most 3/4 of the resident cluster
+    // positions (a fuller one leaves the next launch no room to start early:
+    // batch 4 at 32K ran 9.6 us as 32 of 36 possible 12-CTA clusters, 7.6 us as
+    // 10-CTA ones), then the larger size.
+    int best_stages = INT_MAX, best_full = 1;
     for (int cs = imin(kMaxClusterSize, imin(max_useful, slots / imax(1, pairs))); cs >= 2; --cs) {
-        if ((cs * pairs * 2 >= slots || 2 * cs >= ticket_split) && max_clusters<D, NST>(mem, dev, cs) >= pairs) {
+        if (!(cs * pairs * 2 >= slots || 2 * cs >= ticket_split)) continue;
+        const int mc = max_clusters<D, NST>(mem, dev, cs);
+        if (mc < pairs) continue;
+        const int chunk = ((kmax + cs - 1) / cs + 15) & ~15;   // the kernel's split length
+        const int stages = (chunk + C::KPS - 1) / C::KPS;
+        const int full = 4 * pairs > 3 * mc ? 1 : 0;
+        if (stages < best_stages || (stages == best_stages && full < best_full)) {
+            best_stages = stages;
+            best_full = full;
             pl.n_split = cs;
             pl.cluster = true;
-            break;
         }
     }
     if (!pl.cluster) pl.n_split = ticket_split;
+    pl.sparse = 3 * pl.n_split * pairs < 2 * slots;
     return MASW_OK;
 }
 
@@ -640,10 +657,13 @@ static int launch_plan(masw_mem_t* mem, DecodeParams& prm, int rows, const MmaPl
     return MASW_OK;
 }
 
-// Two stages unless each CTA would stream a long run of keys (e.g. one split
-// per pair at batch 32): then three stages keep more bytes in flight, which
-// matters more than an early start of the next launch.
-constexpr int kLongRunKeys = 1536;
+// Two stages unless each CTA would stream a long run of keys: more than 1536,
+// or more than 1024 when the two-stage grid leaves a third of the resident
+// slots empty (one split of 1090 keys per pair at batch 32: 36.3 -> 28.9 us).
+// Then three stages keep more bytes in flight, which matters more than an
+// early start of the next launch.  (Six splits of 1400 keys per pair on a
+// full grid stay at two stages: 50.2 us against 50.7 with three.)
+constexpr int kLongRunKeys = 1536, kSparseLongRunKeys = 1024;
 
 template <int D>
 static int launch_mma(masw_mem_t* mem, DecodeParams& prm, int G, int rows, int kmax, cudaStream_t stream) {
@@ -651,7 +671,8 @@ static int launch_mma(masw_mem_t* mem, DecodeParams& prm, int G, int rows, int k
     prm.rows_per_pair = GR;
     MmaPlan pl;
     if (int rc = plan_mma<D, 2>(mem, rows, GR, kmax, pl)) return rc;
-    if (kmax / pl.n_split <= kLongRunKeys) return launch_plan<D, 2>(mem, prm, rows, pl, stream);
+    const int run = kmax / pl.n_split;
+    if (run <= (pl.sparse ? kSparseLongRunKeys : kLongRunKeys)) return launch_plan<D, 2>(mem, prm, rows, pl, stream);
     if (int rc = plan_mma<D, 3>(mem, rows, GR, kmax, pl)) return rc;
     return launch_plan<D, 3>(mem, prm, rows, pl, stream);
 }

@@ -531,20 +531,22 @@ def test_draft3b_full_size_sampled():
         p.close()
 
 
-@pytest.mark.parametrize("Hq", [24, 32])
-def test_fused_steps_full_size_sampled(Hq):
+@pytest.mark.parametrize("Hq,B", [(24, 8), (32, 8), (24, 4), (32, 4), (32, 2)])
+def test_fused_steps_full_size_sampled(Hq, B):
     """The fused step and the fused boundary step at the benchmark's launch
-    shape (batch 8, 8 kv heads, 32K prefix, S=4, W=1024, r=512): every split of
-    a (row, head) pair is a CTA of one thread-block cluster, so the shared-memory
-    merge runs with G = 3 or 4 query columns per pair, and with 2G = 6 or 8 at the
-    boundary step, where the slot queries of all eight sequences ride in the same
-    launch.  The new token's row is stored by the split whose keys include it.
-    Two (layer, row) pairs carry CPU-seeded data and are checked against the
-    oracle; the other rows are filled on the device."""
+    shape (batch 8, 8 kv heads, 32K prefix, S=4, W=1024, r=512) and at batch 4
+    and 2: every split of a (row, head) pair is a CTA of one thread-block
+    cluster (6, 10 and 12 CTAs; with 10 the last rank finalises a shorter slice
+    of the output), so the shared-memory merge runs with G = 3 or 4 query
+    columns per pair, and with 2G = 6 or 8 at the boundary step, where the slot
+    queries of all sequences ride in the same launch.  The new token's row is
+    stored by the split whose keys include it.  Two (layer, row) pairs carry
+    CPU-seeded data and are checked against the oracle; the other rows are
+    filled on the device."""
     S, W, r, t0 = 4, 1024, 512, 32768
-    B, L, Hkv, D = 8, 2, 8, 128
-    p = Pair(S, W, r, Hkv, D, L, B, "bf16", Hq, max_seq_len=t0 + 16, tag=f"fsz{Hq}")
-    sampled = {(0, 2), (1, 6)}
+    L, Hkv, D = 2, 8, 128
+    p = Pair(S, W, r, Hkv, D, L, B, "bf16", Hq, max_seq_len=t0 + 16, tag=f"fsz{Hq}_{B}")
+    sampled = {(0, B // 4), (1, B - 2)}
     try:
         g = torch.Generator(device=DEV)
         g.manual_seed(4321)
@@ -602,7 +604,7 @@ def test_fused_steps_full_size_sampled(Hq):
 @pytest.mark.parametrize("Hq", [24, 32])
 def test_fused_steps_one_sequence(Hq):
     """One sequence (8 kv heads, 8K prefix, S=4, W=1024, r=512): each (sequence,
-    head) pair runs as a cluster of 16 CTAs merging in shared memory; fused
+    head) pair runs as a cluster of 12 CTAs merging in shared memory; fused
     steps, and at tau_14 = 8196 the fused boundary step (2G = 6 or 8 query
     columns per pair), across two layers, all rows checked against the oracle."""
     S, W, r, t0 = 4, 1024, 512, 8192
