@@ -1,5 +1,5 @@
 // Greedy speculative acceptance on the target's verify logits ([EN] §2.2 Eq. 1
-// and §3.3 Algorithm 2 step 5; the pages' experiments decode greedily, T = 0).
+// and §3.3 Algorithm 2; the pages' experiments decode greedily, T = 0).
 //
 // For sequence b the target's token at block position j (0..L) is the argmax of
 // logits[b][j][0..V) (ties to the smallest id).  Draft token j is accepted while

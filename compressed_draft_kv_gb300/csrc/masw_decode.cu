@@ -4,7 +4,7 @@
 // under the structured mask, and the full-KV contrast cache.
 //
 // Computes Eq. 2 of [EN] §2.3 for one query token per sequence over the sets
-// of [EN] §3.1 Eq. 4 (draft), [EN] §3.2 Algorithm 1 step 2 (slot write) or
+// of [EN] §3.1 Eq. 4 (draft), [EN] §3.2 Algorithm 1 (slot write) or
 // the whole prefix (full KV).
 //
 // Grid: (n_split, Hkv, rows).  One CTA streams one contiguous share of the

@@ -1,6 +1,6 @@
 // Tensor-core split-KV decode attention for bf16 pools: draft attention over
 // the MASW working memory ([EN] §3.1 Eq. 4 with Eq. 2 of §2.3), the slot-write
-// query under the structured mask ([EN] §3.2 Algorithm 1 step 2), and full-KV
+// query under the structured mask ([EN] §3.2 Algorithm 1), and full-KV
 // decode over the contrast cache.
 //
 // With grouped-query attention the G = Hq/Hkv query heads of a kv head read

@@ -369,7 +369,7 @@ struct Seg {
 // the sink, the window (one run, or two when it wraps around the ring), the
 // slot chain, and -- for a slot write with self-attention -- the caller's own
 // K_g/V_g row.  Draft mode: [EN] §3.1 Eq. 4; slot mode: [EN] §3.2 Algorithm 1
-// step 2 (slots 1..m-1 only); full mode: every raw token.
+// (slots 1..m-1 only); full mode: every raw token.
 template <int ROWB>
 __device__ __forceinline__ int build_segments(const DecodeParams& p, int lb, int h, int z, int t, int mcnt,
                                               Seg* segs) {

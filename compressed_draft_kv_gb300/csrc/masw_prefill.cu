@@ -1,5 +1,5 @@
-// Draft prefill under the structured write mask ([EN] §3.3 Algorithm 2 step 2
-// with the mask of §3.2 Algorithm 1 step 2): one layer of attention over a whole
+// Draft prefill under the structured write mask ([EN] §3.3 Algorithm 2
+// with the mask of §3.2 Algorithm 1): one layer of attention over a whole
 // prefix of T raw tokens with the M = m(T) memory-slot tokens interleaved, then
 // the resulting memory M_0 is stored in the pool.
 //

@@ -119,17 +119,17 @@ const char* masw_last_error(const masw_mem_t* mem);
 /* ---- memory maintenance ---------------------------------------------------- */
 
 /* Append one raw token to every active sequence of `layer` ([EN] §3.3
- * Algorithm 2 step 4): k, v are device [batch, Hkv, D] in the pool dtype.
+ * Algorithm 2): k, v are device [batch, Hkv, D] in the pool dtype.
  * Token i = t+1 goes to sink row i-1 if i <= S, else to ring row (i-S-1) mod
- * (W+R); that write is the eviction of [EN] §3.2 Algorithm 1 step 5.  With
+ * (W+R); that write is the eviction of [EN] §3.2 Algorithm 1.  With
  * full_kv it is also written to row i-1 of the full cache.  active: host
  * [batch] bytes, nonzero = append; NULL = all.  ECAPACITY when t would exceed
  * max_seq_len. */
 int masw_append_kv(masw_mem_t* mem, int layer, const void* k, const void* v,
                    const uint8_t* active, masw_stream_t stream);
 
-/* Memory-slot write at a compression boundary ([EN] §3.2 Algorithm 1 steps
- * 2, 4 and 6) for the n sequences in the host list seq_ids.  For each listed
+/* Memory-slot write at a compression boundary ([EN] §3.2 Algorithm 1)
+ * for the n sequences in the host list seq_ids.  For each listed
  * sequence b, which must have t = tau_m = S + W + m*r for the next chain index
  * m (ESTATE otherwise):
  *   1. the slot query q_g attends, under the structured mask, to M_sink,
@@ -148,7 +148,7 @@ int masw_materialize_slot(masw_mem_t* mem, int layer, const int* seq_ids, int n,
                           float* o_g, float* lse_g, int n_q_heads, masw_stream_t stream);
 
 /* Draft prefill of one (layer, seq) under the structured write mask ([EN] §3.3
- * Algorithm 2 step 2, mask of §3.2 Algorithm 1 step 2): one attention pass over
+ * Algorithm 2, mask of §3.2 Algorithm 1): one attention pass over
  * a prefix of T raw tokens with the M = max(0, (T-S-W)/r) slot tokens
  * interleaved, then M_0 is stored as the sequence's memory (sink rows, the last
  * W+R raw tokens in their ring rows, slots 1..M with position ids tau_1..tau_M,
@@ -172,7 +172,7 @@ int masw_prefill(masw_mem_t* mem, int layer, int seq, int T,
                  masw_stream_t stream);
 
 /* Undo the last t[b] - t_new[i] raw tokens of the listed sequences in every
- * layer ([EN] §3.3 Algorithm 2 step 6): counters go back to t_new and slots
+ * layer ([EN] §3.3 Algorithm 2): counters go back to t_new and slots
  * with tau_m > t_new are dropped.  Needs 0 <= t - t_new <= R in every layer
  * (ESTATE otherwise), because the ring rows of the restored window must not
  * have been overwritten.  seq_ids, t_new: host arrays of n. */
@@ -199,7 +199,7 @@ int masw_full_attn(masw_mem_t* mem, int layer, const void* q, int n_q_heads,
                    float* o, float* lse, masw_stream_t stream);
 
 /* One draft decode step of `layer` in a single launch: masw_append_kv followed
- * by masw_draft_attn ([EN] §3.3 Algorithm 2 step 4 -- the new token joins the
+ * by masw_draft_attn ([EN] §3.3 Algorithm 2 -- the new token joins the
  * window, evicting the oldest, and the query at t+1 attends over M_{t+1}).
  * k, v: device [batch, Hkv, D] (the new token); q: device [batch, n_q_heads, D];
  * o, lse as in masw_draft_attn; active as in masw_append_kv (inactive
@@ -215,9 +215,9 @@ int masw_draft_step(masw_mem_t* mem, int layer, const void* q, const void* k, co
  * followed by masw_materialize_slot for the n listed sequences, which must each
  * be active and reach an unmaterialised boundary tau_m with this step's token
  * (ESTATE otherwise).  At tau_m the slot query's structured mask ([EN] §3.2
- * Algorithm 1 step 2: sink, window at tau_m, slots 1..m-1) is exactly the draft
+ * Algorithm 1: sink, window at tau_m, slots 1..m-1) is exactly the draft
  * query's working set M_{tau_m} (which does not yet hold g_m, [EN] §3.2
- * Algorithm 1 step 1), so both queries share every K/V row read.  Arguments:
+ * Algorithm 1), so both queries share every K/V row read.  Arguments:
  * those of masw_draft_step, then those of masw_materialize_slot.  fp32 pools,
  * more than 4 query heads per kv head, or slot_self_attend = 1 run the two
  * calls as two launches. */
@@ -232,7 +232,7 @@ int masw_full_step(masw_mem_t* mem, int layer, const void* q, const void* k, con
                    const uint8_t* active, int n_q_heads, float* o, float* lse,
                    masw_stream_t stream);
 
-/* Target verify attention ([EN] §3.3 Algorithm 2 step 5), stateless: Lq query
+/* Target verify attention ([EN] §3.3 Algorithm 2), stateless: Lq query
  * positions per sequence against an uncompressed cache, causal inside the
  * block.  Query j (0-based) of sequence b sees keys 0 .. kv_len[b]-Lq+j
  * (kv_len counts the block's own Lq tokens).  bf16 only.
@@ -280,10 +280,10 @@ int masw_verify_attn_noalloc(const void* q, const void* k_cache, const void* v_c
 
 /* ---- speculative acceptance ------------------------------------------------------ */
 
-/* Greedy acceptance of a speculative block ([EN] §2.2 and §3.3 Algorithm 2
- * step 5; the pages' experiments decode greedily, temperature 0).  For each
- * sequence b: tokens[b][j] = argmax over v of logits[b][j][v] for j = 0..L (ties
- * go to the smallest id; NaN entries are skipped); L_acc = the first j < L with
+/* Greedy acceptance of a speculative block ([EN] §2.2 and §3.3 Algorithm 2;
+ * the pages' experiments decode greedily, temperature 0).  For each sequence b:
+ * tokens[b][j] = argmax over v of logits[b][j][v] for j = 0..L (ties go to the
+ * smallest id; NaN entries are skipped); L_acc = the first j < L with
  * draft[b][j] != tokens[b][j], or L when all drafts match; n_emit[b] = L_acc + 1,
  * and the emitted tokens are tokens[b][0 .. L_acc] (accepted drafts, then the
  * target's correction or bonus token).

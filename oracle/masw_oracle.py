@@ -32,21 +32,20 @@ in tests/test_oracle_pins.py; none is "parity unpinned"):
     tokens that have fallen outside sink and window ([EN] §3.1, third bullet),
     not the looser floor(t / r) of the same section's closing sentence;
   * boundary tau_m = S + W + m*r (m >= 1): the step at which the (m*r)-th raw
-    token has left the window ([EN] §3.2 Algorithm 1, input and step 1);
+    token has left the window ([EN] §3.2 Algorithm 1);
   * the slot query g_m reads the local window evaluated at t = tau_m, the sink
-    and slots 1..m-1, and not itself ([EN] §3.2 Algorithm 1 step 2);
+    and slots 1..m-1, and not itself ([EN] §3.2 Algorithm 1);
   * a draft query at step tau_m is issued before g_m is materialised, so it
-    sees m-1 slots; the query at tau_m + 1 sees m (causal order of Algorithm 1
-    step 1: g_m follows raw token tau_m);
+    sees m-1 slots; the query at tau_m + 1 sees m (causal order of Algorithm 1: g_m follows raw token tau_m);
   * slot position id = tau_m + 1, the 1-based id of the raw token that follows
-    g_m ([EN] §3.2 Algorithm 1 step 6);
+    g_m ([EN] §3.2 Algorithm 1);
   * GQA: query head h reads kv head floor(h / G), G = Hq / Hkv;
   * scale = 1 / sqrt(head_dim) unless overridden (Eq. 2 uses d for the head
     dimension; Eq. 3 reuses d for the hidden size);
   * verify: query j (0-based) of an Lq-query block whose last key is token
-    kv_len sees keys 1 .. kv_len - Lq + 1 + j ([EN] §3.3 Algorithm 2 step 5);
+    kv_len sees keys 1 .. kv_len - Lq + 1 + j ([EN] §3.3 Algorithm 2);
   * rollback by k tokens needs k <= R extra ring rows; slots with tau <= t_new
-    are kept ([EN] §3.3 Algorithm 2 step 6).
+    are kept ([EN] §3.3 Algorithm 2).
 """
 
 from __future__ import annotations
@@ -102,7 +101,7 @@ def is_boundary(t: int, S: int, W: int, r: int) -> bool:
 
 def slot_pos_id(m: int, S: int, W: int, r: int) -> int:
     """RoPE position id of g_m: that of the raw token right after it
-    ([EN] §3.2 Algorithm 1 step 6), i.e. tau_m + 1 (1-based)."""
+    ([EN] §3.2 Algorithm 1), i.e. tau_m + 1 (1-based)."""
     return boundary(m, S, W, r) + 1
 
 
@@ -117,7 +116,7 @@ def working_set_size(t: int, S: int, W: int, r: int) -> int:
 
 def draft_mask(t: int, n_slots: int, S: int, W: int) -> np.ndarray:
     """Columns a draft query at step t may read: M_sink u M_local,t u every
-    slot present at call time ([EN] §3.1 Eq. 4; §3.3 Algorithm 2 step 4)."""
+    slot present at call time ([EN] §3.1 Eq. 4; §3.3 Algorithm 2)."""
     raw = np.zeros(t, dtype=bool)
     raw[:min(S, t)] = True
     lo, hi = local_window(t, S, W)
@@ -128,9 +127,9 @@ def draft_mask(t: int, n_slots: int, S: int, W: int) -> np.ndarray:
 
 def slot_write_mask(tau: int, m: int, S: int, W: int,
                     self_attend: bool = False) -> np.ndarray:
-    """Columns slot token g_m may read at boundary tau ([EN] §3.2 Algorithm 1
-    step 2, the structured mask): M_sink, M_local,tau and M_slot,<m, and no
-    other raw token.  Columns cover slots 1..m; slot m (g_m itself) is read
+    """Columns slot token g_m may read at boundary tau ([EN] §3.2 Algorithm 1,
+    the structured mask): M_sink, M_local,tau and M_slot,<m, and no other raw
+    token.  Columns cover slots 1..m; slot m (g_m itself) is read
     only when ``self_attend``."""
     raw = np.zeros(tau, dtype=bool)
     raw[:min(S, tau)] = True
@@ -152,7 +151,7 @@ def full_mask(t: int) -> np.ndarray:
 def verify_mask(kv_len: int, Lq: int) -> np.ndarray:
     """[Lq, kv_len] causal block: the cache holds kv_len tokens of which the last
     Lq are the block; query j sees keys 1..kv_len-Lq+1+j ([EN] §3.3
-    Algorithm 2 step 5: one parallel target pass over the full cache)."""
+    Algorithm 2: one parallel target pass over the full cache)."""
     mask = np.zeros((Lq, kv_len), dtype=bool)
     for j in range(Lq):
         mask[j, :kv_len - Lq + 1 + j] = True
@@ -343,8 +342,8 @@ class MaswOracle:
         self.sim[layer][seq] = sim
 
     def append(self, layer: int, k, v, active=None):
-        """Append one raw token per active sequence ([EN] §3.3 Algorithm 2
-        step 4; eviction is implicit in the window bounds)."""
+        """Append one raw token per active sequence ([EN] §3.3 Algorithm 2;
+        eviction is implicit in the window bounds)."""
         k = np.asarray(k, dtype=np.float64)
         v = np.asarray(v, dtype=np.float64)
         for b in range(self.batch):
@@ -375,7 +374,7 @@ class MaswOracle:
 
     def materialize_slot(self, layer: int, seq_ids, q_g, k_g, v_g):
         """Slot write at boundary tau_m for the listed sequences ([EN] §3.2
-        Algorithm 1 steps 2 and 4): g_m attends under the structured mask, then
+        Algorithm 1): g_m attends under the structured mask, then
         its K/V are appended to the chain.  Returns O_g [n, Hq, D] and LSE."""
         q_g = np.asarray(q_g, dtype=np.float64)
         k_g = np.asarray(k_g, dtype=np.float64)
@@ -413,7 +412,7 @@ class MaswOracle:
 
     def rollback(self, seq_ids, t_new):
         """Discard raw tokens after t_new[i] and slots with tau > t_new[i] in
-        every layer ([EN] §3.3 Algorithm 2 step 6)."""
+        every layer ([EN] §3.3 Algorithm 2)."""
         for i, b in enumerate(seq_ids):
             tn = int(t_new[i])
             for l in range(self.layers):
@@ -431,7 +430,7 @@ class MaswOracle:
 
 def verify_attn(q, k_cache, v_cache, kv_len, scale: float | None = None):
     """Target verify attention over an uncompressed cache ([EN] §3.3
-    Algorithm 2 step 5).  q [B, Lq, Hq, D]; k/v_cache [B, Hkv, Tmax, D];
+    Algorithm 2).  q [B, Lq, Hq, D]; k/v_cache [B, Hkv, Tmax, D];
     kv_len [B] counts the block's own Lq tokens.  Returns O [B, Lq, Hq, D] and
     LSE [B, Lq, Hq]."""
     q = np.asarray(q, dtype=np.float64)
@@ -454,7 +453,7 @@ def verify_attn(q, k_cache, v_cache, kv_len, scale: float | None = None):
 # --------------------------------------------------------------------------
 
 def greedy_accept(logits, draft):
-    """Greedy speculative acceptance ([EN] §2.2, §3.3 Algorithm 2 step 5; the
+    """Greedy speculative acceptance ([EN] §2.2, §3.3 Algorithm 2; the
     experiments use temperature 0).  logits [B, L+1, V], draft [B, L] ->
     tokens [B, L+1] (target argmax per position, first index among ties) and
     n_emit [B] = L_acc + 1, L_acc = number of leading drafts equal to the
@@ -486,10 +485,10 @@ def eq1_speedup(l_acc: float, l_draft: int, t_draft: float, t_target: float) -> 
 
 def prefill_row_mask(kind, idx, T, S, W, r, self_attend=False):
     """Mask row of one prefill query over the columns [raw 1..T] ++ [slot 1..M]
-    ([EN] §3.3 Algorithm 2 step 2 with the structured mask of §3.2 Algorithm 1
-    step 2).  kind "raw": raw token idx (1-based) reads the sink, its local
-    window and the slots with tau_m < idx; kind "slot": slot g_idx reads what the
-    slot write at tau_idx reads (sink, window at tau_idx, slots 1..idx-1)."""
+    ([EN] §3.3 Algorithm 2 with the structured mask of §3.2 Algorithm 1).
+    kind "raw": raw token idx (1-based) reads the sink, its local window and
+    the slots with tau_m < idx; kind "slot": slot g_idx reads what the slot
+    write at tau_idx reads (sink, window at tau_idx, slots 1..idx-1)."""
     M = slot_count(T, S, W, r)
     mask = np.zeros(T + M, dtype=bool)
     if kind == "raw":
@@ -508,8 +507,8 @@ def prefill_row_mask(kind, idx, T, S, W, r, self_attend=False):
 def prefill_attn(S, W, r, q_raw, k_raw, v_raw, q_slot, k_slot, v_slot, scale=None, self_attend=False,
                  raw_rows=None, slot_rows=None):
     """One layer of the draft prefill over T raw tokens with the M = m(T) slot
-    tokens interleaved ([EN] §3.3 Algorithm 2 step 2, with the structured mask of
-    §3.2 Algorithm 1 step 2): raw token i reads the sink, its local window and
+    tokens interleaved ([EN] §3.3 Algorithm 2, with the structured mask of
+    §3.2 Algorithm 1): raw token i reads the sink, its local window and
     the slots materialised before it (tau_m < i); slot g_m reads the sink, the
     window at tau_m and slots 1..m-1.  Columns are [raw 1..T] ++ [slot 1..M].
     q_raw [T, Hq, D], k_raw/v_raw [T, Hkv, D], q_slot [M, Hq, D],
