@@ -1,5 +1,5 @@
-// Target verify attention over an uncompressed cache ([EN] §3.3 Algorithm 2
-// step 5): Lq query positions per sequence, causal inside the block, GQA.
+// Target verify attention over an uncompressed cache ([EN] §3.3 Algorithm 2):
+// Lq query positions per sequence, causal inside the block, GQA.
 //
 // Like the draft prefill this is a dense contraction (the Lq*G query rows of a
 // kv head share every K/V row: 24 flop per byte at Lq = 6, G = 4), so it runs
@@ -32,21 +32,24 @@ constexpr int kVMaxNQ = 32;          // query rows (Lq * G) per (sequence, kv he
 // at the end.  This spreads the exponentials over the four SM sub-partitions
 // (a single softmax warp holding all 64 columns left three of them idle).
 // Lane 0 of warp 4 loads K (TMA) and issues S; lane 0 of warp 5 loads V and
-// issues P V.  The split partials are merged by split_epilogue.  Two CTAs per
-// SM (256 tensor-memory columns and 112 KB of shared memory each).
+// issues P V.  The split partials are merged by split_epilogue.  One CTA per SM
+// (256 tensor-memory columns, 192 KB of shared memory): five K and five V stages
+// keep four blocks of each in flight, and two P buffers let the softmax of
+// block j+1 write its P while P V of block j still reads the other (fewer,
+// deeper streams measured faster than two CTAs per SM with three stages).
 // ---------------------------------------------------------------------------
 namespace vtc {
 using namespace tc;
 constexpr int kBM = 128;                         // MMA rows = tensor-memory lanes
 constexpr int kBN = 64;                          // keys per block
 constexpr int kD = 128;                          // head_dim
-constexpr int kStages = 3;                       // K and V stages
+constexpr int kStages = 5;                       // K and V stages (one CTA per SM)
 constexpr uint32_t kKVBytes = kBN * kD * 2;      // 2 panels of 64 rows x 128 B
-constexpr uint32_t kPBytes = kBM * kBN * 2;      // 1 panel of 128 rows x 128 B
+constexpr uint32_t kPBytes = kBM * kBN * 2;      // a P buffer: 1 panel of 128 rows x 128 B
 constexpr uint32_t kOffK = 0;
 constexpr uint32_t kOffV = kOffK + kStages * kKVBytes;
 constexpr uint32_t kOffP = kOffV + kStages * kKVBytes;
-constexpr uint32_t kSmem = kOffP + kPBytes;      // the barriers are static shared memory
+constexpr uint32_t kSmem = kOffP + 2 * kPBytes;  // two P buffers; the barriers are static shared memory
 constexpr uint32_t kTmemCols = 256;
 constexpr uint32_t kColO = 0;                    // O: columns [0, 128)
 constexpr uint32_t kColS = 128;                  // S: columns [128, 192)
@@ -56,16 +59,17 @@ constexpr uint32_t kColQ = 192;                  // Q (bf16 pairs, the A operand
 constexpr uint32_t kIdescBase = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(kBM >> 4) << 24);
 constexpr uint32_t kIdescS = kIdescBase | ((uint32_t)(kBN >> 3) << 17);
 constexpr uint32_t kIdescO = kIdescBase | (1u << 16) | ((uint32_t)(kD >> 3) << 17);
-__device__ __forceinline__ constexpr int bar_k(int s) { return s; }        // K stage landed (TMA)
-__device__ __forceinline__ constexpr int bar_v(int s) { return 3 + s; }    // V stage landed (TMA)
-constexpr int kBarS = 6;       // S = Q K^T done (MMA commit)
-constexpr int kBarSFree = 7;   // the four softmax warps have read S (4 arrivals)
-constexpr int kBarP = 8;       // the four softmax warps have written P and rescaled O (4 arrivals)
-constexpr int kBarO = 9;       // O += P V done (MMA commit)
-constexpr int kBarQ = 10;      // the four softmax warps have stored Q in tensor memory (4 arrivals)
-constexpr int kBarDone = 11;   // every S MMA done (early exit only)
-constexpr int kBarDoneV = 12;  // every PV MMA done (early exit only)
-constexpr int kNumBars = 13;
+__device__ __forceinline__ constexpr int bar_k(int s) { return s; }             // K stage landed (TMA)
+__device__ __forceinline__ constexpr int bar_v(int s) { return kStages + s; }   // V stage landed (TMA)
+constexpr int kBarS = 2 * kStages;   // S = Q K^T done (MMA commit)
+constexpr int kBarSFree = kBarS + 1; // the four softmax warps have read S (4 arrivals)
+constexpr int kBarQ = kBarS + 2;     // the four softmax warps have stored Q in tensor memory (4 arrivals)
+constexpr int kBarDone = kBarS + 3;  // every S MMA done (early exit only)
+constexpr int kBarDoneV = kBarS + 4; // every PV MMA done (early exit only)
+// P buffer b written and O rescaled (4 arrivals); the PV MMA that read it done (commit)
+__device__ __forceinline__ constexpr int bar_pfull(int b) { return kBarS + 5 + b; }
+__device__ __forceinline__ constexpr int bar_pfree(int b) { return kBarS + 7 + b; }
+constexpr int kNumBars = kBarS + 9;
 // merge layout in the idle stage buffers after the loop: four partial O rows
 // per query row, their (max, sum), the merged rows and (max, sum)
 constexpr uint32_t kOffPartO = 0;                                  // [4][kVMaxNQ][128] f32
@@ -89,7 +93,7 @@ struct VerifyTcParams {
     float scale_log2;
 };
 
-__global__ void __launch_bounds__(192, 2) verify_tc_kernel(const __grid_constant__ VerifyTcParams p) {
+__global__ void __launch_bounds__(192, 1) verify_tc_kernel(const __grid_constant__ VerifyTcParams p) {
     using namespace vtc;
     extern __shared__ __align__(1024) uint8_t vsmem[];
     __shared__ uint64_t bars[kNumBars];
@@ -136,7 +140,7 @@ __global__ void __launch_bounds__(192, 2) verify_tc_kernel(const __grid_constant
     }
     if (tid == 0) {
         for (int i = 0; i < kNumBars; ++i)
-            mbar_init(bars + i, (i == kBarSFree || i == kBarP || i == kBarQ) ? 4 : 1);
+            mbar_init(bars + i, (i == kBarSFree || i == bar_pfull(0) || i == bar_pfull(1) || i == kBarQ) ? 4 : 1);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -159,7 +163,7 @@ __global__ void __launch_bounds__(192, 2) verify_tc_kernel(const __grid_constant
                 tma_load_3d(dst + kKVBytes / 2, m, 64, k0 + blk * kBN, head_row, bar_at(bi));
                 li = blk + 1;
             };
-            for (int blk = 0; blk < imin(2, nblk); ++blk) load(blk);
+            for (int blk = 0; blk < imin(kStages - 1, nblk); ++blk) load(blk);
             bool ok = true;
             if (!is_v) {
                 ok = wait_or_abort(bars + kBarQ, 0, abort_flag, p.status);
@@ -178,29 +182,35 @@ __global__ void __launch_bounds__(192, 2) verify_tc_kernel(const __grid_constant
                                      bd0 + (uint64_t)(((kk >> 2) * (kKVBytes / 2) + (kk & 3) * 32) >> 4), kIdescS,
                                      kk > 0 ? 1u : 0u);
                     umma_commit(bar_at(kBarS));
-                    // K(j+2) takes the stage of K(j-1), whose S the softmax has read
-                    if (j + 2 < nblk) load(j + 2);
+                    // K(j+kStages-1) takes the stage of K(j-1), whose S the softmax has read
+                    if (j + kStages - 1 < nblk) load(j + kStages - 1);
                 }
             } else {
                 for (int j = 0; ok && j < nblk; ++j) {
-                    const int st = j % kStages;
-                    ok = wait_or_abort(bars + kBarP, (uint32_t)j & 1u, abort_flag, p.status);
+                    const int st = j % kStages, pb = j & 1;
+                    ok = wait_or_abort(bars + bar_pfull(pb), (uint32_t)(j >> 1) & 1u, abort_flag, p.status);
                     if (ok) {
                         ok = wait_or_abort(bars + bar_v(st), (uint32_t)(j / kStages) & 1u, abort_flag, p.status);
                         if (ok) lw = j + 1;
                     }
                     if (!ok) break;
                     tc_fence_after();
-                    const uint64_t a0 = sw128_desc(sb + kOffP, 16, 1024);
+                    const uint64_t a0 = sw128_desc(sb + kOffP + pb * kPBytes, 16, 1024);
                     const uint64_t v0 = sw128_desc(sb + kOffV + st * kKVBytes, kKVBytes / 2, 1024);
 #pragma unroll
                     for (int kk = 0; kk < kBN / 16; ++kk)
                         umma_bf16(tmem + kColO, a0 + (uint64_t)((kk * 32) >> 4), v0 + (uint64_t)((kk * 2048) >> 4),
                                   kIdescO, (j > 0 || kk > 0) ? 1u : 0u);
-                    umma_commit(bar_at(kBarO));
-                    // P(j) written means the softmax saw PV(j-1) complete:
-                    // V(j+2) takes the stage of V(j-1)
-                    if (j + 2 < nblk) load(j + 2);
+                    umma_commit(bar_at(bar_pfree(pb)));
+                    // V(j+kStages-1) takes the stage of V(j-1) once PV(j-1) is done
+                    // (the next completion of that P buffer needs P(j+1): no phase is skipped)
+                    if (j + kStages - 1 < nblk) {
+                        if (j >= 1)
+                            ok = wait_or_abort(bars + bar_pfree(pb ^ 1), (uint32_t)((j - 1) >> 1) & 1u, abort_flag,
+                                               p.status);
+                        if (!ok) break;
+                        load(j + kStages - 1);
+                    }
                 }
             }
             if (!ok) {
@@ -235,11 +245,14 @@ __global__ void __launch_bounds__(192, 2) verify_tc_kernel(const __grid_constant
             }
             tmem_st32(tmem + kColQ + lane_off + hh * 32, qv);
         }
-        // this row's P outside the warp's 16 columns stays zero: written once
+        // this row's P outside the warp's 16 columns stays zero: written once per buffer
         const uint32_t prow = sb + kOffP + (uint32_t)(w * 32 + lane) * 128u;
 #pragma unroll
         for (int c = 0; c < 8; ++c)
-            if ((c >> 1) != w) st_shared_v4(prow + ((uint32_t)(c ^ (lane & 7)) << 4), 0u, 0u, 0u, 0u);
+            if ((c >> 1) != w) {
+                st_shared_v4(prow + ((uint32_t)(c ^ (lane & 7)) << 4), 0u, 0u, 0u, 0u);
+                st_shared_v4(prow + kPBytes + ((uint32_t)(c ^ (lane & 7)) << 4), 0u, 0u, 0u, 0u);
+            }
         tmem_wait_st();
         tc_fence_before();
         __syncwarp();
@@ -292,16 +305,27 @@ __global__ void __launch_bounds__(192, 2) verify_tc_kernel(const __grid_constant
             const bool resc = alpha != 1.f && l_run > 0.f;
             l_run = l_run * alpha + (sum_lo + sum_hi);
 
-            // PV(j-1) must be complete before O is rescaled and P is overwritten
-            if (j > 0) {
-                if (!__all_sync(0xffffffffu,
-                                wait_or_abort(bars + kBarO, (uint32_t)(j - 1) & 1u, abort_flag, p.status))) {
+            // P buffer j&1 is free once PV(j-2) is done; O is rescaled only after
+            // PV(j-1) (the next completion of either buffer needs a P not yet written)
+            const int pb = j & 1;
+            if (j >= 2) {
+                if (!__all_sync(0xffffffffu, wait_or_abort(bars + bar_pfree(pb), (uint32_t)((j - 2) >> 1) & 1u,
+                                                           abort_flag, p.status))) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
             }
-            if (__any_sync(0xffffffffu, resc)) {
+            const bool any_resc = __any_sync(0xffffffffu, resc);
+            if (any_resc && j >= 1) {
+                if (!__all_sync(0xffffffffu, wait_or_abort(bars + bar_pfree(pb ^ 1), (uint32_t)((j - 1) >> 1) & 1u,
+                                                           abort_flag, p.status))) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+            }
+            if (any_resc) {
 #pragma unroll
                 for (int c = 0; c < 4; ++c) {
                     uint32_t ov[32];
@@ -314,15 +338,17 @@ __global__ void __launch_bounds__(192, 2) verify_tc_kernel(const __grid_constant
                 tmem_wait_st();
             }
             // this warp's two 16-byte chunks of the row (128-byte swizzle)
-            st_shared_v4(prow + ((uint32_t)((2 * w) ^ (lane & 7)) << 4), pk[0], pk[1], pk[2], pk[3]);
-            st_shared_v4(prow + ((uint32_t)((2 * w + 1) ^ (lane & 7)) << 4), pk[4], pk[5], pk[6], pk[7]);
+            const uint32_t pr = prow + pb * kPBytes;
+            st_shared_v4(pr + ((uint32_t)((2 * w) ^ (lane & 7)) << 4), pk[0], pk[1], pk[2], pk[3]);
+            st_shared_v4(pr + ((uint32_t)((2 * w + 1) ^ (lane & 7)) << 4), pk[4], pk[5], pk[6], pk[7]);
             fence_async_smem();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(bar_at(kBarP));
+            if (lane == 0) mbar_arrive(bar_at(bar_pfull(pb)));
         }
         if (ok && nblk > 0)
-            ok = __all_sync(0xffffffffu, wait_or_abort(bars + kBarO, (uint32_t)(nblk - 1) & 1u, abort_flag, p.status));
+            ok = __all_sync(0xffffffffu, wait_or_abort(bars + bar_pfree((nblk - 1) & 1),
+                                                       (uint32_t)((nblk - 1) >> 1) & 1u, abort_flag, p.status));
         tc_fence_after();
         // this copy's partial O row and (max, sum) -> the stage buffers (idle now)
         float* po = reinterpret_cast<float*>(vsmem + kOffPartO) + ((size_t)w * kVMaxNQ + lane) * kD;
@@ -399,7 +425,7 @@ __global__ void __launch_bounds__(192, 2) verify_tc_kernel(const __grid_constant
 
 // Resident tensor-core verify CTAs per SM: the occupancy query, and the bound
 // from the kernel's attributes (shared memory with the per-block reserve), at
-// most two (256 tensor-memory columns each).
+// most two (256 tensor-memory columns each); one with the current stages.
 static int verify_tc_occupancy() {
     static std::atomic<int> cache[64];
     int dev = 0;
