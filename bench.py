@@ -36,23 +36,34 @@ METRIC = "MASW draft-attn decode steps/s (28 layers x batch 8, 32K prefix)"
 UNIT = "decode steps/s"
 
 
+def _code_hash(paths):
+    """sha256 (first 16 hex) of C/CUDA sources with comments, trailing blanks
+    and empty lines removed: edits to comments leave it unchanged."""
+    import hashlib
+    import re
+    h = hashlib.sha256()
+    for path in paths:
+        with open(path) as f:
+            s = f.read()
+        s = re.sub(r"/\*.*?\*/", "", s, flags=re.S)
+        s = re.sub(r"//[^\n]*", "", s)
+        h.update("\n".join(ln.rstrip() for ln in s.splitlines() if ln.strip()).encode())
+    return h.hexdigest()[:16]
+
+
 def _recorded_traffic():
     """dram read+write bytes per launch of the fused-step kernel from the
-    committed ncu summary, if the kernel sources are unchanged since (hash of
+    committed ncu summary, if the kernel code is unchanged since (code hash of
     masw_decode_mma.cu + masw_internal.cuh); None otherwise."""
-    import hashlib
     import re
     try:
         csrc = os.path.join(ROOT, "compressed_draft_kv_gb300", "csrc")
-        h = hashlib.sha256()
-        for name in ("masw_decode_mma.cu", "masw_internal.cuh"):
-            with open(os.path.join(csrc, name), "rb") as f:
-                h.update(f.read())
+        code = _code_hash([os.path.join(csrc, n) for n in ("masw_decode_mma.cu", "masw_internal.cuh")])
         with open(os.path.join(ROOT, "profiles", "decode_mma_step_b8_32k.md")) as f:
             txt = f.read()
         rec = re.search(r"first 16 hex\): `([0-9a-f]{16})`", txt)
         val = re.search(r"traffic_bytes_per_launch: (\d+)", txt)
-        if rec and val and rec.group(1) == h.hexdigest()[:16]:
+        if rec and val and rec.group(1) == code:
             return int(val.group(1))
     except OSError:
         pass
