@@ -36,18 +36,22 @@ METRIC = "MASW draft-attn decode steps/s (28 layers x batch 8, 32K prefix)"
 UNIT = "decode steps/s"
 
 
-def _code_hash(paths):
-    """sha256 (first 16 hex) of C/CUDA sources with comments, trailing blanks
-    and empty lines removed: edits to comments leave it unchanged."""
-    import hashlib
+def _code_only(src: str) -> str:
+    """C/CUDA source with comments, trailing blanks and empty lines removed."""
     import re
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    src = re.sub(r"//[^\n]*", "", src)
+    return "\n".join(ln.rstrip() for ln in src.splitlines() if ln.strip())
+
+
+def _code_hash(paths):
+    """sha256 (first 16 hex) of the code of C/CUDA sources: edits to comments
+    leave it unchanged."""
+    import hashlib
     h = hashlib.sha256()
     for path in paths:
         with open(path) as f:
-            s = f.read()
-        s = re.sub(r"/\*.*?\*/", "", s, flags=re.S)
-        s = re.sub(r"//[^\n]*", "", s)
-        h.update("\n".join(ln.rstrip() for ln in s.splitlines() if ln.strip()).encode())
+            h.update(_code_only(f.read()).encode())
     return h.hexdigest()[:16]
 
 
