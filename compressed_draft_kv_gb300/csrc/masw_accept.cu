@@ -2,7 +2,9 @@
 // and §3.3 Algorithm 2; the pages' experiments decode greedily, T = 0).
 //
 // For sequence b the target's token at block position j (0..L) is the argmax of
-// logits[b][j][0..V) (ties to the smallest id).  Draft token j is accepted while
+// logits[b][j][0..V) (ties to the smallest id; NaN entries are skipped, since
+// every comparison with NaN is false; a row with nothing but NaN has no token
+// and reports -1, which no draft equals).  Draft token j is accepted while
 // it equals the target's token at j; the first mismatch (or position L when all
 // L drafts match) contributes the target's own token, so L_acc + 1 tokens are
 // emitted and they are exactly tokens[b][0 .. L_acc].
@@ -137,8 +139,10 @@ __global__ void __launch_bounds__(256) accept_kernel(const __grid_constant__ Acc
             if (better(ov, oi, mv, mi)) { mv = ov; mi = oi; }
         }
         if (lane == 0) {
-            p.tokens[b * (p.L + 1) + jj] = mi;
-            if (jj < 64) s_tok[jj] = mi;
+            // no id survives only when every entry of the row is NaN: no greedy token
+            const int tok = mi == 0x7fffffff ? -1 : mi;
+            p.tokens[b * (p.L + 1) + jj] = tok;
+            if (jj < 64) s_tok[jj] = tok;
         }
     }
     __syncthreads();

@@ -59,7 +59,7 @@ __all__ = [
     "local_window", "n_local", "slot_count", "boundary", "is_boundary",
     "slot_pos_id", "working_set_size", "draft_mask", "slot_write_mask",
     "full_mask", "verify_mask", "attention", "IndexSim", "MaswOracle",
-    "verify_attn", "greedy_accept", "eq1_speedup", "prefill_attn",
+    "verify_attn", "greedy_token", "greedy_accept", "eq1_speedup", "prefill_attn",
 ]
 
 
@@ -452,12 +452,26 @@ def verify_attn(q, k_cache, v_cache, kv_len, scale: float | None = None):
 # Speculative acceptance and the speedup model.
 # --------------------------------------------------------------------------
 
+def greedy_token(row) -> int:
+    """The target's greedy token for one logits row: the id of the largest
+    value, the smallest id among ties, NaN entries ignored (+inf and -inf are
+    values like any other).  A row with no value but NaN has no greedy token:
+    -1.  (The pages decode at temperature 0 and say nothing of NaN logits;
+    skipping them is this library's reading.)"""
+    row = np.asarray(row, dtype=np.float64)
+    ids = np.flatnonzero(~np.isnan(row))
+    if ids.size == 0:
+        return -1
+    return int(ids[np.argmax(row[ids])])   # np.argmax: first position of the maximum
+
+
 def greedy_accept(logits, draft):
     """Greedy speculative acceptance ([EN] §2.2, §3.3 Algorithm 2; the
     experiments use temperature 0).  logits [B, L+1, V], draft [B, L] ->
-    tokens [B, L+1] (target argmax per position, first index among ties) and
-    n_emit [B] = L_acc + 1, L_acc = number of leading drafts equal to the
-    target's tokens."""
+    tokens [B, L+1] (greedy_token of each row: argmax, first index among ties,
+    NaN skipped, -1 for an all-NaN row) and n_emit [B] = L_acc + 1, L_acc =
+    number of leading drafts equal to the target's tokens (a draft never equals
+    -1, so an all-NaN row rejects its draft)."""
     logits = np.asarray(logits, dtype=np.float64)
     draft = np.asarray(draft)
     B, L1, V = logits.shape
@@ -466,7 +480,7 @@ def greedy_accept(logits, draft):
     n_emit = np.zeros(B, dtype=np.int64)
     for b in range(B):
         for j in range(L1):
-            tokens[b, j] = int(np.argmax(logits[b, j]))
+            tokens[b, j] = greedy_token(logits[b, j])
         l_acc = 0
         while l_acc < L and draft[b, l_acc] == tokens[b, l_acc]:
             l_acc += 1

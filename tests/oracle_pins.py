@@ -421,7 +421,8 @@ def pin_rollback(o):
 def pin_greedy_accept(o):
     """Greedy acceptance against a hand loop on tiny logits, with the special
     cases: all drafts accepted (bonus token), first draft rejected, ties going
-    to the smallest id."""
+    to the smallest id, NaN entries skipped, +-inf rows, and an all-NaN row
+    (token -1, which rejects the draft at that position)."""
     rng = _rng(21)
     B, L, V = 5, 4, 11
     logits = rng.standard_normal((B, L + 1, V))
@@ -449,6 +450,18 @@ def pin_greedy_accept(o):
     tied[0, 0, [2, 4]] = 1.0
     tok, n = o.greedy_accept(tied, np.array([[2]]))
     assert tok[0, 0] == 2 and n[0] == 2 and tok[0, 1] == 0
+    # NaN entries are skipped, +-inf are values, an all-NaN row has no token
+    # (-1), which no draft equals; expected ids written out by hand
+    nan, inf = math.nan, math.inf
+    rows = [[1.0, nan, 3.0, nan, 3.0, 0.0],          # -> 2 (NaN skipped, tie to the smaller id)
+            [nan, nan, nan, nan, nan, nan],          # -> -1
+            [-inf, nan, -inf, -inf, nan, -inf],      # -> 0 (-inf is a value)
+            [nan, -inf, 5.0, inf, inf, nan],         # -> 3
+            [nan, nan, nan, nan, nan, -2.5]]         # -> 5
+    tok, n = o.greedy_accept(np.array([rows]), np.array([[2, 1, 0, 3]]))
+    assert list(tok[0]) == [2, -1, 0, 3, 5] and n[0] == 2
+    tok, n = o.greedy_accept(np.array([[rows[3], rows[4], rows[1]]]), np.array([[3, 5]]))
+    assert list(tok[0]) == [3, 5, -1] and n[0] == 3
 
 
 def pin_eq1(o):

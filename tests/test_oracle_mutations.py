@@ -64,6 +64,9 @@ MUTATIONS = {
     "verify_causal_shift": ("verify_mask", lambda kv_len, Lq: _verify_shift(kv_len, Lq)),
     "sink_dropped": ("draft_mask", lambda t, n_slots, S, W: _draft_no_sink(t, n_slots, S, W)),
     "accept_one_past_mismatch": ("greedy_accept", lambda logits, draft: _accept_off_by_one(logits, draft)),
+    "greedy_argmax_returns_first_nan": ("greedy_token", lambda row: int(np.argmax(np.asarray(row, np.float64)))),
+    "greedy_nan_as_minus_inf": ("greedy_token",
+                                lambda row: int(np.argmax(np.nan_to_num(np.asarray(row, np.float64), nan=-np.inf)))),
     "prefill_raw_sees_slot_of_its_own_boundary": ("prefill_attn", lambda *a, **k: _prefill_slot_too_early(*a, **k)),
     "eq1_without_verify_cost": ("eq1_speedup", lambda l_acc, l_draft, t_d, t_t: (l_acc + 1.0) / (l_draft * t_d / t_t)
                                 if t_d else l_acc + 1.0),
