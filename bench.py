@@ -274,6 +274,9 @@ class DraftBench:
         return g, n
 
     def time_graph(self, g, warmup: int, steps: int, barrier=None):
+        """Seconds for `steps` back-to-back replays (first to last event), after
+        `warmup` untimed ones; an event between replays also gives each replay's
+        own duration, whose median is kept in self.last_median_s."""
         torch = self.torch
         for _ in range(warmup):
             g.replay()
@@ -281,18 +284,19 @@ class DraftBench:
         if barrier:
             barrier()
         torch.cuda.synchronize()
-        e0 = torch.cuda.Event(enable_timing=True)
-        e1 = torch.cuda.Event(enable_timing=True)
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1)]
         with torch.cuda.stream(self.stream):
-            e0.record(self.stream)
-            for _ in range(steps):
+            ev[0].record(self.stream)
+            for i in range(steps):
                 g.replay()
-            e1.record(self.stream)
+                ev[i + 1].record(self.stream)
         torch.cuda.synchronize()
         if barrier:
             barrier()
         torch.cuda.synchronize()
-        return e0.elapsed_time(e1) / 1e3
+        per = [ev[i].elapsed_time(ev[i + 1]) / 1e3 for i in range(steps)]
+        self.last_median_s = statistics.median(per)
+        return ev[0].elapsed_time(ev[steps]) / 1e3
 
     def kv_bytes_per_decode_step(self, full: bool = False):
         """K/V bytes one decode step reads over all layers and sequences (at the
@@ -579,41 +583,102 @@ def whole_job_rate(world: int, units_per_rank: float, secs: float) -> float:
 
 # ------------------------------------------------------------ CPU oracle --
 
+class OracleIteration:
+    """The CPU oracle, as it stands, on one (layer, sequence) pair of the
+    default workload's 32K state, running the GPU arm's speculative iteration:
+    L_draft x (append + draft attention), the slot write at the step that
+    reaches the compression boundary, and the rollback of the speculative
+    tokens after the last step.  unit() is one (layer, sequence) decode step;
+    a decode step of the workload is layers x batch units (slot writes and
+    rollbacks come in the GPU arm's proportion: one per L_draft units)."""
+
+    def __init__(self):
+        import oracle.masw_oracle as orc
+        from compressed_draft_kv_gb300 import synth
+        self.orc, self.synth = orc, synth
+        w = synth.WORKLOADS[WORKLOAD]
+        self.w = w
+        S, W, r, Hkv, D, prefix = w["S"], w["W"], w["r"], w["Hkv"], w["D"], w["prefix"]
+        n = orc.slot_count(prefix, S, W, r)
+        kr = synth.normal((prefix, Hkv, D), "bf16", "cpu-sample", "k").float().numpy()
+        vr = synth.normal((prefix, Hkv, D), "bf16", "cpu-sample", "v").float().numpy()
+        ks = synth.normal((n, Hkv, D), "bf16", "cpu-sample", "ks").float().numpy()
+        vs = synth.normal((n, Hkv, D), "bf16", "cpu-sample", "vs").float().numpy()
+        self.mem = orc.MaswOracle(S, W, r, Hkv, D, 1, 1, reserve=16)
+        self.mem.load(0, 0, kr, vr, ks, vs)
+        self.prefix = prefix
+        self.i = 0
+        self.units = 0
+        self.slot_writes = 0
+        self.rollbacks = 0
+
+    def unit(self):
+        orc, synth, w = self.orc, self.synth, self.w
+        Hkv, Hq, D = w["Hkv"], w["Hq"], w["D"]
+        s_ = self.i % w["steps"]
+        k = synth.normal((1, Hkv, D), "bf16", "cpu-sample", "k1", s_).float().numpy()
+        v = synth.normal((1, Hkv, D), "bf16", "cpu-sample", "v1", s_).float().numpy()
+        q = synth.normal((1, Hq, D), "bf16", "cpu-sample", "q1", s_).float().numpy()
+        self.mem.append(0, k, v)
+        self.mem.draft_attn(0, q)
+        t = self.mem.t(0, 0)
+        if orc.is_boundary(t, w["S"], w["W"], w["r"]) and self.mem.m(0, 0) == orc.slot_count(t, w["S"], w["W"], w["r"]) - 1:
+            g = synth.normal((1, Hq, D), "bf16", "cpu-sample", "qg").float().numpy()
+            kg = synth.normal((1, Hkv, D), "bf16", "cpu-sample", "kg").float().numpy()
+            self.mem.materialize_slot(0, [0], g, kg, kg)
+            self.slot_writes += 1
+        if s_ == w["steps"] - 1:
+            self.mem.rollback([0], [self.prefix])
+            self.rollbacks += 1
+        self.i += 1
+        self.units += 1
+
+
+def _cores():
+    return len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+
+
 def oracle_sample(seconds_budget: float = 12.0):
-    """The CPU oracle as it stands, on a bounded sample of the workload: one
-    (layer, sequence) of the 32K state, repeatedly appending a token and running
-    one draft attention; scaled to the metric's unit (28 layers x 8 sequences
-    per decode step)."""
-    import numpy as np
-    import oracle.masw_oracle as orc
-    from compressed_draft_kv_gb300 import synth
-    w = synth.WORKLOADS[WORKLOAD]
-    S, W, r, Hkv, D, Hq, prefix = w["S"], w["W"], w["r"], w["Hkv"], w["D"], w["Hq"], w["prefix"]
-    n = orc.slot_count(prefix, S, W, r)
-    kr = synth.normal((prefix, Hkv, D), "bf16", "cpu-sample", "k").float().numpy()
-    vr = synth.normal((prefix, Hkv, D), "bf16", "cpu-sample", "v").float().numpy()
-    ks = synth.normal((n, Hkv, D), "bf16", "cpu-sample", "ks").float().numpy()
-    vs = synth.normal((n, Hkv, D), "bf16", "cpu-sample", "vs").float().numpy()
-    mem = orc.MaswOracle(S, W, r, Hkv, D, 1, 1)
-    mem.load(0, 0, kr, vr, ks, vs)
-    done = 0
+    """cpu_baseline of the GPU arm: the oracle's speculative iteration
+    (OracleIteration) for about `seconds_budget` seconds, as decode steps/s."""
+    it = OracleIteration()
+    w = it.w
     t0 = time.perf_counter()
     while True:
-        k = synth.normal((1, Hkv, D), "bf16", "cpu-sample", "k1", done).float().numpy()
-        q = synth.normal((1, Hq, D), "bf16", "cpu-sample", "q1", done).float().numpy()
-        mem.append(0, k, k)
-        mem.draft_attn(0, q)
-        done += 1
+        it.unit()
         el = time.perf_counter() - t0
-        if el > seconds_budget or done >= 200:
+        if el > seconds_budget or it.units >= 400:
             break
-    per_unit = el / done                              # one (layer, seq) draft step
-    steps_per_s = 1.0 / (per_unit * w["layers"] * w["batch"])
-    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
-    return {"value": steps_per_s, "unit": UNIT, "cores": cores, "kind": "oracle",
-            "sample": f"{done} x (append + draft attention) of one (layer, sequence) at a {prefix}-token "
-                      f"prefix in {el:.1f} s, scaled x{w['layers'] * w['batch']} to one decode step; "
-                      f"numpy fp64, default BLAS threading"}
+    steps_per_s = it.units / el / (w["layers"] * w["batch"])
+    return {"value": steps_per_s, "unit": UNIT, "cores": _cores(), "kind": "oracle",
+            "sample": f"{it.units} (layer, sequence) decode steps of one pair at a {it.prefix}-token prefix "
+                      f"(append + draft attention, {it.slot_writes} slot writes, {it.rollbacks} rollbacks: "
+                      f"the GPU arm's iteration) in {el:.1f} s; a decode step is {w['layers']} x {w['batch']} "
+                      f"such units; numpy fp64, default BLAS threading"}
+
+
+def reference_arm(steps: int, warmup: int):
+    """The reference arm: the CPU oracle timed as it stands.  One reference
+    step = one sequence's decode step through all layers (`layers` units of
+    OracleIteration), i.e. 1/batch of a decode step of the workload; `warmup`
+    untimed steps, then `steps` timed ones."""
+    it = OracleIteration()
+    w = it.w
+    for _ in range(warmup * w["layers"]):
+        it.unit()
+    u0 = it.units
+    t0 = time.perf_counter()
+    for _ in range(steps * w["layers"]):
+        it.unit()
+    el = time.perf_counter() - t0
+    ms_per_step = el * 1e3 / steps
+    value = steps / el / w["batch"]            # decode steps (all layers x batch) per second
+    sample = (f"{steps} timed reference steps after {warmup} untimed; a reference step is one sequence's "
+              f"decode step through all {w['layers']} layers ({w['layers']} x append + draft attention on one "
+              f"(layer, sequence) pair at a {it.prefix}-token prefix, with the GPU arm's slot writes and "
+              f"rollbacks: {it.slot_writes} and {it.rollbacks} in all), 1/{w['batch']} of a decode step; "
+              f"{it.units - u0} units in {el:.1f} s; numpy fp64, default BLAS threading")
+    return {"value": value, "ms_per_step": ms_per_step, "secs": el, "sample": sample, "cores": _cores()}
 
 
 # ------------------------------------------------------- profiling case --
@@ -685,7 +750,7 @@ def main():
     ap.add_argument("--impl", default="masw", choices=["masw", "reference"])
     ap.add_argument("--workload", default=WORKLOAD,
                     choices=["draft3b_28l_b8", "draft3b_28l_b1", "draft8b_b32_ragged", "draft3b_1layer_8k", "paper_s128_w128_r4",
-                             "paper_s128_w128_r8"])
+                             "paper_s128_w128_r8", "swa_w1024"])
     ap.add_argument("--prefix", type=int, default=None, help="override the prefix (all sequences)")
     ap.add_argument("--batch", type=int, default=None, help="override the number of sequences")
     ap.add_argument("--sweep", action="store_true",
@@ -721,15 +786,16 @@ def main():
     if args.impl == "reference":
         if rank != 0:
             return
-        cb = oracle_sample(seconds_budget=max(5.0, min(60.0, 0.5 * args.steps)))
-        ms = 1e3 / cb["value"] * synth.WORKLOADS[WORKLOAD]["steps"]
+        ref = reference_arm(args.steps, args.warmup)
+        cb = {"value": ref["value"], "unit": UNIT, "cores": ref["cores"], "kind": "oracle", "sample": ref["sample"]}
         print(json.dumps({
-            "impl": "reference", "metric": METRIC, "value": cb["value"], "unit": UNIT, "n_gpus": 0,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": f"{WORKLOAD} (CPU oracle sample)", "prefix": prefix},
+            "impl": "reference", "metric": METRIC, "value": ref["value"], "unit": UNIT, "n_gpus": 0,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ref["ms_per_step"],
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "prefix": prefix,
+                       "reference_step": "one sequence's decode step through all layers (1/batch of a decode step)"},
             "cpu_baseline": cb,
-            "e2e": {"value": cb["value"], "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+            "e2e": {"value": ref["value"], "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
         }))
         return
 
@@ -788,6 +854,7 @@ def main():
     full_iters = max(3, args.steps // 5)
     with ClockSampler(local) as clk:
         secs = bench.time_graph(g_draft, args.warmup, args.steps, barrier)
+        median_step_s = bench.last_median_s
         secs_full = bench.time_graph(g_full, 3, full_iters, barrier)
     kern_s, _ = bench.time_draft_kernel(reps=50)
     e2e_s, h2d, d2h = bench.e2e(args.e2e_iters)
@@ -820,11 +887,13 @@ def main():
     full_value = whole_job_rate(world, full_iters * dsteps, secs_full)
     peak, peak_kind = _peaks()
     achieved = total_b / kern_s / 1e9
+    traffic = _recorded_traffic() if args.workload == WORKLOAD and args.batch is None and args.prefix is None else None
     line = {
         "metric": (METRIC if args.workload == WORKLOAD and args.batch is None and args.prefix is None
                    else f"MASW draft-attn decode steps/s ({args.workload}, batch {wl['batch']}, prefix {prefix})"),
         "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": secs / args.steps * 1e3, "higher_is_better": True,
+        "warmup": args.warmup, "ms_per_step": secs / args.steps * 1e3,
+        "ms_per_step_median": median_step_s * 1e3, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": args.workload, "layers": wl["layers"], "batch": wl["batch"], "q_heads": wl["Hq"],
                    "kv_heads": wl["Hkv"], "head_dim": wl["D"],
@@ -839,8 +908,11 @@ def main():
                     "gbs": kv_step_full * full_iters * dsteps / secs_full / 1e9},
         "speedup_vs_full_kv": value / full_value,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                     "frac": achieved / peak, "traffic": (_recorded_traffic() if args.workload == WORKLOAD and args.batch is None
-                                 and args.prefix is None else None),
+                     "frac": achieved / peak, "traffic": traffic,
+                     "traffic_source": ("recorded, not measured in this run: ncu dram__bytes_read.sum + "
+                                        "dram__bytes_write.sum per launch from profiles/decode_mma_step_b8_32k.md, "
+                                        "whose kernel code hash matches the built sources" if traffic is not None
+                                        else "none: no ncu capture of the current kernel code for this workload"),
                      "peak_kind": peak_kind,
                      "kernel": "decode_mma_kernel<128, NST> (masw_draft_step: fused append + draft attention; NST = 2 stages, 3 when each CTA streams a long run of keys)",
                      "bytes_per_launch": total_b, "kv_bytes_per_launch": kv_b,

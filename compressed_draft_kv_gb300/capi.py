@@ -14,6 +14,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(HERE, "libmasw.so")
 
 MASW_OK, MASW_EINVAL, MASW_ENOMEM, MASW_ECAPACITY, MASW_ESTATE, MASW_ECUDA, MASW_ETIMEOUT = 0, -1, -2, -3, -4, -5, -6
+MASW_EGUARD = -7
 MASW_F32, MASW_BF16 = 0, 1
 MASW_MAX_BATCH, MASW_MAX_GROUP = 512, 8
 
@@ -23,7 +24,7 @@ EXPORTS = [
     "masw_materialize_slot", "masw_rollback", "masw_draft_attn", "masw_full_attn",
     "masw_draft_step", "masw_full_step", "masw_draft_step_slot",
     "masw_verify_attn", "masw_verify_workspace_bytes", "masw_verify_attn_noalloc", "masw_mem_load", "masw_mem_export",
-    "masw_query", "masw_sync", "masw_index", "masw_version",
+    "masw_query", "masw_sync", "masw_index", "masw_version", "masw_check_guards",
     "masw_greedy_accept", "masw_greedy_workspace_bytes", "masw_eq1_speedup", "masw_prefill",
     "masw_selftest_timeout",
 ]
@@ -62,6 +63,7 @@ def load() -> ctypes.CDLL:
     sig = {
         "masw_mem_create": [I, I, I, I, I, I, ctypes.POINTER(masw_opts_t), ctypes.POINTER(P)],
         "masw_mem_destroy": [P],
+        "masw_check_guards": [P],
         "masw_append_kv": [P, I, P, P, P, P],
         "masw_materialize_slot": [P, I, IP, I, P, P, P, P, P, I, P],
         "masw_rollback": [P, IP, IP, I, P],
@@ -74,7 +76,7 @@ def load() -> ctypes.CDLL:
         "masw_selftest_timeout": [P, I, P],
         "masw_verify_attn": [P, P, P, P, I, I, I, I, I, I, I, F, P, P, P, Z, P],
         "masw_verify_workspace_bytes": [I, I, I, I, I, I, ctypes.POINTER(Z)],
-        "masw_verify_attn_noalloc": [P, P, P, P, I, I, I, I, I, I, I, F, P, P, P],
+        "masw_verify_attn_noalloc": [P, P, P, P, I, I, I, I, I, I, I, F, P, P, P, P],
         "masw_mem_load": [P, I, I, I, P, P, P, P, I],
         "masw_mem_export": [P, I, I, P, P, IP],
         "masw_query": [P, I, I, ctypes.POINTER(masw_state_t)],
@@ -137,6 +139,12 @@ def masw_mem_create(S, W, r, n_kv_heads, head_dim, layers, batch=1, dtype=MASW_B
 
 def masw_mem_destroy(handle):
     _check(load().masw_mem_destroy(handle))
+
+
+def masw_check_guards(handle):
+    """Raise MaswError(MASW_EGUARD) if a guard band around one of the handle's
+    device buffers was overwritten (synchronises the device)."""
+    _check(load().masw_check_guards(handle), handle)
 
 
 def masw_last_error(handle=None) -> str:
@@ -228,13 +236,15 @@ def masw_verify_attn(q, k_cache, v_cache, kv_len, o, lse=None, workspace=None, s
                                    _stream(stream)))
 
 
-def masw_verify_attn_noalloc(q, k_cache, v_cache, kv_len, o, lse=None, scale=0.0, stream=None):
+def masw_verify_attn_noalloc(q, k_cache, v_cache, kv_len, o, lse=None, scale=0.0, status=None, stream=None):
     """masw_verify_attn for callers that cannot allocate: no workspace, the
-    library's own fixed device array holds the split partials."""
+    library's own fixed device array holds the split partials.  status: an
+    optional device int32 tensor that receives the call's status word."""
     B, Lq, Hq, D = q.shape
     Hkv, Tmax = k_cache.shape[1], k_cache.shape[2]
     _check(load().masw_verify_attn_noalloc(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(kv_len), B, Lq, Hq, Hkv, D,
-                                           Tmax, MASW_BF16, scale, _ptr(o), _ptr(lse), _stream(stream)))
+                                           Tmax, MASW_BF16, scale, _ptr(o), _ptr(lse), _ptr(status),
+                                           _stream(stream)))
 
 
 def masw_greedy_accept(logits, draft, tokens, n_emit, workspace=None, stream=None):

@@ -68,11 +68,28 @@ struct masw_mem {
     void* last_stream = nullptr;
     int last_write_layer = -2;
     std::string err;
+    // Every device buffer above is the middle of one allocation with a guard
+    // band of masw::kGuardBytes on each side, filled with masw::kGuardByte at
+    // create time; masw_check_guards reads the bands back.
+    struct Alloc {
+        void* raw;          // cudaMalloc'd base: [guard][buffer][guard]
+        size_t bytes;       // buffer bytes
+        const char* name;
+    };
+    std::vector<Alloc> allocs;
+    size_t alloc_total = 0;   // bytes allocated (guards included)
+    size_t alloc_limit = 0;   // 0: none; else create refuses to allocate beyond it
 };
 
 namespace masw {
 
 constexpr int kMaxSplit = 256;
+
+// guard bands around every handle-owned device buffer (out-of-bounds write
+// evidence): 4 KiB of 0xC3 before and after; 4 KiB keeps the buffers'
+// 256-byte alignment
+constexpr size_t kGuardBytes = 4096;
+constexpr unsigned char kGuardByte = 0xC3;
 
 // bounded-wait budget: ~2^22 polls with backoff is seconds, far above any
 // legitimate TMA latency; running out records MASW_ETIMEOUT and returns.

@@ -12,6 +12,8 @@
 //   d_pos          : [L][B][M_max] 0-based slot position ids
 #include "masw_internal.cuh"
 
+#include <cstdlib>
+
 #include <algorithm>
 #include <cmath>
 #include <cstring>
@@ -151,10 +153,40 @@ int check_heads(masw_mem_t* mem, int n_q_heads) {
 }
 
 void free_all(masw_mem_t* m) {
-    void* ptrs[] = {m->pool_k, m->pool_v, m->full_k, m->full_v, m->d_t, m->d_m,
-                    m->d_pos, m->d_err, m->part, m->tickets};
-    for (void* p : ptrs)
-        if (p) cudaFree(p);
+    for (const masw_mem::Alloc& a : m->allocs) cudaFree(a.raw);
+    m->allocs.clear();
+    m->alloc_total = 0;
+}
+
+// A handle-owned device buffer of `bytes` with a guard band on each side
+// (filled with kGuardByte); false when the allocation fails or would take the
+// handle past its allocation limit.
+bool guarded_alloc(masw_mem_t* m, void** out, size_t bytes, const char* name) {
+    const size_t raw_bytes = bytes + 2 * kGuardBytes;
+    if (m->alloc_limit && m->alloc_total + raw_bytes > m->alloc_limit) return false;
+    void* raw = nullptr;
+    if (cudaMalloc(&raw, raw_bytes) != cudaSuccess) {
+        cudaGetLastError();
+        return false;
+    }
+    m->allocs.push_back({raw, bytes, name});
+    m->alloc_total += raw_bytes;
+    if (cudaMemset(raw, kGuardByte, kGuardBytes) != cudaSuccess ||
+        cudaMemset((uint8_t*)raw + kGuardBytes + bytes, kGuardByte, kGuardBytes) != cudaSuccess) {
+        cudaGetLastError();
+        return false;
+    }
+    *out = (uint8_t*)raw + kGuardBytes;
+    return true;
+}
+
+// the allocation limit of a new handle: MASW_DEVICE_MEMORY_LIMIT (bytes), 0 = none
+size_t alloc_limit_from_env() {
+    const char* e = std::getenv("MASW_DEVICE_MEMORY_LIMIT");
+    if (!e || !*e) return 0;
+    char* end = nullptr;
+    const unsigned long long v = std::strtoull(e, &end, 10);
+    return (end && *end == '\0') ? (size_t)v : 0;
 }
 
 bool is_device_ptr(const void* p) {
@@ -268,6 +300,15 @@ int masw_mem_create(int S, int W, int r, int n_kv_heads, int head_dim, int layer
         delete m;
         return masw_set_error(nullptr, code, msg);
     };
+    m->alloc_limit = alloc_limit_from_env();
+    {
+        // the pools alone (before any CUDA call): a limit below them is refused here
+        const size_t pool_raw = (size_t)layers * m->B * n_kv_heads * m->C * head_dim * m->esize + 2 * kGuardBytes;
+        if (m->alloc_limit && 2 * pool_raw > m->alloc_limit)
+            return fail(MASW_ENOMEM, "create: the pool needs " + std::to_string(2 * pool_raw) +
+                                         " bytes, above the allocation limit (MASW_DEVICE_MEMORY_LIMIT) of " +
+                                         std::to_string(m->alloc_limit));
+    }
     if (cudaGetDevice(&m->device) != cudaSuccess) return fail(MASW_ECUDA, "create: no CUDA device");
     if (cudaDeviceGetAttribute(&m->num_sms, cudaDevAttrMultiProcessorCount, m->device) != cudaSuccess)
         return fail(MASW_ECUDA, "create: cannot query the device");
@@ -275,27 +316,28 @@ int masw_mem_create(int S, int W, int r, int n_kv_heads, int head_dim, int layer
     const size_t rowb = (size_t)head_dim * m->esize;
     const size_t blocks = (size_t)layers * m->B * n_kv_heads;
     const size_t pool_bytes = blocks * m->C * rowb;
-    if (cudaMalloc(&m->pool_k, pool_bytes) != cudaSuccess || cudaMalloc(&m->pool_v, pool_bytes) != cudaSuccess)
+    if (!guarded_alloc(m, &m->pool_k, pool_bytes, "pool_k") || !guarded_alloc(m, &m->pool_v, pool_bytes, "pool_v"))
         return fail(MASW_ENOMEM, "create: pool allocation failed");
     if (cudaMemset(m->pool_k, 0, pool_bytes) != cudaSuccess || cudaMemset(m->pool_v, 0, pool_bytes) != cudaSuccess)
         return fail(MASW_ECUDA, "create: pool clear failed");
     if (m->full_kv) {
         const size_t fb = blocks * (size_t)m->max_seq_len * rowb;
-        if (cudaMalloc(&m->full_k, fb) != cudaSuccess || cudaMalloc(&m->full_v, fb) != cudaSuccess)
+        if (!guarded_alloc(m, &m->full_k, fb, "full_k") || !guarded_alloc(m, &m->full_v, fb, "full_v"))
             return fail(MASW_ENOMEM, "create: full-KV cache allocation failed");
     }
     const size_t lb = (size_t)layers * m->B;
     const size_t lbh = lb * n_kv_heads;
-    if (cudaMalloc(&m->d_t, lbh * sizeof(int)) != cudaSuccess || cudaMalloc(&m->d_m, lbh * sizeof(int)) != cudaSuccess ||
-        cudaMalloc(&m->d_pos, std::max<size_t>(1, lb * m->M_max) * sizeof(int)) != cudaSuccess ||
-        cudaMalloc(&m->d_err, 4 * sizeof(int)) != cudaSuccess)
+    if (!guarded_alloc(m, (void**)&m->d_t, lbh * sizeof(int), "d_t") ||
+        !guarded_alloc(m, (void**)&m->d_m, lbh * sizeof(int), "d_m") ||
+        !guarded_alloc(m, (void**)&m->d_pos, std::max<size_t>(1, lb * m->M_max) * sizeof(int), "d_pos") ||
+        !guarded_alloc(m, (void**)&m->d_err, 4 * sizeof(int), "d_err"))
         return fail(MASW_ENOMEM, "create: counter allocation failed");
     // split scratch: enough partials for ~3 CTAs per SM at G <= 8
     const size_t pairs = (size_t)m->B * n_kv_heads;
     const size_t splits = std::min<size_t>(kMaxSplit, std::max<size_t>(8, (3 * (size_t)m->num_sms + pairs - 1) / pairs));
     m->part_floats = pairs * splits * MASW_MAX_GROUP * (head_dim + 2);
-    if (cudaMalloc(&m->part, m->part_floats * sizeof(float)) != cudaSuccess ||
-        cudaMalloc(&m->tickets, pairs * sizeof(unsigned)) != cudaSuccess)
+    if (!guarded_alloc(m, (void**)&m->part, m->part_floats * sizeof(float), "part") ||
+        !guarded_alloc(m, (void**)&m->tickets, pairs * sizeof(unsigned), "tickets"))
         return fail(MASW_ENOMEM, "create: scratch allocation failed");
     if (cudaMemset(m->d_t, 0, lbh * sizeof(int)) != cudaSuccess || cudaMemset(m->d_m, 0, lbh * sizeof(int)) != cudaSuccess ||
         cudaMemset(m->d_pos, 0xff, std::max<size_t>(1, lb * m->M_max) * sizeof(int)) != cudaSuccess ||
@@ -304,6 +346,27 @@ int masw_mem_create(int S, int W, int r, int n_kv_heads, int head_dim, int layer
         cudaDeviceSynchronize() != cudaSuccess)
         return fail(MASW_ECUDA, "create: counter clear failed");
     *out = m;
+    return MASW_OK;
+}
+
+int masw_check_guards(masw_mem_t* mem) {
+    if (!mem) return masw_set_error(nullptr, MASW_EINVAL, "check_guards: NULL handle");
+    MASW_CUDA_TRY(mem, cudaDeviceSynchronize());
+    std::vector<unsigned char> band(kGuardBytes);
+    for (const masw_mem::Alloc& a : mem->allocs) {
+        for (int side = 0; side < 2; ++side) {
+            const uint8_t* src = (const uint8_t*)a.raw + (side ? kGuardBytes + a.bytes : 0);
+            MASW_CUDA_TRY(mem, cudaMemcpy(band.data(), src, kGuardBytes, cudaMemcpyDeviceToHost));
+            for (size_t i = 0; i < kGuardBytes; ++i)
+                if (band[i] != kGuardByte) {
+                    const long long off = side ? (long long)(a.bytes + i) : (long long)i - (long long)kGuardBytes;
+                    return masw_set_error(mem, MASW_EGUARD,
+                                          std::string("check_guards: ") + a.name + " overwritten at byte offset " +
+                                              std::to_string(off) + " (buffer of " + std::to_string(a.bytes) +
+                                              " bytes)");
+                }
+        }
+    }
     return MASW_OK;
 }
 

@@ -590,16 +590,17 @@ extern "C" int masw_verify_attn(const void* q, const void* k_cache, const void* 
 // part of the library image: every GPU that loads the library holds these
 // 4 MiB + 16 KiB until the process exits.
 //
-// Limits: B * Hkv <= kNoAllocMaxPairs; when the partials of the usual split
-// count would not fit in kNoAllocPartBytes the call uses fewer splits (one
-// split needs no partials at all), so it is never refused for length alone.
+// Limits: B * Hkv <= kNoAllocMaxPairs.  The partials of the usual split count
+// fit in kNoAllocPartBytes on any GPU with up to about 250 SMs (the split count
+// stops at one CTA per SM, and NQ <= 32 rows of 130 floats per split): on a
+// 152-SM GB300 they take at most ~2.5 MB.  The loop that lowers the split count
+// when they would not fit is a guard for larger devices.
 // All calls share the array and each leaves its partials in it; the tickets
-// are cleared on the stream at the start of every call.  Two calls that
-// overlap on the GPU (different streams, or different host threads) race on
-// the array and give wrong results: serialise them.
+// and the status word are cleared on the stream at the start of every call,
+// and the status word can be copied out to the caller after the kernel.  Two
+// calls that overlap on the GPU (different streams, or different host threads)
+// race on the array and give wrong results: serialise them.
 // ---------------------------------------------------------------------------
-#include <mutex>
-
 namespace masw {
 constexpr size_t kNoAllocPartBytes = (size_t)4 << 20;
 constexpr int kNoAllocMaxPairs = 4096;
@@ -608,30 +609,27 @@ constexpr size_t kNoAllocBytes = kNoAllocPartBytes + (size_t)kNoAllocMaxPairs * 
 
 static __device__ __align__(256) uint8_t g_noalloc_scratch[masw::kNoAllocBytes];
 
-// Device address of g_noalloc_scratch per device.  In host code the array's
-// name is only a host-side stand-in; the kernel must be given this address.
-static void* g_noalloc_ptr[64];
-static std::mutex g_noalloc_mu;
-
-static int noalloc_scratch(int dev, void** out) {
-    std::lock_guard<std::mutex> lock(g_noalloc_mu);
-    if (!g_noalloc_ptr[dev]) {
-        void* p = nullptr;
-        cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
-        if (e != cudaSuccess || !p) {
-            cudaGetLastError();
-            return masw_set_error(nullptr, MASW_ECUDA, std::string("verify_noalloc: cudaGetSymbolAddress: ") +
-                                                           cudaGetErrorString(e));
-        }
-        g_noalloc_ptr[dev] = p;
+// Device address of g_noalloc_scratch in the current context.  In host code the
+// array's name is only a host-side stand-in; the kernel must be given this
+// address.  It is looked up on every call (a table lookup in the runtime, no
+// allocation) rather than cached, so it stays right when a context is torn
+// down and re-created (cudaDeviceReset), which reloads the module and moves
+// the array.
+static int noalloc_scratch(void** out) {
+    void* p = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess || !p) {
+        cudaGetLastError();
+        return masw_set_error(nullptr, MASW_ECUDA,
+                              std::string("verify_noalloc: cudaGetSymbolAddress: ") + cudaGetErrorString(e));
     }
-    *out = g_noalloc_ptr[dev];
+    *out = p;
     return MASW_OK;
 }
 
 extern "C" int masw_verify_attn_noalloc(const void* q, const void* k_cache, const void* v_cache, const int* kv_len,
                                         int B, int Lq, int Hq, int Hkv, int D, int Tmax, int dtype, float scale,
-                                        float* o, float* lse, masw_stream_t stream) {
+                                        float* o, float* lse, int* status, masw_stream_t stream) {
     if (!q || !k_cache || !v_cache || !kv_len || !o)
         return masw_set_error(nullptr, MASW_EINVAL, "verify_noalloc: NULL pointer");
     if (dtype != MASW_BF16) return masw_set_error(nullptr, MASW_EINVAL, "verify_noalloc: only MASW_BF16 is supported");
@@ -644,15 +642,15 @@ extern "C" int masw_verify_attn_noalloc(const void* q, const void* k_cache, cons
                                   "; use masw_verify_attn with a workspace");
     if (((uintptr_t)q | (uintptr_t)k_cache | (uintptr_t)v_cache) & 15)
         return masw_set_error(nullptr, MASW_EINVAL, "verify_noalloc: q and caches must be 16-byte aligned");
-    if (((uintptr_t)o | (uintptr_t)lse | (uintptr_t)kv_len) & 3)
-        return masw_set_error(nullptr, MASW_EINVAL, "verify_noalloc: o, lse and kv_len must be 4-byte aligned");
-    int dev = 0, sms = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64 || num_sms_current(&sms)) {
+    if (((uintptr_t)o | (uintptr_t)lse | (uintptr_t)kv_len | (uintptr_t)status) & 3)
+        return masw_set_error(nullptr, MASW_EINVAL, "verify_noalloc: o, lse, kv_len and status must be 4-byte aligned");
+    int sms = 0;
+    if (num_sms_current(&sms)) {
         cudaGetLastError();
         return masw_set_error(nullptr, MASW_ECUDA, "verify_noalloc: cannot query the current device");
     }
     void* scratch = nullptr;
-    if ((rc = noalloc_scratch(dev, &scratch))) return rc;
+    if ((rc = noalloc_scratch(&scratch))) return rc;
     const int G = Hq / Hkv, NQ = G * Lq;
     int n_split = verify_splits(B, Hkv, Tmax, sms, (NQ + 7) / 8);
     while (n_split > 1 && verify_part_bytes(B, Hkv, NQ, n_split) > kNoAllocPartBytes) --n_split;
@@ -665,6 +663,13 @@ extern "C" int masw_verify_attn_noalloc(const void* q, const void* k_cache, cons
     if (e != cudaSuccess)
         return masw_set_error(nullptr, MASW_ECUDA, std::string("verify_noalloc: ") + cudaGetErrorString(e));
     const float sl2 = (scale > 0.f ? scale : 1.0f / sqrtf((float)D)) * 1.4426950408889634f;
-    return launch_verify_tc(q, k_cache, v_cache, kv_len, B, Lq, Hq, Hkv, Tmax, sl2, o, lse, scratch, kNoAllocPartBytes,
-                            n_split, st, "verify_noalloc");
+    rc = launch_verify_tc(q, k_cache, v_cache, kv_len, B, Lq, Hq, Hkv, Tmax, sl2, o, lse, scratch, kNoAllocPartBytes,
+                          n_split, st, "verify_noalloc");
+    if (rc || !status) return rc;
+    // the status word follows the B * Hkv tickets (launch_verify_tc's layout)
+    const void* word = (const uint8_t*)scratch + kNoAllocPartBytes + (size_t)B * Hkv * sizeof(unsigned);
+    e = cudaMemcpyAsync(status, word, sizeof(int), cudaMemcpyDeviceToDevice, st);
+    if (e != cudaSuccess)
+        return masw_set_error(nullptr, MASW_ECUDA, std::string("verify_noalloc: status copy: ") + cudaGetErrorString(e));
+    return MASW_OK;
 }

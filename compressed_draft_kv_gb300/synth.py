@@ -31,6 +31,10 @@ WORKLOADS = {
                                dtype="bf16", seed=5, steps=5),
     "paper_s128_w128_r8": dict(Hq=24, Hkv=8, D=128, layers=28, batch=8, prefix=32768, S=128, W=128, r=8,
                                dtype="bf16", seed=6, steps=5),
+    # sliding-window attention, the pages' SWA baseline: no sink, no slots (r
+    # beyond the longest sequence), a 1,024-token window, on the 3B-draft shape
+    "swa_w1024": dict(Hq=24, Hkv=8, D=128, layers=28, batch=8, prefix=32768, S=0, W=1024, r=1 << 20,
+                      dtype="bf16", seed=8, steps=5),
     "draft8b_b32_ragged": dict(Hq=32, Hkv=8, D=128, layers=32, batch=32, prefix_lo=16384, prefix_hi=32768,
                                S=4, W=2048, r=1024, dtype="bf16", seed=4, steps=8),
 }

@@ -60,6 +60,7 @@ extern "C" {
 #define MASW_ESTATE     -4  /* call not valid in the current state (e.g. not at a boundary) */
 #define MASW_ECUDA      -5  /* a CUDA runtime call failed */
 #define MASW_ETIMEOUT   -6  /* a bounded device-side wait ran out (kernel returned early) */
+#define MASW_EGUARD     -7  /* a guard band around a handle-owned buffer was overwritten */
 
 /* ---- element types ------------------------------------------------------- */
 #define MASW_F32   0
@@ -106,12 +107,27 @@ typedef struct {
  * head_dim must be 64 or 128.  opts may be NULL (batch 1, bf16, max_seq_len
  * 32768).  Allocates the pool (K and V: layers*batch*Hkv*(S+W+R+M_max)*D
  * elements each), the optional full-KV cache, counters and split scratch on
- * the current device.  On failure *out is NULL. */
+ * the current device.  On failure *out is NULL.
+ * Every handle-owned device buffer carries a 4 KiB guard band on each side
+ * (see masw_check_guards).  If the environment variable
+ * MASW_DEVICE_MEMORY_LIMIT holds a byte count, create allocates at most that
+ * much device memory in total (guards included) and otherwise fails with
+ * MASW_ENOMEM, freeing what it had allocated: a way to exercise the
+ * out-of-memory path without exhausting the device.  A limit below the pool's
+ * own size is refused before any CUDA call. */
 int masw_mem_create(int S, int W, int r, int n_kv_heads, int head_dim, int layers,
                     const masw_opts_t* opts, masw_mem_t** out);
 
 /* Free everything the handle owns.  NULL is accepted.  Synchronises the device. */
 int masw_mem_destroy(masw_mem_t* mem);
+
+/* Out-of-bounds write check: synchronises the device, then reads back the guard
+ * bands (4 KiB of 0xC3 before and after each handle-owned device buffer: the
+ * pools, the full-KV cache, counters, slot ids, split partials and tickets)
+ * and returns MASW_OK if all are intact, MASW_EGUARD otherwise (the message
+ * names the buffer and the byte offset of the first changed guard byte; a
+ * negative offset lies before the buffer).  Synchronous. */
+int masw_check_guards(masw_mem_t* mem);
 
 /* Message for the last failing call on `mem` (or on a NULL handle / stateless call). */
 const char* masw_last_error(const masw_mem_t* mem);
@@ -263,30 +279,39 @@ int masw_verify_workspace_bytes(int B, int Lq, int Hq, int Hkv, int D, int Tmax,
  * code that only receives input and output pointers (for example a plugin
  * slot in another inference engine), code whose device memory is owned by a
  * framework's own allocator, or a loop that cannot afford the device-wide
- * synchronisation a cudaMalloc may cause.  Arguments and results are those of
- * masw_verify_attn.  The split partials live in a fixed array inside the
- * library image (4 MiB + 16 KiB, held by every GPU that loads the library
- * until the process exits); larger problems run with fewer key splits.
- * Limit: B * Hkv <= 4096 (EINVAL beyond, with a message).  The first call on a
- * device looks up the array's device address (cudaGetSymbolAddress); make that
- * first call before any stream capture on that device.  Every call reuses the
- * same array (tickets are cleared on the stream at the start of each call), so
- * calls that overlap on the GPU -- other streams, other host threads -- race
- * and must be serialised by the caller. */
+ * synchronisation a cudaMalloc may cause.  q, caches, kv_len, o, lse, scale
+ * and the size rules are those of masw_verify_attn.  The split partials live
+ * in a fixed array inside the library image (4 MiB + 16 KiB, held by every GPU
+ * that loads the library until the process exits).
+ * status: device int, or NULL.  When given, the call copies its status word
+ * there on the stream once the kernel is done: 0, MASW_ETIMEOUT (a bounded wait
+ * inside the kernel gave up; that call's O and LSE are undefined) or
+ * MASW_EINVAL (the kernel found its shared memory misaligned).  With NULL such
+ * a failure goes unreported, because the next call clears the word.
+ * Limit: B * Hkv <= 4096 (EINVAL beyond, with a message).  Each call looks up
+ * the array's device address with cudaGetSymbolAddress (no allocation); the
+ * first call on a device also loads the library's device code there, so make
+ * that first call before any stream capture on that device.  Every call reuses
+ * the same array (tickets and status are cleared on the stream at the start of
+ * each call), so calls that overlap on the GPU -- other streams, other host
+ * threads -- race and must be serialised by the caller. */
 int masw_verify_attn_noalloc(const void* q, const void* k_cache, const void* v_cache,
                              const int* kv_len, int B, int Lq, int Hq, int Hkv, int D,
                              int Tmax, int dtype, float scale, float* o, float* lse,
-                             masw_stream_t stream);
+                             int* status, masw_stream_t stream);
 
 /* ---- speculative acceptance ------------------------------------------------------ */
 
 /* Greedy acceptance of a speculative block ([EN] §2.2 and §3.3 Algorithm 2;
  * the pages' experiments decode greedily, temperature 0).  For each sequence b:
  * tokens[b][j] = argmax over v of logits[b][j][v] for j = 0..L (ties go to the
- * smallest id; NaN entries are skipped); L_acc = the first j < L with
- * draft[b][j] != tokens[b][j], or L when all drafts match; n_emit[b] = L_acc + 1,
- * and the emitted tokens are tokens[b][0 .. L_acc] (accepted drafts, then the
- * target's correction or bonus token).
+ * smallest id; NaN entries are skipped; +inf and -inf count as values; a row
+ * whose entries are all NaN has no greedy token and gets -1); L_acc = the first
+ * j < L with draft[b][j] != tokens[b][j], or L when all drafts match (drafts
+ * are ids >= 0, so a -1 row rejects its draft); n_emit[b] = L_acc + 1, and the
+ * emitted tokens are tokens[b][0 .. L_acc] (accepted drafts, then the target's
+ * correction or bonus token; that last token is -1 when its row was all NaN,
+ * which the caller must treat as "no token").
  * logits: device [B, L+1, V] (dtype MASW_BF16 or MASW_F32); draft: device int
  * [B, L]; tokens: device int [B, L+1]; n_emit: device int [B]; workspace:
  * device scratch of masw_greedy_workspace_bytes() bytes (16-byte aligned; zero-filled

@@ -56,8 +56,11 @@ class Pair:
 
     def close(self):
         if self.h:
-            capi.masw_mem_destroy(self.h)
-            self.h = None
+            try:
+                capi.masw_check_guards(self.h)   # no kernel wrote outside a handle-owned buffer
+            finally:
+                capi.masw_mem_destroy(self.h)
+                self.h = None
 
     def load(self, layer, seq, t, seed=0):
         n = orc.slot_count(t, self.S, self.W, self.r)
@@ -124,8 +127,8 @@ class Pair:
         fn = capi.masw_full_step if full else capi.masw_draft_step
         fn(self.h, layer, q.to(DEV), k.to(DEV), v.to(DEV), o, lse, active=active)
         self.ref.append(layer, k.float().numpy(), v.float().numpy(), active=active)
-        want, want_l = (self.ref.full_attn if full else self.ref.draft_attn)(layer, q.float().numpy())
         if check:
+            want, want_l = (self.ref.full_attn if full else self.ref.draft_attn)(layer, q.float().numpy())
             capi.masw_sync(self.h)
             assert_close(o, want, self.dtype, f"{'full' if full else 'draft'} step O l={layer} step={self.step}")
             assert_close(lse, want_l, self.dtype, "step LSE")
@@ -199,3 +202,31 @@ class Pair:
             assert np.array_equal(vb[:, self.S + Wc + j], self.ref.slot_v[layer][seq][j])
             # library ids are 0-based: tau_j, the id of the raw token after g_j
             assert pos[j] == self.ref.slot_tau[layer][seq][j] == orc.slot_pos_id(j + 1, self.S, self.W, self.r) - 1
+
+
+GUARD_BYTES = 4096
+GUARD_BYTE = 0xC3
+
+
+class Guarded:
+    """A caller-owned device buffer with a guard band of GUARD_BYTES (0xC3) on
+    each side, for out-of-bounds write checks of the handle-less calls (their
+    workspaces and outputs).  `.t` is the buffer, viewed as dtype and shape."""
+
+    def __init__(self, shape, dtype, zero=True):
+        n = 1
+        for x in shape:
+            n *= x
+        nbytes = n * torch.tensor([], dtype=dtype).element_size()
+        self.raw = torch.full((nbytes + 2 * GUARD_BYTES,), GUARD_BYTE, dtype=torch.uint8, device=DEV)
+        mid = self.raw[GUARD_BYTES:GUARD_BYTES + nbytes]
+        if zero:
+            mid.zero_()
+        self.nbytes = nbytes
+        self.t = mid.view(dtype).view(*shape) if n else mid.view(dtype)
+
+    def check(self, what=""):
+        torch.cuda.synchronize()
+        lo = self.raw[:GUARD_BYTES]
+        hi = self.raw[GUARD_BYTES + self.nbytes:]
+        assert bool((lo == GUARD_BYTE).all()) and bool((hi == GUARD_BYTE).all()), f"{what}: guard band overwritten"

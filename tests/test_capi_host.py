@@ -102,3 +102,22 @@ def test_eq1_speedup_matches_oracle():
     for args in [(5, 5, 0.0, 1.0), (0, 5, 1.0, 1.0), (3.65, 5, 13.94, 40.0), (4.72, 5, 0.2, 1.0)]:
         assert abs(capi.masw_eq1_speedup(*args) - o.eq1_speedup(*args)) < 1e-12
     assert capi.masw_eq1_speedup(1, 5, 1.0, 0.0) == -1.0
+
+
+def test_allocation_limit_refuses_before_any_cuda_call(monkeypatch):
+    """MASW_DEVICE_MEMORY_LIMIT below the pool's size: create fails with
+    MASW_ENOMEM before touching the device (so this runs without a GPU), the
+    handle stays NULL and the message names the limit."""
+    lib = ensure_built()
+    monkeypatch.setenv("MASW_DEVICE_MEMORY_LIMIT", "1048576")
+    opts = capi.masw_opts_t(8, capi.MASW_BF16, 32768, 0.0, 0, 0, 16)
+    h = ctypes.c_void_p(1234)
+    rc = lib.masw_mem_create(4, 1024, 512, 8, 128, 28, ctypes.byref(opts), ctypes.byref(h))
+    assert rc == capi.MASW_ENOMEM
+    assert h.value is None
+    assert b"MASW_DEVICE_MEMORY_LIMIT" in lib.masw_last_error(None)
+
+
+def test_check_guards_rejects_a_null_handle():
+    lib = ensure_built()
+    assert lib.masw_check_guards(None) == capi.MASW_EINVAL

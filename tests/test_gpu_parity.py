@@ -10,7 +10,7 @@ import torch
 
 import oracle.masw_oracle as orc
 from compressed_draft_kv_gb300 import capi, synth
-from gpu_helpers import DEV, Pair, assert_close, to_np
+from gpu_helpers import DEV, Guarded, Pair, assert_close, to_np
 from libmasw_fixture import ensure_built
 
 pytestmark = pytest.mark.gpu
@@ -359,9 +359,11 @@ def test_greedy_accept(dtype, B, L, V):
     want_tok, want_n = orc.greedy_accept(lf, draft)
     dl = logits.to(DEV)
     dd = torch.from_numpy(np.ascontiguousarray(draft, dtype=np.int32)).to(DEV)
-    tok = torch.full((B, L + 1), -7, dtype=torch.int32, device=DEV)
-    n = torch.full((B,), -7, dtype=torch.int32, device=DEV)
-    ws = torch.zeros(capi.masw_greedy_workspace_bytes(B, L, V), dtype=torch.uint8, device=DEV)
+    gws = Guarded((capi.masw_greedy_workspace_bytes(B, L, V),), torch.uint8)
+    ws = gws.t
+    gtok = Guarded((B, L + 1), torch.int32)
+    gn = Guarded((B,), torch.int32)
+    tok, n = gtok.t, gn.t
     for call in range(3):   # one zero-filled workspace, reused: every call leaves its tickets at zero
         tok.fill_(-7)
         n.fill_(-7)
@@ -370,6 +372,72 @@ def test_greedy_accept(dtype, B, L, V):
         assert np.array_equal(tok.cpu().numpy(), want_tok), call
         assert np.array_equal(n.cpu().numpy(), want_n), call
     assert not ws[-4 * B:].any()   # the per-sequence tickets (the workspace's last B words) are zero again
+    for g_, name in ((gws, "workspace"), (gtok, "tokens"), (gn, "n_emit")):
+        g_.check(f"greedy {name}")
+
+
+@pytest.mark.parametrize("dtype,V", [("bf16", 128256), ("f32", 3001)])
+def test_greedy_accept_nan_and_inf(dtype, V):
+    """NaN entries are skipped, +-inf are values, an all-NaN row gives token -1
+    (rejecting its draft; as the bonus row it is emitted as -1), bit-exact
+    against the oracle; bf16 over many vocabulary chunks, f32 on the unaligned
+    (scalar) path."""
+    B, L = 3, 4
+    logits = synth.normal((B, L + 1, V), dtype, "accept-nan", V).float()
+    nan, inf = float("nan"), float("inf")
+    x = logits
+    x[0, 0, ::97] = nan                                   # NaN sprinkled over a normal row
+    x[0, 0, 5] = 40.0
+    x[0, 0, 3] = nan                                      # NaN before the maximum
+    x[0, 1, :] = nan                                      # all NaN: no token
+    x[1, 0, :] = -inf
+    x[1, 0, ::3] = nan                                    # -inf and NaN only: first -inf id
+    x[1, 1, V // 2] = inf
+    x[1, 1, V - 1] = inf                                  # +inf tie: the smaller id
+    x[1, 1, 7] = nan
+    x[1, 2, :] = nan
+    x[1, 2, V - 1] = -inf                                 # NaN but for one -inf at the end
+    top = int(x[1, 3].argmax())
+    x[1, 3, top] = nan                                    # NaN where the maximum was
+    x[1, 4, :] = nan                                      # the bonus row all NaN
+    logits = x.to(torch.bfloat16) if dtype == "bf16" else x
+    lf = logits.float().numpy()
+    want_tok, _ = orc.greedy_accept(lf, np.zeros((B, L), dtype=np.int64))
+    draft = np.array(want_tok[:, :L], dtype=np.int64)
+    draft[0, 1] = 11                                      # row (0, 1) has no token: rejected anyway
+    draft[2, 2] = (want_tok[2, 2] + 1) % V                # an ordinary rejection
+    want_tok, want_n = orc.greedy_accept(lf, draft)
+    assert want_tok[0, 1] == -1 and want_tok[1, 4] == -1 and want_tok[1, 0] == 1
+    assert list(want_n) == [2, L + 1, 3]
+    dl = logits.contiguous().to(DEV)
+    dd = torch.from_numpy(np.ascontiguousarray(draft, dtype=np.int32)).to(DEV)
+    tok = torch.full((B, L + 1), -7, dtype=torch.int32, device=DEV)
+    n = torch.full((B,), -7, dtype=torch.int32, device=DEV)
+    ws = torch.zeros(capi.masw_greedy_workspace_bytes(B, L, V), dtype=torch.uint8, device=DEV)
+    for call in range(2):
+        capi.masw_greedy_accept(dl, dd, tok, n, workspace=ws)
+        torch.cuda.synchronize()
+        assert np.array_equal(tok.cpu().numpy(), want_tok), call
+        assert np.array_equal(n.cpu().numpy(), want_n), call
+
+
+def test_allocation_limit_frees_what_create_had_allocated(monkeypatch):
+    """With MASW_DEVICE_MEMORY_LIMIT above the pools' size but below the full-KV
+    cache, create allocates the two pools, is refused the cache, returns
+    MASW_ENOMEM and frees the pools: device free memory is unchanged."""
+    torch.cuda.synchronize()
+    free0 = torch.cuda.mem_get_info(DEV)[0]
+    monkeypatch.setenv("MASW_DEVICE_MEMORY_LIMIT", str(200 << 20))   # pools: ~143 MB; cache: ~4.3 GB
+    with pytest.raises(capi.MaswError) as ei:
+        capi.masw_mem_create(4, 1024, 512, 8, 128, 4, batch=8, dtype=capi.MASW_BF16, max_seq_len=32768,
+                             full_kv=True)
+    assert ei.value.code == capi.MASW_ENOMEM
+    torch.cuda.synchronize()
+    assert abs(torch.cuda.mem_get_info(DEV)[0] - free0) < (8 << 20)
+    monkeypatch.delenv("MASW_DEVICE_MEMORY_LIMIT")
+    h = capi.masw_mem_create(4, 1024, 512, 8, 128, 4, batch=8, dtype=capi.MASW_BF16, max_seq_len=32768)
+    capi.masw_check_guards(h)
+    capi.masw_mem_destroy(h)
 
 
 def test_state_errors():
@@ -433,20 +501,25 @@ def test_verify_workspace_reuse_leaves_tickets_zero():
     results of each call match the oracle."""
     B, Lq, Hq, Hkv, Tmax, D = 2, 6, 32, 8, 1500, 128
     need = capi.masw_verify_workspace_bytes(B, Lq, Hq, Hkv, D, Tmax)
-    ws = torch.zeros(need, dtype=torch.uint8, device=DEV)
+    gws = Guarded((need,), torch.uint8)          # zero-filled, with guard bands on both sides
+    ws = gws.t
     for call, kv_len in enumerate([[1500, 900], [1200, 1500], [64, 700]]):
         seed = 900 + call
         q = synth.normal((B, Lq, Hq, D), "bf16", "verify", seed, "q")
         k = synth.normal((B, Hkv, Tmax, D), "bf16", "verify", seed, "k")
         v = synth.normal((B, Hkv, Tmax, D), "bf16", "verify", seed, "v")
         kl = torch.tensor(kv_len, dtype=torch.int32)
-        o = torch.empty(B, Lq, Hq, D, device=DEV)
-        capi.masw_verify_attn(q.to(DEV), k.to(DEV), v.to(DEV), kl.to(DEV), o, workspace=ws)
+        go = Guarded((B, Lq, Hq, D), torch.float32)
+        gl = Guarded((B, Lq, Hq), torch.float32)
+        capi.masw_verify_attn(q.to(DEV), k.to(DEV), v.to(DEV), kl.to(DEV), go.t, gl.t, workspace=ws)
         torch.cuda.synchronize()
-        want, _ = orc.verify_attn(q.float().numpy(), k.float().numpy(), v.float().numpy(), kv_len, None)
-        assert_close(o, want, "bf16", f"verify call {call}")
+        want, want_l = orc.verify_attn(q.float().numpy(), k.float().numpy(), v.float().numpy(), kv_len, None)
+        assert_close(go.t, want, "bf16", f"verify call {call}")
+        assert_close(gl.t, want_l, "bf16", f"verify LSE call {call}")
         tail = ws[need - 16 - B * Hkv * 4:].view(torch.int32)   # tickets, then the status word
         assert int(tail.abs().sum()) == 0, f"call {call} left tickets/status {tail.tolist()}"
+        for g_, name in ((gws, "workspace"), (go, "O"), (gl, "LSE")):
+            g_.check(f"verify call {call} {name}")
 
 
 def test_verify_peaky_softmax_and_scale():
@@ -480,11 +553,13 @@ def test_draft3b_full_size_sampled():
             for b in range(B):
                 if (l, b) in sampled:
                     p.load(l, b, t0, seed=2)
-                else:                               # unchecked rows: device-filled
+                else:                               # unchecked rows: device-filled, K != V
                     kr = torch.randn(t0, Hkv, D, generator=g, device=DEV).to(torch.bfloat16)
+                    vr = torch.randn(t0, Hkv, D, generator=g, device=DEV).to(torch.bfloat16)
                     ks = torch.randn(n, Hkv, D, generator=g, device=DEV).to(torch.bfloat16)
-                    capi.masw_mem_load(p.h, l, b, kr, kr, ks, ks)
-                    del kr, ks
+                    vs = torch.randn(n, Hkv, D, generator=g, device=DEV).to(torch.bfloat16)
+                    capi.masw_mem_load(p.h, l, b, kr, vr, ks, vs)
+                    del kr, vr, ks, vs
         for step in range(1, 6):
             p.step = step
             for l in range(L):
@@ -531,6 +606,71 @@ def test_draft3b_full_size_sampled():
         p.close()
 
 
+@pytest.mark.slow
+@pytest.mark.parametrize("prefix", [4096, 8192, 16384, 24576, 32768])
+def test_config3_every_pair_at_each_prefix(prefix):
+    """The 28-layer, batch-8 sweep's launch shape (24q/8kv heads, S=4, W=1024,
+    r=512) at every prefix of the sweep, 4K..32K, whose working sets (1033 to
+    1089 keys) give different split and cluster plans.  Two layers stand for 28
+    (the grid does not depend on the layer count).  Every (layer, row) pair
+    carries CPU-seeded data; the five fused steps of the benchmark's iteration
+    run in its order (the boundary tau = prefix + 4 is crossed at step 4 by
+    every sequence, so step 4 is the fused boundary step with all eight slot
+    queries), and at steps 4 and 5 every pair's draft output, and at step 4
+    every slot output, is compared with the oracle; then every pair's memory is
+    checked row by row."""
+    S, W, r, t0 = 4, 1024, 512, prefix
+    B, L, Hkv, D, Hq = 8, 2, 8, 128, 24
+    assert orc.is_boundary(t0 + 4, S, W, r)
+    p = Pair(S, W, r, Hkv, D, L, B, "bf16", Hq, max_seq_len=t0 + 16, reserve=16, tag=f"cfg3_{prefix}")
+    try:
+        for l in range(L):
+            for b in range(B):
+                p.load(l, b, t0, seed=5)
+        for step in range(1, 6):
+            p.step = step
+            for l in range(L):
+                if step == 4:
+                    p.fstep_slot(l, list(range(B)))
+                else:
+                    p.fstep(l, check=step == 5)
+        capi.masw_sync(p.h)
+        for l in range(L):
+            for b in range(B):
+                assert p.ref.m(l, b) == orc.slot_count(t0 + 5, S, W, r)
+                p.check_state(l, b)
+    finally:
+        p.close()
+
+
+@pytest.mark.slow
+def test_swa_special_case_full_size():
+    """Sliding-window attention, the pages' SWA baseline, as a special case of
+    the memory: S = 0, no slots (r beyond the longest sequence), W = 1024, on
+    the 3B-draft launch shape (batch 8, 24q/8kv, 32K prefix, ring reserve 16).
+    Every (layer, row) pair carries CPU-seeded data; five fused steps, every
+    pair's output compared with the oracle at the first and last step, and every
+    pair's memory checked row by row (no slot is ever written)."""
+    S, W, r, t0 = 0, 1024, 1 << 20, 32768
+    B, L, Hkv, D, Hq = 8, 2, 8, 128, 24
+    p = Pair(S, W, r, Hkv, D, L, B, "bf16", Hq, max_seq_len=t0 + 16, reserve=16, tag="swa")
+    try:
+        for l in range(L):
+            for b in range(B):
+                p.load(l, b, t0, seed=6)
+        for step in range(1, 6):
+            p.step = step
+            for l in range(L):
+                p.fstep(l, check=step in (1, 5))
+        capi.masw_sync(p.h)
+        for l in range(L):
+            for b in range(B):
+                assert p.ref.m(l, b) == 0 and orc.working_set_size(t0 + 5, S, W, r) == W
+                p.check_state(l, b)
+    finally:
+        p.close()
+
+
 @pytest.mark.parametrize("Hq,B", [(24, 8), (32, 8), (24, 4), (32, 4), (32, 2)])
 def test_fused_steps_full_size_sampled(Hq, B):
     """The fused step and the fused boundary step at the benchmark's launch
@@ -555,11 +695,13 @@ def test_fused_steps_full_size_sampled(Hq, B):
             for b in range(B):
                 if (l, b) in sampled:
                     p.load(l, b, t0, seed=3)
-                else:
+                else:                               # unchecked rows: device-filled, K != V
                     kr = torch.randn(t0, Hkv, D, generator=g, device=DEV).to(torch.bfloat16)
+                    vr = torch.randn(t0, Hkv, D, generator=g, device=DEV).to(torch.bfloat16)
                     ks = torch.randn(n, Hkv, D, generator=g, device=DEV).to(torch.bfloat16)
-                    capi.masw_mem_load(p.h, l, b, kr, kr, ks, ks)
-                    del kr, ks
+                    vs = torch.randn(n, Hkv, D, generator=g, device=DEV).to(torch.bfloat16)
+                    capi.masw_mem_load(p.h, l, b, kr, vr, ks, vs)
+                    del kr, vr, ks, vs
         for step in range(1, 7):
             p.step = step
             boundary = step == 4          # tau_62 = 4 + 1024 + 62*512 = 32772 for every sequence
@@ -627,69 +769,90 @@ def test_fused_steps_one_sequence(Hq):
         p.close()
 
 
-def test_draft8b_large_batch_long_runs_sampled():
+def test_draft8b_large_batch_every_sequence():
     """The large-batch launch shape (batch 32, 32q/8kv, W = 2048, r = 1024,
-    ragged prefixes 16K..32K): one split per (sequence, head) streams ~2080 keys,
-    which selects the three-stage kernel.  Eight fused steps with per-sequence
-    slot writes at each sequence's own boundary; two sequences carry CPU-seeded
-    data checked against the oracle, the rest are filled on the device."""
-    S, W, r = 4, 2048, 1024
+    ragged prefixes 16K..32K, each snapped down as the benchmark does so that
+    sequence b reaches its compression boundary at draft step b mod 8 + 1): one
+    split per (sequence, head) streams ~2080 keys, which selects the three-stage
+    kernel.  Eight fused steps with per-sequence slot writes.  Every sequence
+    carries CPU-seeded data; every sequence's draft output and slot output at
+    its boundary step, and every draft output at the last step, are compared
+    with the oracle's mask and attention over that sequence's columns (kept
+    here in preallocated arrays, so the 32 histories are not re-copied at each
+    append); two sequences' memories are also checked row by row."""
+    S, W, r, steps = 4, 2048, 1024, 8
     B, Hkv, D, G = 32, 8, 128, 4
     Hq = Hkv * G
-    prefixes = synth.ragged_prefixes(B, 16384, 32768, "long-runs")
-    # two checked sequences, one of them two steps before its boundary
-    prefixes[5] = S + W + 20 * r - 2
-    sampled = [5, 17]
-    p = Pair(S, W, r, Hkv, D, 1, B, "bf16", Hq, max_seq_len=32768 + 64, reserve=16, tag="cfg5")
+    prefixes = []
+    for b, p0 in enumerate(synth.ragged_prefixes(B, 16384, 32768, "long-runs")):
+        t = p0
+        while not orc.is_boundary(t + b % steps + 1, S, W, r):
+            t -= 1
+        prefixes.append(t)
+    tracked = [5, 17]
+    p = Pair(S, W, r, Hkv, D, 1, B, "bf16", Hq, max_seq_len=32768 + 64, reserve=16, tag="cfg5all")
     try:
-        g = torch.Generator(device=DEV)
-        g.manual_seed(99)
+        raw_k, raw_v, slot_k, slot_v, t_of, m_of = [], [], [], [], [], []
         for b in range(B):
             t = prefixes[b]
-            if b in sampled:
-                p.load(0, b, t, seed=3)
-            else:
-                n = orc.slot_count(t, S, W, r)
-                kr = torch.randn(t, Hkv, D, generator=g, device=DEV).to(torch.bfloat16)
-                ks = torch.randn(max(n, 1), Hkv, D, generator=g, device=DEV).to(torch.bfloat16)
-                capi.masw_mem_load(p.h, 0, b, kr, kr, ks[:n] if n else None, ks[:n] if n else None)
-                del kr, ks
-        tcur = list(prefixes)
-        crossed = False
-        for step in range(8):
+            n = orc.slot_count(t, S, W, r)
+            kr, vr = (synth.normal((t, Hkv, D), "bf16", p.tag, nm, b) for nm in ("k", "v"))
+            ks, vs = (synth.normal((n, Hkv, D), "bf16", p.tag, nm, b) for nm in ("ks", "vs"))
+            capi.masw_mem_load(p.h, 0, b, kr, vr, ks if n else None, vs if n else None)
+            rk, rv = np.zeros((t + steps, Hkv, D), np.float32), np.zeros((t + steps, Hkv, D), np.float32)
+            rk[:t], rv[:t] = kr.float().numpy(), vr.float().numpy()
+            sk, sv = np.zeros((n + 1, Hkv, D), np.float32), np.zeros((n + 1, Hkv, D), np.float32)
+            sk[:n], sv[:n] = ks.float().numpy(), vs.float().numpy()
+            raw_k.append(rk), raw_v.append(rv), slot_k.append(sk), slot_v.append(sv)
+            t_of.append(t), m_of.append(n)
+            if b in tracked:
+                p.ref.load(0, b, rk[:t], rv[:t], sk[:n], sv[:n])
+            del kr, vr, ks, vs
+
+        def columns(b, t, m):
+            return (np.concatenate([raw_k[b][:t], slot_k[b][:m]]), np.concatenate([raw_v[b][:t], slot_v[b][:m]]))
+
+        checked_slots = 0
+        for step in range(steps):
             p.step = step
-            due = [b for b in range(B) if orc.is_boundary(tcur[b] + 1, S, W, r)]
-            k = p.rand((B, Hkv, D), "k")
-            v = p.rand((B, Hkv, D), "v")
-            q = p.rand((B, Hq, D), "q")
+            due = [b for b in range(B) if orc.is_boundary(t_of[b] + 1, S, W, r)]
+            assert due == [b for b in range(B) if b % steps == step]
+            k, v, q = p.rand((B, Hkv, D), "k"), p.rand((B, Hkv, D), "v"), p.rand((B, Hq, D), "q")
             o = torch.empty(B, Hq, D, device=DEV)
             lse = torch.empty(B, Hq, device=DEV)
-            if due:
-                n = len(due)
-                qg, kg, vg = p.rand((n, Hq, D), "qg"), p.rand((n, Hkv, D), "kg"), p.rand((n, Hkv, D), "vg")
-                og = torch.empty(n, Hq, D, device=DEV)
-                capi.masw_draft_step_slot(p.h, 0, q.to(DEV), k.to(DEV), v.to(DEV), o, due, qg.to(DEV), kg.to(DEV),
-                                          vg.to(DEV), og, lse=lse)
-            else:
-                capi.masw_draft_step(p.h, 0, q.to(DEV), k.to(DEV), v.to(DEV), o, lse)
-            tcur = [t + 1 for t in tcur]
-            p.ref.append(0, k.float().numpy(), v.float().numpy(), active=[b in sampled for b in range(B)])
-            for sb in sampled:
-                Kc, Vc = p.ref._columns(0, sb)
-                mask = orc.draft_mask(p.ref.t(0, sb), p.ref.m(0, sb), S, W)
-                wo, wl = orc.attention(q.float().numpy()[sb], Kc, Vc, mask, p.ref.scale)
-                assert_close(o[sb], wo, "bf16", f"cfg5 draft b={sb} step={step}")
-                assert_close(lse[sb], wl, "bf16", "cfg5 draft LSE")
-                if sb in due:
-                    crossed = True
-                    i = due.index(sb)
-                    w, _ = p.ref.materialize_slot(0, [sb], qg.float().numpy()[i:i + 1], kg.float().numpy()[i:i + 1],
-                                                  vg.float().numpy()[i:i + 1])
-                    assert_close(og[i:i + 1], w, "bf16", f"cfg5 slot b={sb} step={step}")
-        assert crossed and p.ref.m(0, 5) == orc.slot_count(prefixes[5] + 8, S, W, r)
-        capi.masw_sync(p.h)
-        for sb in sampled:
-            p.check_state(0, sb)
+            n = len(due)
+            qg, kg, vg = p.rand((n, Hq, D), "qg"), p.rand((n, Hkv, D), "kg"), p.rand((n, Hkv, D), "vg")
+            og = torch.empty(n, Hq, D, device=DEV)
+            lg = torch.empty(n, Hq, device=DEV)
+            capi.masw_draft_step_slot(p.h, 0, q.to(DEV), k.to(DEV), v.to(DEV), o, due, qg.to(DEV), kg.to(DEV),
+                                      vg.to(DEV), og, lse, lg)
+            capi.masw_sync(p.h)
+            kf, vf, qf = k.float().numpy(), v.float().numpy(), q.float().numpy()
+            qgf, kgf, vgf = qg.float().numpy(), kg.float().numpy(), vg.float().numpy()
+            for b in range(B):
+                raw_k[b][t_of[b]], raw_v[b][t_of[b]] = kf[b], vf[b]
+                t_of[b] += 1
+            p.ref.append(0, kf, vf, active=[b in tracked for b in range(B)])
+            for b in sorted(set(due) | (set(range(B)) if step == steps - 1 else set())):
+                Kc, Vc = columns(b, t_of[b], m_of[b])
+                wo, wl = orc.attention(qf[b], Kc, Vc, orc.draft_mask(t_of[b], m_of[b], S, W), p.ref.scale)
+                assert_close(o[b], wo, "bf16", f"cfg5 draft b={b} step={step}")
+                assert_close(lse[b], wl, "bf16", f"cfg5 draft LSE b={b} step={step}")
+            for i, b in enumerate(due):
+                tau, m = t_of[b], m_of[b] + 1
+                slot_k[b][m - 1], slot_v[b][m - 1] = kgf[i], vgf[i]
+                m_of[b] = m
+                Kc, Vc = columns(b, tau, m)
+                wo, wl = orc.attention(qgf[i], Kc, Vc, orc.slot_write_mask(tau, m, S, W), p.ref.scale)
+                assert_close(og[i], wo, "bf16", f"cfg5 slot b={b} step={step}")
+                assert_close(lg[i], wl, "bf16", f"cfg5 slot LSE b={b} step={step}")
+                checked_slots += 1
+                if b in tracked:
+                    p.ref.materialize_slot(0, [b], qgf[i:i + 1], kgf[i:i + 1], vgf[i:i + 1])
+        assert checked_slots == B
+        assert all(m_of[b] == orc.slot_count(prefixes[b] + steps, S, W, r) for b in range(B))
+        for b in tracked:
+            p.check_state(0, b)
     finally:
         p.close()
 

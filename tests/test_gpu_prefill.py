@@ -111,9 +111,10 @@ def test_prefill_rejects_bad_calls():
 
 def test_prefill_full_size_sampled_rows():
     """The benchmark's launch configuration (3B-draft attention shape, 32K prefix,
-    S = 4, W = 1024, r = 512, 61 slots): sampled raw rows (sink, first window,
-    first boundaries, middle, last) and slot rows against the oracle's per-row
-    evaluation, and the stored memory bit for bit."""
+    S = 4, W = 1024, r = 512, 61 slots): raw rows (sink, first window, first
+    boundaries, middle, last, and one in every 128-row query tile) and every
+    slot row against the oracle's per-row evaluation, and the stored memory bit
+    for bit."""
     import numpy as np
     from compressed_draft_kv_gb300 import synth
     S, W, r, Hkv, G, T, D = 4, 1024, 512, 8, 3, 32768, 128
@@ -133,9 +134,12 @@ def test_prefill_full_size_sampled_rows():
                           o_r, l_r, o_s, l_s)
         capi.masw_sync(p.h)
         rng = np.random.default_rng(17)
+        # the special rows, one seeded row in every 128-row query tile of the
+        # launch, and every slot row
+        per_tile = [int(rng.integers(j + 1, min(j + 128, T) + 1)) for j in range(0, T, 128)]
         raw_rows = sorted(set([1, 3, 4, 5, 64, 129, S + W, S + W + 1, S + W + r, S + W + r + 1, 16384, T - 1, T]
-                              + rng.integers(1, T + 1, 8).tolist()))
-        slot_rows = sorted(set([1, 2, M // 2, M - 1, M]))
+                              + per_tile))
+        slot_rows = list(range(1, M + 1))
         want = orc.prefill_attn(S, W, r, qr.float().numpy(), kr.float().numpy(), vr.float().numpy(),
                                 qs.float().numpy(), ks.float().numpy(), vs.float().numpy(),
                                 raw_rows=raw_rows, slot_rows=slot_rows)

@@ -5,9 +5,10 @@ cudaMalloc -- code that only receives input and output pointers, code whose
 device memory belongs to another allocator, or a loop that cannot afford the
 device-wide synchronisation an allocation may cause.  This test calls it through
 the C ABI twice in a row, with different shapes, and checks each result against
-masw_verify_attn (which takes a caller workspace) within the tolerance the other
-bf16 tests use.  The second shape is large enough that the fixed scratch holds
-fewer key splits than the workspace version uses.
+masw_verify_attn (which takes a caller workspace) and against the CPU oracle,
+within the tolerance the other bf16 tests use, and that the status word the call
+copies out is 0.  (Both shapes run the usual split count: at one CTA per SM the
+partials stay far below the fixed array on this GPU.)
 
 The file name makes pytest collect it last, so a run that stops at the first
 failure has run every other test before this one.
@@ -15,6 +16,7 @@ failure has run every other test before this one.
 import pytest
 import torch
 
+import oracle.masw_oracle as orc
 from compressed_draft_kv_gb300 import capi, synth
 from gpu_helpers import DEV, assert_close
 from libmasw_fixture import ensure_built
@@ -45,10 +47,16 @@ def test_noalloc_verify_matches_workspace_verify_twice():
         capi.masw_verify_attn(q, k, v, kl, o_ref, l_ref)
         o = torch.full((B, Lq, Hq, 128), float("nan"), device=DEV)
         lse = torch.full((B, Lq, Hq), float("nan"), device=DEV)
-        capi.masw_verify_attn_noalloc(q, k, v, kl, o, lse)
+        status = torch.full((1,), -99, dtype=torch.int32, device=DEV)
+        capi.masw_verify_attn_noalloc(q, k, v, kl, o, lse, status=status)
         torch.cuda.synchronize()
-        assert_close(o, o_ref.double().cpu().numpy(), "bf16", f"noalloc O B={B} T={Tmax}")
-        assert_close(lse, l_ref.double().cpu().numpy(), "bf16", f"noalloc LSE B={B} T={Tmax}")
+        assert int(status.item()) == capi.MASW_OK
+        assert_close(o, o_ref.double().cpu().numpy(), "bf16", f"noalloc O vs workspace B={B} T={Tmax}")
+        assert_close(lse, l_ref.double().cpu().numpy(), "bf16", f"noalloc LSE vs workspace B={B} T={Tmax}")
+        o_or, l_or = orc.verify_attn(q.float().cpu().numpy(), k.float().cpu().numpy(), v.float().cpu().numpy(),
+                                     kv_len)
+        assert_close(o, o_or, "bf16", f"noalloc O vs oracle B={B} T={Tmax}")
+        assert_close(lse, l_or, "bf16", f"noalloc LSE vs oracle B={B} T={Tmax}")
 
 
 def test_noalloc_rejects_sizes_beyond_its_limit():
