@@ -413,6 +413,8 @@ int masw_launch_decode(masw_mem_t* mem, int mode, int layer, const void* q, int 
     for (int i = 0; i < n_rows; ++i) {
         const int b = seq_ids ? seq_ids[i] : i;
         prm.seq_ids[i] = (short)b;
+        prm.t_spec[i] = mem->h_t[(size_t)layer * mem->B + b];
+        prm.m_spec[i] = mem->h_m[(size_t)layer * mem->B + b];
         kmax = imax(kmax, host_keys(mem, mode, layer, b) + (step_active ? 1 : 0));
     }
     // split count: about three CTAs per SM in total, at least 64 keys per split,

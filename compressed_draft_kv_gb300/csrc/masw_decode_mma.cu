@@ -157,6 +157,13 @@ __global__ void __launch_bounds__(128, NST_ == 2 ? 3 : 2) decode_mma_kernel(cons
     const int G = p.Hq / p.Hkv;
     const int si = p.q_slot ? (int)p.slot_of[z] : -1;   // fused slot query of this row, if any
     const int NR = si >= 0 ? 2 * G : G;                  // query columns of this pair
+    // The pair's query rows into L2 now: they are read right after the
+    // dependency wait, and an L2 prefetch is safe before it (it only warms L2,
+    // which the previous kernel's writes update).
+    if (tid == 32) {
+        prefetch_l2((const uint8_t*)p.q + ((size_t)z * p.Hq + (size_t)h * G) * ROWB, (uint32_t)(G * ROWB));
+        if (si >= 0) prefetch_l2((const uint8_t*)p.q_slot + ((size_t)si * p.Hq + (size_t)h * G) * ROWB, (uint32_t)(G * ROWB));
+    }
     // cluster merge: rank k finalises elements [k*per, (k+1)*per) of the pair's
     // NR x D output (per a multiple of 4, so 16-byte pushes never straddle two
     // ranks) and receives, from each of the n_split ranks, that slice and the
@@ -173,10 +180,12 @@ __global__ void __launch_bounds__(128, NST_ == 2 ? 3 : 2) decode_mma_kernel(cons
         }
         cluster_arrive_relaxed();
     }
-    // Segment table, built speculatively before the PDL wait (the counters are
-    // read while the previous kernel drains) and verified after it; the copies
-    // of the first stages are issued on the speculative table, and rebuilt and
-    // reissued in the rare case the previous kernel changed this head's counters.
+    // Segment table, built speculatively from the host mirror's counters (no
+    // global read before the first copies) and verified against the device
+    // counters, which are read after the dependency wait but compared only
+    // after the main loop; in the rare case they differ (the previous kernel
+    // changed this head's counters, or a graph replays from another state) the
+    // table is rebuilt and the loop runs again.
     const size_t ci = (size_t)lb * p.Hkv + h;
     auto build = [&](int t, int mcnt) {
         s_m_before = mcnt;
@@ -196,7 +205,7 @@ __global__ void __launch_bounds__(128, NST_ == 2 ? 3 : 2) decode_mma_kernel(cons
         s_start[n] = acc;
         s_nseg = n;
     };
-    if (tid == 0) build(*(volatile const int*)(p.d_t + ci), *(volatile const int*)(p.d_m + ci));
+    if (tid == 0) build(p.t_spec[z], p.m_spec[z]);
     __syncthreads();
 
     int nseg = s_nseg;
@@ -282,27 +291,12 @@ __global__ void __launch_bounds__(128, NST_ == 2 ? 3 : 2) decode_mma_kernel(cons
             qb[ks][1] = real ? *reinterpret_cast<const uint32_t*>(qrow + d + 8) : 0u;
         }
     }
-    if (tid == 0) s_respec = (p.d_t[ci] != s_t || p.d_m[ci] != s_m_before) ? 1 : 0;
-    __syncthreads();
-    if (!s_respec && !early) {
-#pragma unroll
-        for (int c = 0; c < NST - 1; ++c) {
-            if (c < nstage) load_stage(c);
-            cp_async_commit();
-        }
+    int dev_t = 0, dev_m = 0;                        // thread 0 only: compared after the loop
+    if (tid == 0) {
+        dev_t = *(volatile const int*)(p.d_t + ci);
+        dev_m = *(volatile const int*)(p.d_m + ci);
     }
-    if (s_respec) {   // the previous kernel changed the counters: drop the speculative stages
-        pre = false;
-        cp_async_wait<0>();
-        __syncthreads();
-        if (tid == 0) build(p.d_t[ci], p.d_m[ci]);
-        __syncthreads();
-        nseg = s_nseg;
-        total = s_start[nseg];
-        chunk = (((total + p.n_split - 1) / p.n_split) + 15) & ~15;
-        r0 = imin(total, split * chunk);
-        r1 = imin(total, r0 + chunk);
-        nstage = (r1 - r0 + KPS - 1) / KPS;
+    if (!early) {
 #pragma unroll
         for (int c = 0; c < NST - 1; ++c) {
             if (c < nstage) load_stage(c);
@@ -315,79 +309,101 @@ __global__ void __launch_bounds__(128, NST_ == 2 ? 3 : 2) decode_mma_kernel(cons
     if (p.cluster) cluster_wait();                   // every peer's receive mbarrier is initialised
 
     const float sl2 = p.scale_log2;
-    float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f};
+    float m_run[2], l_run[2];
     float acc[KS][4];
+    for (int attempt = 0;; ++attempt) {
+        m_run[0] = m_run[1] = -INFINITY;
+        l_run[0] = l_run[1] = 0.f;
 #pragma unroll
-    for (int mt = 0; mt < KS; ++mt) acc[mt][0] = acc[mt][1] = acc[mt][2] = acc[mt][3] = 0.f;
+        for (int mt = 0; mt < KS; ++mt) acc[mt][0] = acc[mt][1] = acc[mt][2] = acc[mt][3] = 0.f;
 
-    // copy group g holds stage g (with pre, the first iteration commits none)
-    for (int c = 0; c < nstage; ++c) {
-        if (pre && c == 0)
-            cp_async_wait<NST - 1>();
-        else
-            cp_async_wait<NST - 2>();
-        __syncthreads();
-        if (!(pre && c == 0)) {
-            const int cn = c + NST - 1;   // refill the stage consumed in the previous iteration
-            if (cn < nstage) load_stage(cn);
-            cp_async_commit();
-        }
-        const uint32_t sk = sbase + (uint32_t)(c % NST) * C::STAGE;
-        const uint32_t sv = sk + KPS * ROWB;
-        const int kw = warp * 16;
-        const int key_tile = r0 + c * KPS + kw;
-        if (key_tile < r1) {
-            // two accumulators (even and odd k-steps) halve the dependent MMA chain
-            float s[4] = {0.f, 0.f, 0.f, 0.f}, s2[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-            for (int ks = 0; ks < KS; ++ks) {
-                uint32_t a0, a1, a2, a3;
-                ldsm_x4(sk + swz_off<ROWB>(kw + (lane & 7) + ((lane >> 3) & 1) * 8, ks * 2 + (lane >> 4)), a0, a1,
-                        a2, a3);
-                mma16816((ks & 1) ? s2 : s, a0, a1, a2, a3, qb[ks][0], qb[ks][1]);
+        // copy group g holds stage g (with pre, the first iteration commits none)
+        for (int c = 0; c < nstage; ++c) {
+            if (pre && c == 0)
+                cp_async_wait<NST - 1>();
+            else
+                cp_async_wait<NST - 2>();
+            __syncthreads();
+            if (!(pre && c == 0)) {
+                const int cn = c + NST - 1;   // refill the stage consumed in the previous iteration
+                if (cn < nstage) load_stage(cn);
+                cp_async_commit();
             }
+            const uint32_t sk = sbase + (uint32_t)(c % NST) * C::STAGE;
+            const uint32_t sv = sk + KPS * ROWB;
+            const int kw = warp * 16;
+            const int key_tile = r0 + c * KPS + kw;
+            if (key_tile < r1) {
+                // two accumulators (even and odd k-steps) halve the dependent MMA chain
+                float s[4] = {0.f, 0.f, 0.f, 0.f}, s2[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-            for (int e = 0; e < 4; ++e) s[e] += s2[e];
-            float x[4];
+                for (int ks = 0; ks < KS; ++ks) {
+                    uint32_t a0, a1, a2, a3;
+                    ldsm_x4(sk + swz_off<ROWB>(kw + (lane & 7) + ((lane >> 3) & 1) * 8, ks * 2 + (lane >> 4)), a0, a1,
+                            a2, a3);
+                    mma16816((ks & 1) ? s2 : s, a0, a1, a2, a3, qb[ks][0], qb[ks][1]);
+                }
 #pragma unroll
-            for (int e = 0; e < 4; ++e) x[e] = s[e] * sl2;
-            if (key_tile + 16 > r1) {                   // the split's last, partial tile (warp-uniform)
-                const int key_a = key_tile + (lane >> 2), key_b = key_a + 8;
-                if (key_a >= r1) x[0] = x[1] = -INFINITY;
-                if (key_b >= r1) x[2] = x[3] = -INFINITY;
-            }
-            float pr[4];
+                for (int e = 0; e < 4; ++e) s[e] += s2[e];
+                float x[4];
 #pragma unroll
-            for (int e = 0; e < 2; ++e) {
-                float mx = fmaxf(x[e], x[e + 2]);
-                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
-                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
-                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
-                const float m_new = fmaxf(m_run[e], mx);   // finite: key_tile < r1
-                const float alpha = fast_ex2(m_run[e] - m_new);
-                pr[e] = fast_ex2(x[e] - m_new);
-                pr[e + 2] = fast_ex2(x[e + 2] - m_new);
-                l_run[e] = l_run[e] * alpha + pr[e] + pr[e + 2];
-                m_run[e] = m_new;
+                for (int e = 0; e < 4; ++e) x[e] = s[e] * sl2;
+                if (key_tile + 16 > r1) {                   // the split's last, partial tile (warp-uniform)
+                    const int key_a = key_tile + (lane >> 2), key_b = key_a + 8;
+                    if (key_a >= r1) x[0] = x[1] = -INFINITY;
+                    if (key_b >= r1) x[2] = x[3] = -INFINITY;
+                }
+                float pr[4];
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    float mx = fmaxf(x[e], x[e + 2]);
+                    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+                    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+                    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+                    const float m_new = fmaxf(m_run[e], mx);   // finite: key_tile < r1
+                    const float alpha = fast_ex2(m_run[e] - m_new);
+                    pr[e] = fast_ex2(x[e] - m_new);
+                    pr[e + 2] = fast_ex2(x[e + 2] - m_new);
+                    l_run[e] = l_run[e] * alpha + pr[e] + pr[e + 2];
+                    m_run[e] = m_new;
+#pragma unroll
+                    for (int mt = 0; mt < KS; ++mt) {
+                        acc[mt][e] *= alpha;
+                        acc[mt][e + 2] *= alpha;
+                    }
+                }
+                const uint32_t pb0 = movmatrix_t(pack_bf16(pr[0], pr[1]));
+                const uint32_t pb1 = movmatrix_t(pack_bf16(pr[2], pr[3]));
 #pragma unroll
                 for (int mt = 0; mt < KS; ++mt) {
-                    acc[mt][e] *= alpha;
-                    acc[mt][e + 2] *= alpha;
+                    uint32_t a0, a1, a2, a3;
+                    ldsm_x4_t(sv + swz_off<ROWB>(kw + (lane & 7) + (lane >> 4) * 8, mt * 2 + ((lane >> 3) & 1)), a0, a1,
+                              a2, a3);
+                    mma16816(acc[mt], a0, a1, a2, a3, pb0, pb1);
                 }
             }
-            const uint32_t pb0 = movmatrix_t(pack_bf16(pr[0], pr[1]));
-            const uint32_t pb1 = movmatrix_t(pack_bf16(pr[2], pr[3]));
+        }
+        cp_async_wait<0>();
+        if (tid == 0) s_respec = (attempt == 0 && (dev_t != s_t || dev_m != s_m_before)) ? 1 : 0;
+        __syncthreads();
+        if (!s_respec) break;
+        // the table was built from counters that are not the device's: rebuild
+        // it from the device counters and run the loop again
+        if (tid == 0) build(dev_t, dev_m);
+        __syncthreads();
+        nseg = s_nseg;
+        total = s_start[nseg];
+        chunk = (((total + p.n_split - 1) / p.n_split) + 15) & ~15;
+        r0 = imin(total, split * chunk);
+        r1 = imin(total, r0 + chunk);
+        nstage = (r1 - r0 + KPS - 1) / KPS;
+        pre = false;
 #pragma unroll
-            for (int mt = 0; mt < KS; ++mt) {
-                uint32_t a0, a1, a2, a3;
-                ldsm_x4_t(sv + swz_off<ROWB>(kw + (lane & 7) + (lane >> 4) * 8, mt * 2 + ((lane >> 3) & 1)), a0, a1,
-                          a2, a3);
-                mma16816(acc[mt], a0, a1, a2, a3, pb0, pb1);
-            }
+        for (int c = 0; c < NST - 1; ++c) {
+            if (c < nstage) load_stage(c);
+            cp_async_commit();
         }
     }
-    cp_async_wait<0>();
-    __syncthreads();
     // the new token's row into its pool row (no CTA of this launch reads the row
     // it overwrites), by the split whose keys include it: that split streamed the
     // row from the caller's buffer into its last stage or the one before, and no

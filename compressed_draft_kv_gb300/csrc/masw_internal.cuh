@@ -111,6 +111,10 @@ __device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
                  : "memory");
 }
+// hint: bring `bytes` (a multiple of 16, 16-byte aligned) at `src` into L2
+__device__ __forceinline__ void prefetch_l2(const void* src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
 // contiguous global -> shared bulk copy (TMA engine), completes on `bar`
 __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
     asm volatile(
@@ -374,6 +378,10 @@ struct DecodeParams {
     short slot_of[MASW_MAX_BATCH];
     unsigned active[MASW_MAX_BATCH / 32];
     short seq_ids[MASW_MAX_BATCH];
+    // the host mirror's counters of each row at launch time: the source of the
+    // speculative segment table (checked against the device counters in-kernel)
+    int t_spec[MASW_MAX_BATCH];
+    int m_spec[MASW_MAX_BATCH];
 };
 
 struct Seg {

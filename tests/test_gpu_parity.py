@@ -911,6 +911,59 @@ def test_graph_replay_matches_eager():
         p.close()
 
 
+@pytest.mark.parametrize("D,G", [(128, 3), (64, 4)])
+def test_graph_replays_from_a_later_state_rebuild_the_segment_table(D, G):
+    """A captured fused step replayed without a rollback: every replay after the
+    first starts from a state the launches were not captured in, so the
+    speculative segment table each CTA builds from the counters known at
+    capture is wrong; the kernel must find that out from the device counters,
+    rebuild the table and run its loop again.  Outputs are checked against the
+    oracle at every replay, and the device counters advance by one per replay."""
+    S, W, r, Hkv = 4, 64, 16, 2
+    B, L, Hq = 2, 2, Hkv * G
+    p = Pair(S, W, r, Hkv, D, L, B, "bf16", Hq, max_seq_len=1024, tag=f"replay{D}")
+    try:
+        t0 = S + W + 3 * r + 1       # the next boundary is 15 tokens away
+        for l in range(L):
+            for b in range(B):
+                p.load(l, b, t0, seed=l * 10 + b)
+        k = [p.rand((B, Hkv, D), "k", l) for l in range(L)]
+        v = [p.rand((B, Hkv, D), "v", l) for l in range(L)]
+        q = [p.rand((B, Hq, D), "q", l) for l in range(L)]
+        kd, vd, qd = ([x.to(DEV) for x in xs] for xs in (k, v, q))
+        outs = [torch.empty(B, Hq, D, device=DEV) for _ in range(L)]
+
+        def step():
+            for l in range(L):
+                capi.masw_draft_step(p.h, l, qd[l], kd[l], vd[l], outs[l])
+
+        def oracle_step(what):
+            for l in range(L):
+                p.ref.append(l, k[l].float().numpy(), v[l].float().numpy())
+                want, _ = p.ref.draft_attn(l, q[l].float().numpy())
+                assert_close(outs[l], want, "bf16", f"{what} l={l}")
+
+        stream = torch.cuda.Stream()
+        with torch.cuda.stream(stream):
+            step()                   # eager: kernels configured, state t0 + 1
+        torch.cuda.synchronize()
+        oracle_step("eager")
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            step()                   # captured from the host's view of state t0 + 1
+        for rep in range(4):
+            for o in outs:
+                o.zero_()
+            graph.replay()
+            torch.cuda.synchronize()
+            oracle_step(f"replay {rep}")
+            st = capi.masw_query(p.h, 0, 0)
+            assert st["dev_t"] == t0 + 2 + rep and st["dev_m"] == orc.slot_count(t0 + 2 + rep, S, W, r)
+        capi.masw_sync(p.h)
+    finally:
+        p.close()
+
+
 def test_bounded_wait_timeout_is_reported_and_the_context_survives():
     """Failure detection without a fault: a bounded wait on a barrier nothing
     arrives on runs out, masw_sync reports MASW_ETIMEOUT (once), and the same
