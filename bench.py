@@ -719,6 +719,30 @@ def profile_case(kind: str, prefix: int):
             capi.masw_verify_attn(q, kc, vc, kl, o)
         torch.cuda.synchronize()
         return
+    if kind == "step_b1":
+        # the pages' decoding setting: one sequence through all 28 layers of the
+        # 3B-draft memory (4.5 MB per layer, 126 MB per decode step, about the
+        # size of L2), three iterations of 28 fused steps and the rollback, so a
+        # capture of the second iteration's launches sees what the first left in L2
+        L1 = w["layers"]
+        h = capi.masw_mem_create(S, W, r, Hkv, D, L1, batch=1, dtype=capi.MASW_BF16, max_seq_len=prefix + 32,
+                                 rollback_reserve=16)
+        n = max(0, (prefix - S - W) // r)
+        kr = torch.randn(prefix, Hkv, D, generator=g, device=dev).to(torch.bfloat16)
+        vr = torch.randn(prefix, Hkv, D, generator=g, device=dev).to(torch.bfloat16)
+        ks = torch.randn(n, Hkv, D, generator=g, device=dev).to(torch.bfloat16)
+        for l in range(L1):
+            capi.masw_mem_load(h, l, 0, kr, vr, ks, ks)
+        q = [torch.randn(1, Hq, D, generator=g, device=dev).to(torch.bfloat16) for _ in range(L1)]
+        kn = [torch.randn(1, Hkv, D, generator=g, device=dev).to(torch.bfloat16) for _ in range(L1)]
+        o = torch.empty(1, Hq, D, device=dev)
+        for _ in range(3):
+            for l in range(L1):
+                capi.masw_draft_step(h, l, q[l], kn[l], kn[l], o)
+            capi.masw_rollback(h, [0], [prefix])
+        torch.cuda.synchronize()
+        capi.masw_mem_destroy(h)
+        return
     full = kind == "full"
     h = capi.masw_mem_create(S, W, r, Hkv, D, L, batch=B, dtype=capi.MASW_BF16, max_seq_len=prefix + 8,
                              full_kv=full)
@@ -761,7 +785,7 @@ def main():
     ap.add_argument("--no-prefill", action="store_true")
     ap.add_argument("--prefill-only", action="store_true",
                     help="only the draft prefill of one sequence through all layers (one JSON line)")
-    ap.add_argument("--profile-case", choices=["draft", "step", "full", "verify", "prefill"], default=None,
+    ap.add_argument("--profile-case", choices=["draft", "step", "step_b1", "full", "verify", "prefill"], default=None,
                     help="run a few launches of one kernel on a small state (4 layers) for an ncu capture")
     args = ap.parse_args()
     if args.warmup < 3:
