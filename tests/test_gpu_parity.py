@@ -169,6 +169,62 @@ def test_ragged_batch_active_mask_and_edges():
         p.close()
 
 
+def test_maximum_batch_ragged_active_and_boundaries():
+    """The largest batch a handle holds (MASW_MAX_BATCH = 512 sequences), every
+    sequence at its own prefix: fused steps with an active mask over all 16
+    words of the mask, and at each step the fused slot write for exactly the
+    sequences that reach a boundary (row ids up to 511); every sequence's
+    output is compared with the oracle at every step, and a sample of memories
+    row by row."""
+    S, W, r, Hkv, G, D = 2, 6, 3, 1, 3, 64
+    B = capi.MASW_MAX_BATCH
+    p = Pair(S, W, r, Hkv, D, 1, B, "bf16", Hkv * G, max_seq_len=64, tag="maxbatch")
+    try:
+        for b in range(B):
+            p.load(0, b, b % 23, seed=1)
+        for step in range(6):
+            p.step = step
+            active = [int((b + step) % 5 != 0) for b in range(B)]
+            due = [b for b in range(B) if active[b] and orc.is_boundary(p.ref.t(0, b) + 1, S, W, r)
+                   and p.ref.m(0, b) == orc.slot_count(p.ref.t(0, b) + 1, S, W, r) - 1]
+            if due:
+                p.fstep_slot(0, due, active=active)
+            else:
+                p.fstep(0, active=active)
+        capi.masw_sync(p.h)
+        for b in (0, 1, 255, 256, 510, 511):
+            p.check_state(0, b)
+    finally:
+        p.close()
+
+
+@pytest.mark.parametrize("S,W,r,dtype", [(0, 1, 1, "bf16"), (1, 1, 1, "f32"), (0, 2, 3, "bf16"), (3, 1, 5, "f32")])
+def test_degenerate_windows_and_rates(S, W, r, dtype):
+    """Degenerate memories: a one-token window, a slot for every evicted token
+    (r = 1), no sink, a slot rate above the window: fused steps from an empty
+    memory through many boundaries, the fused slot write at each, checked
+    against the oracle at every step and row by row at the end."""
+    Hkv, G, D = 2, 2, 64
+    B, T = 2, 40
+    p = Pair(S, W, r, Hkv, D, 1, B, dtype, Hkv * G, max_seq_len=T + 4, tag=f"degen{S}{W}{r}")
+    try:
+        for step in range(T):
+            p.step = step
+            due = [b for b in range(B) if orc.is_boundary(p.ref.t(0, b) + 1, S, W, r)]
+            if due and dtype == "bf16":
+                p.fstep_slot(0, due)
+            else:
+                p.fstep(0)
+                if due:
+                    p.materialize(0, due)
+        capi.masw_sync(p.h)
+        for b in range(B):
+            assert p.ref.m(0, b) == orc.slot_count(T, S, W, r)
+            p.check_state(0, b)
+    finally:
+        p.close()
+
+
 def test_no_sink_r_larger_than_w_and_scale():
     """S = 0 (pure window plus slots), r > W, an explicit softmax scale."""
     p = Pair(0, 16, 40, 2, 128, 1, 2, "bf16", 4, max_seq_len=600, scale=0.05, tag="nosink")
