@@ -109,7 +109,7 @@ decode_kernel(const __grid_constant__ DecodeParams p) {
         const int mcnt = p.d_m[(size_t)lb * p.Hkv + h];
         s_m_before = mcnt;
         s_t = t;
-        const int n = build_segments<ROWB>(p, lb, h, z, t, mcnt, segs);
+        const int n = build_segments_checked<ROWB>(p, lb, h, z, t, mcnt, segs);
         s_nseg = n;
         for (int s = 0; s < NST; ++s) mbar_init(&bars[s], 1);
         fence_mbar_init();
@@ -427,6 +427,22 @@ int masw_launch_decode(masw_mem_t* mem, int mode, int layer, const void* q, int 
     while (n_split > 1 && masw_decode_part_floats(n_rows, mem->Hkv, G, mem->D, n_split) > mem->part_floats)
         --n_split;
     prm.n_split = n_split;
+    if (mem->check_segments && mem->dtype == MASW_BF16) {
+        // the tables the tensor-core kernel builds from the host mirror, before it runs
+        Seg segs[5];
+        for (int z = 0; z < n_rows; ++z)
+            for (int h = 0; h < mem->Hkv; ++h) {
+                const int lbz = layer * mem->B + prm.seq_ids[z];
+                const int n = mem->D == 128
+                                  ? build_segments<256>(prm, lbz, h, z, prm.t_spec[z], prm.m_spec[z], segs)
+                                  : build_segments<128>(prm, lbz, h, z, prm.t_spec[z], prm.m_spec[z], segs);
+                const bool ok = mem->D == 128 ? segments_in_block<256>(prm, lbz, h, z, segs, n)
+                                              : segments_in_block<128>(prm, lbz, h, z, segs, n);
+                if (!ok)
+                    return masw_set_error(mem, MASW_EGUARD, "decode: segment table of row " + std::to_string(z) +
+                                                                ", head " + std::to_string(h) + " leaves its block");
+            }
+    }
     int rc;
     if (mem->dtype == MASW_BF16)
         rc = masw_launch_decode_mma(mem, prm, G, n_rows, kmax, stream);

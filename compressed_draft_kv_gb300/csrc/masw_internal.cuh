@@ -79,6 +79,9 @@ struct masw_mem {
     std::vector<Alloc> allocs;
     size_t alloc_total = 0;   // bytes allocated (guards included)
     size_t alloc_limit = 0;   // 0: none; else create refuses to allocate beyond it
+    // MASW_CHECK_SEGMENTS=1 at create: every decode launch checks, on the host,
+    // the segment tables its CTAs will build from the host mirror
+    bool check_segments = false;
 };
 
 namespace masw {
@@ -396,7 +399,7 @@ struct Seg {
 // K_g/V_g row.  Draft mode: [EN] §3.1 Eq. 4; slot mode: [EN] §3.2 Algorithm 1
 // (slots 1..m-1 only); full mode: every raw token.
 template <int ROWB>
-__device__ __forceinline__ int build_segments(const DecodeParams& p, int lb, int h, int z, int t, int mcnt,
+__host__ __device__ __forceinline__ int build_segments(const DecodeParams& p, int lb, int h, int z, int t, int mcnt,
                                               Seg* segs) {
     // fused step: the query sees token t+1, whose K/V row comes straight from
     // the caller's buffer; the pool holds tokens 1..t
@@ -432,6 +435,54 @@ __device__ __forceinline__ int build_segments(const DecodeParams& p, int lb, int
         segs[n++] = Seg{(const uint8_t*)p.k_g + off, (const uint8_t*)p.v_g + off, 1};
     }
     return n;
+}
+
+// Out-of-bounds check of the index model's result: every run of pool rows must
+// lie inside its own (layer, sequence, kv head) block and in its region -- the
+// sink in rows [0, S), window runs in the ring rows [S, S + Wc), the slot chain
+// in [S + Wc, S + Wc + M_max); full-KV runs inside the block's max_seq_len rows
+// -- a caller row must be the one the API places for (row z, head h), and no two
+// runs may overlap.  Pointer comparisons only (it also runs on the host, over
+// the speculative tables, when a handle checks its launches).
+template <int ROWB>
+__host__ __device__ inline bool segments_in_block(const DecodeParams& p, int lb, int h, int z, const Seg* segs, int n) {
+    const bool full = p.mode == kDevModeFull;
+    const uint8_t* kb = (const uint8_t*)(full ? p.full_k : p.pool_k);
+    const ptrdiff_t dv = (const uint8_t*)(full ? p.full_v : p.pool_v) - kb;
+    const size_t rows = full ? (size_t)p.Tmax : (size_t)p.C;
+    const uint8_t* b0 = kb + ((size_t)lb * p.Hkv + h) * rows * ROWB;
+    const uint8_t* b1 = full ? b0 + rows * ROWB : b0 + (size_t)p.S * ROWB;
+    const uint8_t* b2 = b1 + (size_t)(full ? 0 : p.Wc) * ROWB;
+    const uint8_t* b3 = b2 + (size_t)(full ? 0 : p.M_max) * ROWB;
+    const uint8_t* own_k = p.k_g ? (const uint8_t*)p.k_g + ((size_t)z * p.Hkv + h) * ROWB : nullptr;
+    const uint8_t* own_v = p.v_g ? (const uint8_t*)p.v_g + ((size_t)z * p.Hkv + h) * ROWB : nullptr;
+    bool ok = n <= 5;
+    for (int s = 0; s < n; ++s) {
+        const Seg& g = segs[s];
+        const uint8_t* e = g.k + (size_t)g.len * ROWB;
+        if (g.k == own_k) {
+            ok = ok && g.len == 1 && g.v == own_v;
+            continue;
+        }
+        const uint8_t* lo = g.k < b1 ? b0 : (g.k < b2 ? b1 : b2);
+        const uint8_t* hi = g.k < b1 ? b1 : (g.k < b2 ? b2 : b3);
+        ok = ok && g.len >= 1 && g.k >= lo && e <= hi && g.v - g.k == dv;
+        for (int q = 0; q < s; ++q)
+            if (segs[q].k != own_k) ok = ok && (e <= segs[q].k || segs[q].k + (size_t)segs[q].len * ROWB <= g.k);
+    }
+    return ok;
+}
+
+// build_segments plus that check on the device, for the tables built from the
+// device counters; a table that fails is recorded in d_err[3] (masw_sync
+// reports it as MASW_EGUARD) and replaced by an empty one, so no copy leaves
+// its block.
+template <int ROWB>
+__device__ int build_segments_checked(const DecodeParams& p, int lb, int h, int z, int t, int mcnt, Seg* segs) {
+    const int n = build_segments<ROWB>(p, lb, h, z, t, mcnt, segs);
+    if (segments_in_block<ROWB>(p, lb, h, z, segs, n)) return n;
+    atomicExch(p.d_err + 3, 1);
+    return 0;
 }
 
 // After the attention of pair (row z, head h) is final -- its last split, or

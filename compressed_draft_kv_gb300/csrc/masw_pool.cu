@@ -302,6 +302,10 @@ int masw_mem_create(int S, int W, int r, int n_kv_heads, int head_dim, int layer
     };
     m->alloc_limit = alloc_limit_from_env();
     {
+        const char* e = std::getenv("MASW_CHECK_SEGMENTS");
+        m->check_segments = e && e[0] == '1';
+    }
+    {
         // the pools alone (before any CUDA call): a limit below them is refused here
         const size_t pool_raw = (size_t)layers * m->B * n_kv_heads * m->C * head_dim * m->esize + 2 * kGuardBytes;
         if (m->alloc_limit && 2 * pool_raw > m->alloc_limit)
@@ -747,9 +751,12 @@ int masw_sync(masw_mem_t* mem, masw_stream_t stream) {
     MASW_CUDA_TRY(mem, cudaStreamSynchronize((cudaStream_t)stream));
     int err[4] = {0, 0, 0, 0};
     MASW_CUDA_TRY(mem, cudaMemcpy(err, mem->d_err, sizeof(err), cudaMemcpyDeviceToHost));
-    if (err[0] || err[1] || err[2]) {
+    if (err[0] || err[1] || err[2] || err[3]) {
         const int zero[4] = {0, 0, 0, 0};
         MASW_CUDA_TRY(mem, cudaMemcpy(mem->d_err, zero, sizeof(zero), cudaMemcpyHostToDevice));
+        if (err[3])
+            return masw_set_error(mem, MASW_EGUARD,
+                                  "a decode kernel's segment table left its (layer, sequence, kv head) block");
         if (err[0]) return masw_set_error(mem, MASW_ETIMEOUT, "a device-side bounded wait ran out");
         if (err[2]) return masw_set_error(mem, MASW_ECUDA, "a kernel's shared memory was not 1024-byte aligned");
         return masw_set_error(mem, MASW_ECAPACITY, "a device-side append exceeded max_seq_len");

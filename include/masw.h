@@ -60,7 +60,8 @@ extern "C" {
 #define MASW_ESTATE     -4  /* call not valid in the current state (e.g. not at a boundary) */
 #define MASW_ECUDA      -5  /* a CUDA runtime call failed */
 #define MASW_ETIMEOUT   -6  /* a bounded device-side wait ran out (kernel returned early) */
-#define MASW_EGUARD     -7  /* a guard band around a handle-owned buffer was overwritten */
+#define MASW_EGUARD     -7  /* out of bounds: a guard band around a handle-owned buffer was
+                               overwritten, or a decode kernel's segment table left its block */
 
 /* ---- element types ------------------------------------------------------- */
 #define MASW_F32   0
@@ -352,7 +353,9 @@ int masw_mem_export(masw_mem_t* mem, int layer, int seq, void* k_out, void* v_ou
 int masw_query(masw_mem_t* mem, int layer, int seq, masw_state_t* out);
 
 /* Wait for the stream, then report any error recorded by a kernel since the
- * last masw_sync (MASW_ETIMEOUT) or by the CUDA runtime (MASW_ECUDA). */
+ * last masw_sync (MASW_ETIMEOUT; MASW_EGUARD when a decode kernel found its
+ * segment table outside its block and skipped the copies; MASW_ECAPACITY) or
+ * by the CUDA runtime (MASW_ECUDA). */
 int masw_sync(masw_mem_t* mem, masw_stream_t stream);
 
 /* Failure-detection self-test: launch a kernel whose bounded wait (the helper

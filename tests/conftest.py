@@ -10,6 +10,11 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 if HERE not in sys.path:
     sys.path.insert(0, HERE)
 
+# every decode launch of a test checks, on the host, that the segment tables its
+# CTAs build from the host mirror stay inside their (layer, sequence, kv head)
+# block; a handle reads this when it is created
+os.environ.setdefault("MASW_CHECK_SEGMENTS", "1")
+
 
 def pytest_configure(config):
     config.addinivalue_line("markers", "gpu: needs a CUDA GPU (GB300, sm_103a) and the built library")

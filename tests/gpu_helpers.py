@@ -57,6 +57,7 @@ class Pair:
     def close(self):
         if self.h:
             try:
+                capi.masw_sync(self.h)           # no device-side error (segment tables in bounds, ...)
                 capi.masw_check_guards(self.h)   # no kernel wrote outside a handle-owned buffer
             finally:
                 capi.masw_mem_destroy(self.h)
