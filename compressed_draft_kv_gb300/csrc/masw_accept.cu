@@ -41,6 +41,10 @@ __global__ void __launch_bounds__(256) accept_kernel(const __grid_constant__ Acc
     pdl_wait();
     pdl_trigger();
     const int c = blockIdx.x, j = blockIdx.y, b = blockIdx.z, tid = threadIdx.x;
+    // the sequence's first 64 draft tokens, read now so that the last CTA
+    // compares them from shared memory instead of waiting on global reads
+    __shared__ int s_draft[64];
+    if (tid < imin(p.L, 64)) s_draft[tid] = __ldg(p.draft + (size_t)b * p.L + tid);
     const int row = b * (p.L + 1) + j;
     const int v0 = c * p.chunk, v1 = imin(p.V, v0 + p.chunk);
     float bv = -INFINITY;
@@ -150,7 +154,8 @@ __global__ void __launch_bounds__(256) accept_kernel(const __grid_constant__ Acc
         int l_acc = p.L;
         for (int jj = 0; jj < p.L; ++jj) {
             const int tj = jj < 64 ? s_tok[jj] : __ldcg(p.tokens + b * (p.L + 1) + jj);
-            if (p.draft[b * p.L + jj] != tj) { l_acc = jj; break; }
+            const int dj = jj < 64 ? s_draft[jj] : __ldg(p.draft + (size_t)b * p.L + jj);
+            if (dj != tj) { l_acc = jj; break; }
         }
         p.n_emit[b] = l_acc + 1;
         p.tickets[b] = 0u;
