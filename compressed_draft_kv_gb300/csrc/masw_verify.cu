@@ -8,6 +8,7 @@
 // keys in blocks of 64 and keeps S, O and Q in tensor memory; splits over the
 // key axis are merged by split_epilogue.
 #include "masw_internal.cuh"
+#include "masw_splits.h"
 #include "masw_tc.cuh"
 
 #include <atomic>
@@ -456,14 +457,9 @@ static int verify_tc_occupancy() {
 }
 
 // Split count shared by the launcher and the workspace query: one wave of the
-// resident CTA slots, at least 256 keys per split.
-static int verify_splits(int B, int Hkv, int Tmax, int num_sms, int NT) {
-    (void)NT;
-    const int pairs = B * Hkv;
-    const int slots = verify_tc_occupancy() * num_sms;
-    int n = imax(1, slots / pairs);
-    n = imin(n, imax(1, (Tmax + 255) / 256));
-    return imin(n, kVMaxSplit);
+// resident CTA slots, at least 256 keys per split (masw_splits.h).
+static int verify_splits(int B, int Hkv, int Tmax, int num_sms) {
+    return verify_split_plan(B * Hkv, verify_tc_occupancy() * num_sms, Tmax, kVMaxSplit);
 }
 
 static int num_sms_current(int* out) {
@@ -474,8 +470,7 @@ static int num_sms_current(int* out) {
 }
 
 static size_t verify_part_bytes(int B, int Hkv, int NQ, int n_split) {
-    const size_t partb = (size_t)B * Hkv * n_split * NQ * (kVD + 2) * sizeof(float);
-    return ((partb + 255) / 256) * 256;
+    return verify_partial_bytes(B * Hkv, NQ, kVD, n_split);
 }
 
 }  // namespace masw
@@ -498,7 +493,7 @@ extern "C" int masw_verify_workspace_bytes(int B, int Lq, int Hq, int Hkv, int D
     int sms = 0;
     if (num_sms_current(&sms)) return masw_set_error(nullptr, MASW_ECUDA, "cannot query the current device");
     const int NQ = (Hq / Hkv) * Lq;
-    const int n_split = verify_splits(B, Hkv, Tmax, sms, (NQ + 7) / 8);
+    const int n_split = verify_splits(B, Hkv, Tmax, sms);
     *bytes = verify_part_bytes(B, Hkv, NQ, n_split) + (size_t)B * Hkv * sizeof(unsigned) + 16;
     return MASW_OK;
 }
@@ -566,7 +561,7 @@ extern "C" int masw_verify_attn(const void* q, const void* k_cache, const void* 
     int sms = 0;
     if (num_sms_current(&sms)) return masw_set_error(nullptr, MASW_ECUDA, "verify: cannot query the device");
     const int G = Hq / Hkv, NQ = G * Lq;
-    const int n_split = verify_splits(B, Hkv, Tmax, sms, (NQ + 7) / 8);
+    const int n_split = verify_splits(B, Hkv, Tmax, sms);
     const size_t partb = verify_part_bytes(B, Hkv, NQ, n_split);
     if (workspace_bytes < partb + (size_t)B * Hkv * sizeof(unsigned) + 16)
         return masw_set_error(nullptr, MASW_EINVAL, "verify: workspace too small");
@@ -652,8 +647,8 @@ extern "C" int masw_verify_attn_noalloc(const void* q, const void* k_cache, cons
     void* scratch = nullptr;
     if ((rc = noalloc_scratch(&scratch))) return rc;
     const int G = Hq / Hkv, NQ = G * Lq;
-    int n_split = verify_splits(B, Hkv, Tmax, sms, (NQ + 7) / 8);
-    while (n_split > 1 && verify_part_bytes(B, Hkv, NQ, n_split) > kNoAllocPartBytes) --n_split;
+    const int n_split = noalloc_split_plan(B * Hkv, NQ, kVD, Tmax, verify_tc_occupancy() * sms, kVMaxSplit,
+                                           kNoAllocPartBytes);
     cudaStream_t st = (cudaStream_t)stream;
     // the library's static array cannot be re-zeroed by the caller after a
     // failed call, so this variant clears the tickets and the status word on
