@@ -115,7 +115,12 @@ typedef struct {
  * much device memory in total (guards included) and otherwise fails with
  * MASW_ENOMEM, freeing what it had allocated: a way to exercise the
  * out-of-memory path without exhausting the device.  A limit below the pool's
- * own size is refused before any CUDA call. */
+ * own size is refused before any CUDA call.  If MASW_CHECK_SEGMENTS is "1" at
+ * create, every bf16 decode launch of the handle first checks on the host that
+ * each run of pool rows its CTAs will copy lies inside its own (layer,
+ * sequence, kv head) block and region, and fails with MASW_EGUARD (nothing
+ * launched) otherwise: a debug mode, a few microseconds of host time per
+ * launch. */
 int masw_mem_create(int S, int W, int r, int n_kv_heads, int head_dim, int layers,
                     const masw_opts_t* opts, masw_mem_t** out);
 
