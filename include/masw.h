@@ -119,8 +119,8 @@ typedef struct {
  * create, every bf16 decode launch of the handle first checks on the host that
  * each run of pool rows its CTAs will copy lies inside its own (layer,
  * sequence, kv head) block and region, and fails with MASW_EGUARD (nothing
- * launched) otherwise: a debug mode, a few microseconds of host time per
- * launch. */
+ * launched) otherwise: a debug mode, whose host time per launch grows with
+ * rows x kv heads. */
 int masw_mem_create(int S, int W, int r, int n_kv_heads, int head_dim, int layers,
                     const masw_opts_t* opts, masw_mem_t** out);
 
