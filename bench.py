@@ -707,6 +707,19 @@ def profile_case(kind: str, prefix: int):
         torch.cuda.synchronize()
         capi.masw_mem_destroy(h)
         return
+    if kind == "accept":
+        # greedy acceptance on the bench's shape (batch 8, L_draft = 5, a
+        # 128,256-token vocabulary, bf16): one call on each of 4 logit buffers
+        ab, al, av = 8, 5, 128256
+        logits = [torch.randn(ab, al + 1, av, generator=g, device=dev).to(torch.bfloat16) for _ in range(4)]
+        draft = torch.randint(0, av, (ab, al), generator=g, device=dev, dtype=torch.int32)
+        tokens = torch.empty(ab, al + 1, dtype=torch.int32, device=dev)
+        n_emit = torch.empty(ab, dtype=torch.int32, device=dev)
+        ws = torch.zeros(capi.masw_greedy_workspace_bytes(ab, al, av), dtype=torch.uint8, device=dev)
+        for x in logits:
+            capi.masw_greedy_accept(x, draft, tokens, n_emit, workspace=ws)
+        torch.cuda.synchronize()
+        return
     if kind == "verify":
         vb, Lq, Hq8 = 4, 6, 32
         T = prefix + Lq
@@ -785,7 +798,8 @@ def main():
     ap.add_argument("--no-prefill", action="store_true")
     ap.add_argument("--prefill-only", action="store_true",
                     help="only the draft prefill of one sequence through all layers (one JSON line)")
-    ap.add_argument("--profile-case", choices=["draft", "step", "step_b1", "full", "verify", "prefill"], default=None,
+    ap.add_argument("--profile-case", choices=["draft", "step", "step_b1", "full", "verify", "prefill", "accept"],
+                    default=None,
                     help="run a few launches of one kernel on a small state (4 layers) for an ncu capture")
     args = ap.parse_args()
     if args.warmup < 3:
