@@ -78,6 +78,10 @@ struct PrefillParams {
     CUtensorMap tm_v_raw;
     CUtensorMap tm_k_slot;   // [M][Hkv][128]
     CUtensorMap tm_v_slot;
+    CUtensorMap tm_k_sink;   // raw K/V, box 8 x 1 x 64: the first 8 rows of a merged sink + slot block
+    CUtensorMap tm_v_sink;
+    CUtensorMap tm_k_slot56; // slot K/V, box 56 x 1 x 64: its other 56 rows
+    CUtensorMap tm_v_slot56;
     const __nv_bfloat16* q_raw;    // [T][Hq][128]
     const __nv_bfloat16* q_slot;   // [M][Hq][128]
     float* o_raw;            // [T][Hq][128]
@@ -90,8 +94,16 @@ struct PrefillParams {
     int slot_rows;           // slots per slot CTA
     int slot_pack;           // G: a slot CTA holds the rows of all G query heads of one kv head
                              // (row = slot * G + head), 1: one query head per slot CTA
+    int merge_ok;            // 1: S <= 8 and the merged-block maps exist
     float scale_log2;
 };
+
+// bits [lo, hi) of a 64-column block (0 <= lo, hi <= 64; empty when hi <= lo)
+__device__ __forceinline__ uint64_t col_bits(int lo, int hi) {
+    const uint64_t a = hi >= 64 ? ~0ull : ((1ull << hi) - 1ull);
+    const uint64_t b = lo >= 64 ? ~0ull : ((1ull << lo) - 1ull);
+    return a & ~b;
+}
 
 // mbarriers of one CTA
 __device__ __forceinline__ constexpr int bar_k(int s) { return s; }        // K stage landed (TMA)
@@ -168,9 +180,14 @@ __global__ void __launch_bounds__(192, 2) prefill_kernel(const __grid_constant__
             hi2 = p.self_attend ? m : m - 1;
         }
     }
+    // The sink (S <= 8 keys) and a slot prefix of at most 56 slots share one
+    // block when both are present: rows 0..7 of the stage come from the raw
+    // arrays, rows 8..63 from the slot arrays, and a row sees columns
+    // [0, hi0) and [8, 8 + hi2) of it.  It saves the tile a block of 64 keys.
+    const bool merged = p.merge_ok && b0 > 0 && b2 > 0 && b2 <= kBN - 8;
     const int bs1 = (b0 + kBN - 1) / kBN;
     const int bs2 = bs1 + (b1 - a1 + kBN - 1) / kBN;
-    const int nblk = bs2 + (b2 + kBN - 1) / kBN;
+    const int nblk = bs2 + (merged ? 0 : (b2 + kBN - 1) / kBN);
     // range index and first key of block blk
     auto block_of = [&](int blk, int& k, int& key0) {
         k = (blk >= bs1 ? 1 : 0) + (blk >= bs2 ? 1 : 0);
@@ -229,8 +246,21 @@ __global__ void __launch_bounds__(192, 2) prefill_kernel(const __grid_constant__
                 const int bi = is_v ? bar_v(st) : bar_k(st);
                 const uint32_t dst = sb + (is_v ? kOffV : kOffK) + st * kKVBytes;
                 mbar_expect_tx(bars + bi, kKVBytes);
-                tma_load_3d(dst, m, 0, kvh, key0, bar_at(bi));
-                tma_load_3d(dst + kKVBytes / 2, m, 64, kvh, key0, bar_at(bi));
+                if (merged && k == 0) {
+                    // 8 raw rows (1 KB per 64-column panel) then 56 slot rows at
+                    // the next 1024-byte boundary: the same bytes and swizzle
+                    // phase as one 64-row box
+                    const CUtensorMap* ms = is_v ? &p.tm_v_sink : &p.tm_k_sink;
+                    const CUtensorMap* mg = is_v ? &p.tm_v_slot56 : &p.tm_k_slot56;
+#pragma unroll
+                    for (int pn = 0; pn < 2; ++pn) {
+                        tma_load_3d(dst + pn * (kKVBytes / 2), ms, 64 * pn, kvh, 0, bar_at(bi));
+                        tma_load_3d(dst + pn * (kKVBytes / 2) + 1024, mg, 64 * pn, kvh, 0, bar_at(bi));
+                    }
+                } else {
+                    tma_load_3d(dst, m, 0, kvh, key0, bar_at(bi));
+                    tma_load_3d(dst + kKVBytes / 2, m, 64, kvh, key0, bar_at(bi));
+                }
                 li = blk + 1;
             };
             for (int b = 0; b < imin(2, nblk); ++b) load(b);
@@ -341,9 +371,14 @@ __global__ void __launch_bounds__(192, 2) prefill_kernel(const __grid_constant__
             float x[64];
 #pragma unroll
             for (int e = 0; e < 64; ++e) x[e] = __uint_as_float(sv[e >> 5][e & 31]);
-            if (e_lo > 0 || e_hi < kBN) {
+            // visible columns as a bit mask: [e_lo, e_hi), or in the merged
+            // block the sink columns [0, hi0) and the slot columns [8, 8 + hi2)
+            const uint64_t vis = (merged && k == 0) ? (col_bits(0, hi0) | col_bits(8, 8 + hi2)) : col_bits(e_lo, e_hi);
+            if (vis != ~0ull) {
+                const uint32_t v_lo = (uint32_t)vis, v_hi = (uint32_t)(vis >> 32);
 #pragma unroll
-                for (int e = 0; e < 64; ++e) x[e] = (e >= e_lo && e < e_hi) ? x[e] : -INFINITY;
+                for (int e = 0; e < 64; ++e)
+                    x[e] = (((e < 32 ? v_lo : v_hi) >> (e & 31)) & 1u) ? x[e] : -INFINITY;
             }
             // row max of the raw scores (scale > 0 commutes with max): 3-input
             // max in four chains
@@ -582,6 +617,11 @@ extern "C" int masw_prefill(masw_mem_t* mem, int layer, int seq, int T, const vo
     if (M > 0)
         maps = maps && make_map(&p.tm_k_slot, k_slot, M, Hkv, tcp::kBN) && make_map(&p.tm_v_slot, v_slot, M, Hkv, tcp::kBN);
     if (!maps) return masw_set_error(mem, MASW_EINVAL, "prefill: cannot describe the inputs as TMA tensors");
+    // maps of the merged sink + slot block (8 raw rows, then 56 slot rows)
+    if (M > 0 && mem->S >= 1 && mem->S <= 8)
+        p.merge_ok = make_map(&p.tm_k_sink, k_raw, T, Hkv, 8) && make_map(&p.tm_v_sink, v_raw, T, Hkv, 8) &&
+                     make_map(&p.tm_k_slot56, k_slot, M, Hkv, tcp::kBN - 8) &&
+                     make_map(&p.tm_v_slot56, v_slot, M, Hkv, tcp::kBN - 8);
     p.q_raw = (const __nv_bfloat16*)q_raw;
     p.q_slot = (const __nv_bfloat16*)q_slot;
     p.o_raw = o_raw;
