@@ -9,7 +9,9 @@
 // from the caller's raw and slot K/V arrays ([T, Hkv, D], [M, Hkv, D]).  For one
 // tile of query rows the visible keys are a few contiguous ranges (sink, window
 // band, slot prefix), and for one row each range is a single interval, so the
-// mask is two compares per score.
+// mask of a 64-key block is one or two intervals of columns (a bit mask per
+// row, skipped for blocks every row sees whole).  With S <= 8 the sink and a
+// slot prefix of up to 56 slots share one block.
 //
 // Fifth-generation tensor cores, one CTA per (128-row query tile, query head),
 // two CTAs per SM:
