@@ -35,6 +35,19 @@ __host__ __device__ inline bool is_boundary(int t, int S, int W, int r) {
 }
 // ring row of non-sink token i in a ring of Wc rows
 __host__ __device__ inline int ring_row(int i, int S, int Wc) { return (i - S - 1) % Wc; }
+// Row `pos` (0-based) of the interleaved order of a prefix of T raw tokens and
+// its M slots -- slot token g_m right after raw token tau_m = S + W + m r, the
+// order in which the pages' prefill writes the memory --: the raw token i
+// (1-based, > 0) or -m for slot m.  Past the first S + W raw tokens the order
+// repeats r raw tokens and one slot, M times, then raw tokens only.
+__host__ __device__ inline int interleaved_row(int pos, int S, int W, int r, int M) {
+    const int q = pos - (S + W);
+    if (q < r) return pos + 1;
+    const int k = q / (r + 1);
+    if (k >= M) return pos + 1 - M;
+    const int o = q - k * (r + 1);
+    return o < r ? S + W + k * r + o + 1 : -(k + 1);
+}
 
 }  // namespace masw
 

@@ -92,10 +92,6 @@ struct PrefillParams {
     float* lse_slot;         // [M][Hq] or null
     int* d_err;
     int T, M, S, W, r, Hq, Hkv, self_attend;
-    int slot_ctas;           // CTAs of slot query rows (first in the grid: their key bands are longer)
-    int slot_rows;           // slots per slot CTA
-    int slot_pack;           // G: a slot CTA holds the rows of all G query heads of one kv head
-                             // (row = slot * G + head), 1: one query head per slot CTA
     int merge_ok;            // 1: S <= 8 and the merged-block maps exist
     float scale_log2;
 };
@@ -134,53 +130,34 @@ __global__ void __launch_bounds__(192, 2) prefill_kernel(const __grid_constant__
     auto bar_at = [&](int i) { return sb + kOffBar + 8u * (uint32_t)i; };
 
     const int G = p.Hq / p.Hkv;
-    const bool slot_tile = (int)blockIdx.x < p.slot_ctas;
-    // packed slot CTAs: blockIdx.y is the kv head and the rows are (slot, head)
-    // pairs of its G query heads, which share the slot's mask and K/V
-    const int pack = slot_tile ? p.slot_pack : 1;
-    if (pack > 1 && (int)blockIdx.y >= p.Hkv) return;           // no work: uniform exit before any sync
-    const int kvh = pack > 1 ? (int)blockIdx.y : (int)blockIdx.y / G;
-    const int rpt = slot_tile ? p.slot_rows : kBM;               // positions (slots) of this CTA
-    const int q0 = ((int)blockIdx.x - (slot_tile ? 0 : p.slot_ctas)) * rpt;
-    const int nq = slot_tile ? p.M : p.T;
-    const int q1 = imin(nq, q0 + rpt);                           // the CTA's positions [q0, q1)
+    const int hq = (int)blockIdx.y, kvh = hq / G;                // query head and its kv head
     const int S = p.S, W = p.W, r = p.r;
-
-    const int qrow = q0 + (pack > 1 ? tid / pack : tid);         // this thread's position
-    const int hq = pack > 1 ? kvh * G + tid % pack : (int)blockIdx.y;   // and query head
-    const bool live = tid < kBM && (pack == 1 || tid < rpt * pack) && qrow < q1;
+    // The CTA's rows [q0, q1) of the interleaved order of the T + M query rows.
+    // A slot row g_m has the mask of raw row tau_m (the sink, the window at
+    // tau_m, slots 1..m-1), so slot rows ride in the raw tiles with tau_m as
+    // their position.
+    const int q0 = (int)blockIdx.x * kBM, q1 = imin(p.T + p.M, q0 + kBM);
+    const bool live = tid < kBM && q0 + tid < q1;
+    auto eff = [&](int x) { return x > 0 ? x : S + W + (-x) * r; };
+    const int xr = live ? interleaved_row(q0 + tid, S, W, r, p.M) : 1;   // this row: raw token (> 0) or slot (< 0)
 
     // visible key ranges of the CTA: 0 = sink and 1 = window band (raw rows),
     // 2 = slot prefix (slot rows), each [a_k, b_k) possibly empty; this thread's
     // row sees the interval [lo_k, hi_k) of range k.  Kept in scalars (no
     // dynamically indexed arrays) so that nothing spills to local memory.
-    int b0 = 0, a1 = 0, b1 = 0, b2 = 0;
-    int lo1 = 0, hi0 = 0, hi1 = 0, hi2 = 0;
-    if (!slot_tile) {
-        const int i0 = q0 + 1, i1 = q1, i = qrow + 1;   // 1-based raw positions
-        b0 = imin(S, i1);
-        a1 = imax(S + 1, i0 - W + 1) - 1;
-        b1 = imax(a1, i1);
-        b2 = slot_count(i1 - 1, S, W, r);
-        lo1 = imax(S + 1, i - W + 1) - 1;
-        if (live) {
-            hi0 = imin(S, i);
-            hi1 = i;
-            hi2 = slot_count(i - 1, S, W, r);
-        }
-    } else {
-        const int m0 = q0 + 1, m1 = q1, m = qrow + 1;   // 1-based slot indices
-        const int tau0 = S + W + m0 * r, tau1 = S + W + m1 * r, tau = S + W + m * r;
-        b0 = S;
-        a1 = imax(S, tau0 - W);
-        b1 = tau1;
-        b2 = imax(0, p.self_attend ? m1 : m1 - 1);
-        lo1 = tau - W;
-        if (live) {
-            hi0 = S;
-            hi1 = tau;
-            hi2 = p.self_attend ? m : m - 1;
-        }
+    const int i_first = eff(interleaved_row(q0, S, W, r, p.M)), i_last = eff(interleaved_row(q1 - 1, S, W, r, p.M));
+    const int b0 = imin(S, i_last);
+    const int a1 = imax(S + 1, i_first - W + 1) - 1;
+    const int b1 = imax(a1, i_last);
+    // slots with tau < i_last (a slot row with self-attention also sees itself)
+    const int b2 = slot_count(p.self_attend ? i_last : i_last - 1, S, W, r);
+    const int i = eff(xr);
+    const int lo1 = imax(S + 1, i - W + 1) - 1;
+    int hi0 = 0, hi1 = 0, hi2 = 0;
+    if (live) {
+        hi0 = imin(S, i);
+        hi1 = i;
+        hi2 = xr > 0 ? slot_count(i - 1, S, W, r) : (p.self_attend ? -xr : -xr - 1);
     }
     // The sink (S <= 8 keys) and a slot prefix of at most 56 slots share one
     // block when both are present: rows 0..7 of the stage come from the raw
@@ -202,8 +179,8 @@ __global__ void __launch_bounds__(192, 2) prefill_kernel(const __grid_constant__
     // CTA allocates tensor memory and initialises its barriers
     uint4 qreg[16];
     if (warp < 4) {
-        const __nv_bfloat16* qsrc = slot_tile ? p.q_slot : p.q_raw;
-        const uint4* qp = reinterpret_cast<const uint4*>(qsrc + ((size_t)(live ? qrow : 0) * p.Hq + hq) * kD);
+        const __nv_bfloat16* qsrc = xr > 0 ? p.q_raw + (size_t)(xr - 1) * p.Hq * kD : p.q_slot + (size_t)(-xr - 1) * p.Hq * kD;
+        const uint4* qp = reinterpret_cast<const uint4*>(qsrc + (size_t)hq * kD);
 #pragma unroll
         for (int c = 0; c < 16; ++c) qreg[c] = live ? __ldg(qp + c) : make_uint4(0u, 0u, 0u, 0u);
     }
@@ -454,8 +431,6 @@ __global__ void __launch_bounds__(192, 2) prefill_kernel(const __grid_constant__
             ok = __all_sync(0xffffffffu,
                             wait_or_abort(bars + kBarO, (uint32_t)(nblk - 1) & 1u, abort_flag, p.d_err));
         tc_fence_after();
-        float* obase = slot_tile ? p.o_slot : p.o_raw;
-        float* lbase = slot_tile ? p.lse_slot : p.lse_raw;
         const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
         // O / l through a swizzled 32 x 32 tile per warp in the (now idle) K
         // stages: thread `lane` writes 32 columns of its row, then each store
@@ -466,11 +441,12 @@ __global__ void __launch_bounds__(192, 2) prefill_kernel(const __grid_constant__
             float* rowp[8];                              // global row of tile row 4 i + lane / 8, or null
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
-                const int t = warp * 32 + i * 4 + (lane >> 3);
-                const int qr = q0 + (pack > 1 ? t / pack : t);
-                const int hh = pack > 1 ? kvh * G + t % pack : (int)blockIdx.y;
-                const bool lv = (pack == 1 || t < rpt * pack) && qr < q1;
-                rowp[i] = lv ? obase + ((size_t)qr * p.Hq + hh) * kD : nullptr;
+                const int tl = i * 4 + (lane >> 3);     // row warp * 32 + tl, owned by lane tl
+                const int x = __shfl_sync(0xffffffffu, xr, tl);
+                const bool lv = q0 + warp * 32 + tl < q1;
+                rowp[i] = !lv ? nullptr
+                              : (x > 0 ? p.o_raw + ((size_t)(x - 1) * p.Hq + hq) * kD
+                                       : p.o_slot + ((size_t)(-x - 1) * p.Hq + hq) * kD);
             }
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
@@ -494,9 +470,9 @@ __global__ void __launch_bounds__(192, 2) prefill_kernel(const __grid_constant__
                 __syncwarp();
             }
         }
-        if (live && lbase)
-            lbase[(size_t)qrow * p.Hq + hq] =
-                l_run > 0.f ? (m_run + __log2f(l_run)) * 0.6931471805599453f : -INFINITY;
+        float* lp = xr > 0 ? (p.lse_raw ? p.lse_raw + (size_t)(xr - 1) * p.Hq + hq : nullptr)
+                           : (p.lse_slot ? p.lse_slot + (size_t)(-xr - 1) * p.Hq + hq : nullptr);
+        if (live && lp) *lp = l_run > 0.f ? (m_run + __log2f(l_run)) * 0.6931471805599453f : -INFINITY;
     }
     tc_fence_before();
     __syncthreads();
@@ -639,14 +615,9 @@ extern "C" int masw_prefill(masw_mem_t* mem, int layer, int seq, int T, const vo
     p.Hq = n_q_heads;
     p.Hkv = Hkv;
     p.self_attend = mem->self_attend;
-    const int raw_ctas = (T + tcp::kBM - 1) / tcp::kBM;
-    // slot rows per tile: extra rows widen the tile's window band by r keys
-    // each, worth it while that stays below the keys every slot row reads anyway
-    p.slot_rows = imin(tcp::kBM, imax(1, (mem->S + mem->W + M / 2) / mem->r + 1));
     p.scale_log2 = mem->scale * 1.4426950408889634f;
-    p.slot_pack = p.slot_rows * (n_q_heads / Hkv) <= tcp::kBM ? n_q_heads / Hkv : 1;
-    p.slot_ctas = (M + p.slot_rows - 1) / p.slot_rows;
-    const int tiles = p.slot_ctas + raw_ctas;
+    // 128-row tiles of the T + M query rows in interleaved order
+    const int tiles = (T + M + tcp::kBM - 1) / tcp::kBM;
     cudaStream_t st = (cudaStream_t)stream;
     static std::atomic<bool> configured[64];   // per device, set once (idempotent)
     if (!configured[mem->device & 63].load(std::memory_order_acquire)) {

@@ -123,5 +123,25 @@ int main() {
         s2[n] = s2[0];
         out("six_runs_ok", segments_in_block<kRowB>(f.p, 3, 1, 2, s2, n + 1));
     }
+    // 4. the prefill's interleaved row order against a brute-force construction
+    //    (raw tokens in order, slot m appended right after raw token tau_m)
+    {
+        long rows = 0, bad = 0;
+        for (int S : {0, 1, 4, 8, 128})
+            for (int W : {1, 3, 16, 128, 1024})
+                for (int r : {1, 2, 3, 4, 16, 512})
+                    for (int T : {1, 5, 60, 100, 257, 333, 1024, 2100}) {
+                        const int M = slot_count(T, S, W, r);
+                        int pos = 0;
+                        for (int i = 1; i <= T; ++i) {
+                            bad += interleaved_row(pos++, S, W, r, M) != i;
+                            if (is_boundary(i, S, W, r)) bad += interleaved_row(pos++, S, W, r, M) != -((i - S - W) / r);
+                        }
+                        bad += pos != T + M;
+                        rows += pos;
+                    }
+        out("interleaved_rows", rows);
+        out("interleaved_mismatches", bad);
+    }
     return 0;
 }

@@ -1,6 +1,7 @@
 """The decode kernels' segment-table bounds test, on the host: every table the
 index model builds from in-range counters lies inside its (layer, sequence,
-kv head) block, and tables with a planted fault are refused.
+kv head) block, and tables with a planted fault are refused; and the prefill's
+interleaved row order matches a brute-force construction.
 
 The library runs this test on every decode launch's speculative tables when a
 handle is created with MASW_CHECK_SEGMENTS=1 (the GPU tests set it), and the
@@ -37,6 +38,10 @@ EXPECTED = {
     "empty_run_ok": 0,
     "other_heads_block_ok": 0,
     "six_runs_ok": 0,
+    # the prefill's interleaved query order (raw tokens, slot m right after raw
+    # token tau_m) against brute force over 1200 (S, W, r, T) shapes
+    "interleaved_rows": 745024,
+    "interleaved_mismatches": 0,
 }
 
 
