@@ -13,6 +13,10 @@
 // row, skipped for blocks every row sees whole).  With S <= 8 the sink and a
 // slot prefix of up to 56 slots share one block.
 //
+// Query tiles cover the T + M rows in that interleaved order (slot token g_m
+// right after raw token tau_m): a slot row has the mask of raw row tau_m, so it
+// shares that tile's key ranges.
+//
 // Fifth-generation tensor cores, one CTA per (128-row query tile, query head),
 // two CTAs per SM:
 //   * the four softmax warps load their rows of Q once and store them in tensor
