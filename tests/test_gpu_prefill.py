@@ -10,10 +10,14 @@ from gpu_helpers import DEV, Pair
 
 pytestmark = pytest.mark.gpu
 
-# (S, W, r, Hkv, G, T): several 64-row tiles with ragged tails, slot tiles of
-# W/r + 1 rows, r > W (one slot per tile), no sink, prefixes inside the sink and
-# inside the first window, the paper's S = W = 128 with r = 4
+# (S, W, r, Hkv, G, T): several 128-row tiles of the interleaved order with
+# ragged tails, r > W (one slot per tile), no sink, prefixes inside the sink and
+# inside the first window, r = 1 (a slot after every raw token past S + W: half
+# the rows of a tile are slot rows, and slot prefixes below and above the 56 a
+# merged sink + slot block holds), the paper's S = W = 128 with r = 4
 CASES = [
+    (4, 8, 1, 2, 4, 200),
+    (1, 3, 2, 1, 2, 140),
     (4, 16, 4, 2, 4, 100),
     (4, 16, 4, 1, 8, 257),
     (0, 32, 8, 2, 2, 200),
