@@ -342,9 +342,12 @@ class DraftBench:
     def e2e(self, iters: int):
         """The same iteration through the public API with host buffers: every
         iteration copies all of its inputs (q, k, v of every decode step and
-        layer, the slot tokens' q, k, v) in from one pinned host buffer, makes the
-        library calls eagerly (no graph), and reads every O back into one pinned
-        host buffer, all inside the timed region."""
+        layer, the slot tokens' q, k, v) in from a pinned host buffer, makes the
+        library calls eagerly (no graph), and reads every O back into a pinned
+        host buffer, all inside the timed region.  Device and host buffers are
+        doubled so that, on a second stream, iteration i+1's inputs are copied in
+        and iteration i's outputs copied out while iteration i+1 computes (one
+        copy each way per iteration, ordered by events)."""
         torch, c = self.torch, self.capi
         ins = [x for row in self.q for x in row] + [x for row in self.k for x in row] + \
               [x for row in self.v for x in row] + list(self.qg) + list(self.kg) + list(self.vg)
@@ -352,54 +355,87 @@ class DraftBench:
         for x in ins:
             offs.append(tot)
             tot += x.numel() * x.element_size()
+        SL = self.steps * self.L
+        n_out = SL * self.B * self.Hq * self.D + self.L * self.qg[0].shape[0] * self.Hq * self.D
+        per = self.B * self.Hq * self.D
+        pg = self.qg[0].shape[0] * self.Hq * self.D
         host_in = torch.empty(tot, dtype=torch.uint8).pin_memory()
-        dev_in = torch.empty(tot, dtype=torch.uint8, device=self.dev)
         for x, o_ in zip(ins, offs):
             n = x.numel() * x.element_size()
             host_in[o_:o_ + n].copy_(x.reshape(-1).view(torch.uint8).cpu())
-        views = [dev_in[o_:o_ + x.numel() * x.element_size()].view(x.dtype).view(x.shape) for x, o_ in zip(ins, offs)]
-        SL = self.steps * self.L
-        dq = [views[i * self.L:(i + 1) * self.L] for i in range(self.steps)]
-        dk = [views[SL + i * self.L:SL + (i + 1) * self.L] for i in range(self.steps)]
-        dv = [views[2 * SL + i * self.L:2 * SL + (i + 1) * self.L] for i in range(self.steps)]
-        dqg, dkg, dvg = views[3 * SL:3 * SL + self.L], views[3 * SL + self.L:3 * SL + 2 * self.L], \
-            views[3 * SL + 2 * self.L:]
-        n_out = SL * self.B * self.Hq * self.D + self.L * self.qg[0].shape[0] * self.Hq * self.D
-        dev_out = torch.empty(n_out, device=self.dev)
-        host_out = torch.empty(n_out).pin_memory()
-        per = self.B * self.Hq * self.D
-        do = [[dev_out[(s_ * self.L + l) * per:(s_ * self.L + l + 1) * per].view(self.B, self.Hq, self.D)
-               for l in range(self.L)] for s_ in range(self.steps)]
-        pg = self.qg[0].shape[0] * self.Hq * self.D
-        dog = [dev_out[SL * per + l * pg:SL * per + (l + 1) * pg].view(-1, self.Hq, self.D) for l in range(self.L)]
-        st = self.stream.cuda_stream
+        host_out = [torch.empty(n_out).pin_memory() for _ in range(2)]
+        bufs = []
+        for _ in range(2):
+            dev_in = torch.empty(tot, dtype=torch.uint8, device=self.dev)
+            views = [dev_in[o_:o_ + x.numel() * x.element_size()].view(x.dtype).view(x.shape) for x, o_ in zip(ins, offs)]
+            dev_out = torch.empty(n_out, device=self.dev)
+            bufs.append({
+                "in": dev_in, "out": dev_out,
+                "q": [views[i * self.L:(i + 1) * self.L] for i in range(self.steps)],
+                "k": [views[SL + i * self.L:SL + (i + 1) * self.L] for i in range(self.steps)],
+                "v": [views[2 * SL + i * self.L:2 * SL + (i + 1) * self.L] for i in range(self.steps)],
+                "qg": views[3 * SL:3 * SL + self.L], "kg": views[3 * SL + self.L:3 * SL + 2 * self.L],
+                "vg": views[3 * SL + 2 * self.L:],
+                "o": [[dev_out[(s_ * self.L + l) * per:(s_ * self.L + l + 1) * per].view(self.B, self.Hq, self.D)
+                       for l in range(self.L)] for s_ in range(self.steps)],
+                "og": [dev_out[SL * per + l * pg:SL * per + (l + 1) * pg].view(-1, self.Hq, self.D)
+                       for l in range(self.L)],
+            })
+        st = self.stream
+        cs = torch.cuda.Stream(device=self.dev)
+        ev = lambda: torch.cuda.Event()
         h2d, d2h = tot, n_out * 4
 
-        def run():
-            dev_in.copy_(host_in, non_blocking=True)
+        def compute(bf):
             for s_ in range(self.steps):
                 due = self.due[s_]
                 for l in range(self.L):
                     if due:
                         n = len(due)
-                        c.masw_draft_step_slot(self.h, l, dq[s_][l], dk[s_][l], dv[s_][l], do[s_][l], due,
-                                               dqg[l][:n], dkg[l][:n], dvg[l][:n], dog[l][:n], stream=st)
+                        c.masw_draft_step_slot(self.h, l, bf["q"][s_][l], bf["k"][s_][l], bf["v"][s_][l],
+                                               bf["o"][s_][l], due, bf["qg"][l][:n], bf["kg"][l][:n],
+                                               bf["vg"][l][:n], bf["og"][l][:n], stream=st.cuda_stream)
                     else:
-                        c.masw_draft_step(self.h, l, dq[s_][l], dk[s_][l], dv[s_][l], do[s_][l], stream=st)
-            c.masw_rollback(self.h, self.seqs, self.prefixes, stream=st)
-            host_out.copy_(dev_out, non_blocking=True)
-            self.stream.synchronize()
+                        c.masw_draft_step(self.h, l, bf["q"][s_][l], bf["k"][s_][l], bf["v"][s_][l],
+                                          bf["o"][s_][l], stream=st.cuda_stream)
+            c.masw_rollback(self.h, self.seqs, self.prefixes, stream=st.cuda_stream)
 
-        with torch.cuda.stream(self.stream):
-            run()
-            torch.cuda.synchronize()
-            e0 = torch.cuda.Event(enable_timing=True)
-            e1 = torch.cuda.Event(enable_timing=True)
-            e0.record(self.stream)
-            for _ in range(iters):
-                run()
-            e1.record(self.stream)
-            torch.cuda.synchronize()
+        def run(n_it):
+            in_ready = [None, None]      # H2D of the buffer's current iteration done
+            done = [None, None]          # compute of the buffer's current iteration done
+            out_done = [None, None]      # D2H of the buffer's last outputs done
+            with torch.cuda.stream(cs):
+                bufs[0]["in"].copy_(host_in, non_blocking=True)
+                in_ready[0] = ev()
+                in_ready[0].record(cs)
+            for i in range(n_it):
+                cur, nxt = i % 2, (i + 1) % 2
+                st.wait_event(in_ready[cur])
+                if out_done[cur] is not None:
+                    st.wait_event(out_done[cur])        # this buffer's previous outputs are on the host
+                compute(bufs[cur])
+                done[cur] = ev()
+                done[cur].record(st)
+                with torch.cuda.stream(cs):
+                    if i + 1 < n_it:
+                        if i >= 1:
+                            cs.wait_event(done[nxt])    # iteration i-1 no longer reads that buffer
+                        bufs[nxt]["in"].copy_(host_in, non_blocking=True)
+                        in_ready[nxt] = ev()
+                        in_ready[nxt].record(cs)
+                    cs.wait_event(done[cur])
+                    host_out[cur].copy_(bufs[cur]["out"], non_blocking=True)
+                    out_done[cur] = ev()
+                    out_done[cur].record(cs)
+
+        run(2)
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(cs)
+        run(iters)
+        e1.record(cs)      # after the last D2H, which follows the last iteration's compute
+        torch.cuda.synchronize()
         return e0.elapsed_time(e1) / 1e3, h2d, d2h
 
     def close(self):
@@ -960,7 +996,9 @@ def main():
         "e2e": {"value": world * dsteps / e2e_per, "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h,
                 "how": "per iteration: one copy of all q/k/v inputs from pinned host memory, eager C-ABI calls "
-                       "(no graph), one copy of every O back to pinned host memory"},
+                       "(no graph), one copy of every O back to pinned host memory; buffers doubled so that "
+                       "iteration i+1's inputs come in and iteration i's outputs go out on a copy stream "
+                       "while iteration i+1 computes"},
     }
     if verify:
         # draft / target attention time per sequence: L_draft draft steps of the
