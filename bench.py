@@ -841,7 +841,7 @@ def main():
                     help="MASW vs full-KV decode steps/s at prefixes 4K..32K (one JSON line)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-verify", action="store_true")
-    ap.add_argument("--e2e-iters", type=int, default=5)
+    ap.add_argument("--e2e-iters", type=int, default=20)
     ap.add_argument("--no-prefill", action="store_true")
     ap.add_argument("--prefill-only", action="store_true",
                     help="only the draft prefill of one sequence through all layers (one JSON line)")
